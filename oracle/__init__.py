@@ -1,0 +1,181 @@
+"""CPU oracle for the FP8 weight-only linear layer (numpy front end).
+
+TEST INFRASTRUCTURE ONLY: imported by tests/, by the smoke check and by the
+benchmark's CPU-baseline leg, never by the library.  The arithmetic lives in
+fp8w_oracle.c (plain C, fp64 for the linear layer); this module only moves
+numpy arrays across ctypes.
+
+Each function follows page "kadirnar/kernel-agent fp8-weights", section
+"The contract", unless its docstring names another passage.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+ACT_BF16 = 1
+ACT_F16 = 2
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        lib = ctypes.CDLL(path)
+        c = ctypes
+        P = c.c_void_p
+        lib.oracle_e4m3_decode.restype = c.c_double
+        lib.oracle_e4m3_decode.argtypes = [c.c_uint8]
+        lib.oracle_e4m3_encode.restype = c.c_uint8
+        lib.oracle_e4m3_encode.argtypes = [c.c_float]
+        lib.oracle_row_scale.restype = c.c_float
+        lib.oracle_row_scale.argtypes = [P, c.c_int64]
+        lib.oracle_quantize.restype = None
+        lib.oracle_quantize.argtypes = [P, c.c_int64, c.c_int64, P, P]
+        lib.oracle_dequantize.restype = None
+        lib.oracle_dequantize.argtypes = [P, P, c.c_int64, c.c_int64, P]
+        lib.oracle_round_bf16.restype = c.c_uint16
+        lib.oracle_round_bf16.argtypes = [c.c_double]
+        lib.oracle_round_f16.restype = c.c_uint16
+        lib.oracle_round_f16.argtypes = [c.c_double]
+        lib.oracle_bf16_value.restype = c.c_double
+        lib.oracle_bf16_value.argtypes = [c.c_uint16]
+        lib.oracle_f16_value.restype = c.c_double
+        lib.oracle_f16_value.argtypes = [c.c_uint16]
+        lib.oracle_linear.restype = c.c_int
+        lib.oracle_linear.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P,
+                                      c.c_int64, P, P, c.c_int]
+        lib.oracle_fp8_error.restype = None
+        lib.oracle_fp8_error.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
+        lib.oracle_e4m3_encode_many.restype = None
+        lib.oracle_e4m3_encode_many.argtypes = [P, c.c_int64, P]
+        lib.oracle_round_bf16_many.restype = None
+        lib.oracle_round_bf16_many.argtypes = [P, c.c_int64, P]
+        lib.oracle_round_f16_many.restype = None
+        lib.oracle_round_f16_many.argtypes = [P, c.c_int64, P]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one OCP e4m3 byte (NaN for 0x7F/0xFF)."""
+    return _load().oracle_e4m3_decode(int(code) & 0xFF)
+
+
+def e4m3_decode_table() -> np.ndarray:
+    """fp64 values of all 256 codes, index = code."""
+    lib = _load()
+    return np.array([lib.oracle_e4m3_decode(b) for b in range(256)], dtype=np.float64)
+
+
+def e4m3_encode(v) -> np.ndarray:
+    """Round-to-nearest-even, saturating e4m3 encode of fp32 values."""
+    v = _c(np.atleast_1d(v), np.float32)
+    out = np.empty(v.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode_many(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def row_scale(row) -> np.float32:
+    row = _c(row, np.float32)
+    return np.float32(_load().oracle_row_scale(_ptr(row), row.size))
+
+
+def quantize(w):
+    """W[N,K] fp32 -> (codes uint8 [N,K], scales fp32 [N])."""
+    w = _c(w, np.float32)
+    n, k = w.shape
+    codes = np.empty((n, k), dtype=np.uint8)
+    scales = np.empty(n, dtype=np.float32)
+    _load().oracle_quantize(_ptr(w), n, k, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def dequantize(codes, scales) -> np.ndarray:
+    """fp64 W' = scale[n] * e4m3val(codes[n,k])."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    n, k = codes.shape
+    out = np.empty((n, k), dtype=np.float64)
+    _load().oracle_dequantize(_ptr(codes), _ptr(scales), n, k, _ptr(out))
+    return out
+
+
+def round_bf16(v) -> np.ndarray:
+    """fp64 -> bf16 bits (uint16), one RNE rounding."""
+    v = _c(np.atleast_1d(v), np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().oracle_round_bf16_many(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def round_f16(v) -> np.ndarray:
+    """fp64 -> fp16 bits (uint16), one RNE rounding."""
+    v = _c(np.atleast_1d(v), np.float64)
+    out = np.empty(v.shape, dtype=np.uint16)
+    _load().oracle_round_f16_many(_ptr(v), v.size, _ptr(out))
+    return out
+
+
+def act_values(bits, act: int) -> np.ndarray:
+    """fp64 values of bf16 (act=1) or fp16 (act=2) bit patterns."""
+    lib = _load()
+    f = lib.oracle_f16_value if act == ACT_F16 else lib.oracle_bf16_value
+    flat = np.asarray(bits, dtype=np.uint16).ravel()
+    return np.array([f(int(b)) for b in flat], dtype=np.float64).reshape(np.shape(bits))
+
+
+def linear(x_bits, act: int, codes, scales, bias=None, threads: int = 1,
+           want_acc: bool = False):
+    """y[M,N] = round_act(scale[n] * sum_k x[m,k] e4m3val(q[n,k]) + bias[n]).
+
+    x_bits: uint16 [M,K] bf16/fp16 bit patterns.  Returns y bits (uint16
+    [M,N]) and, with want_acc, also the unrounded fp64 value.
+    """
+    x_bits = _c(x_bits, np.uint16)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    bias = None if bias is None else _c(bias, np.float32)
+    m, k = x_bits.shape
+    n, k2 = codes.shape
+    if k != k2 or scales.shape != (n,) or (bias is not None and bias.shape != (n,)):
+        raise ValueError("oracle.linear: shape mismatch")
+    y = np.empty((m, n), dtype=np.uint16)
+    acc = np.empty((m, n), dtype=np.float64) if want_acc else None
+    rc = _load().oracle_linear(_ptr(x_bits), act, m, k, _ptr(codes), _ptr(scales),
+                               _ptr(bias), n, _ptr(y), _ptr(acc), int(threads))
+    if rc != 0:
+        raise RuntimeError("oracle.linear: thread start failed")
+    return (y, acc) if want_acc else y
+
+
+def fp8_error(w, codes, scales) -> dict:
+    """Weight report: rel_l2, worst_channel_rel_l2, underflow, crest."""
+    w = _c(w, np.float32)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    n, k = w.shape
+    out = np.zeros(4, dtype=np.float64)
+    _load().oracle_fp8_error(_ptr(w), n, k, _ptr(codes), _ptr(scales), _ptr(out))
+    return {"rel_l2": out[0], "worst_channel_rel_l2": out[1],
+            "underflow": out[2], "crest": out[3]}
+
+
+def host_cores() -> int:
+    """Cores this process may run on (for the CPU baseline's thread count)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
