@@ -1,0 +1,494 @@
+"""Benchmark of the FP8 weight-only linear layer on one GB300 (or N replicas).
+
+One step = one pass of the decode-layer stack of an 8B-style block (hidden
+4096, 32 q / 8 kv heads of 128, intermediate 14336): the q, k, v, o, gate, up
+and down linears run back to back at M = 1, then M = 8, then M = 32 tokens
+(21 fp8w_linear calls), weights quantised once beforehand with fp8w_quantize.
+Inputs are seeded synthetic data of those shapes (W ~ N(0, 0.02), bias ~
+N(0, 0.01), x bf16 ~ N(0, 1)); nothing is cached between steps.
+
+value = algorithmic bytes of the step (codes N*K + scale 4N + bias 4N + x
+2MK + y 2MN per call) / device time of the step, in GB/s, timed over
+replays of the step captured in a CUDA graph.  Each step streams 654 MB of
+codes; two weight replicas alternate between the M passes so every weight
+read comes from HBM (inputs larger than L2, no reuse within 436 MB).
+
+Also printed: the quantiser's throughput on the seven matrices, per-kernel
+durations from an instrumented replay (device events recorded between the
+launches inside the graph), the roofline fraction of the dominant kernel,
+an end-to-end figure through the Python API with pinned host buffers, the
+CPU oracle on a bounded sample, and SM clocks sampled during the timed loop.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+import argparse
+import ctypes
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synthetic  # noqa: E402
+
+METRIC = "FP8-weight linear effective GB/s and % of GB300 HBM peak at M=1..32"
+WORKLOAD = ("decode_stack: 8B-style block linears q[4096x4096], k[1024x4096], v[1024x4096], "
+            "o[4096x4096], gate[14336x4096], up[14336x4096], down[4096x14336] ([N x K]) back to back "
+            "at M=1, 8, 32; bf16 activations, e4m3 per-channel weights, fp32 bias")
+
+
+def step_calls():
+    """(M, matrix name, N, K) of every linear call of one step, in order."""
+    return [(m, name, n, k) for m in synthetic.DECODE_STACK_M for (name, n, k) in synthetic.DECODE_STACK]
+
+
+def call_bytes(m, n, k, with_bias=True):
+    return n * k + 4 * n + (4 * n if with_bias else 0) + 2 * m * k + 2 * m * n
+
+
+def step_bytes():
+    return sum(call_bytes(m, n, k) for (m, _, n, k) in step_calls())
+
+
+def step_flops():
+    return sum(2 * m * n * k for (m, _, n, k) in step_calls())
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    return 6800.0, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+# ------------------------------------------------------------ dist helpers --
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------ clock sampler --
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------- device event helpers --
+
+class DriverEvents:
+    """cuEventRecordWithFlags(EXTERNAL) so that events recorded during graph
+    capture become timing nodes of the graph."""
+
+    def __init__(self):
+        self.cu = ctypes.CDLL("libcuda.so.1")
+        self.cu.cuEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_uint]
+        self.cu.cuEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        self.cu.cuEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
+        self.cu.cuEventDestroy_v2.argtypes = [ctypes.c_void_p]
+        self.events = []
+
+    def create(self):
+        ev = ctypes.c_void_p()
+        rc = self.cu.cuEventCreate(ctypes.byref(ev), 0)
+        if rc != 0:
+            raise RuntimeError("cuEventCreate failed: %d" % rc)
+        self.events.append(ev)
+        return ev
+
+    def record(self, ev, stream_handle):
+        rc = self.cu.cuEventRecordWithFlags(ev, ctypes.c_void_p(stream_handle), 1)
+        if rc != 0:
+            raise RuntimeError("cuEventRecordWithFlags failed: %d" % rc)
+
+    def elapsed_ms(self, a, b):
+        ms = ctypes.c_float()
+        rc = self.cu.cuEventElapsedTime(ctypes.byref(ms), a, b)
+        if rc != 0:
+            raise RuntimeError("cuEventElapsedTime failed: %d" % rc)
+        return float(ms.value)
+
+    def close(self):
+        for ev in self.events:
+            self.cu.cuEventDestroy_v2(ev)
+        self.events = []
+
+
+# ------------------------------------------------------------- CPU baseline --
+
+CPU_STRIDE = 16  # the CPU sample takes every 16th output channel of every call
+
+
+def cpu_sample(m_list=synthetic.DECODE_STACK_M):
+    """Inputs of the CPU sample: every call of the step, channels n % 16 == 0."""
+    import oracle
+    out = []
+    for m in m_list:
+        for (name, n, k) in synthetic.DECODE_STACK:
+            c = synthetic.case("decode_stack", m, name)
+            cols = np.arange(0, n, CPU_STRIDE)
+            codes, scales = oracle.quantize(c["w"][cols])
+            out.append((c["x"], codes, scales, c["bias"][cols], m, len(cols), k))
+    return out
+
+
+def run_cpu(sample, threads):
+    import oracle
+    t0 = time.perf_counter()
+    for (x, codes, scales, bias, m, n, k) in sample:
+        oracle.linear(x, oracle.ACT_BF16, codes, scales, bias, threads=threads)
+    dt = time.perf_counter() - t0
+    nbytes = sum(call_bytes(m, n, k) for (_, _, _, _, m, n, k) in sample)
+    return nbytes / dt / 1e9, dt
+
+
+def cpu_baseline_obj(gbs, dt, cores):
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": "the full step (21 calls, M=1,8,32) restricted to every %dth output channel; "
+                      "plain C fp64 oracle, %d threads; %.2f s" % (CPU_STRIDE, cores, dt)}
+
+
+# ------------------------------------------------------------------- ours --
+
+def build_state(torch, fw, dev, replicas=2):
+    """Quantise the seven matrices on the GPU; keep codes, scales, bias resident."""
+    mats = {}
+    wdev = {}
+    for (name, n, k) in synthetic.DECODE_STACK:
+        c = synthetic.case("decode_stack", 1, name)
+        w = torch.from_numpy(c["w"]).to(dev)
+        codes, scales = fw.quantize(w)
+        bias = torch.from_numpy(c["bias"]).to(dev)
+        reps = [codes] + [codes.clone() for _ in range(replicas - 1)]
+        mats[name] = {"codes": reps, "scales": scales, "bias": bias, "n": n, "k": k}
+        wdev[name] = w
+    xs, ys = {}, {}
+    for (m, name, n, k) in step_calls():
+        c = synthetic.case("decode_stack", m, name)
+        xs[(m, name)] = torch.from_numpy(c["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+        ys[(m, name)] = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize()
+    return mats, wdev, xs, ys
+
+
+def enqueue_step(fw, mats, xs, ys, events=None, ev_list=None, stream_handle=None):
+    launches = 0
+    for i, (m, name, n, k) in enumerate(step_calls()):
+        mt = mats[name]
+        rep = synthetic.DECODE_STACK_M.index(m) % len(mt["codes"])
+        if events is not None:
+            events.record(ev_list[i], stream_handle)
+        fw.linear(xs[(m, name)], mt["codes"][rep], mt["scales"], mt["bias"], out=ys[(m, name)])
+        launches += 1
+    if events is not None:
+        events.record(ev_list[len(step_calls())], stream_handle)
+    return launches
+
+
+def kernel_name(m):
+    if m == 1:
+        return "fp8w::gemv_kernel<4,2,bf16>|<1,8,bf16>"
+    return "fp8w::skinny_kernel<%d,bf16>" % (16 if m <= 16 else 32)
+
+
+def run_ours(args, torch, dist):
+    import fp8_weight_only_gb300 as fw
+    ws, rank, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    mats, wdev, xs, ys = build_state(torch, fw, dev)
+    s = torch.cuda.Stream(device=dev)
+
+    # warm-up eagerly (module load, attribute setup), then capture the step
+    with torch.cuda.stream(s):
+        for _ in range(max(1, args.warmup)):
+            enqueue_step(fw, mats, xs, ys)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        launches_per_step = enqueue_step(fw, mats, xs, ys)
+    for _ in range(args.warmup):
+        g.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    n_ranks = ws
+    value = step_bytes() * n_ranks * args.steps / (ms_total / 1e3) / 1e9
+
+    # instrumented replay: external events between the launches inside a graph
+    per_call = None
+    try:
+        evs = DriverEvents()
+        ev_list = [evs.create() for _ in range(len(step_calls()) + 1)]
+        gi = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gi, stream=s):
+            enqueue_step(fw, mats, xs, ys, evs, ev_list, s.cuda_stream)
+        reps = max(3, min(args.steps, 20))
+        acc = np.zeros(len(step_calls()))
+        for _ in range(2):
+            gi.replay()
+        torch.cuda.synchronize()
+        for _ in range(reps):
+            gi.replay()
+            torch.cuda.synchronize()
+            acc += [evs.elapsed_ms(ev_list[i], ev_list[i + 1]) for i in range(len(step_calls()))]
+        per_call = acc / reps
+        del gi
+    except (OSError, RuntimeError) as e:  # pragma: no cover - reported in the JSON
+        per_call = None
+        instr_err = str(e)
+    peak, peak_src = peaks()
+
+    result = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+              "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+              "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+              "dtype_detail": "e4m3 weights x bf16 activations, fp32 accumulate, bf16 out",
+              "data": "synthetic",
+              "config": {"workload": WORKLOAD, "M": list(synthetic.DECODE_STACK_M), "calls_per_step": 21,
+                         "bytes_per_step": step_bytes(), "flops_per_step": step_flops(),
+                         "l2": "inputs larger than L2: 654 MB of codes per step, two weight replicas "
+                               "alternate between the M passes",
+                         "graph": "step captured in one CUDA graph", "parallelism": "replicas (dp%d)" % ws},
+              "clocks": clocks, "gpu_launches": launches_per_step * args.steps,
+              "frac_of_hbm_peak": round(value / n_ranks / peak, 4), "peak_source": peak_src}
+
+    if per_call is not None:
+        calls = step_calls()
+        by_kernel = {}
+        by_m = {}
+        for (m, name, n, k), ms in zip(calls, per_call):
+            kn = kernel_name(m)
+            d = by_kernel.setdefault(kn, {"ms": 0.0, "bytes": 0, "launches": 0})
+            d["ms"] += ms
+            d["bytes"] += call_bytes(m, n, k)
+            d["launches"] += 1
+            e = by_m.setdefault(m, {"ms": 0.0, "bytes": 0})
+            e["ms"] += ms
+            e["bytes"] += call_bytes(m, n, k)
+        total = sum(d["ms"] for d in by_kernel.values())
+        top = max(by_kernel, key=lambda kk: by_kernel[kk]["ms"])
+        d = by_kernel[top]
+        achieved = d["bytes"] / d["launches"] / (d["ms"] / d["launches"] / 1e3) / 1e9
+        result["roofline"] = {"bound": "hbm", "kernel": top, "achieved": round(achieved, 1),
+                              "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                              "traffic": None, "share": round(d["ms"] / total, 4),
+                              "note": "achieved = algorithmic bytes per launch / mean launch duration "
+                                      "(device events between launches in an instrumented graph replay); "
+                                      "peak is " + peak_src}
+        result["kernels"] = {kk: {"share": round(v["ms"] / total, 4), "launches_per_step": v["launches"],
+                                  "ms_per_step": round(v["ms"], 5),
+                                  "gbs": round(v["bytes"] / (v["ms"] / 1e3) / 1e9, 1)}
+                             for kk, v in by_kernel.items()}
+        result["per_m"] = {str(m): {"ms": round(v["ms"], 5), "gbs": round(v["bytes"] / (v["ms"] / 1e3) / 1e9, 1),
+                                    "frac": round(v["bytes"] / (v["ms"] / 1e3) / 1e9 / peak, 4)}
+                           for m, v in by_m.items()}
+        result["per_call_us"] = {"%s@M%d" % (name, m): round(ms * 1e3, 2)
+                                 for (m, name, n, k), ms in zip(calls, per_call)}
+    else:
+        result["roofline"] = {"bound": "hbm", "achieved": None, "peak": peak, "unit": "GB/s", "frac": None,
+                              "traffic": None, "note": "instrumented replay failed: " + instr_err}
+
+    # quantiser throughput on the seven matrices (load-time step)
+    qcodes = {name: torch.empty_like(mats[name]["codes"][0]) for name in wdev}
+    qscales = {name: torch.empty_like(mats[name]["scales"]) for name in wdev}
+    with torch.cuda.stream(s):
+        for _ in range(2):
+            for name in wdev:
+                fw.quantize(wdev[name], qcodes[name], qscales[name])
+    torch.cuda.synchronize()
+    q0 = torch.cuda.Event(enable_timing=True)
+    q1 = torch.cuda.Event(enable_timing=True)
+    qreps = 5
+    with torch.cuda.stream(s):
+        q0.record(s)
+        for _ in range(qreps):
+            for name in wdev:
+                fw.quantize(wdev[name], qcodes[name], qscales[name])
+        q1.record(s)
+    torch.cuda.synchronize()
+    qbytes = sum(5 * n * k + 4 * n for (_, n, k) in synthetic.DECODE_STACK)
+    qms = q0.elapsed_time(q1) / qreps
+    result["quantize"] = {"gbs": round(qbytes / (qms / 1e3) / 1e9, 1), "ms_per_pass": round(qms, 4),
+                          "frac": round(qbytes / (qms / 1e3) / 1e9 / peak, 4),
+                          "bytes_per_pass": qbytes, "note": "7 matrices, 5 B/element + 4 B/row, eager launches"}
+    for name in wdev:
+        assert torch.equal(qcodes[name], mats[name]["codes"][0])
+
+    # end to end through the Python API: pinned host x in, pinned host y out
+    hx = {key: t.cpu().pin_memory() for key, t in xs.items()}
+    hy = {key: torch.empty(t.shape, dtype=t.dtype).pin_memory() for key, t in ys.items()}
+    h2d = sum(t.numel() * 2 for t in hx.values())
+    d2h = sum(t.numel() * 2 for t in hy.values())
+
+    def e2e_step():
+        for key in hx:
+            xs[key].copy_(hx[key], non_blocking=True)
+        enqueue_step(fw, mats, xs, ys)
+        for key in hy:
+            hy[key].copy_(ys[key], non_blocking=True)
+
+    with torch.cuda.stream(s):
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(s):
+        for _ in range(args.steps):
+            e2e_step()
+        s.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if dist is not None:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    result["e2e"] = {"value": round(step_bytes() * n_ranks * args.steps / e2e_s / 1e9, 2), "unit": "GB/s",
+                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                     "ms_per_step": round(e2e_s / args.steps * 1e3, 4),
+                     "note": "eager fp8w.linear calls, copies from/to pinned host memory, wall clock"}
+    err = fw.device_error()
+    if err != 0:
+        result["device_error"] = err
+    return result
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_env()
+
+    if args.impl == "reference":
+        # the reference arm is the CPU oracle, timed on the host cores
+        if rank != 0:
+            return
+        import oracle
+        cores = oracle.host_cores()
+        sample = cpu_sample()
+        for _ in range(args.warmup):
+            run_cpu(sample[:1], cores)
+        tot_bytes, tot_s = 0, 0.0
+        for _ in range(args.steps):
+            gbs, dt = run_cpu(sample, cores)
+            tot_s += dt
+            tot_bytes += gbs * dt * 1e9
+        value = tot_bytes / tot_s / 1e9
+        out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": ws,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tot_s / args.steps * 1e3, 3),
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+               "data": "synthetic",
+               "config": {"workload": WORKLOAD, "M": list(synthetic.DECODE_STACK_M),
+                          "sample": "every %dth output channel of every call" % CPU_STRIDE},
+               "cpu_baseline": cpu_baseline_obj(value, tot_s / args.steps, cores),
+               "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(out))
+        return
+
+    import torch
+    dist = None
+    if ws > 1:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl")
+        dist = tdist
+    result = run_ours(args, torch, dist)
+    if rank == 0 and not args.no_cpu:
+        import oracle
+        cores = oracle.host_cores()
+        gbs, dt = run_cpu(cpu_sample(), cores)
+        result["cpu_baseline"] = cpu_baseline_obj(gbs, dt, cores)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(result))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,142 @@
+"""fp8_weight_only_gb300 -- Python binding of libfp8w (include/fp8w.h).
+
+Argument marshalling only: every step of the layer runs in the library's
+CUDA kernels.  PyTorch supplies device memory and the current stream.  There
+is no CPU fallback: if libfp8w.so is missing or a call fails, an exception is
+raised.
+
+    codes, scales = quantize(w)                 # w: [N, K] fp32 CUDA tensor
+    y = linear(x, codes, scales, bias)          # x: [M, K] bf16/fp16 CUDA tensor
+"""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libfp8w.so")
+
+FP8W_BF16 = 1
+FP8W_F16 = 2
+KERNEL_AUTO, KERNEL_GEMV, KERNEL_SKINNY = 0, 1, 2
+
+SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_ex", "fp8w_status_string",
+           "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version")
+
+
+class Fp8wError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(msg)
+        self.status = status
+
+
+class LinearConfig(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("split_k", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libfp8w (ctypes.CDLL); raises if it was never built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise Fp8wError(-1, "libfp8w.so is not built (run __graft_entry__.build() or "
+                                "python fp8_weight_only_gb300/build.py)")
+        L = ctypes.CDLL(LIB_PATH)
+        c, P = ctypes, ctypes.c_void_p
+        L.fp8w_quantize.restype = c.c_int
+        L.fp8w_quantize.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
+        L.fp8w_linear.restype = c.c_int
+        L.fp8w_linear.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P]
+        L.fp8w_linear_ex.restype = c.c_int
+        L.fp8w_linear_ex.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P,
+                                     c.POINTER(LinearConfig), P]
+        L.fp8w_status_string.restype = c.c_char_p
+        L.fp8w_status_string.argtypes = [c.c_int]
+        L.fp8w_last_cuda_error.restype = c.c_char_p
+        L.fp8w_last_cuda_error.argtypes = []
+        L.fp8w_device_error.restype = c.c_int
+        L.fp8w_device_error.argtypes = []
+        L.fp8w_abi_version.restype = c.c_int
+        L.fp8w_abi_version.argtypes = []
+        _lib = L
+    return _lib
+
+
+def _check(status):
+    if status != 0:
+        L = lib()
+        msg = L.fp8w_status_string(status).decode()
+        if status == 5:
+            msg += ": " + L.fp8w_last_cuda_error().decode()
+        raise Fp8wError(status, msg)
+
+
+def _stream(t):
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _act(dtype):
+    import torch
+    if dtype == torch.bfloat16:
+        return FP8W_BF16
+    if dtype == torch.float16:
+        return FP8W_F16
+    raise TypeError("activations must be bfloat16 or float16, got %s" % dtype)
+
+
+def quantize(w, codes=None, scales=None):
+    """W[N, K] fp32 (CUDA, contiguous) -> (codes uint8 [N, K], scales fp32 [N])."""
+    import torch
+    if w.dtype != torch.float32 or not w.is_cuda or w.dim() != 2 or not w.is_contiguous():
+        raise TypeError("w must be a contiguous 2-D float32 CUDA tensor")
+    n, k = w.shape
+    if codes is None:
+        codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((n,), dtype=torch.float32, device=w.device)
+    _check(lib().fp8w_quantize(_ptr(w), n, k, _ptr(codes), _ptr(scales), _stream(w)))
+    return codes, scales
+
+
+def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, split_k=0):
+    """y[M, N] = round(scale[n] * sum_k x[m, k] * e4m3(codes[n, k]) + bias[n])."""
+    import torch
+    if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
+        raise TypeError("x must be a contiguous 2-D CUDA tensor")
+    for name, t, dt in (("codes", codes, torch.uint8), ("scales", scales, torch.float32),
+                        ("bias", bias, torch.float32)):
+        if t is not None and (t.dtype != dt or not t.is_cuda or not t.is_contiguous()):
+            raise TypeError("%s must be a contiguous %s CUDA tensor" % (name, dt))
+    m, k = x.shape
+    n = codes.shape[0]
+    if codes.dim() != 2 or codes.shape[1] != k or scales.numel() != n or \
+            (bias is not None and bias.numel() != n):
+        raise ValueError("shape mismatch: x %s, codes %s, scales %s, bias %s" % (
+            tuple(x.shape), tuple(codes.shape), tuple(scales.shape),
+            None if bias is None else tuple(bias.shape)))
+    if out is None:
+        out = torch.empty((m, n), dtype=x.dtype, device=x.device)
+    elif out.shape != (m, n) or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, N] tensor of x's dtype")
+    act = _act(x.dtype)
+    L = lib()
+    if kernel == KERNEL_AUTO and split_k == 0:
+        st = L.fp8w_linear(_ptr(x), act, m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
+                           _ptr(out), _stream(x))
+    else:
+        cfg = LinearConfig(kernel, split_k)
+        st = L.fp8w_linear_ex(_ptr(x), act, m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
+                              _ptr(out), ctypes.byref(cfg), _stream(x))
+    _check(st)
+    return out
+
+
+def device_error():
+    """Nonzero if a kernel gave up a bounded wait since the last call (syncs)."""
+    return lib().fp8w_device_error()

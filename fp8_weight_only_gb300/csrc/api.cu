@@ -1,0 +1,100 @@
+// api.cu -- the C ABI of libfp8w (declared in include/fp8w.h): argument
+// checks on the host, then dispatch to the kernels.  Nothing here allocates
+// device memory or synchronises (except fp8w_device_error, which says so).
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+
+#include <cuda_runtime.h>
+
+#include "../../include/fp8w.h"
+#include "fp8w_internal.h"
+
+namespace {
+
+thread_local char g_last_cuda_error[256] = "";
+
+fp8w_status cuda_status(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return FP8W_OK;
+    std::snprintf(g_last_cuda_error, sizeof g_last_cuda_error, "%s: %s (%d)", what, cudaGetErrorString(e),
+                  static_cast<int>(e));
+    return FP8W_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool valid_k(int64_t k) { return k >= 16 && k <= FP8W_MAX_K && (k % 16) == 0; }
+
+fp8w_status check_linear(const void* x, int act, int64_t m, int64_t k, const uint8_t* codes,
+                         const float* scales, const float* bias, int64_t n, const void* y) {
+    if (!x || !codes || !scales || !y) return FP8W_ERR_NULL;
+    if (act != FP8W_BF16 && act != FP8W_F16) return FP8W_ERR_DTYPE;
+    if (m < 1 || n < 1 || m > FP8W_MAX_DIM || n > FP8W_MAX_DIM || !valid_k(k)) return FP8W_ERR_SHAPE;
+    if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 4) || (bias && !aligned(bias, 4)) ||
+        !aligned(y, 2))
+        return FP8W_ERR_ALIGN;
+    return FP8W_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+fp8w_status fp8w_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes, float* scales, void* stream) {
+    if (!w || !codes || !scales) return FP8W_ERR_NULL;
+    if (n < 1 || n > FP8W_MAX_DIM || !valid_k(k)) return FP8W_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 4)) return FP8W_ERR_ALIGN;
+    return cuda_status(fp8w::launch_quantize(w, n, k, codes, scales, static_cast<cudaStream_t>(stream)),
+                       "fp8w_quantize launch");
+}
+
+fp8w_status fp8w_linear_ex(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
+                           const float* scales, const float* bias, int64_t n, void* y,
+                           const fp8w_linear_config* config, void* stream) {
+    fp8w_status st = check_linear(x, act_dtype, m, k, codes, scales, bias, n, y);
+    if (st != FP8W_OK) return st;
+    int kernel = config ? config->kernel : FP8W_KERNEL_AUTO;
+    int split = config ? config->split_k : 0;
+    if (kernel == FP8W_KERNEL_AUTO) kernel = (m == 1) ? FP8W_KERNEL_GEMV : FP8W_KERNEL_SKINNY;
+    if (kernel == FP8W_KERNEL_GEMV && m != 1) return FP8W_ERR_CONFIG;
+    if (kernel != FP8W_KERNEL_GEMV && kernel != FP8W_KERNEL_SKINNY) return FP8W_ERR_CONFIG;
+    if (kernel == FP8W_KERNEL_SKINNY && split != 0) {
+        const int64_t nkb = (k + 127) / 128;
+        if ((split != 1 && split != 2 && split != 4 && split != 8) || split > fp8w::skinny_max_split() ||
+            split > nkb)
+            return FP8W_ERR_CONFIG;
+    }
+    fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, scales, bias, y};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (kernel == FP8W_KERNEL_GEMV) return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear gemv launch");
+    return cuda_status(fp8w::launch_skinny(a, split, s), "fp8w_linear tensor-core launch");
+}
+
+fp8w_status fp8w_linear(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
+                        const float* scales, const float* bias, int64_t n, void* y, void* stream) {
+    return fp8w_linear_ex(x, act_dtype, m, k, codes, scales, bias, n, y, nullptr, stream);
+}
+
+const char* fp8w_status_string(int status) {
+    switch (status) {
+        case FP8W_OK: return "ok";
+        case FP8W_ERR_NULL: return "a required pointer is NULL";
+        case FP8W_ERR_SHAPE: return "shape out of range (need m,n >= 1, 16 <= k <= 65536, k % 16 == 0)";
+        case FP8W_ERR_ALIGN: return "pointer misaligned (x, codes, w: 16 B; scales, bias: 4 B; y: 2 B)";
+        case FP8W_ERR_DTYPE: return "activation dtype must be FP8W_BF16 or FP8W_F16";
+        case FP8W_ERR_CUDA: return "CUDA call failed (see fp8w_last_cuda_error)";
+        case FP8W_ERR_CONFIG: return "invalid explicit launch configuration";
+        default: return "unknown status";
+    }
+}
+
+const char* fp8w_last_cuda_error(void) { return g_last_cuda_error; }
+
+int fp8w_device_error(void) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+    return fp8w::read_skinny_device_error();
+}
+
+int fp8w_abi_version(void) { return FP8W_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,328 @@
+// fp8w_device.cuh -- device-side building blocks shared by the libfp8w kernels
+// (sm_103a only): streaming loads, e4m3 decoding, mbarrier waits with a time
+// limit, TMA tensor loads, tcgen05 (TMEM / tensor core) wrappers and cluster
+// shared-memory access.  Every wrapper is a single PTX instruction or a short
+// fixed sequence written out here.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#if defined(__CUDA_ARCH__) && (__CUDA_ARCH__ != 1030)
+#error "libfp8w is built for sm_103a only"
+#endif
+
+namespace fp8w {
+
+// Bounded waits: a wait that has not succeeded after this long gives up,
+// records an error code and lets the kernel wind down instead of hanging.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+enum DeviceError : int {
+    kErrNone = 0,
+    kErrWaitTma = 1,      // consumer gave up waiting for a TMA stage
+    kErrWaitMma = 2,      // waiting for tensor-core completion
+    kErrWaitDequant = 3,  // MMA issuer gave up waiting for a dequantised stage
+    kErrWaitSlot = 4,     // producer gave up waiting for a free stage
+    kErrWaitDrain = 5     // giving up on in-flight copies at exit
+};
+
+// ---------------------------------------------------------------- loads --
+
+// 16 bytes, read-only, not kept in L1 (the codes are streamed exactly once).
+__device__ __forceinline__ uint4 ldg_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ float4 ldg_stream_f4(const float* p) {
+    float4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint64_t globaltimer() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// ------------------------------------------------------------ e4m3 codec --
+
+// Two e4m3 codes (low byte = first) -> f16x2 (first code in the low half),
+// hardware conversion, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t two) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(two));
+    return h;
+}
+
+// Four codes (byte i = code i) -> two f16x2 words (codes 0,1 and 2,3).
+__device__ __forceinline__ void e4m3x4_to_f16x2(uint32_t w, uint32_t& p01, uint32_t& p23) {
+    p01 = e4m3x2_to_f16x2(static_cast<uint16_t>(w & 0xFFFFu));
+    p23 = e4m3x2_to_f16x2(static_cast<uint16_t>(w >> 16));
+}
+
+// Four codes (byte i = code i) -> two bf16x2 words, exact, by integer moves:
+// the byte S.EEEE.MMM is laid out as the bf16 pattern S.0000EEEE.MMM0000,
+// whose value is the e4m3 value times 2^-120 (e4m3 subnormals become bf16
+// subnormals), then one packed bf16 multiply by 2^120 restores the value.
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+constexpr uint32_t kBf16x2Pow2_120 = 0x7B807B80u;  // bf16 2^120 in both halves
+
+__device__ __forceinline__ void e4m3x4_to_bf16x2(uint32_t w, uint32_t& p01, uint32_t& p23) {
+    const uint32_t lo = (w << 4) & 0xF0F0F0F0u;                         // E0 M2 M1 M0 0000
+    const uint32_t hi = ((w >> 4) & 0x07070707u) | (w & 0x80808080u);  // S 0000 E3 E2 E1
+    p01 = bf16x2_mul(__byte_perm(lo, hi, 0x5140), kBf16x2Pow2_120);
+    p23 = bf16x2_mul(__byte_perm(lo, hi, 0x7362), kBf16x2Pow2_120);
+}
+
+// Two fp32 values -> two saturating, round-to-nearest-even e4m3 codes
+// (first argument in the low byte).
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float first, float second) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(second), "f"(first));
+    return r;
+}
+
+__device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t h2) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+}
+__device__ __forceinline__ float bf16_lo_to_f32(uint32_t b2) { return __uint_as_float(b2 << 16); }
+__device__ __forceinline__ float bf16_hi_to_f32(uint32_t b2) { return __uint_as_float(b2 & 0xFFFF0000u); }
+
+// ------------------------------------------------------------- mbarrier --
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete.  Returns false if the
+// CTA-wide abort flag is raised meanwhile or the time limit passes.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 63u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer() - t0 > kWaitLimitNs) return false;
+        }
+    }
+}
+
+// Wait with a time limit only (used while winding down after an abort).
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!mbar_try_wait(bar, parity)) {
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    }
+    return true;
+}
+
+// Warp-uniform wait: every lane waits, and the warp proceeds only if all
+// lanes saw the phase complete (so warp-collective instructions that follow
+// are never reached by part of a warp).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+    const bool ok = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// ------------------------------------------------------------------ TMA --
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2-D tiled load of the box at (x = inner coordinate, y = row) into shared
+// memory; completion is counted in bytes on `bar`.  `policy` is an L2 cache
+// policy from createpolicy.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// -------------------------------------------------------------- tcgen05 --
+
+// TMEM allocation (executed by one full warp): writes the base address to
+// shared memory at `dst`.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Each thread of the warp writes 8 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+// Each thread of the warp reads 16 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, "
+        "[%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]: M = 128 rows of A (one per TMEM lane), N
+// and the operand types from the instruction descriptor, K = 16.  Issued by
+// one thread.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation issued so far by this
+// thread has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): K-major operand in the
+// 128-byte swizzled canonical layout -- rows of 128 bytes, 8-row atoms of
+// 1024 bytes (SBO), 16-byte chunk c of row r stored at chunk c ^ (r % 8).
+// `addr` is the shared address of the first element used (the atom must be
+// 1024-byte aligned; advancing along K inside the atom adds bytes here).
+__device__ __forceinline__ uint64_t smem_desc_sw128_kmajor(uint32_t addr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);    // start address
+    d |= static_cast<uint64_t>(1u) << 16;                  // LBO (unused for swizzled K-major)
+    d |= static_cast<uint64_t>(1024u >> 4) << 32;          // SBO: 8 rows x 128 B
+    d |= static_cast<uint64_t>(1u) << 46;                  // descriptor version (tcgen05)
+    d |= static_cast<uint64_t>(2u) << 61;                  // layout: 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor for kind::f16: fp32 accumulator, A and B both bf16
+// (bf16 = true) or both fp16, both K-major, M = 128, N = n.
+__host__ __device__ constexpr uint32_t idesc_f16(bool bf16, uint32_t n) {
+    return (1u << 4)                          // D format: f32
+           | ((bf16 ? 1u : 0u) << 7)          // A format
+           | ((bf16 ? 1u : 0u) << 10)         // B format
+           | ((n >> 3) << 17)                 // N / 8
+           | ((128u >> 4) << 24);             // M / 16
+}
+
+// -------------------------------------------------------------- cluster --
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// ------------------------------------------------------------- epilogue --
+
+template <bool kBf16>
+__device__ __forceinline__ uint16_t round_out(float v) {
+    if constexpr (kBf16) {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    } else {
+        return __half_as_ushort(__float2half_rn(v));
+    }
+}
+
+}  // namespace fp8w

@@ -1,0 +1,35 @@
+// fp8w_internal.h -- launch functions shared between the kernels' translation
+// units and the C ABI layer (api.cu).  Host-side only.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace fp8w {
+
+struct LinearArgs {
+    const void* x;
+    int act;  // FP8W_BF16 / FP8W_F16
+    int64_t m, k, n;
+    const uint8_t* codes;
+    const float* scales;
+    const float* bias;  // may be null
+    void* y;
+};
+
+// K1: codes/scales from fp32 weights.
+cudaError_t launch_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes, float* scales,
+                            cudaStream_t st);
+
+// K2: m == 1.
+cudaError_t launch_gemv(const LinearArgs& a, cudaStream_t st);
+
+// K3: 1 <= m <= 32 per launch (the caller slices larger m).  split_k = 0
+// picks the cluster size from the shape.
+cudaError_t launch_skinny(const LinearArgs& a, int split_k, cudaStream_t st);
+int skinny_max_split();
+
+// Kernel-recorded wait failures (0 = none); reading clears them.
+int read_skinny_device_error();
+
+}  // namespace fp8w

@@ -1,0 +1,138 @@
+/*
+ * fp8w.h -- C ABI of libfp8w, the FP8 weight-only linear layer for one
+ * GB300 (sm_103a).
+ *
+ * The operation (page "kadirnar/kernel-agent fp8-weights", section "The
+ * contract"):
+ *
+ *   quantise once, per output channel n of a weight W[N,K] (nn.Linear
+ *   [out, in], row-major):
+ *     scale[n] = amax_k |W[n,k]| / 448          (fp32 division; 1.0 if 0)
+ *     q[n,k]   = e4m3( W[n,k] / scale[n] )      (OCP e4m3fn, round to nearest
+ *                                                even, saturated to +-448)
+ *   then, per call, with activations x[M,K] in bf16 or fp16:
+ *     y[m,n]   = round_act( scale[n] * sum_k x[m,k] * q[n,k] + bias[n] )
+ *   accumulated in fp32; scale and bias applied in fp32 with one rounding
+ *   to the activation dtype.
+ *
+ * Conventions shared by every entry point:
+ *  - Every data pointer is a DEVICE pointer owned by the caller.  The
+ *    library allocates no device memory, frees nothing and never
+ *    synchronises: it enqueues kernels on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream) and returns.  Calls can be captured in a
+ *    CUDA graph.
+ *  - Arguments are checked on the host before any launch; on an error the
+ *    outputs are untouched and no work is enqueued.  FP8W_ERR_CUDA means a
+ *    CUDA runtime call failed (fp8w_last_cuda_error() names it).  Faults
+ *    inside a kernel surface on the caller's next synchronisation.
+ *  - A kernel that gives up a bounded wait (it never should) records a
+ *    nonzero code that fp8w_device_error() returns.
+ *  - All matrices are row-major and densely packed (row stride = columns).
+ */
+#ifndef FP8W_H
+#define FP8W_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define FP8W_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define FP8W_API __attribute__((visibility("default")))
+#else
+#define FP8W_API
+#endif
+
+typedef enum fp8w_status {
+    FP8W_OK = 0,
+    FP8W_ERR_NULL = 1,      /* a required pointer is NULL */
+    FP8W_ERR_SHAPE = 2,     /* m, n or k out of range, or k % 16 != 0 */
+    FP8W_ERR_ALIGN = 3,     /* a pointer breaks its alignment rule */
+    FP8W_ERR_DTYPE = 4,     /* activation dtype is not FP8W_BF16 / FP8W_F16 */
+    FP8W_ERR_CUDA = 5,      /* a CUDA runtime/driver call failed */
+    FP8W_ERR_CONFIG = 6     /* an explicit launch configuration is invalid */
+} fp8w_status;
+
+/* Activation / output dtypes. */
+enum { FP8W_BF16 = 1, FP8W_F16 = 2 };
+
+/* Largest supported reduction length and row count. */
+#define FP8W_MAX_K 65536
+#define FP8W_MAX_DIM 2147483647LL
+
+/*
+ * fp8w_quantize -- steps "row amax", "scale" and "encode" of the contract
+ * (page "kadirnar/kernel-agent fp8-weights", "The contract"; the saturating
+ * conversion is page "tensormux Write an FP8 kernel", step 4).
+ *
+ *   w      [n, k] fp32, device, 16-byte aligned; values must be finite
+ *          (non-finite weights are a precondition violation, not checked).
+ *   codes  [n, k] uint8 OCP e4m3fn bytes, device, 16-byte aligned (output).
+ *   scales [n] fp32, device, 4-byte aligned (output).
+ *   1 <= n <= FP8W_MAX_DIM, 16 <= k <= FP8W_MAX_K, k % 16 == 0.
+ *
+ * Codes and scales are exact functions of w: scale = fp32(amax / 448), or
+ * 1.0 when that quotient is 0; code = nearest-even e4m3 of fp32(w / scale).
+ */
+FP8W_API fp8w_status fp8w_quantize(const float *w, int64_t n, int64_t k,
+                          uint8_t *codes, float *scales, void *stream);
+
+/*
+ * fp8w_linear -- steps "stream codes", "decode", "contract", "epilogue" and
+ * "dispatch" of the contract (page "kadirnar/kernel-agent fp8-weights",
+ * sections "The contract" and "Dequantise in registers": GEMV for M = 1,
+ * a tensor-core kernel from M = 2).
+ *
+ *   x      [m, k] bf16 or fp16 bits (act_dtype), device, 16-byte aligned.
+ *   codes  [n, k] e4m3 bytes from fp8w_quantize, device, 16-byte aligned.
+ *   scales [n] fp32, device, 4-byte aligned.
+ *   bias   [n] fp32, device, 4-byte aligned, or NULL for no bias.
+ *   y      [m, n] in act_dtype, device, 2-byte aligned (output).
+ *   1 <= m <= FP8W_MAX_DIM, 1 <= n <= FP8W_MAX_DIM, 16 <= k <= FP8W_MAX_K,
+ *   k % 16 == 0.  x and y must not overlap codes, scales or bias.
+ *
+ * m == 1 runs the GEMV kernel; 2 <= m <= 32 the tensor-core kernel; m > 32
+ * the tensor-core kernel over 32-row slabs (correct, not tuned).
+ */
+FP8W_API fp8w_status fp8w_linear(const void *x, int act_dtype, int64_t m, int64_t k,
+                        const uint8_t *codes, const float *scales,
+                        const float *bias, int64_t n, void *y, void *stream);
+
+/* Explicit kernel choice, for tests and tuning; fp8w_linear uses
+ * kernel = FP8W_KERNEL_AUTO and split_k = 0. */
+enum { FP8W_KERNEL_AUTO = 0, FP8W_KERNEL_GEMV = 1, FP8W_KERNEL_SKINNY = 2 };
+
+typedef struct fp8w_linear_config {
+    int kernel;   /* FP8W_KERNEL_*; GEMV requires m == 1 */
+    int split_k;  /* tensor-core kernel: CTAs per cluster sharing one channel
+                     tile along k (1..8); 0 = chosen from the shape */
+    int reserved[6];
+} fp8w_linear_config;
+
+FP8W_API fp8w_status fp8w_linear_ex(const void *x, int act_dtype, int64_t m, int64_t k,
+                           const uint8_t *codes, const float *scales,
+                           const float *bias, int64_t n, void *y,
+                           const fp8w_linear_config *config, void *stream);
+
+/* Human-readable name of a status code (static string). */
+FP8W_API const char *fp8w_status_string(int status);
+
+/* Name of the last failing CUDA call in this thread ("" if none). */
+FP8W_API const char *fp8w_last_cuda_error(void);
+
+/* Code recorded by a kernel that gave up a bounded wait on the current
+ * device (0 = none), and clears it.  Synchronises the device first. */
+FP8W_API int fp8w_device_error(void);
+
+/* FP8W_ABI_VERSION of the loaded library. */
+FP8W_API int fp8w_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8W_H */

@@ -1,0 +1,90 @@
+"""The C-ABI library loads and exports every symbol include/fp8w.h declares,
+and rejects bad arguments on the host before any CUDA call (no GPU needed:
+every case below fails a host-side check first)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_weight_only_gb300 as fw
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    txt = open(os.path.join(ROOT, "include", "fp8w.h")).read()
+    return sorted(set(re.findall(r"FP8W_API\s+[\w\s\*]+?\b(fp8w_\w+)\s*\(", txt)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert _declared() == sorted(fw.SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol():
+    L = fw.lib()
+    for name in _declared():
+        assert hasattr(L, name), name
+    assert L.fp8w_abi_version() == 1
+
+
+def test_status_strings():
+    L = fw.lib()
+    for s in range(7):
+        assert L.fp8w_status_string(s)
+    assert L.fp8w_status_string(99) == b"unknown status"
+
+
+A16 = ctypes.c_void_p(0x100000)        # 16-byte aligned fake device addresses
+B16 = ctypes.c_void_p(0x200000)
+C16 = ctypes.c_void_p(0x300000)
+D16 = ctypes.c_void_p(0x400000)
+
+
+def _lin(x=A16, act=1, m=1, k=64, codes=B16, scales=C16, bias=None, n=8, y=D16, cfg=None):
+    L = fw.lib()
+    if cfg is None:
+        return L.fp8w_linear(x, act, m, k, codes, scales, bias, n, y, None)
+    return L.fp8w_linear_ex(x, act, m, k, codes, scales, bias, n, y, ctypes.byref(cfg), None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), 1), (dict(codes=None), 1), (dict(scales=None), 1), (dict(y=None), 1),
+    (dict(act=0), 4), (dict(act=3), 4),
+    (dict(m=0), 2), (dict(n=0), 2), (dict(k=0), 2), (dict(k=8), 2), (dict(k=40), 2),
+    (dict(k=65536 + 16), 2), (dict(m=-1), 2), (dict(n=2 ** 31), 2),
+    (dict(x=ctypes.c_void_p(0x100008)), 3), (dict(codes=ctypes.c_void_p(0x200004)), 3),
+    (dict(scales=ctypes.c_void_p(0x300002)), 3), (dict(bias=ctypes.c_void_p(0x500001)), 3),
+    (dict(y=ctypes.c_void_p(0x400001)), 3),
+])
+def test_linear_rejects_bad_arguments(kw, status):
+    assert _lin(**kw) == status
+
+
+@pytest.mark.parametrize("cfg", [
+    fw.LinearConfig(fw.KERNEL_GEMV, 0),        # gemv needs m == 1 (m = 2 below)
+    fw.LinearConfig(7, 0),                     # unknown kernel
+    fw.LinearConfig(fw.KERNEL_SKINNY, 3),      # split must be 1, 2, 4 or 8
+    fw.LinearConfig(fw.KERNEL_SKINNY, 16),
+    fw.LinearConfig(fw.KERNEL_SKINNY, 4),      # k = 256 has only 2 k-blocks
+])
+def test_linear_rejects_bad_config(cfg):
+    assert _lin(m=2, k=256, cfg=cfg) == 6
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, 4, 64, B16, C16), 1), ((A16, 4, 64, None, C16), 1), ((A16, 4, 64, B16, None), 1),
+    ((A16, 0, 64, B16, C16), 2), ((A16, 4, 24, B16, C16), 2), ((A16, 4, 0, B16, C16), 2),
+    ((ctypes.c_void_p(0x100004), 4, 64, B16, C16), 3),
+    ((A16, 4, 64, ctypes.c_void_p(0x200008), C16), 3),
+    ((A16, 4, 64, B16, ctypes.c_void_p(0x300001)), 3),
+])
+def test_quantize_rejects_bad_arguments(args, status):
+    assert fw.lib().fp8w_quantize(*args, None) == status
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(fw, "_lib", None)
+    monkeypatch.setattr(fw, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(fw.Fp8wError):
+        fw.lib()

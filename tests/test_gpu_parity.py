@@ -1,0 +1,325 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle.
+
+Codes and scales must be bit-exact; outputs within the stated tolerance
+(rel_l2 <= 2e-3, per-row cosine >= 0.9999), and bit-identical where the
+result is exact in fp32 regardless of summation order.  Output buffers are
+poisoned before every call and surrounded by canary bytes, so a skipped or
+out-of-bounds write fails.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic
+from tests.parity import assert_parity, compare
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("needs a GPU", allow_module_level=True)
+
+import fp8_weight_only_gb300 as fw  # noqa: E402
+
+DEV = torch.device("cuda:0")
+CANARY = 64          # elements of canary on each side of an output
+POISON16 = 0x7FC1    # a NaN pattern in bf16 (and a NaN in fp16)
+
+
+def _dt(act):
+    return torch.bfloat16 if act == oracle.ACT_BF16 else torch.float16
+
+
+def _guarded(n_elems, dtype, fill):
+    """A device buffer with canaries around a poisoned payload."""
+    buf = torch.empty(n_elems + 2 * CANARY, dtype=dtype, device=DEV)
+    buf.view(torch.uint8 if dtype == torch.uint8 else torch.int16)
+    if dtype == torch.uint8:
+        buf.fill_(0xA5)
+    else:
+        buf.view(torch.int16).fill_(np.int16(np.uint16(fill).view(np.int16)))
+    return buf, buf[CANARY:CANARY + n_elems]
+
+
+def _check_canaries(buf, n_elems, fill):
+    head = buf[:CANARY]
+    tail = buf[CANARY + n_elems:]
+    if buf.dtype == torch.uint8:
+        assert bool((head == 0xA5).all()) and bool((tail == 0xA5).all()), "canary overwritten"
+    else:
+        v = np.int16(np.uint16(fill).view(np.int16))
+        assert bool((head.view(torch.int16) == int(v)).all()), "canary before output overwritten"
+        assert bool((tail.view(torch.int16) == int(v)).all()), "canary after output overwritten"
+
+
+def gpu_quantize(w_np):
+    n, k = w_np.shape
+    w = torch.from_numpy(w_np).to(DEV)
+    cbuf, codes = _guarded(n * k, torch.uint8, 0)
+    codes = codes.view(n, k)
+    sbuf = torch.full((n + 2 * CANARY,), -7.0, dtype=torch.float32, device=DEV)
+    scales = sbuf[CANARY:CANARY + n]
+    fw.quantize(w, codes, scales)
+    torch.cuda.synchronize()
+    _check_canaries(cbuf, n * k, 0)
+    assert bool((sbuf[:CANARY] == -7.0).all()) and bool((sbuf[CANARY + n:] == -7.0).all())
+    return codes.cpu().numpy(), scales.cpu().numpy()
+
+
+def gpu_linear(x_bits, act, codes, scales, bias, kernel=fw.KERNEL_AUTO, split_k=0):
+    m, k = x_bits.shape
+    n = codes.shape[0]
+    dt = _dt(act)
+    x = torch.from_numpy(x_bits.view(np.int16)).to(DEV).view(dt)
+    c = torch.from_numpy(np.ascontiguousarray(codes)).to(DEV)
+    s = torch.from_numpy(np.ascontiguousarray(scales)).to(DEV)
+    b = None if bias is None else torch.from_numpy(np.ascontiguousarray(bias)).to(DEV)
+    ybuf, y = _guarded(m * n, dt, POISON16)
+    fw.linear(x, c, s, b, out=y.view(m, n), kernel=kernel, split_k=split_k)
+    torch.cuda.synchronize()
+    _check_canaries(ybuf, m * n, POISON16)
+    assert fw.device_error() == 0
+    return y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(m, n)
+
+
+# --------------------------------------------------------------- quantise --
+
+@pytest.mark.parametrize("shape,seed,kind", [
+    ((1, 16), 1, "normal"), ((3, 48), 2, "normal"), ((129, 1040), 3, "t"),
+    ((1024, 1024), 4, "normal"), ((300, 4096), 5, "t"), ((77, 14336), 6, "normal"),
+    ((5, 16384), 7, "t"), ((3, 20000 // 16 * 16), 8, "normal"), ((2, 65536), 9, "t"),
+])
+def test_quantize_bit_exact(shape, seed, kind):
+    rng = np.random.default_rng(seed)
+    n, k = shape
+    if kind == "t":
+        w = (rng.standard_t(3, size=shape) * 0.02).astype(np.float32)
+    else:
+        w = (rng.standard_normal(shape) * 10.0 ** rng.uniform(-8, 3, size=(n, 1))).astype(np.float32)
+    w[0, : min(k, 7)] = 0.0
+    if n > 2:
+        w[1] = 0.0                         # all-zero row -> scale 1
+        w[2, 3] = np.float32(1e-45)        # underflowing amax -> scale 1
+        w[2, 4] = np.float32(-1e-45)
+    codes, scales = gpu_quantize(w)
+    rc, rs = oracle.quantize(w)
+    assert np.array_equal(scales.view(np.uint32), rs.view(np.uint32))
+    bad = np.nonzero(codes != rc)
+    assert bad[0].size == 0, (bad[0][:5], bad[1][:5], codes[bad][:5], rc[bad][:5], w[bad][:5])
+
+
+def test_quantize_configs_bit_exact():
+    for name in ("tiny_gemv", "outlier_gemv", "fp16_template"):
+        w = synthetic.case(name)["w"]
+        codes, scales = gpu_quantize(w)
+        rc, rs = oracle.quantize(w)
+        assert np.array_equal(scales.view(np.uint32), rs.view(np.uint32)), name
+        assert np.array_equal(codes, rc), name
+
+
+@pytest.mark.parametrize("matrix", [s[0] for s in synthetic.DECODE_STACK])
+def test_quantize_decode_stack_bit_exact(matrix):
+    w = synthetic.case("decode_stack", 1, matrix)["w"]
+    codes, scales = gpu_quantize(w)
+    rc, rs = oracle.quantize(w)
+    assert np.array_equal(scales.view(np.uint32), rs.view(np.uint32))
+    assert np.array_equal(codes, rc)
+
+
+def test_quantize_every_reachable_fp32_bit_exact():
+    """Rows [448, v...] have scale exactly 1, so their codes are e4m3(v): this
+    sweeps every fp32 pattern in [2^-12, 448] of both signs, plus a strided
+    sample of everything smaller (subnormals included), through the kernel's
+    hardware conversion, against the oracle's encoder."""
+    lo = np.float32(2.0 ** -12).view(np.uint32)
+    hi = np.float32(448.0).view(np.uint32)
+    dense = np.arange(lo, hi + 1, dtype=np.uint32)
+    sparse = np.arange(0, lo, 4099, dtype=np.uint32)
+    pos = np.concatenate([dense, sparse])
+    vals = np.concatenate([pos, pos | np.uint32(0x80000000)]).view(np.float32)
+    k = 4096
+    per_row = k - 1
+    rows = -(-vals.size // per_row)
+    pad = np.zeros(rows * per_row, dtype=np.float32)
+    pad[: vals.size] = vals
+    w = np.empty((rows, k), dtype=np.float32)
+    w[:, 0] = 448.0
+    w[:, 1:] = pad.reshape(rows, per_row)
+    del pad
+    wd = torch.from_numpy(w).to(DEV)
+    codes, scales = fw.quantize(wd)
+    torch.cuda.synchronize()
+    assert bool((scales == 1.0).all())
+    got = codes[:, 1:].reshape(-1)[: vals.size].cpu().numpy()
+    want = oracle.e4m3_encode(vals)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, (vals[bad[:8]], got[bad[:8]], want[bad[:8]])
+
+
+# ----------------------------------------------------------------- linear --
+
+def _case(seed, m, n, k, act, with_bias=True, std=0.02):
+    c = synthetic.random_case(seed, m, n, k, act=act, std=std, with_bias=with_bias)
+    codes, scales = oracle.quantize(c["w"])
+    return c, codes, scales
+
+
+SHAPES = [  # (m, n, k): several tiles and ragged tails in n and k
+    (1, 1, 16), (1, 33, 48), (1, 300, 1040), (1, 1024, 1024), (1, 257, 4096), (1, 130, 14336),
+    (1, 64, 20000 // 16 * 16), (1, 40, 65536),
+    (2, 300, 1040), (3, 129, 4096), (4, 1024, 1024), (7, 257, 2064), (8, 640, 4096),
+    (16, 300, 1040), (17, 300, 1040), (22, 4096, 1024), (31, 129, 256), (32, 1000, 4096),
+    (33, 300, 1040), (70, 260, 528), (2, 128, 16), (5, 513, 14336),
+]
+
+
+@pytest.mark.parametrize("act", [oracle.ACT_BF16, oracle.ACT_F16])
+@pytest.mark.parametrize("m,n,k", SHAPES)
+def test_linear_parity(m, n, k, act):
+    c, codes, scales = _case(1000 * m + n + k + act, m, n, k, act, with_bias=(n % 2 == 0))
+    y = gpu_linear(c["x"], act, codes, scales, c["bias"])
+    ref = oracle.linear(c["x"], act, codes, scales, c["bias"])
+    assert_parity(y, ref, act, (m, n, k))
+
+
+@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("m", [1, 2, 9, 32])
+def test_skinny_every_split(m, split):
+    c, codes, scales = _case(77 + m + split, m, 520, 2048, oracle.ACT_BF16)
+    y = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], kernel=fw.KERNEL_SKINNY,
+                   split_k=split)
+    ref = oracle.linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"])
+    assert_parity(y, ref, oracle.ACT_BF16, (m, split))
+
+
+@pytest.mark.parametrize("act", [oracle.ACT_BF16, oracle.ACT_F16])
+@pytest.mark.parametrize("kernel,m", [(fw.KERNEL_GEMV, 1), (fw.KERNEL_SKINNY, 1), (fw.KERNEL_SKINNY, 5),
+                                      (fw.KERNEL_SKINNY, 32)])
+def test_exact_cases_bit_identical(kernel, m, act):
+    """Power-of-two scales, small-integer activations and weights whose codes
+    lie in [1/8, 8] (plus the 448 that fixes the scale): every product and
+    partial sum is a multiple of 2^-6 below 2^14, so the fp32 accumulation is
+    exact in any order and the output must equal the oracle bit for bit."""
+    rng = np.random.default_rng(5 + m + act)
+    n, k = 300, 512
+    t = oracle.e4m3_decode_table()
+    mid = np.nonzero(np.isfinite(t) & (np.abs(t) >= 0.125) & (np.abs(t) <= 8.0))[0]
+    p = 2.0 ** (np.arange(n) % 9 - 4)
+    w = (t[rng.choice(mid, size=(n, k))] * p[:, None]).astype(np.float32)
+    w[np.arange(n), np.arange(n) % k] = (448.0 * p).astype(np.float32)
+    codes, scales = oracle.quantize(w)
+    assert np.array_equal(scales, p.astype(np.float32))
+    xi = rng.integers(-3, 4, size=(m, k)).astype(np.float32)
+    to_bits = synthetic.to_f16_bits if act == oracle.ACT_F16 else synthetic.to_bf16_bits
+    x = to_bits(xi)
+    bias = (rng.integers(-2, 3, size=n) * p).astype(np.float32)
+    y = gpu_linear(x, act, codes, scales, bias, kernel=kernel)
+    ref = oracle.linear(x, act, codes, scales, bias)
+    assert np.array_equal(y, ref)
+
+
+def test_one_hot_reads_every_code():
+    """x = e_j reads column j of the quantised weight: y[n] = RN(scale[n] * e4m3(q[n, j])),
+    with scale a power of two so the product is exact; column j holds all 254
+    finite codes down the rows."""
+    t = oracle.e4m3_decode_table()
+    fin = [b for b in range(256) if np.isfinite(t[b])]
+    n, k = 256, 64
+    w = np.zeros((n, k), dtype=np.float32)
+    w[:, 0] = 448.0
+    w[: len(fin), 5] = t[fin]
+    codes, scales = oracle.quantize(w)
+    assert np.all(scales == 1.0)
+    for act in (oracle.ACT_BF16, oracle.ACT_F16):
+        to_bits = synthetic.to_f16_bits if act == oracle.ACT_F16 else synthetic.to_bf16_bits
+        for m, kern in ((1, fw.KERNEL_GEMV), (1, fw.KERNEL_SKINNY), (3, fw.KERNEL_SKINNY)):
+            xf = np.zeros((m, k), dtype=np.float32)
+            xf[:, 5] = 1.0
+            y = gpu_linear(to_bits(xf), act, codes, scales, None, kernel=kern)
+            ref = oracle.linear(to_bits(xf), act, codes, scales, None)
+            assert np.array_equal(y, ref), (act, m, kern)
+
+
+def test_bias_none_equals_zero_bias_and_runs_are_deterministic():
+    c, codes, scales = _case(99, 8, 700, 4096, oracle.ACT_BF16)
+    for m in (1, 8):
+        x = c["x"][:m]
+        a = gpu_linear(x, oracle.ACT_BF16, codes, scales, None)
+        b = gpu_linear(x, oracle.ACT_BF16, codes, scales, np.zeros(700, np.float32))
+        d = gpu_linear(x, oracle.ACT_BF16, codes, scales, None)
+        assert np.array_equal(a, b) and np.array_equal(a, d)
+
+
+def test_cuda_graph_capture_replays_identically():
+    c, codes, scales = _case(7, 8, 1000, 4096, oracle.ACT_BF16)
+    x = torch.from_numpy(c["x"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    cd = torch.from_numpy(codes).to(DEV)
+    sd = torch.from_numpy(scales).to(DEV)
+    bd = torch.from_numpy(c["bias"]).to(DEV)
+    y1 = torch.empty((1, 1000), dtype=torch.bfloat16, device=DEV)
+    y8 = torch.empty((8, 1000), dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        fw.linear(x[:1], cd, sd, bd, out=y1)
+        fw.linear(x, cd, sd, bd, out=y8)
+    torch.cuda.synchronize()
+    ref1, ref8 = y1.clone(), y8.clone()
+    y1.zero_()
+    y8.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fw.linear(x[:1], cd, sd, bd, out=y1)
+        fw.linear(x, cd, sd, bd, out=y8)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y1, ref1) and torch.equal(y8, ref8)
+
+
+# -------------------------------------------- full-size workloads, sampled --
+
+def _sampled_parity(case, kernel=fw.KERNEL_AUTO, n_sample=384):
+    act = case["act"]
+    codes, scales = gpu_quantize(case["w"])
+    rc, rs = oracle.quantize(case["w"])
+    assert np.array_equal(codes, rc) and np.array_equal(scales.view(np.uint32), rs.view(np.uint32))
+    y = gpu_linear(case["x"], act, codes, scales, case["bias"], kernel=kernel)
+    n = case["n"]
+    rng = np.random.default_rng(n + case["m"])
+    cols = np.unique(np.concatenate([rng.choice(n, size=min(n_sample, n), replace=False),
+                                     [0, n - 1, min(127, n - 1), min(128, n - 1)]]))
+    bias = None if case["bias"] is None else case["bias"][cols]
+    ref = oracle.linear(case["x"], act, rc[cols], rs[cols], bias, threads=oracle.host_cores())
+    return assert_parity(y[:, cols], ref, act, (case["m"], case["n"], case["k"]))
+
+
+@pytest.mark.parametrize("name", ["tiny_gemv", "outlier_gemv", "fp16_template"])
+def test_config_parity_full(name):
+    case = synthetic.case(name)
+    act = case["act"]
+    codes, scales = oracle.quantize(case["w"])
+    y = gpu_linear(case["x"], act, codes, scales, case["bias"])
+    ref = oracle.linear(case["x"], act, codes, scales, case["bias"], threads=oracle.host_cores())
+    assert_parity(y, ref, act, name)
+    if name == "outlier_gemv":
+        yb = gpu_linear(case["x"], act, codes, scales, np.zeros(case["n"], np.float32))
+        assert np.array_equal(y, yb)
+
+
+@pytest.mark.parametrize("m", synthetic.SKINNY_M)
+def test_skinny_sweep_sampled(m):
+    _sampled_parity(synthetic.case("skinny_sweep", m))
+
+
+@pytest.mark.parametrize("m", synthetic.DECODE_STACK_M)
+@pytest.mark.parametrize("matrix", [s[0] for s in synthetic.DECODE_STACK])
+def test_decode_stack_sampled(matrix, m):
+    _sampled_parity(synthetic.case("decode_stack", m, matrix), n_sample=256)
+
+
+def test_m1_tensor_core_path_matches_gemv_tolerance():
+    case = synthetic.case("decode_stack", 1, "gate")
+    codes, scales = oracle.quantize(case["w"])
+    yg = gpu_linear(case["x"], 1, codes, scales, case["bias"], kernel=fw.KERNEL_GEMV)
+    yt = gpu_linear(case["x"], 1, codes, scales, case["bias"], kernel=fw.KERNEL_SKINNY)
+    c = compare(yt, yg, 1)
+    assert c["rel_l2"] <= 2e-3 and c["min_cosine"] >= 0.9999, c
