@@ -173,11 +173,11 @@ class DriverEvents:
 
 # ------------------------------------------------------------- CPU baseline --
 
-CPU_STRIDE = 16  # the CPU sample takes every 16th output channel of every call
+CPU_STRIDE = 2  # the CPU sample takes every 2nd output channel of every call
 
 
 def cpu_sample(m_list=synthetic.DECODE_STACK_M):
-    """Inputs of the CPU sample: every call of the step, channels n % 16 == 0."""
+    """Inputs of the CPU sample: every call of the step, every CPU_STRIDE-th channel."""
     import oracle
     out = []
     for m in m_list:
@@ -432,14 +432,65 @@ def run_ours(args, torch, dist):
     return result
 
 
+def run_profile_case(args):
+    """One decode-stack linear, for ncu captures and launch-shape sweeps: eager
+    launches first (what ncu captures), then --reps launches captured in a
+    CUDA graph and replayed, timed with events (device time per launch)."""
+    import torch
+    import fp8_weight_only_gb300 as fw
+    name, m = args.profile.split(":")
+    m = int(m)
+    dev = torch.device("cuda:0")
+    c = synthetic.case("decode_stack", m, name)
+    w = torch.from_numpy(c["w"]).to(dev)
+    codes, scales = fw.quantize(w)
+    del w
+    nrep = max(3, -(-3 * 129 * 2 ** 20 // codes.numel()))   # replicas covering > 3x L2
+    reps = [codes] + [codes.clone() for _ in range(nrep - 1)]
+    bias = torch.from_numpy(c["bias"]).to(dev)
+    x = torch.from_numpy(c["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty((m, c["n"]), dtype=torch.bfloat16, device=dev)
+    for i in range(3):
+        fw.linear(x, reps[i % nrep], scales, bias, out=y, kernel=args.kernel)
+    torch.cuda.synchronize()
+    out = {"case": args.profile, "kernel": args.kernel, "bytes": call_bytes(m, c["n"], c["k"])}
+    if args.reps > 3:
+        s = torch.cuda.Stream()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for i in range(args.reps):
+                fw.linear(x, reps[i % nrep], scales, bias, out=y, kernel=args.kernel)
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (3 * args.reps)
+        out.update({"us_per_launch": round(us, 3), "gbs": round(out["bytes"] / (us / 1e6) / 1e9, 1)})
+    print(json.dumps(out))
+    assert fw.device_error() == 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-baseline leg")
+    ap.add_argument("--profile", default=None, metavar="MATRIX:M",
+                    help="profiling case: quantise one decode-stack matrix and run fp8w_linear --reps times "
+                         "(three weight replicas, so every read comes from HBM); prints per-launch times")
+    ap.add_argument("--reps", type=int, default=4)
+    ap.add_argument("--kernel", type=int, default=0, help="with --profile: 0 auto, 1 gemv, 2 tensor-core")
     args = ap.parse_args()
+    if args.profile:
+        run_profile_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_env()

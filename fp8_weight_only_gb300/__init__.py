@@ -18,8 +18,9 @@ FP8W_BF16 = 1
 FP8W_F16 = 2
 KERNEL_AUTO, KERNEL_GEMV, KERNEL_SKINNY = 0, 1, 2
 
-SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_ex", "fp8w_status_string",
-           "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version")
+SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_workspace_size", "fp8w_linear_ex",
+           "fp8w_status_string", "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version")
+ABI_VERSION = 2
 
 
 class Fp8wError(RuntimeError):
@@ -29,7 +30,7 @@ class Fp8wError(RuntimeError):
 
 
 class LinearConfig(ctypes.Structure):
-    _fields_ = [("kernel", ctypes.c_int), ("split_k", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
+    _fields_ = [("kernel", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
 
 
 _lib = None
@@ -47,9 +48,11 @@ def lib():
         L.fp8w_quantize.restype = c.c_int
         L.fp8w_quantize.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
         L.fp8w_linear.restype = c.c_int
-        L.fp8w_linear.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P]
+        L.fp8w_linear.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P, c.c_size_t, P]
+        L.fp8w_linear_workspace_size.restype = c.c_size_t
+        L.fp8w_linear_workspace_size.argtypes = [c.c_int64, c.c_int64, c.c_int64]
         L.fp8w_linear_ex.restype = c.c_int
-        L.fp8w_linear_ex.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P,
+        L.fp8w_linear_ex.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P, c.c_size_t,
                                      c.POINTER(LinearConfig), P]
         L.fp8w_status_string.restype = c.c_char_p
         L.fp8w_status_string.argtypes = [c.c_int]
@@ -104,7 +107,29 @@ def quantize(w, codes=None, scales=None):
     return codes, scales
 
 
-def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, split_k=0):
+_workspaces = {}
+
+
+def workspace(device, nbytes):
+    """The zero-filled scratch buffer of a device, grown on demand.
+
+    One buffer per device: calls that may run concurrently on several streams
+    must pass their own `workspace_buffer`.  Growing allocates, so the first
+    tensor-core call on a device must not happen during CUDA-graph capture
+    (run it once eagerly first)."""
+    import torch
+    key = device.index if device.index is not None else torch.cuda.current_device()
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        if torch.cuda.is_current_stream_capturing():
+            raise Fp8wError(7, "fp8w workspace must be allocated before CUDA-graph capture: "
+                               "run the call once eagerly first")
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_buffer=None):
     """y[M, N] = round(scale[n] * sum_k x[m, k] * e4m3(codes[n, k]) + bias[n])."""
     import torch
     if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
@@ -126,13 +151,19 @@ def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, split_k=0)
         raise ValueError("out must be a contiguous [M, N] tensor of x's dtype")
     act = _act(x.dtype)
     L = lib()
-    if kernel == KERNEL_AUTO and split_k == 0:
+    stream = _stream(x)
+    need = L.fp8w_linear_workspace_size(max(m, 2) if kernel == KERNEL_SKINNY else m, n, k)
+    ws = None
+    if need:
+        ws = workspace_buffer if workspace_buffer is not None else workspace(x.device, need)
+    ws_ptr, ws_bytes = (_ptr(ws), ws.numel()) if ws is not None else (None, 0)
+    if kernel == KERNEL_AUTO:
         st = L.fp8w_linear(_ptr(x), act, m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
-                           _ptr(out), _stream(x))
+                           _ptr(out), ws_ptr, ws_bytes, stream)
     else:
-        cfg = LinearConfig(kernel, split_k)
+        cfg = LinearConfig(kernel)
         st = L.fp8w_linear_ex(_ptr(x), act, m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
-                              _ptr(out), ctypes.byref(cfg), _stream(x))
+                              _ptr(out), ws_ptr, ws_bytes, ctypes.byref(cfg), stream)
     _check(st)
     return out
 

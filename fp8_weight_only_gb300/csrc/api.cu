@@ -48,31 +48,42 @@ fp8w_status fp8w_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes, 
                        "fp8w_quantize launch");
 }
 
+static size_t skinny_ws(void) {
+    int sms = 0;
+    if (fp8w::device_sm_count(sms) != cudaSuccess) return 0;
+    return fp8w::skinny_workspace_size(sms);
+}
+
+size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k) {
+    (void)n;
+    (void)k;
+    return m == 1 ? 0 : skinny_ws();
+}
+
 fp8w_status fp8w_linear_ex(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
-                           const float* scales, const float* bias, int64_t n, void* y,
-                           const fp8w_linear_config* config, void* stream) {
+                           const float* scales, const float* bias, int64_t n, void* y, void* workspace,
+                           size_t workspace_bytes, const fp8w_linear_config* config, void* stream) {
     fp8w_status st = check_linear(x, act_dtype, m, k, codes, scales, bias, n, y);
     if (st != FP8W_OK) return st;
     int kernel = config ? config->kernel : FP8W_KERNEL_AUTO;
-    int split = config ? config->split_k : 0;
     if (kernel == FP8W_KERNEL_AUTO) kernel = (m == 1) ? FP8W_KERNEL_GEMV : FP8W_KERNEL_SKINNY;
     if (kernel == FP8W_KERNEL_GEMV && m != 1) return FP8W_ERR_CONFIG;
     if (kernel != FP8W_KERNEL_GEMV && kernel != FP8W_KERNEL_SKINNY) return FP8W_ERR_CONFIG;
-    if (kernel == FP8W_KERNEL_SKINNY && split != 0) {
-        const int64_t nkb = (k + 127) / 128;
-        if ((split != 1 && split != 2 && split != 4 && split != 8) || split > fp8w::skinny_max_split() ||
-            split > nkb)
-            return FP8W_ERR_CONFIG;
-    }
     fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, scales, bias, y};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (kernel == FP8W_KERNEL_GEMV) return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear gemv launch");
-    return cuda_status(fp8w::launch_skinny(a, split, s), "fp8w_linear tensor-core launch");
+    if (!workspace || !aligned(workspace, 256)) return FP8W_ERR_WORKSPACE;
+    const size_t need = skinny_ws();
+    if (need == 0) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear device query");
+    if (workspace_bytes < need) return FP8W_ERR_WORKSPACE;
+    return cuda_status(fp8w::launch_skinny(a, workspace, s), "fp8w_linear tensor-core launch");
 }
 
 fp8w_status fp8w_linear(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
-                        const float* scales, const float* bias, int64_t n, void* y, void* stream) {
-    return fp8w_linear_ex(x, act_dtype, m, k, codes, scales, bias, n, y, nullptr, stream);
+                        const float* scales, const float* bias, int64_t n, void* y, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+    return fp8w_linear_ex(x, act_dtype, m, k, codes, scales, bias, n, y, workspace, workspace_bytes, nullptr,
+                          stream);
 }
 
 const char* fp8w_status_string(int status) {
@@ -84,6 +95,7 @@ const char* fp8w_status_string(int status) {
         case FP8W_ERR_DTYPE: return "activation dtype must be FP8W_BF16 or FP8W_F16";
         case FP8W_ERR_CUDA: return "CUDA call failed (see fp8w_last_cuda_error)";
         case FP8W_ERR_CONFIG: return "invalid explicit launch configuration";
+        case FP8W_ERR_WORKSPACE: return "workspace NULL, not 256-byte aligned or smaller than fp8w_linear_workspace_size";
         default: return "unknown status";
     }
 }
@@ -92,7 +104,9 @@ const char* fp8w_last_cuda_error(void) { return g_last_cuda_error; }
 
 int fp8w_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
-    return fp8w::read_skinny_device_error();
+    const int a = fp8w::read_skinny_device_error();
+    const int b = fp8w::read_gemv_device_error();
+    return a ? a : b;
 }
 
 int fp8w_abi_version(void) { return FP8W_ABI_VERSION; }

@@ -24,12 +24,14 @@ cudaError_t launch_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes
 // K2: m == 1.
 cudaError_t launch_gemv(const LinearArgs& a, cudaStream_t st);
 
-// K3: 1 <= m <= 32 per launch (the caller slices larger m).  split_k = 0
-// picks the cluster size from the shape.
-cudaError_t launch_skinny(const LinearArgs& a, int split_k, cudaStream_t st);
-int skinny_max_split();
+// K3: any m (32-row slabs, one launch each); needs a workspace of
+// skinny_workspace_size(sms) bytes, zero-filled before its first use.
+cudaError_t launch_skinny(const LinearArgs& a, void* workspace, cudaStream_t st);
+size_t skinny_workspace_size(int sms);
+cudaError_t device_sm_count(int& sms);
 
 // Kernel-recorded wait failures (0 = none); reading clears them.
 int read_skinny_device_error();
+int read_gemv_device_error();
 
 }  // namespace fp8w

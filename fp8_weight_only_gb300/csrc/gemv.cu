@@ -1,22 +1,26 @@
 // gemv.cu -- kernel K2: the M = 1 linear layer (GEMV) on CUDA cores.
 //
 // Page "kadirnar/kernel-agent fp8-weights", section "Dequantise in
-// registers": 128-bit streaming loads of 16 e4m3 codes past L1
-// (ld.global.nc.L1::no_allocate), hardware e4m3x2 -> f16x2 conversion in
-// registers, fp32 FMA, warp-shuffle reduction, scale (and bias) applied once
-// per output in the epilogue.
+// registers": the codes are streamed once past L1, each pair is converted
+// to f16x2 by the hardware e4m3x2 conversion (exact) and widened to fp32,
+// fp32 FMA against x, a shuffle reduction, scale (and bias) applied once per
+// output in the epilogue.
 //
-// GB300 layout of the work: the reduction dimension is split over the whole
-// CTA (thread t owns the 16-code chunks t, t+T, t+2T, ... of every row), so
-// each thread keeps its slice of x in fp32 registers for the life of the CTA
-// and the codes are the only HBM stream.  A persistent grid of
-// (SMs x resident CTAs) walks the rows interleaved (CTA b takes rows
-// b, b+G, b+2G, ...), R rows per step, which keeps the per-SM work within
-// one row of equal.  Per step each thread has R x C independent 16-byte
-// loads in flight.  The R partial sums are reduced across each warp by a
-// transposing shuffle tree (R-1 + log2(32/R) shuffles for R rows) and across
-// warps through shared memory.  HBM bytes per output channel: K (codes) + 4
-// (scale) + 4 (bias) + 2 (y); x (2K bytes) is read once per CTA from L2.
+// GB300 layout of the work:
+//  * Persistent grid, one CTA per SM; CTA c owns the contiguous rows
+//    [c*N/P, (c+1)*N/P), so every SM streams the same bytes (+-1 row).
+//  * The last warp moves R whole rows per stage (R*K contiguous bytes) with
+//    one 1-D TMA bulk copy into a shared-memory ring of ~160 KB, so ~160 KB
+//    per SM is in flight without occupying registers.
+//  * 16 compute warps (512 threads).  A row's 16-code chunks are spread over
+//    T_row threads (G = 512 / T_row row groups work on different rows);
+//    each thread keeps its chunks of x in fp32 registers for the whole
+//    kernel, so after start-up the codes are the only HBM stream.
+//  * Per stage, each group reduces its rows with a transposing shuffle tree
+//    and shared memory; one thread per row applies scale and bias.
+// HBM bytes per output channel: K (codes) + 4 (scale) + 4 (bias) + 2 (y).
+// K > 16384 (a row longer than a stage) runs the chunked variant at the end
+// of this file.
 #include <mutex>
 
 #include "fp8w_device.cuh"
@@ -24,7 +28,14 @@
 
 namespace fp8w {
 
-constexpr int kGemvMaxThreads = 256;
+static __device__ int g_gemv_error;
+
+constexpr int kGemvComputeThreads = 512;
+constexpr int kGemvThreads = kGemvComputeThreads + 32;
+constexpr int kGemvRingBytes = 160 * 1024;
+constexpr int kGemvMaxRowsPerStage = 32;
+constexpr int kGemvMaxStages = 16;
+constexpr int kGemvMaxK = 16384;
 
 // Reduce R per-thread values across a warp.  On return, lane l holds the
 // warp total of row l / (32 / R) if l % (32 / R) == 0.
@@ -74,6 +85,13 @@ __device__ __forceinline__ void load_x_chunk(const uint16_t* x, int64_t chunk, f
     }
 }
 
+// f16x2 -> two fp32 (halves selected in the register, no extraction).
+__device__ __forceinline__ void f16x2_to_f32x2(uint32_t h, float& lo, float& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h));
+}
+
 // acc += sum over 16 codes of x * e4m3(code).
 __device__ __forceinline__ float dot16(const uint4 c, const float (&xr)[16], float acc) {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
@@ -81,138 +99,262 @@ __device__ __forceinline__ float dot16(const uint4 c, const float (&xr)[16], flo
     for (int q = 0; q < 4; ++q) {
         uint32_t h01, h23;
         e4m3x4_to_f16x2(w[q], h01, h23);
-        acc = fmaf(xr[4 * q + 0], f16_lo_to_f32(h01), acc);
-        acc = fmaf(xr[4 * q + 1], f16_hi_to_f32(h01), acc);
-        acc = fmaf(xr[4 * q + 2], f16_lo_to_f32(h23), acc);
-        acc = fmaf(xr[4 * q + 3], f16_hi_to_f32(h23), acc);
+        float a, b, c2, d;
+        f16x2_to_f32x2(h01, a, b);
+        f16x2_to_f32x2(h23, c2, d);
+        acc = fmaf(xr[4 * q + 0], a, acc);
+        acc = fmaf(xr[4 * q + 1], b, acc);
+        acc = fmaf(xr[4 * q + 2], c2, acc);
+        acc = fmaf(xr[4 * q + 3], d, acc);
     }
     return acc;
 }
 
-template <int C, int R, bool kBf16>
-__global__ void __launch_bounds__(kGemvMaxThreads) gemv_kernel(const uint16_t* __restrict__ x,
-                                                               const uint8_t* __restrict__ codes,
-                                                               const float* __restrict__ scales,
-                                                               const float* __restrict__ bias,
-                                                               uint16_t* __restrict__ y, int64_t n, int64_t k) {
-    __shared__ float red[2][R][kGemvMaxThreads / 32];
-    const int T = blockDim.x;
-    const int nwarps = T >> 5;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t nchunks = k >> 4;
-    const int64_t per_pass = static_cast<int64_t>(T) * C;
-    const int64_t npasses = (nchunks + per_pass - 1) / per_pass;
-    const int64_t G = gridDim.x;
+__device__ __forceinline__ void compute_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kGemvComputeThreads) : "memory");
+}
 
-    float xr[C][16];
-    auto load_x = [&](int64_t pass) {
-#pragma unroll
-        for (int j = 0; j < C; ++j) {
-            const int64_t ch = pass * per_pass + threadIdx.x + static_cast<int64_t>(T) * j;
-            if (ch < nchunks) {
-                load_x_chunk<kBf16>(x, ch, xr[j]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) xr[j][e] = 0.0f;
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+struct GemvGeom {
+    int rows_per_stage;  // R
+    int stages;          // S
+    int t_row;           // threads per row
+    int groups;          // 512 / t_row
+    uint32_t stage_bytes;
+};
+
+// C = chunks per thread, RPG = rows per group per stage (R / groups).
+template <int C, int RPG, bool kBf16>
+__global__ void __launch_bounds__(kGemvThreads, 1)
+    gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes, const float* __restrict__ scales,
+                const float* __restrict__ bias, uint16_t* __restrict__ y, int64_t n, int64_t k, GemvGeom geo) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+    const uint32_t ring = smem_u32(smem);
+    const uint32_t bar_full = ring + kGemvRingBytes;                 // [S]
+    const uint32_t bar_empty = bar_full + 8 * kGemvMaxStages;       // [S]
+    float* red = reinterpret_cast<float*>(smem + kGemvRingBytes + 16 * kGemvMaxStages);  // [R][16 warps]
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kGemvMaxRowsPerStage * 16);
+    // written only by compute threads before a compute barrier, so they all
+    // read the same value after it and leave the loop together
+    volatile int* cmp_abort = abort_flag + 1;
+
+    const int S = geo.stages, R = geo.rows_per_stage;
+    const int64_t P = gridDim.x;
+    const int64_t row0 = blockIdx.x * n / P, row1 = (blockIdx.x + 1) * n / P;
+    const int64_t nst = (row1 - row0 + R - 1) / R;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps_compute = kGemvComputeThreads / 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, nwarps_compute);
+        }
+        *abort_flag = 0;
+        *cmp_abort = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    if (warp == nwarps_compute) {
+        // ---------------------------------------------------- producer --
+        if ((threadIdx.x & 31) == 0) {
+            const uint64_t pol = policy_evict_first();
+            int64_t issued = 0;
+            for (int64_t st = 0; st < nst; ++st) {
+                const int s = static_cast<int>(st % S);
+                const uint32_t ph = static_cast<uint32_t>((st / S) & 1);
+                if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
+                    *abort_flag = 1;
+                    atomicCAS(&g_gemv_error, 0, kErrWaitSlot);
+                    break;
+                }
+                const int64_t r0 = row0 + st * R;
+                const int64_t rows = (row1 - r0) < R ? (row1 - r0) : R;
+                const uint32_t bytes = static_cast<uint32_t>(rows * k);
+                mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
+                bulk_load(ring + s * geo.stage_bytes, codes + r0 * k, bytes, bar_full + 8 * s, pol);
+                ++issued;
+            }
+            if (*abort_flag) {
+                for (int64_t st = (issued > S ? issued - S : 0); st < issued; ++st)
+                    if (!mbar_wait_drain(bar_full + 8 * (st % S), static_cast<uint32_t>((st / S) & 1)))
+                        atomicCAS(&g_gemv_error, 0, kErrWaitDrain);
             }
         }
-    };
-    if (npasses == 1) load_x(0);
+        return;
+    }
 
-    int buf = 0;
-    for (int64_t step = 0;; ++step) {
-        const int64_t first = blockIdx.x + G * step * R;
-        if (first >= n) break;
-        float p[R];
+    // -------------------------------------------------------- compute --
+    const int t = threadIdx.x;
+    const int g = t / geo.t_row, tr = t % geo.t_row;
+    const int lane = t & 31;
+    const int64_t nchunks = k >> 4;
+    float xr[C][16];
 #pragma unroll
-        for (int r = 0; r < R; ++r) p[r] = 0.0f;
-        for (int64_t pass = 0; pass < npasses; ++pass) {
-            if (npasses > 1) load_x(pass);
-            uint4 cw[R][C];
+    for (int j = 0; j < C; ++j) {
+        const int64_t ch = tr + static_cast<int64_t>(geo.t_row) * j;
+        if (ch < nchunks) {
+            load_x_chunk<kBf16>(x, ch, xr[j]);
+        } else {
 #pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const int64_t row = first + G * r;
+            for (int e = 0; e < 16; ++e) xr[j][e] = 0.0f;
+        }
+    }
+    const int warps_per_row = geo.t_row >> 5;
+    const int warp_in_group = (t % geo.t_row) >> 5;
+    for (int64_t st = 0; st < nst; ++st) {
+        const int s = static_cast<int>(st % S);
+        if (!mbar_wait_warp(bar_full + 8 * s, static_cast<uint32_t>((st / S) & 1), abort_flag)) {
+            *cmp_abort = 1;
+            *abort_flag = 1;
+            atomicCAS(&g_gemv_error, 0, kErrWaitTma);
+        }
+        compute_bar();
+        if (*cmp_abort) break;
+        const int64_t r0 = row0 + st * R;
+        const uint8_t* stage = smem + s * geo.stage_bytes;
+        float p[RPG];
+#pragma unroll
+        for (int i = 0; i < RPG; ++i) {
+            p[i] = 0.0f;
+            const int rr = g + i * geo.groups;  // row within the stage
+            if (r0 + rr < row1) {
+                const uint8_t* rowp = stage + static_cast<int64_t>(rr) * k;
 #pragma unroll
                 for (int j = 0; j < C; ++j) {
-                    const int64_t ch = pass * per_pass + threadIdx.x + static_cast<int64_t>(T) * j;
-                    if (row < n && ch < nchunks)
-                        cw[r][j] = ldg_stream_v4(codes + row * k + ch * 16);
-                    else
-                        cw[r][j] = make_uint4(0u, 0u, 0u, 0u);
+                    const int64_t ch = tr + static_cast<int64_t>(geo.t_row) * j;
+                    if (ch < nchunks) p[i] = dot16(*reinterpret_cast<const uint4*>(rowp + ch * 16), xr[j], p[i]);
                 }
             }
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int j = 0; j < C; ++j) p[r] = dot16(cw[r][j], xr[j], p[r]);
         }
-        const float wsum = warp_reduce_rows<R>(p);
-        constexpr int kStride = 32 / R;
-        if ((lane % kStride) == 0) red[buf][lane / kStride][warp] = wsum;
-        __syncthreads();
-        if (threadIdx.x < R) {
-            const int64_t row = first + G * threadIdx.x;
-            if (row < n) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        const float wsum = warp_reduce_rows<RPG>(p);
+        constexpr int kStride = 32 / RPG;
+        if ((lane % kStride) == 0) red[(g + (lane / kStride) * geo.groups) * 16 + warp_in_group] = wsum;
+        compute_bar();
+        if (t < R) {
+            const int64_t row = r0 + t;
+            if (row < row1) {
                 float acc = 0.0f;
-                for (int w = 0; w < nwarps; ++w) acc += red[buf][threadIdx.x][w];
+                for (int w = 0; w < warps_per_row; ++w) acc += red[t * 16 + w];
                 const float b = bias ? bias[row] : 0.0f;
                 y[row] = round_out<kBf16>(fmaf(acc, scales[row], b));
             }
         }
-        buf ^= 1;
+        // red is rewritten only after the next stage's first compute_bar
     }
 }
 
-template <int C, int R, bool kBf16>
-static cudaError_t launch_cfg(const LinearArgs& a, int threads, cudaStream_t st) {
-    auto kern = gemv_kernel<C, R, kBf16>;
-    // resident CTAs per SM, per device and block size (8 warp counts)
-    static int cache[64][kGemvMaxThreads / 32 + 1];
-    static std::mutex mu;
+// ------------------------------------------------ long rows (K > 16384) --
+// Rows longer than a stage: one warp-contiguous pass per row, x re-read
+// from L2 per row (correct, not tuned).
+template <bool kBf16>
+__global__ void __launch_bounds__(256) gemv_long_kernel(const uint16_t* __restrict__ x,
+                                                        const uint8_t* __restrict__ codes,
+                                                        const float* __restrict__ scales,
+                                                        const float* __restrict__ bias, uint16_t* __restrict__ y,
+                                                        int64_t n, int64_t k) {
+    __shared__ float red[8];
+    const int64_t nchunks = k >> 4;
+    for (int64_t row = blockIdx.x; row < n; row += gridDim.x) {
+        float acc = 0.0f;
+        for (int64_t ch = threadIdx.x; ch < nchunks; ch += 256) {
+            float xr[16];
+            load_x_chunk<kBf16>(x, ch, xr);
+            acc = dot16(ldg_stream_v4(codes + row * k + ch * 16), xr, acc);
+        }
+        float v[1] = {acc};
+        const float wsum = warp_reduce_rows<1>(v);
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = wsum;
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float s = 0.0f;
+            for (int w = 0; w < 8; ++w) s += red[w];
+            const float b = bias ? bias[row] : 0.0f;
+            y[row] = round_out<kBf16>(fmaf(s, scales[row], b));
+        }
+        __syncthreads();
+    }
+}
+
+static constexpr uint32_t gemv_smem_bytes() {
+    return kGemvRingBytes + 16 * kGemvMaxStages + kGemvMaxRowsPerStage * 16 * 4 + 16 + 128;  // + flags, align
+}
+
+template <int C, int RPG, bool kBf16>
+static cudaError_t launch_cfg(const LinearArgs& a, const GemvGeom& geo, int sms, cudaStream_t st) {
+    auto kern = gemv_kernel<C, RPG, kBf16>;
+    static std::once_flag attr_once[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    int sms = 0, occ = 0;
-    {
-        std::lock_guard<std::mutex> lk(mu);
-        int& slot = cache[dev][threads / 32];
-        if (slot == 0) {
-            e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-            if (e != cudaSuccess) return e;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, 0);
-            if (e != cudaSuccess) return e;
-            slot = sms * (occ < 1 ? 1 : occ);
-        }
-        sms = slot;
-        occ = 1;
-    }
-    int64_t grid = static_cast<int64_t>(sms) * occ;
-    if (grid > a.n) grid = a.n;
-    kern<<<static_cast<unsigned>(grid), threads, 0, st>>>(static_cast<const uint16_t*>(a.x), a.codes, a.scales,
-                                                          a.bias, static_cast<uint16_t*>(a.y), a.n, a.k);
+    cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once[dev & 63], [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gemv_smem_bytes());
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int64_t grid = a.n < sms ? a.n : sms;
+    kern<<<static_cast<unsigned>(grid), kGemvThreads, gemv_smem_bytes(), st>>>(
+        static_cast<const uint16_t*>(a.x), a.codes, a.scales, a.bias, static_cast<uint16_t*>(a.y), a.n, a.k, geo);
     return cudaGetLastError();
 }
 
 template <bool kBf16>
 static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
+    int sms = 0;
+    cudaError_t e = device_sm_count(sms);
+    if (e != cudaSuccess) return e;
+    if (a.k > kGemvMaxK) {
+        const int64_t grid = a.n < 4 * sms ? a.n : 4 * sms;
+        gemv_long_kernel<kBf16><<<static_cast<unsigned>(grid), 256, 0, st>>>(
+            static_cast<const uint16_t*>(a.x), a.codes, a.scales, a.bias, static_cast<uint16_t*>(a.y), a.n, a.k);
+        return cudaGetLastError();
+    }
     const int64_t nchunks = a.k / 16;
-    // chunks per thread: fit the row in one pass of <= 256 threads when possible
-    if (nchunks <= 256) {
-        const int threads = static_cast<int>(((nchunks + 31) / 32) * 32);
-        return launch_cfg<1, 8, kBf16>(a, threads, st);
-    }
-    if (nchunks <= 512) {
-        const int threads = static_cast<int>((((nchunks + 1) / 2 + 31) / 32) * 32);
-        return launch_cfg<2, 4, kBf16>(a, threads, st);
-    }
-    int threads = static_cast<int>((((nchunks + 3) / 4 + 31) / 32) * 32);
-    if (threads > kGemvMaxThreads) threads = kGemvMaxThreads;
-    return launch_cfg<4, 2, kBf16>(a, threads, st);
+    GemvGeom geo;
+    geo.t_row = static_cast<int>(nchunks >= kGemvComputeThreads ? kGemvComputeThreads : ((nchunks + 31) / 32) * 32);
+    // t_row must divide 512: round up to 32, 64, 128, 256 or 512
+    int tr = 32;
+    while (tr < geo.t_row) tr *= 2;
+    geo.t_row = tr;
+    geo.groups = kGemvComputeThreads / geo.t_row;
+    // ~16 KB per stage: rows = groups x (1, 2 or 4), at most 32
+    int64_t target = 16384 / a.k;
+    if (target > kGemvMaxRowsPerStage) target = kGemvMaxRowsPerStage;
+    int rpg_sel = 1;
+    while (rpg_sel < 4 && static_cast<int64_t>(geo.groups) * rpg_sel * 2 <= target) rpg_sel *= 2;
+    const int rows = geo.groups * rpg_sel;
+    geo.rows_per_stage = rows;
+    geo.stage_bytes = static_cast<uint32_t>(((rows * a.k + 127) / 128) * 128);
+    geo.stages = static_cast<int>(kGemvRingBytes / geo.stage_bytes);
+    if (geo.stages > kGemvMaxStages) geo.stages = kGemvMaxStages;
+    const int rpg = rows / geo.groups;
+    const int c = static_cast<int>((nchunks + geo.t_row - 1) / geo.t_row);
+    if (c == 1 && rpg == 1) return launch_cfg<1, 1, kBf16>(a, geo, sms, st);
+    if (c == 1 && rpg == 2) return launch_cfg<1, 2, kBf16>(a, geo, sms, st);
+    if (c == 1 && rpg == 4) return launch_cfg<1, 4, kBf16>(a, geo, sms, st);
+    if (c == 2 && rpg == 1) return launch_cfg<2, 1, kBf16>(a, geo, sms, st);
+    return cudaErrorNotSupported;
 }
 
 cudaError_t launch_gemv(const LinearArgs& a, cudaStream_t st) {
     return a.act == 1 ? launch_dt<true>(a, st) : launch_dt<false>(a, st);
+}
+
+int read_gemv_device_error() {
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_gemv_error, sizeof v) != cudaSuccess) return -1;
+    if (v) cudaMemcpyToSymbol(g_gemv_error, &zero, sizeof zero);
+    return v;
 }
 
 }  // namespace fp8w

@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define FP8W_ABI_VERSION 1
+#define FP8W_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define FP8W_API __attribute__((visibility("default")))
@@ -54,7 +54,8 @@ typedef enum fp8w_status {
     FP8W_ERR_ALIGN = 3,     /* a pointer breaks its alignment rule */
     FP8W_ERR_DTYPE = 4,     /* activation dtype is not FP8W_BF16 / FP8W_F16 */
     FP8W_ERR_CUDA = 5,      /* a CUDA runtime/driver call failed */
-    FP8W_ERR_CONFIG = 6     /* an explicit launch configuration is invalid */
+    FP8W_ERR_CONFIG = 6,    /* an explicit launch configuration is invalid */
+    FP8W_ERR_WORKSPACE = 7  /* workspace NULL, misaligned or too small */
 } fp8w_status;
 
 /* Activation / output dtypes. */
@@ -92,30 +93,42 @@ FP8W_API fp8w_status fp8w_quantize(const float *w, int64_t n, int64_t k,
  *   scales [n] fp32, device, 4-byte aligned.
  *   bias   [n] fp32, device, 4-byte aligned, or NULL for no bias.
  *   y      [m, n] in act_dtype, device, 2-byte aligned (output).
+ *   workspace, workspace_bytes: device scratch for the tensor-core kernel,
+ *          256-byte aligned, at least fp8w_linear_workspace_size(m, n, k)
+ *          bytes (NULL/0 allowed when that size is 0).  It must be
+ *          zero-filled once before its first use; every completed call
+ *          leaves it ready for the next.  Calls that may run at the same
+ *          time (other streams) need separate workspaces.
  *   1 <= m <= FP8W_MAX_DIM, 1 <= n <= FP8W_MAX_DIM, 16 <= k <= FP8W_MAX_K,
- *   k % 16 == 0.  x and y must not overlap codes, scales or bias.
+ *   k % 16 == 0.  x and y must not overlap codes, scales, bias or workspace.
  *
- * m == 1 runs the GEMV kernel; 2 <= m <= 32 the tensor-core kernel; m > 32
- * the tensor-core kernel over 32-row slabs (correct, not tuned).
+ * m == 1 runs the GEMV kernel; m >= 2 the tensor-core kernel, one launch per
+ * 32 rows of x (m > 32 re-streams the weight per slab: correct, not tuned).
  */
 FP8W_API fp8w_status fp8w_linear(const void *x, int act_dtype, int64_t m, int64_t k,
                         const uint8_t *codes, const float *scales,
-                        const float *bias, int64_t n, void *y, void *stream);
+                        const float *bias, int64_t n, void *y,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes fp8w_linear needs for this shape on the current device
+ * (0 when the GEMV kernel is used). */
+FP8W_API size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k);
 
 /* Explicit kernel choice, for tests and tuning; fp8w_linear uses
- * kernel = FP8W_KERNEL_AUTO and split_k = 0. */
+ * FP8W_KERNEL_AUTO. */
 enum { FP8W_KERNEL_AUTO = 0, FP8W_KERNEL_GEMV = 1, FP8W_KERNEL_SKINNY = 2 };
 
 typedef struct fp8w_linear_config {
     int kernel;   /* FP8W_KERNEL_*; GEMV requires m == 1 */
-    int split_k;  /* tensor-core kernel: CTAs per cluster sharing one channel
-                     tile along k (1..8); 0 = chosen from the shape */
-    int reserved[6];
+    int reserved[7];
 } fp8w_linear_config;
 
+/* fp8w_linear with an explicit configuration (NULL = automatic).  The
+ * tensor-core kernel at m == 1 needs the workspace of the m == 2 shape. */
 FP8W_API fp8w_status fp8w_linear_ex(const void *x, int act_dtype, int64_t m, int64_t k,
                            const uint8_t *codes, const float *scales,
                            const float *bias, int64_t n, void *y,
+                           void *workspace, size_t workspace_bytes,
                            const fp8w_linear_config *config, void *stream);
 
 /* Human-readable name of a status code (static string). */

@@ -25,12 +25,12 @@ def test_library_exports_every_declared_symbol():
     L = fw.lib()
     for name in _declared():
         assert hasattr(L, name), name
-    assert L.fp8w_abi_version() == 1
+    assert L.fp8w_abi_version() == fw.ABI_VERSION
 
 
 def test_status_strings():
     L = fw.lib()
-    for s in range(7):
+    for s in range(8):
         assert L.fp8w_status_string(s)
     assert L.fp8w_status_string(99) == b"unknown status"
 
@@ -41,11 +41,12 @@ C16 = ctypes.c_void_p(0x300000)
 D16 = ctypes.c_void_p(0x400000)
 
 
-def _lin(x=A16, act=1, m=1, k=64, codes=B16, scales=C16, bias=None, n=8, y=D16, cfg=None):
+def _lin(x=A16, act=1, m=1, k=64, codes=B16, scales=C16, bias=None, n=8, y=D16, cfg=None, ws=None,
+         ws_bytes=0):
     L = fw.lib()
     if cfg is None:
-        return L.fp8w_linear(x, act, m, k, codes, scales, bias, n, y, None)
-    return L.fp8w_linear_ex(x, act, m, k, codes, scales, bias, n, y, ctypes.byref(cfg), None)
+        return L.fp8w_linear(x, act, m, k, codes, scales, bias, n, y, ws, ws_bytes, None)
+    return L.fp8w_linear_ex(x, act, m, k, codes, scales, bias, n, y, ws, ws_bytes, ctypes.byref(cfg), None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -62,14 +63,19 @@ def test_linear_rejects_bad_arguments(kw, status):
 
 
 @pytest.mark.parametrize("cfg", [
-    fw.LinearConfig(fw.KERNEL_GEMV, 0),        # gemv needs m == 1 (m = 2 below)
-    fw.LinearConfig(7, 0),                     # unknown kernel
-    fw.LinearConfig(fw.KERNEL_SKINNY, 3),      # split must be 1, 2, 4 or 8
-    fw.LinearConfig(fw.KERNEL_SKINNY, 16),
-    fw.LinearConfig(fw.KERNEL_SKINNY, 4),      # k = 256 has only 2 k-blocks
+    fw.LinearConfig(fw.KERNEL_GEMV),           # gemv needs m == 1 (m = 2 below)
+    fw.LinearConfig(7),                        # unknown kernel
+    fw.LinearConfig(-1),
 ])
 def test_linear_rejects_bad_config(cfg):
     assert _lin(m=2, k=256, cfg=cfg) == 6
+
+
+@pytest.mark.parametrize("ws,ws_bytes", [(None, 0), (None, 1 << 30), (ctypes.c_void_p(0x600010), 1 << 30)])
+def test_tensor_core_path_rejects_missing_or_misaligned_workspace(ws, ws_bytes):
+    # NULL or non-256-byte-aligned workspace is refused before any CUDA call
+    assert _lin(m=2, k=256, ws=ws, ws_bytes=ws_bytes) == 7
+    assert _lin(m=1, k=256, ws=ws, ws_bytes=ws_bytes, cfg=fw.LinearConfig(fw.KERNEL_SKINNY)) == 7
 
 
 @pytest.mark.parametrize("args,status", [

@@ -66,7 +66,7 @@ def gpu_quantize(w_np):
     return codes.cpu().numpy(), scales.cpu().numpy()
 
 
-def gpu_linear(x_bits, act, codes, scales, bias, kernel=fw.KERNEL_AUTO, split_k=0):
+def gpu_linear(x_bits, act, codes, scales, bias, kernel=fw.KERNEL_AUTO):
     m, k = x_bits.shape
     n = codes.shape[0]
     dt = _dt(act)
@@ -75,7 +75,7 @@ def gpu_linear(x_bits, act, codes, scales, bias, kernel=fw.KERNEL_AUTO, split_k=
     s = torch.from_numpy(np.ascontiguousarray(scales)).to(DEV)
     b = None if bias is None else torch.from_numpy(np.ascontiguousarray(bias)).to(DEV)
     ybuf, y = _guarded(m * n, dt, POISON16)
-    fw.linear(x, c, s, b, out=y.view(m, n), kernel=kernel, split_k=split_k)
+    fw.linear(x, c, s, b, out=y.view(m, n), kernel=kernel)
     torch.cuda.synchronize()
     _check_canaries(ybuf, m * n, POISON16)
     assert fw.device_error() == 0
@@ -182,14 +182,37 @@ def test_linear_parity(m, n, k, act):
     assert_parity(y, ref, act, (m, n, k))
 
 
-@pytest.mark.parametrize("split", [1, 2, 4, 8])
+@pytest.mark.parametrize("n,k", [
+    (128, 128),      # one unit: a single CTA
+    (1000, 256),     # 16 units: fewer units than SMs
+    (2432, 1024),    # 19 tiles x 8 k-blocks = 152 units
+    (2560, 1024),    # 160 units: every CTA one unit, a few two
+    (1100, 4096),    # 9 tiles x 32: tiles split across several CTAs
+    (300, 14336),    # 3 tiles x 112 k-blocks: ~50 CTAs per tile
+    (20000, 272),    # 157 tiles x 3 (ragged k): tiles straddling CTAs
+])
 @pytest.mark.parametrize("m", [1, 2, 9, 32])
-def test_skinny_every_split(m, split):
-    c, codes, scales = _case(77 + m + split, m, 520, 2048, oracle.ACT_BF16)
-    y = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], kernel=fw.KERNEL_SKINNY,
-                   split_k=split)
-    ref = oracle.linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"])
-    assert_parity(y, ref, oracle.ACT_BF16, (m, split))
+def test_tensor_core_partitions(m, n, k):
+    """Stream-K partitions of every kind: whole tiles, tiles shared by two or
+    by many CTAs (finished from the workspace by the last to arrive), fewer
+    units than SMs, ragged N and K."""
+    c, codes, scales = _case(77 + m + n + k, m, n, k, oracle.ACT_BF16)
+    y = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], kernel=fw.KERNEL_SKINNY)
+    ref = oracle.linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], threads=oracle.host_cores())
+    assert_parity(y, ref, oracle.ACT_BF16, (m, n, k))
+
+
+def test_workspace_left_ready_across_shapes():
+    """Back-to-back calls of different shapes share one workspace: each call
+    must leave the arrival counters at zero for the next."""
+    shapes = [(8, 1100, 4096), (3, 300, 14336), (32, 2560, 1024), (8, 1100, 4096)]
+    for i, (m, n, k) in enumerate(shapes):
+        c, codes, scales = _case(500 + i, m, n, k, oracle.ACT_BF16)
+        y = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], kernel=fw.KERNEL_SKINNY)
+        ref = oracle.linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], threads=oracle.host_cores())
+        assert_parity(y, ref, oracle.ACT_BF16, (m, n, k))
+    ws = fw._workspaces[0]
+    assert int(ws[:4096].view(torch.int32).abs().sum()) == 0   # 1024 arrival counters
 
 
 @pytest.mark.parametrize("act", [oracle.ACT_BF16, oracle.ACT_F16])
