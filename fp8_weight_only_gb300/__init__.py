@@ -30,7 +30,7 @@ class Fp8wError(RuntimeError):
 
 
 class LinearConfig(ctypes.Structure):
-    _fields_ = [("kernel", ctypes.c_int), ("reserved", ctypes.c_int * 7)]
+    _fields_ = [("kernel", ctypes.c_int), ("ctas", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
 
 
 _lib = None
@@ -129,8 +129,11 @@ def workspace(device, nbytes):
     return ws
 
 
-def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_buffer=None):
-    """y[M, N] = round(scale[n] * sum_k x[m, k] * e4m3(codes[n, k]) + bias[n])."""
+def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_buffer=None, ctas=0):
+    """y[M, N] = round(scale[n] * sum_k x[m, k] * e4m3(codes[n, k]) + bias[n]).
+
+    kernel and ctas (the tensor-core kernel's grid size, 0 = from the shape)
+    override the automatic launch choice, for tests and tuning."""
     import torch
     if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
         raise TypeError("x must be a contiguous 2-D CUDA tensor")
@@ -157,11 +160,11 @@ def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_
     if need:
         ws = workspace_buffer if workspace_buffer is not None else workspace(x.device, need)
     ws_ptr, ws_bytes = (_ptr(ws), ws.numel()) if ws is not None else (None, 0)
-    if kernel == KERNEL_AUTO:
+    if kernel == KERNEL_AUTO and ctas == 0:
         st = L.fp8w_linear(_ptr(x), act, m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
                            _ptr(out), ws_ptr, ws_bytes, stream)
     else:
-        cfg = LinearConfig(kernel)
+        cfg = LinearConfig(kernel, ctas)
         st = L.fp8w_linear_ex(_ptr(x), act, m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
                               _ptr(out), ws_ptr, ws_bytes, ctypes.byref(cfg), stream)
     _check(st)

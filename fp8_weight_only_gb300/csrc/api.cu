@@ -69,6 +69,8 @@ fp8w_status fp8w_linear_ex(const void* x, int act_dtype, int64_t m, int64_t k, c
     if (kernel == FP8W_KERNEL_AUTO) kernel = (m == 1) ? FP8W_KERNEL_GEMV : FP8W_KERNEL_SKINNY;
     if (kernel == FP8W_KERNEL_GEMV && m != 1) return FP8W_ERR_CONFIG;
     if (kernel != FP8W_KERNEL_GEMV && kernel != FP8W_KERNEL_SKINNY) return FP8W_ERR_CONFIG;
+    const int ctas = config ? config->ctas : 0;
+    if (ctas < 0 || (ctas != 0 && kernel == FP8W_KERNEL_GEMV)) return FP8W_ERR_CONFIG;
     fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, scales, bias, y};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (kernel == FP8W_KERNEL_GEMV) return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear gemv launch");
@@ -76,7 +78,12 @@ fp8w_status fp8w_linear_ex(const void* x, int act_dtype, int64_t m, int64_t k, c
     const size_t need = skinny_ws();
     if (need == 0) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear device query");
     if (workspace_bytes < need) return FP8W_ERR_WORKSPACE;
-    return cuda_status(fp8w::launch_skinny(a, workspace, s), "fp8w_linear tensor-core launch");
+    if (ctas != 0) {
+        int sms = 0;
+        if (fp8w::device_sm_count(sms) != cudaSuccess) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear device query");
+        if (ctas > sms) return FP8W_ERR_CONFIG;
+    }
+    return cuda_status(fp8w::launch_skinny(a, workspace, ctas, s), "fp8w_linear tensor-core launch");
 }
 
 fp8w_status fp8w_linear(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,

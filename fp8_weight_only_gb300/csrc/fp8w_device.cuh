@@ -16,9 +16,11 @@
 
 namespace fp8w {
 
-// Bounded waits: a wait that has not succeeded after this long gives up,
-// records an error code and lets the kernel wind down instead of hanging.
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+// Bounded waits: a wait that has not succeeded after this many SM cycles
+// (about 2 s at 2 GHz) gives up, records an error code and lets the kernel
+// wind down instead of hanging.  Measured on the SM's own cycle counter,
+// which only moves forward with the SM clock.
+constexpr long long kWaitLimitCycles = 4000000000ll;
 
 enum DeviceError : int {
     kErrNone = 0,
@@ -48,11 +50,7 @@ __device__ __forceinline__ float4 ldg_stream_f4(const float* p) {
     return v;
 }
 
-__device__ __forceinline__ uint64_t globaltimer() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
+__device__ __forceinline__ long long cycles() { return clock64(); }
 
 // ------------------------------------------------------------ e4m3 codec --
 
@@ -146,21 +144,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // CTA-wide abort flag is raised meanwhile or the time limit passes.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
+    const long long t0 = cycles();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
             if (*abort_flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs) return false;
+            if (cycles() - t0 > kWaitLimitCycles) return false;
         }
     }
 }
 
 // Wait with a time limit only (used while winding down after an abort).
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer();
+    const long long t0 = cycles();
     while (!mbar_try_wait(bar, parity)) {
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+        if (cycles() - t0 > kWaitLimitCycles) return false;
     }
     return true;
 }
@@ -312,6 +310,16 @@ __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
+}
+
+// ------------------------------------------- programmatic dependent launch --
+
+// Wait until the preceding grid in the stream has completed and its memory
+// operations are visible (no-op when launched without the PDL attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next grid in the stream to begin launching.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ------------------------------------------------------------- epilogue --

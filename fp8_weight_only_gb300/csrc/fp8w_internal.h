@@ -26,7 +26,8 @@ cudaError_t launch_gemv(const LinearArgs& a, cudaStream_t st);
 
 // K3: any m (32-row slabs, one launch each); needs a workspace of
 // skinny_workspace_size(sms) bytes, zero-filled before its first use.
-cudaError_t launch_skinny(const LinearArgs& a, void* workspace, cudaStream_t st);
+// ctas > 0 fixes the grid size (1..sms), 0 picks it from the shape.
+cudaError_t launch_skinny(const LinearArgs& a, void* workspace, int ctas, cudaStream_t st);
 size_t skinny_workspace_size(int sms);
 cudaError_t device_sm_count(int& sms);
 

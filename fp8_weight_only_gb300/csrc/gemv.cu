@@ -162,15 +162,19 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         fence_mbar_init();
     }
     __syncthreads();
+    // the next kernel in the stream may start its prologue; it waits for
+    // this grid before touching global memory
+    pdl_launch_dependents();
 
     if (warp == nwarps_compute) {
         // ---------------------------------------------------- producer --
         if ((threadIdx.x & 31) == 0) {
             const uint64_t pol = policy_evict_first();
+            pdl_wait();  // the codes may come from the previous kernel
             int64_t issued = 0;
+            int s = 0;
+            uint32_t ph = 0;  // stage slot and its phase, advanced without division
             for (int64_t st = 0; st < nst; ++st) {
-                const int s = static_cast<int>(st % S);
-                const uint32_t ph = static_cast<uint32_t>((st / S) & 1);
                 if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
                     *abort_flag = 1;
                     atomicCAS(&g_gemv_error, 0, kErrWaitSlot);
@@ -182,6 +186,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                 mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
                 bulk_load(ring + s * geo.stage_bytes, codes + r0 * k, bytes, bar_full + 8 * s, pol);
                 ++issued;
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
             }
             if (*abort_flag) {
                 for (int64_t st = (issued > S ? issued - S : 0); st < issued; ++st)
@@ -197,6 +205,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     const int g = t / geo.t_row, tr = t % geo.t_row;
     const int lane = t & 31;
     const int64_t nchunks = k >> 4;
+    pdl_wait();  // x, scales and bias may come from the previous kernel, and y may still be read by it
     float xr[C][16];
 #pragma unroll
     for (int j = 0; j < C; ++j) {
@@ -210,16 +219,24 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
     const int warps_per_row = geo.t_row >> 5;
     const int warp_in_group = (t % geo.t_row) >> 5;
+    int s = 0;
+    uint32_t ph = 0;
     for (int64_t st = 0; st < nst; ++st) {
-        const int s = static_cast<int>(st % S);
-        if (!mbar_wait_warp(bar_full + 8 * s, static_cast<uint32_t>((st / S) & 1), abort_flag)) {
+        const int64_t r0 = row0 + st * R;
+        // the epilogue threads fetch their row's scale and bias before the
+        // stage's data arrives, off the critical path
+        float sc = 0.0f, b = 0.0f;
+        if (t < R && r0 + t < row1) {
+            sc = scales[r0 + t];
+            b = bias ? bias[r0 + t] : 0.0f;
+        }
+        if (!mbar_wait_warp(bar_full + 8 * s, ph, abort_flag)) {
             *cmp_abort = 1;
             *abort_flag = 1;
             atomicCAS(&g_gemv_error, 0, kErrWaitTma);
         }
         compute_bar();
         if (*cmp_abort) break;
-        const int64_t r0 = row0 + st * R;
         const uint8_t* stage = smem + s * geo.stage_bytes;
         float p[RPG];
 #pragma unroll
@@ -237,6 +254,10 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        if (++s == S) {
+            s = 0;
+            ph ^= 1u;
+        }
         const float wsum = warp_reduce_rows<RPG>(p);
         constexpr int kStride = 32 / RPG;
         if ((lane % kStride) == 0) red[(g + (lane / kStride) * geo.groups) * 16 + warp_in_group] = wsum;
@@ -246,8 +267,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             if (row < row1) {
                 float acc = 0.0f;
                 for (int w = 0; w < warps_per_row; ++w) acc += red[t * 16 + w];
-                const float b = bias ? bias[row] : 0.0f;
-                y[row] = round_out<kBf16>(fmaf(acc, scales[row], b));
+                y[row] = round_out<kBf16>(fmaf(acc, sc, b));
             }
         }
         // red is rewritten only after the next stage's first compute_bar
@@ -303,9 +323,19 @@ static cudaError_t launch_cfg(const LinearArgs& a, const GemvGeom& geo, int sms,
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t grid = a.n < sms ? a.n : sms;
-    kern<<<static_cast<unsigned>(grid), kGemvThreads, gemv_smem_bytes(), st>>>(
-        static_cast<const uint16_t*>(a.x), a.codes, a.scales, a.bias, static_cast<uint16_t*>(a.y), a.n, a.k, geo);
-    return cudaGetLastError();
+    // programmatic dependent launch: set-up overlaps the previous kernel's tail
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kGemvThreads);
+    cfg.dynamicSmemBytes = gemv_smem_bytes();
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint16_t*>(a.x), a.codes, a.scales, a.bias,
+                              static_cast<uint16_t*>(a.y), a.n, a.k, geo);
 }
 
 template <bool kBf16>

@@ -120,7 +120,10 @@ enum { FP8W_KERNEL_AUTO = 0, FP8W_KERNEL_GEMV = 1, FP8W_KERNEL_SKINNY = 2 };
 
 typedef struct fp8w_linear_config {
     int kernel;   /* FP8W_KERNEL_*; GEMV requires m == 1 */
-    int reserved[7];
+    int ctas;     /* tensor-core kernel only: CTAs of its persistent grid,
+                     1..number of SMs, or 0 to choose from the shape; must be
+                     0 for the GEMV kernel */
+    int reserved[6];  /* must be 0 */
 } fp8w_linear_config;
 
 /* fp8w_linear with an explicit configuration (NULL = automatic).  The

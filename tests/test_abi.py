@@ -66,9 +66,14 @@ def test_linear_rejects_bad_arguments(kw, status):
     fw.LinearConfig(fw.KERNEL_GEMV),           # gemv needs m == 1 (m = 2 below)
     fw.LinearConfig(7),                        # unknown kernel
     fw.LinearConfig(-1),
+    fw.LinearConfig(fw.KERNEL_SKINNY, -3),     # negative grid size
 ])
 def test_linear_rejects_bad_config(cfg):
     assert _lin(m=2, k=256, cfg=cfg) == 6
+
+
+def test_gemv_rejects_a_grid_size():
+    assert _lin(m=1, k=256, cfg=fw.LinearConfig(fw.KERNEL_GEMV, 8)) == 6
 
 
 @pytest.mark.parametrize("ws,ws_bytes", [(None, 0), (None, 1 << 30), (ctypes.c_void_p(0x600010), 1 << 30)])
