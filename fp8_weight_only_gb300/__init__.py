@@ -19,7 +19,8 @@ FP8W_F16 = 2
 KERNEL_AUTO, KERNEL_GEMV, KERNEL_SKINNY = 0, 1, 2
 
 SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_workspace_size", "fp8w_linear_ex",
-           "fp8w_status_string", "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version")
+           "fp8w_status_string", "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version",
+           "fp8w_linear_noalloc")
 ABI_VERSION = 2
 
 
@@ -54,6 +55,8 @@ def lib():
         L.fp8w_linear_ex.restype = c.c_int
         L.fp8w_linear_ex.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P, c.c_size_t,
                                      c.POINTER(LinearConfig), P]
+        L.fp8w_linear_noalloc.restype = c.c_int
+        L.fp8w_linear_noalloc.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P]
         L.fp8w_status_string.restype = c.c_char_p
         L.fp8w_status_string.argtypes = [c.c_int]
         L.fp8w_last_cuda_error.restype = c.c_char_p

@@ -93,6 +93,22 @@ fp8w_status fp8w_linear(const void* x, int act_dtype, int64_t m, int64_t k, cons
                           stream);
 }
 
+fp8w_status fp8w_linear_noalloc(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
+                                const float* scales, const float* bias, int64_t n, void* y, void* stream) {
+    fp8w_status st = check_linear(x, act_dtype, m, k, codes, scales, bias, n, y);
+    if (st != FP8W_OK) return st;
+    fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, scales, bias, y};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (m == 1) return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear_noalloc gemv launch");
+    const size_t need = skinny_ws();
+    if (need == 0) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear_noalloc device query");
+    if (need > fp8w::static_scratch_bytes()) return FP8W_ERR_SCRATCH;
+    void* scratch = nullptr;
+    const fp8w_status ss = cuda_status(fp8w::static_scratch(&scratch, s), "fp8w_linear_noalloc scratch set-up");
+    if (ss != FP8W_OK) return ss;
+    return cuda_status(fp8w::launch_skinny(a, scratch, 0, s), "fp8w_linear_noalloc tensor-core launch");
+}
+
 const char* fp8w_status_string(int status) {
     switch (status) {
         case FP8W_OK: return "ok";
@@ -103,6 +119,9 @@ const char* fp8w_status_string(int status) {
         case FP8W_ERR_CUDA: return "CUDA call failed (see fp8w_last_cuda_error)";
         case FP8W_ERR_CONFIG: return "invalid explicit launch configuration";
         case FP8W_ERR_WORKSPACE: return "workspace NULL, not 256-byte aligned or smaller than fp8w_linear_workspace_size";
+        case FP8W_ERR_SCRATCH:
+            return "this device needs more scratch than fp8w_linear_noalloc's static FP8W_STATIC_SCRATCH_BYTES "
+                   "(more SMs than it covers): use fp8w_linear with a workspace";
         default: return "unknown status";
     }
 }

@@ -29,6 +29,11 @@ cudaError_t launch_gemv(const LinearArgs& a, cudaStream_t st);
 // ctas > 0 fixes the grid size (1..sms), 0 picks it from the shape.
 cudaError_t launch_skinny(const LinearArgs& a, void* workspace, int ctas, cudaStream_t st);
 size_t skinny_workspace_size(int sms);
+// Library-owned scratch of fp8w_linear_noalloc (a static device array of
+// static_scratch_bytes()); the first call per device looks up its address and
+// enqueues a clear of its counters on st.
+cudaError_t static_scratch(void** ptr, cudaStream_t st);
+size_t static_scratch_bytes();
 cudaError_t device_sm_count(int& sms);
 
 // Kernel-recorded wait failures (0 = none); reading clears them.

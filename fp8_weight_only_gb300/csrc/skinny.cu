@@ -52,6 +52,7 @@
 
 #include "fp8w_device.cuh"
 #include "fp8w_internal.h"
+#include "../../include/fp8w.h"
 
 namespace fp8w {
 
@@ -102,7 +103,9 @@ struct SkinnySmem {
 constexpr int kMaxCtas = 1024;
 constexpr size_t kWsCountersBytes = kMaxCtas * 4;
 __host__ __device__ constexpr size_t ws_slot_floats() { return static_cast<size_t>(kMaxNT) * kTileN; }
-size_t skinny_workspace_bytes(int p) { return kWsCountersBytes + 2 * static_cast<size_t>(p) * ws_slot_floats() * 4; }
+constexpr size_t skinny_workspace_bytes(int p) {
+    return kWsCountersBytes + 2 * static_cast<size_t>(p) * ws_slot_floats() * 4;
+}
 // A split CTA takes at least this many units, so a small matrix is not cut
 // into more partial tiles than it has k-blocks to share.
 constexpr int64_t kMinUnitsPerCta = 4;
@@ -724,6 +727,39 @@ cudaError_t launch_skinny(const LinearArgs& a, void* workspace, int ctas, cudaSt
     if (a.m <= 16)
         return bf16 ? launch_nt<16, true>(a, workspace, ctas, st) : launch_nt<16, false>(a, workspace, ctas, st);
     return bf16 ? launch_nt<32, true>(a, workspace, ctas, st) : launch_nt<32, false>(a, workspace, ctas, st);
+}
+
+// Library-owned scratch for fp8w_linear_noalloc: the workspace of a grid of
+// up to kStaticScratchCtas CTAs, in device memory that exists as soon as this
+// module is loaded on a device, so that entry point allocates nothing.
+constexpr int kStaticScratchCtas = 160;
+constexpr size_t kStaticScratchBytes = skinny_workspace_bytes(kStaticScratchCtas);
+static_assert(kStaticScratchBytes == FP8W_STATIC_SCRATCH_BYTES, "fp8w.h states the static scratch size");
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+
+size_t static_scratch_bytes() { return kStaticScratchBytes; }
+
+// First call on a device (with that device current): look up the array's
+// address and enqueue a clear of its arrival counters on `st`, ahead of the
+// kernel that will use them.  Later calls return the cached address.
+cudaError_t static_scratch(void** ptr, cudaStream_t st) {
+    static std::mutex mu;
+    static void* ptrs[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_static_scratch);
+        if (e != cudaSuccess) return e;
+        e = cudaMemsetAsync(p, 0, kWsCountersBytes, st);
+        if (e != cudaSuccess) return e;
+        ptrs[dev] = p;
+    }
+    *ptr = ptrs[dev];
+    return cudaSuccess;
 }
 
 int read_skinny_device_error() {

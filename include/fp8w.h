@@ -55,7 +55,9 @@ typedef enum fp8w_status {
     FP8W_ERR_DTYPE = 4,     /* activation dtype is not FP8W_BF16 / FP8W_F16 */
     FP8W_ERR_CUDA = 5,      /* a CUDA runtime/driver call failed */
     FP8W_ERR_CONFIG = 6,    /* an explicit launch configuration is invalid */
-    FP8W_ERR_WORKSPACE = 7  /* workspace NULL, misaligned or too small */
+    FP8W_ERR_WORKSPACE = 7, /* workspace NULL, misaligned or too small */
+    FP8W_ERR_SCRATCH = 8    /* fp8w_linear_noalloc: the device needs more
+                               scratch than the library's static maximum */
 } fp8w_status;
 
 /* Activation / output dtypes. */
@@ -133,6 +135,37 @@ FP8W_API fp8w_status fp8w_linear_ex(const void *x, int act_dtype, int64_t m, int
                            const float *bias, int64_t n, void *y,
                            void *workspace, size_t workspace_bytes,
                            const fp8w_linear_config *config, void *stream);
+
+/*
+ * fp8w_linear_noalloc -- fp8w_linear without a caller-provided workspace.
+ * The pages have no counterpart: the operation is fp8w_linear's, and this
+ * entry point exists only because the tensor-core kernel needs scratch.  It
+ * serves callers that cannot hand over a device buffer: a plain C host
+ * program whose device pointers come from another runtime and which has no
+ * device allocator of its own, or a serving loop that must not allocate
+ * once running (cudaMalloc can synchronise the device, and a fixed memory
+ * budget leaves no room for ad-hoc buffers).  It calls no allocator.
+ *
+ * Arguments, checks, kernels and results are those of fp8w_linear.  The
+ * scratch is a static device array of FP8W_STATIC_SCRATCH_BYTES bytes that
+ * the library module holds on every device it is loaded on (the workspace of
+ * a grid of up to 160 CTAs, one per SM); a device whose workspace would be
+ * larger is refused with FP8W_ERR_SCRATCH before any launch.
+ *
+ * First call on a device: looks up the array's address (with that device
+ * current) and enqueues a clear of its counters on `stream` ahead of the
+ * kernel; make that first call before any CUDA-graph capture.  Every
+ * completed call leaves the scratch ready for the next one.
+ *
+ * All calls on one device share the one scratch, so calls that may overlap
+ * on the GPU (on other streams, or from other host threads) race and can
+ * return wrong results: keep them in one stream, or use fp8w_linear with a
+ * workspace per stream.
+ */
+#define FP8W_STATIC_SCRATCH_BYTES 5246976u
+FP8W_API fp8w_status fp8w_linear_noalloc(const void *x, int act_dtype, int64_t m, int64_t k,
+                                const uint8_t *codes, const float *scales,
+                                const float *bias, int64_t n, void *y, void *stream);
 
 /* Human-readable name of a status code (static string). */
 FP8W_API const char *fp8w_status_string(int status);

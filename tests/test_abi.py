@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_status_strings():
     L = fw.lib()
-    for s in range(8):
+    for s in range(9):
         assert L.fp8w_status_string(s)
     assert L.fp8w_status_string(99) == b"unknown status"
 
@@ -99,3 +99,15 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(fw, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(fw.Fp8wError):
         fw.lib()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(x=None), 1), (dict(y=None), 1), (dict(act=3), 4), (dict(m=0), 2), (dict(k=40), 2),
+    (dict(codes=ctypes.c_void_p(0x200004)), 3),
+])
+def test_noalloc_entry_rejects_bad_arguments_on_the_host(kw, status):
+    a = dict(x=A16, act=1, m=2, k=64, codes=B16, scales=C16, bias=None, n=8, y=D16)
+    a.update(kw)
+    L = fw.lib()
+    assert L.fp8w_linear_noalloc(a["x"], a["act"], a["m"], a["k"], a["codes"], a["scales"], a["bias"],
+                                 a["n"], a["y"], None) == status
