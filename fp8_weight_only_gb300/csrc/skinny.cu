@@ -13,33 +13,44 @@
 //    [c*U/P, (c+1)*U/P).  P is the tile count when that nearly fills the GPU
 //    (every tile whole, nothing to combine), else a multiple of it or the SM
 //    count (stream-K).  A tile that straddles CTAs is finished by the last
-//    contributor to arrive: partial fp32 tiles go to a caller-provided
-//    workspace and are summed in CTA order (deterministic); nothing waits on
-//    another CTA.  A CTA first runs the partial piece at the end of its
-//    range, so its fix-ups overlap its other work.
-//  * Units are dealt round-robin to three lanes; lane g is dequantising
-//    warpgroup g plus MMA issuer g, with private rings in shared memory and
-//    TMEM, so every mbarrier has one producer and one in-order consumer.
-//    (Consumers taking turns on one shared ring could run two phases ahead
-//    of a slow one and pass a completed phase of the same parity.)
-//  * Warp 0 streams each unit's 128 x 128 code tile into its lane's code
-//    slots, and warp 4 its M x 128 activation tile into the lane's
-//    activation slots, with TMA (128-byte swizzle; rows past N or M and k past
-//    K read as zeros).  A code tile is freed as soon as it has been read, an
-//    activation tile when its MMAs are done.
-//  * In each lane, thread r of the warpgroup reads the 128 codes of channel
-//    r (conflict-free through the swizzle), converts them exactly to bf16 /
-//    fp16 in registers and stores them with tcgen05.st into the lane's TMEM A
-//    slot, where they are the A operand of the MMA (A from tensor memory: the
-//    dequantised weight never touches shared memory).
-//  * Each lane's MMA warp (one issuing thread) issues tcgen05.mma.kind::f16
-//    (M = 128, N = 16 or 32 tokens, K = 16) into the lane's double-buffered
-//    TMEM accumulator and returns slots with tcgen05.commit.  A tcgen05.mma
-//    costs its issuing thread tens of cycles whatever its size, so one issuer
-//    could not keep up with the weight stream at N <= 32; three can.
-//  * One epilogue warpgroup reads the lanes' accumulators of a finished tile
-//    with tcgen05.ld (thread r holds channel r for every token), sums them in
-//    a fixed order while the next tile accumulates, and stores
+//    contributor: partial fp32 tiles go to a caller-provided workspace and
+//    are summed in CTA order (deterministic); nothing waits on another CTA.
+//    A CTA runs the partial piece at the end of its range first, so by the
+//    time it finishes the piece at the start of its range the other
+//    contributors are usually done, and it sums their partials straight
+//    from its registers without publishing its own.
+//  * Warp 0 streams each unit's 128 x 128 code tile with TMA (128-byte
+//    swizzle; rows past N and k past K read as zeros) into the code ring of
+//    one of three dequantising warpgroups (units are dealt round-robin);
+//    warp 1 streams the unit's M x 128 activation tile (an L2 hit) into a
+//    ring read by the MMA warps.  The activation ring is deeper than the code
+//    rings, so each activation tile enters the SM's TMA queue no later than
+//    its unit's code tile and never waits behind the whole code ring.  The
+//    two producer warps set up their own barriers and start streaming
+//    without waiting for the other warps to come up.  Every ring has one
+//    producer and one in-order consumer.
+//  * In each warpgroup, thread r reads the 128 codes of channel r
+//    (conflict-free through the swizzle), converts them exactly to bf16 /
+//    fp16 in registers and stores them with tcgen05.st into one of the
+//    group's two TMEM A slots, where they are the A operand of the MMA (A
+//    from tensor memory: the dequantised weight never touches shared
+//    memory).  Two slots let a group convert the next unit while the MMAs
+//    still read the previous one.
+//  * Unit u uses A slot u % 6 (warpgroup u % 3, its slot (u / 3) % 2) and
+//    activation slot u % kXSlots.
+//  * Warps 2 and 3, the MMA warps, take alternate units in order and issue
+//    each unit's eight tcgen05.mma.kind::f16 (M = 128, N = 16 or 32 tokens,
+//    K = 16) into their own TMEM accumulator of the tile (double-buffered
+//    across tiles), then free the operand slots with tcgen05.commit.  Each
+//    warp runs its loop whole and elect.sync picks the issuing lane (issued
+//    that way an MMA costs the warp ~20-30 cycles); a warp tests its next
+//    unit's barriers, without blocking, before this unit's MMAs, because a
+//    barrier wait costs about as much as a unit's eight MMAs.  One issuing
+//    warp per accumulator keeps that accumulator's MMAs in order; two keep up
+//    with the weight stream.
+//  * One epilogue warpgroup reads a finished tile's two accumulators with
+//    tcgen05.ld (thread r holds channel r for every token), adds them in a
+//    fixed order while the next tile accumulates, and stores
 //    y = round(fma(acc, scale, bias)) or, for a split tile, its partial.
 //  * The control loops divide nothing per unit: a cursor walks (tile,
 //    k-block), since a 64-bit division costs a lone thread hundreds of cycles.
@@ -60,40 +71,58 @@ static __device__ int g_skinny_error;
 
 constexpr int kTileN = 128;                 // output channels per tile (MMA M)
 constexpr int kBlockK = 128;                // k per unit
-constexpr int kLanes = 3;                   // dequant warpgroup + MMA issuer pairs
-// warps: 0 code TMA, 1..3 MMA issuers (warp 1 also owns TMEM), 4 x TMA,
-// 5..8 epilogue, 9..20 dequant (4 per lane)
-constexpr int kXWarp = 1 + kLanes;
-constexpr int kFirstEpilogueWarp = kXWarp + 1;
+constexpr int kLanes = 3;                   // dequantising warpgroups
+constexpr int kASlots = 2;                  // TMEM A slots per warpgroup
+// warps: 0 code TMA, 1 activation TMA, 2-3 MMA (warp 2 also owns TMEM),
+// 4..7 epilogue, 8..19 the dequantising warpgroups (4 warps each)
+constexpr int kXWarp = 1;
+constexpr int kMmaWarp = 2;
+constexpr int kMmaWarps = 2;
+constexpr int kFirstEpilogueWarp = kMmaWarp + kMmaWarps;
 constexpr int kFirstDequantWarp = kFirstEpilogueWarp + 4;
-constexpr int kThreads = 32 * (kFirstDequantWarp + 4 * kLanes);  // 672
+constexpr int kThreads = 32 * (kFirstDequantWarp + 4 * kLanes);  // 640
+// named barriers: 0 __syncthreads, 1 epilogue, 2 TMEM ready, 3 start-up
+constexpr uint32_t kBarEpilogue = 1, kBarTmem = 2, kBarStart = 3;
 constexpr int kTmemCols = 512;              // one CTA per SM
 constexpr int kAColsPerSlot = kBlockK / 2;  // two 16-bit values per column
-constexpr int kDCol0 = kLanes * kAColsPerSlot;  // 192: accumulators after the A slots
+constexpr int kDCol0 = kLanes * kASlots * kAColsPerSlot;  // 384: accumulators after the A slots
 constexpr uint32_t kCodeStageBytes = kTileN * kBlockK;  // 16 KB
 constexpr int kMaxNT = 32;
-static_assert(kDCol0 + kLanes * 2 * kMaxNT <= kTmemCols, "TMEM columns");
+static_assert(kDCol0 + kMmaWarps * 2 * kMaxNT <= kTmemCols, "TMEM columns");
 
 template <int NT>
 struct SkinnySmem {
-    // per lane: code slots (freed once read) and activation slots (freed
-    // when the MMA is done), as many as ~221 KB of shared memory holds
-    static constexpr int kCodeSlots = NT == 16 ? 4 : 3;
-    static constexpr int kXSlots = NT == 16 ? 2 : 3;
+    // per warpgroup: freed as soon as read (9 tiles in flight per SM: deeper
+    // rings on every SM make the HBM stream slower, not faster)
+    static constexpr int kCodeSlots = 3;
+    static constexpr int kXSlots = NT == 16 ? 12 : 8;  // activation ring (freed when the unit's MMAs are done)
+    static_assert(kXSlots % kMmaWarps == 0 && (kLanes * kASlots) % kMmaWarps == 0, "slots alternate between MMA warps");
     static constexpr uint32_t kXBoxBytes = NT * 128;          // 64 k x NT rows x 2 B
     static constexpr uint32_t kXStageBytes = 2 * kXBoxBytes;  // 128 k
     static constexpr uint32_t kCodesOff = 0;
     static constexpr uint32_t kXOff = kCodesOff + kLanes * kCodeSlots * kCodeStageBytes;
-    static constexpr uint32_t kBarOff = kXOff + kLanes * kXSlots * kXStageBytes;
-    // per lane: cfull, cempty [kCodeSlots]; xfull, xempty [kXSlots]; afull;
-    // aempty; dready, dfree [2]; drain
-    static constexpr uint32_t kBarsPerLane = 2 * kCodeSlots + 2 * kXSlots + 7;
-    static constexpr uint32_t kNumBars = kLanes * kBarsPerLane;
+    static constexpr uint32_t kBarOff = kXOff + kXSlots * kXStageBytes;
+    // per warpgroup: cfull, cempty [kCodeSlots]
+    static constexpr uint32_t kBarsPerLane = 2 * kCodeSlots;
+    // then: aready, afree [6]; xfull, xempty [kXSlots]; dfree [2];
+    // dready [MMA warp][2]; drain [MMA warp]
+    static constexpr int kASlotsAll = kLanes * kASlots;
+    static constexpr uint32_t kLaneBars = kLanes * kBarsPerLane;
+    static constexpr uint32_t kNumBars = kLaneBars + 2 * kASlotsAll + 2 * kXSlots + 2 + 3 * kMmaWarps;
     // tmem base, abort flag, last-contributor flag, epilogue abort flag
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
     static constexpr uint32_t kBytes = kMiscOff + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
     static_assert(kAlloc <= 227 * 1024, "shared memory");
+    // arrivals per phase: cempty, aready and dfree one per warp of a
+    // warpgroup, the others one
+    static __device__ __forceinline__ uint32_t arrivals(uint32_t i) {
+        if (i < kLaneBars) return (i % kBarsPerLane) >= static_cast<uint32_t>(kCodeSlots) ? 4u : 1u;
+        const uint32_t gi = i - kLaneBars;
+        if (gi < static_cast<uint32_t>(kASlotsAll)) return 4u;  // aready
+        const uint32_t di = static_cast<uint32_t>(2 * kASlotsAll + 2 * kXSlots);
+        return (gi == di || gi == di + 1) ? 4u : 1u;            // dfree
+    }
 };
 
 // Workspace: [kMaxCtas arrival counters (uint32)][2 partial-tile slots per
@@ -168,7 +197,7 @@ __device__ __forceinline__ void record_error(int code, volatile int* abort_flag,
     atomicCAS(&g_skinny_error, 0, code * 1000 + (bar ? static_cast<int>((bar - bar0) / 8) + 1 : 0));
 }
 
-__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync %0, 128;" ::"n"(kBarEpilogue) : "memory"); }
 
 // Arrival count of a split tile: release orders this CTA's partial stores
 // (made visible to this thread by the preceding CTA barrier) before the
@@ -177,11 +206,6 @@ __device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t* counter) {
     uint32_t old;
     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
     return old;
-}
-
-// lane g has a unit among [it0, it0 + len) iff one index is = g mod kLanes
-__device__ __forceinline__ bool lane_has(int g, int it0, int len) {
-    return len >= kLanes || ((g - it0 % kLanes + kLanes) % kLanes) < len;
 }
 
 template <int NT, bool kBf16>
@@ -198,15 +222,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto lbar = [&](int g, int i) { return bar0 + 8u * (g * L::kBarsPerLane + i); };
     auto cfull = [&](int g, int s) { return lbar(g, s); };
     auto cempty = [&](int g, int s) { return lbar(g, kCS + s); };
-    auto xfull = [&](int g, int s) { return lbar(g, 2 * kCS + s); };
-    auto xempty = [&](int g, int s) { return lbar(g, 2 * kCS + kXS + s); };
-    auto afull = [&](int g) { return lbar(g, 2 * kCS + 2 * kXS); };
-    auto aempty = [&](int g) { return lbar(g, 2 * kCS + 2 * kXS + 1); };
-    auto dready = [&](int g, int d) { return lbar(g, 2 * kCS + 2 * kXS + 2 + d); };
-    auto dfree = [&](int g, int d) { return lbar(g, 2 * kCS + 2 * kXS + 4 + d); };
-    auto drain = [&](int g) { return lbar(g, 2 * kCS + 2 * kXS + 6); };
+    constexpr int kAS = L::kASlotsAll;
+    auto gbar = [&](int i) { return bar0 + 8u * (L::kLaneBars + i); };
+    auto aready = [&](int r) { return gbar(r); };
+    auto afree = [&](int r) { return gbar(kAS + r); };
+    auto xfull = [&](int s) { return gbar(2 * kAS + s); };
+    auto xempty = [&](int s) { return gbar(2 * kAS + kXS + s); };
+    auto dfree = [&](int d) { return gbar(2 * kAS + 2 * kXS + d); };
+    auto dready = [&](int w, int d) { return gbar(2 * kAS + 2 * kXS + 2 + 2 * w + d); };
+    auto drain = [&](int w) { return gbar(2 * kAS + 2 * kXS + 2 + 2 * kMmaWarps + w); };
     auto code_smem = [&](int g, int s) { return L::kCodesOff + (g * kCS + s) * kCodeStageBytes; };
-    auto x_smem = [&](int g, int s) { return L::kXOff + (g * kXS + s) * L::kXStageBytes; };
+    auto x_smem = [&](int s) { return L::kXOff + s * L::kXStageBytes; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
     volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8);
@@ -237,44 +263,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         return cu;
     };
 
-    if (threadIdx.x == 0) {
-        for (int g = 0; g < kLanes; ++g) {
-            for (int s = 0; s < kCS; ++s) {
-                mbar_init(cfull(g, s), 1);
-                mbar_init(cempty(g, s), 4);
-            }
-            for (int s = 0; s < kXS; ++s) {
-                mbar_init(xfull(g, s), 1);
-                mbar_init(xempty(g, s), 1);
-            }
-            mbar_init(afull(g), 4);
-            mbar_init(aempty(g), 1);
-            for (int d = 0; d < 2; ++d) {
-                mbar_init(dready(g, d), 1);
-                mbar_init(dfree(g, d), 4);
-            }
-            mbar_init(drain(g), 1);
+    // Start-up: warp 1 sets up the activation ring's barriers, warp 0 all the
+    // others; each then arrives at the start-up barrier without waiting and
+    // begins streaming, while the other warps wait there for both.
+    if (warp <= kXWarp) {
+        const uint32_t xb0 = static_cast<uint32_t>(L::kLaneBars + 2 * kAS);  // xfull, xempty: [xb0, xb1)
+        const uint32_t xb1 = xb0 + static_cast<uint32_t>(2 * kXS);
+        if (warp == 0) {
+            for (uint32_t i = lane; i < L::kNumBars; i += 32)
+                if (i < xb0 || i >= xb1) mbar_init(bar0 + 8 * i, L::arrivals(i));
+        } else {
+            for (uint32_t i = xb0 + lane; i < xb1; i += 32) mbar_init(bar0 + 8 * i, L::arrivals(i));
         }
-        *abort_flag = 0;
-        *ep_abort = 0;
+        if (lane == 0) {
+            *abort_flag = 0;  // written by both producer warps before either can raise it
+            if (warp == 0) *ep_abort = 0;
+            tma_prefetch_desc(warp == 0 ? &map_codes : &map_x);
+        }
         fence_mbar_init();
-        tma_prefetch_desc(&map_codes);
-        tma_prefetch_desc(&map_x);
+        asm volatile("bar.arrive %0, %1;" ::"n"(kBarStart), "n"(kThreads) : "memory");
+    } else {
+        asm volatile("bar.sync %0, %1;" ::"n"(kBarStart), "n"(kThreads) : "memory");
     }
-    __syncthreads();
     // let the next kernel in the stream start launching; its CTAs wait for
     // this grid to complete before they read or write global memory
     pdl_launch_dependents();
-    // TMEM is allocated by warp 1 while the code producer already streams;
-    // every other warp meets warp 1 at named barrier 2 first.
+    // TMEM is allocated by the MMA warp while the producers already stream;
+    // the warps that use it meet the MMA warp at a named barrier first.
     uint32_t tmem = 0;
-    if (warp != 0) {
-        if (warp == 1) {
+    if (warp >= kMmaWarp) {
+        if (warp == kMmaWarp) {
             tmem_alloc(smem_u32(tmem_slot), kTmemCols);
             tmem_relinquish();
         }
         tc_fence_before();
-        asm volatile("bar.sync 2, %0;" ::"n"(kThreads - 32) : "memory");
+        asm volatile("bar.sync %0, %1;" ::"n"(kBarTmem), "n"(kThreads - 32 * kMmaWarp) : "memory");
         tc_fence_after();
         tmem = *tmem_slot;
     }
@@ -285,11 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t pol_stream = policy_evict_first();
             pdl_wait();
             UnitCursor cu = cursor0();
-            int g = 0, j = 0;  // lane of the unit, and its index within the lane
+            int g = 0, j = 0;  // warpgroup of the unit, and its index within the group
+            int s = 0;         // == j % kCS
+            uint32_t ph = 0;   // == (j / kCS) & 1
             int issued = 0;
             for (int it = 0; it < iters; ++it, cu.next()) {
-                const int s = j % kCS;
-                if (!mbar_wait(cempty(g, s), static_cast<uint32_t>(((j / kCS) & 1) ^ 1), abort_flag)) {
+                if (!mbar_wait(cempty(g, s), ph ^ 1u, abort_flag)) {
                     record_error(kErrWaitSlot, abort_flag, cempty(g, s), bar0);
                     break;
                 }
@@ -300,11 +324,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (++g == kLanes) {
                     g = 0;
                     ++j;
+                    if (++s == kCS) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
             if (*abort_flag) {
                 // let every copy still in flight land before the CTA exits:
-                // the last fills of each lane's slots
+                // the last fills of each group's slots
                 for (int g2 = 0; g2 < kLanes; ++g2) {
                     const int n_g2 = (issued - g2 + kLanes - 1) / kLanes;
                     for (int jj = (n_g2 > kCS ? n_g2 - kCS : 0); jj < n_g2; ++jj)
@@ -317,97 +345,118 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ----------------------------------------- activation-tile producer --
         if (lane == 0) {
             const uint64_t pol_keep = policy_evict_last();
-            pdl_wait();
+            pdl_wait();  // x may come from the previous kernel
             UnitCursor cu = cursor0();
-            int g = 0, j = 0;
+            int s = 0;
+            uint32_t ph = 0;
             int issued = 0;
             for (int it = 0; it < iters; ++it, cu.next()) {
-                const int s = j % kXS;
-                if (!mbar_wait(xempty(g, s), static_cast<uint32_t>(((j / kXS) & 1) ^ 1), abort_flag)) {
-                    record_error(kErrWaitSlot, abort_flag, xempty(g, s), bar0);
+                if (!mbar_wait(xempty(s), ph ^ 1u, abort_flag)) {
+                    record_error(kErrWaitSlot, abort_flag, xempty(s), bar0);
                     break;
                 }
                 const int32_t kk = cu.kb * kBlockK;
-                const uint32_t xs = sbase + x_smem(g, s);
-                mbar_arrive_expect_tx(xfull(g, s), L::kXStageBytes);
-                tma_load_2d(xs, &map_x, kk, m_row0, xfull(g, s), pol_keep);
-                tma_load_2d(xs + L::kXBoxBytes, &map_x, kk + 64, m_row0, xfull(g, s), pol_keep);
+                const uint32_t xs = sbase + x_smem(s);
+                mbar_arrive_expect_tx(xfull(s), L::kXStageBytes);
+                tma_load_2d(xs, &map_x, kk, m_row0, xfull(s), pol_keep);
+                tma_load_2d(xs + L::kXBoxBytes, &map_x, kk + 64, m_row0, xfull(s), pol_keep);
                 ++issued;
-                if (++g == kLanes) {
-                    g = 0;
-                    ++j;
+                if (++s == kXS) {
+                    s = 0;
+                    ph ^= 1u;
                 }
             }
             if (*abort_flag) {
-                for (int g2 = 0; g2 < kLanes; ++g2) {
-                    const int n_g2 = (issued - g2 + kLanes - 1) / kLanes;
-                    for (int jj = (n_g2 > kXS ? n_g2 - kXS : 0); jj < n_g2; ++jj)
-                        if (!mbar_wait_drain(xfull(g2, jj % kXS), static_cast<uint32_t>((jj / kXS) & 1)))
-                            atomicCAS(&g_skinny_error, 0, kErrWaitDrain * 1000);
-                }
+                for (int jj = (issued > kXS ? issued - kXS : 0); jj < issued; ++jj)
+                    if (!mbar_wait_drain(xfull(jj % kXS), static_cast<uint32_t>((jj / kXS) & 1)))
+                        atomicCAS(&g_skinny_error, 0, kErrWaitDrain * 1000);
             }
         }
-    } else if (warp < kXWarp) {
-        // ---------------------------------------------- MMA issuers (1..3) --
-        const int me = warp - 1;
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(kBf16, NT);
-            UnitCursor cu = cursor0();
-            int seg = 0;
-            int j = 0;  // this lane's units so far
-            bool failed = false;
-            for (int it = 0; it < iters && !failed; ++seg) {
-                // one segment (the units of one tile) per pass
-                const int seg_len = cu.seg_left(iters);
-                const int d = seg & 1;
-                const uint32_t d_tmem = tmem + kDCol0 + (me * 2 + d) * NT;
-                // the epilogue has drained this accumulator (two segments ago)
-                if (!mbar_wait(dfree(me, d), static_cast<uint32_t>(((seg >> 1) & 1) ^ 1), abort_flag)) {
-                    record_error(kErrWaitMma, abort_flag, dfree(me, d), bar0);
-                    break;
-                }
-                bool mine_first = true, any = false;
-                for (int jj = 0; jj < seg_len; ++jj, ++it, cu.next()) {
-                    if (it % kLanes != me) continue;
-                    const int s = j % kXS;
-                    if (!mbar_wait(xfull(me, s), static_cast<uint32_t>((j / kXS) & 1), abort_flag)) {
-                        record_error(kErrWaitTma, abort_flag, xfull(me, s), bar0);
-                        failed = true;
-                        break;
-                    }
-                    if (!mbar_wait(afull(me), static_cast<uint32_t>(j & 1), abort_flag)) {
-                        record_error(kErrWaitDequant, abort_flag, afull(me), bar0);
-                        failed = true;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t xs = sbase + x_smem(me, s);
+    } else if (warp < kFirstEpilogueWarp) {
+        // ----------------------------------------------------- MMA warps --
+        // Warp w issues the units it with it % 2 == w.  The whole warp runs
+        // the loop (every condition is warp-uniform) and elect.sync picks the
+        // lane that issues and commits.  Both warps walk every unit to keep
+        // the tile segments in step.
+        const int w = warp - kMmaWarp;
+        constexpr uint32_t idesc = idesc_f16(kBf16, NT);
+        UnitCursor cu = cursor0();
+        int seg = 0, jj = 0;
+        int seg_len = iters > 0 ? cu.seg_left(iters) : 0;
+        int ra = w, rx = w;          // slots of this warp's next unit: A (unit % 6), activation (unit % kXS)
+        uint32_t pa = 0, px = 0;     // their phase parities
+        bool mine_in_seg = false;    // this warp has issued into the segment's accumulator
+        bool failed = false;
+        if (w < iters && (!mbar_wait_warp(aready(ra), pa, abort_flag) || !mbar_wait_warp(xfull(rx), px, abort_flag))) {
+            if (lane == 0) record_error(kErrWaitDequant, abort_flag, aready(ra), bar0);
+            failed = true;
+        }
+        for (int it = 0; it < iters && !failed; ++it) {
+            const int d = seg & 1;
+            if (jj == 0 &&
+                !mbar_wait_warp(dfree(d), static_cast<uint32_t>(((seg >> 1) & 1) ^ 1), abort_flag)) {
+                // the epilogue has not drained this accumulator (two segments ago)
+                if (lane == 0) record_error(kErrWaitMma, abort_flag, dfree(d), bar0);
+                break;
+            }
+            if ((it & 1) == w) {
+                // test this warp's next unit (it + 2) now; the answer is used
+                // after this unit's MMAs, which hide the tests' latency
+                const int ran = ra + kMmaWarps >= kAS ? ra + kMmaWarps - kAS : ra + kMmaWarps;
+                const int rxn = rx + kMmaWarps >= kXS ? rx + kMmaWarps - kXS : rx + kMmaWarps;
+                const uint32_t pan = ran < ra ? pa ^ 1u : pa;
+                const uint32_t pxn = rxn < rx ? px ^ 1u : px;
+                const bool more = it + kMmaWarps < iters;
+                const bool next_a = !more || mbar_test_wait(aready(ran), pan);
+                const bool next_x = !more || mbar_test_wait(xfull(rxn), pxn);
+                tc_fence_after();
+                const uint32_t xs = sbase + x_smem(rx);
+                const uint32_t a_tmem = tmem + ra * kAColsPerSlot;  // slot ra = (group ra % 3, A slot ra / 3)
+                const uint32_t d_tmem = tmem + kDCol0 + (w * 2 + d) * NT;
 #pragma unroll
-                    for (int q = 0; q < kBlockK / 16; ++q) {
-                        const uint32_t a_tmem = tmem + me * kAColsPerSlot + q * 8;
-                        const uint64_t b_desc =
-                            smem_desc_sw128_kmajor(xs + (q >> 2) * L::kXBoxBytes + (q & 3) * 32);
-                        mma_f16_ts(d_tmem, a_tmem, b_desc, idesc, !(mine_first && q == 0));
-                    }
-                    mine_first = false;
-                    any = true;
-                    tc_commit(aempty(me));
-                    tc_commit(xempty(me, s));
-                    ++j;
+                for (int q = 0; q < kBlockK / 16; ++q) {
+                    const uint64_t b_desc = smem_desc_sw128_kmajor(xs + (q >> 2) * L::kXBoxBytes + (q & 3) * 32);
+                    mma_f16_ts_warp(d_tmem, a_tmem + q * 8, b_desc, idesc, mine_in_seg || q > 0);
                 }
-                if (failed) break;
-                // the accumulator is ready when this lane's MMAs of the tile are done
-                if (any)
-                    tc_commit(dready(me, d));
-                else
-                    mbar_arrive(dready(me, d));
+                tc_commit_warp(afree(ra));
+                tc_commit_warp(xempty(rx));
+                mine_in_seg = true;
+                ra = ran;
+                rx = rxn;
+                pa = pan;
+                px = pxn;
+                if (more && !__all_sync(0xffffffffu, next_a) && !mbar_wait_warp(aready(ra), pa, abort_flag)) {
+                    if (lane == 0) record_error(kErrWaitDequant, abort_flag, aready(ra), bar0);
+                    failed = true;
+                }
+                if (more && !failed && !__all_sync(0xffffffffu, next_x) &&
+                    !mbar_wait_warp(xfull(rx), px, abort_flag)) {
+                    if (lane == 0) record_error(kErrWaitTma, abort_flag, xfull(rx), bar0);
+                    failed = true;
+                }
             }
-            // every MMA issued above completes before TMEM is released
-            tc_commit(drain(me));
-            if (!mbar_wait_drain(drain(me), 0)) atomicCAS(&g_skinny_error, 0, kErrWaitDrain * 1000);
+            cu.next();
+            if (++jj == seg_len) {
+                // this warp's accumulator is ready when its MMAs of the tile are
+                // done (at once if it had no unit in the tile)
+                if (mine_in_seg) {
+                    tc_commit_warp(dready(w, d));
+                } else if (lane == 0) {
+                    mbar_arrive(dready(w, d));
+                }
+                __syncwarp();
+                mine_in_seg = false;
+                ++seg;
+                jj = 0;
+                if (it + 1 < iters) seg_len = cu.seg_left(iters);
+            }
         }
+        // every MMA issued above completes before TMEM is released
+        tc_commit_warp(drain(w));
+        if (!mbar_wait_drain(drain(w), 0) && lane == 0) atomicCAS(&g_skinny_error, 0, kErrWaitDrain * 1000);
+        __syncwarp();
     } else if (warp < kFirstDequantWarp) {
-        // ------------------------------------------- epilogue (warps 5-8) --
+        // ------------------------------------------- epilogue (warps 4-7) --
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // channel within the tile == TMEM lane
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -426,9 +475,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             it += seg_len;
             for (int jj = 0; jj < seg_len; ++jj) cu.next();
             const int d = seg & 1;
+            int64_t c_lo = 0, c_hi = 0;
+            if (!whole) {
+                c_lo = part.owner(tile * nkb);
+                c_hi = part.owner((tile + 1) * nkb - 1);
+                // every other contributor already arrived: this CTA finishes
+                // the tile from its registers (checked while the MMAs run)
+                if (etid == 0) *last_flag = ld_acquire_gpu(&counters[c_lo]) == static_cast<uint32_t>(c_hi - c_lo);
+            }
             bool ok = true;
-            for (int g = 0; g < kLanes; ++g)
-                ok = mbar_wait_warp(dready(g, d), static_cast<uint32_t>((seg >> 1) & 1), abort_flag) && ok;
+            for (int w = 0; w < kMmaWarps; ++w)
+                ok = mbar_wait_warp(dready(w, d), static_cast<uint32_t>((seg >> 1) & 1), abort_flag) && ok;
             if (!ok) {
                 if (lane == 0) *ep_abort = 1;
                 record_error(kErrWaitMma, abort_flag);
@@ -437,29 +494,67 @@ __global__ void __launch_bounds__(kThreads, 1)
             // by them, before this barrier), so their named barriers stay matched
             epilogue_bar();
             if (*ep_abort) break;
+            const bool early = !whole && *last_flag;
             tc_fence_after();
             const int64_t col = tile * kTileN + r;
             const float sc = col < n ? scales[col] : 0.0f;
             const float b = (bias && col < n) ? bias[col] : 0.0f;
             const int64_t slot = 2 * c + (tile == t_first ? 0 : 1);
             float* mine = slots + slot * ws_slot_floats() + r * kMaxNT;
-            // 16 tokens at a time: sum the lanes' accumulators in a fixed
-            // order, then store y (whole tile) or publish the partial
+            const bool lo_first = !whole && part.begin(c_lo) == tile * nkb;
+            // every contributor after c_lo starts inside this tile (its first
+            // slot); c_lo used its first slot only if it starts exactly at the
+            // tile's first unit
+            auto slot_of = [&](int64_t cc) -> const float4* {
+                const int64_t cs = 2 * cc + ((cc > c_lo || lo_first) ? 0 : 1);
+                return reinterpret_cast<const float4*>(slots + cs * ws_slot_floats() + r * kMaxNT);
+            };
+            // 16 tokens at a time, only as many as there are rows
 #pragma unroll 1
-            for (int h = 0; h < NT / 16; ++h) {
+            for (int h = 0; h < NT / 16 && h * 16 < m_rows; ++h) {
+                // the MMA warps' accumulators, warp 0's first; a warp with no
+                // unit in the segment (a one-unit segment) wrote nothing
                 float acc[16];
 #pragma unroll
                 for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
 #pragma unroll
-                for (int g = 0; g < kLanes; ++g) {
-                    if (!lane_has(g, it0, seg_len)) continue;
+                for (int w = 0; w < kMmaWarps; ++w) {
+                    if (seg_len < kMmaWarps && ((it0 + kMmaWarps - w) % kMmaWarps) >= seg_len) continue;
                     uint32_t v[16];
-                    tmem_ld_x16(lane_addr + kDCol0 + (g * 2 + d) * NT + h * 16, v);
+                    tmem_ld_x16(lane_addr + kDCol0 + (w * 2 + d) * NT + h * 16, v);
                     tmem_wait_ld();
 #pragma unroll
                     for (int q = 0; q < 16; ++q) acc[q] += __uint_as_float(v[q]);
                 }
-                if (whole) {
+                if (whole || early) {
+                    if (early) {
+                        // contributors in CTA order, this CTA's own partial from
+                        // registers: the same sum the publishing path forms
+                        float tot[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) tot[q] = 0.0f;
+                        for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
+                            if (cc == c) {
+#pragma unroll
+                                for (int q = 0; q < 16; ++q) tot[q] += acc[q];
+                                continue;
+                            }
+                            float4 v[4];
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                v[q] = h * 16 + 4 * q < m_rows ? __ldcg(slot_of(cc) + h * 4 + q)
+                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                tot[4 * q] += v[q].x;
+                                tot[4 * q + 1] += v[q].y;
+                                tot[4 * q + 2] += v[q].z;
+                                tot[4 * q + 3] += v[q].w;
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) acc[q] = tot[q];
+                    }
                     if (col < n) {
 #pragma unroll
                         for (int q = 0; q < 16; ++q)
@@ -470,87 +565,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float4* dst = reinterpret_cast<float4*>(mine + h * 16);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                        if (h * 16 + 4 * q < m_rows)
+                            dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
                 }
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0)
-                for (int g = 0; g < kLanes; ++g) mbar_arrive(dfree(g, d));
+            if (lane == 0) mbar_arrive(dfree(d));
 
             if (!whole) {
-                // partial tile: count, and let the last contributor finish it
-                epilogue_bar();
-                const int64_t c_lo = part.owner(tile * nkb);
-                const int64_t c_hi = part.owner((tile + 1) * nkb - 1);
-                if (etid == 0) {
-                    const uint32_t old = arrive_acq_rel(&counters[c_lo]);
-                    const bool is_last = old == static_cast<uint32_t>(c_hi - c_lo);
-                    if (is_last) atomicExch(&counters[c_lo], 0u);
-                    *last_flag = is_last ? 1 : 0;
-                }
-                epilogue_bar();
-                if (*last_flag) {
-                    // every contributor after c_lo starts inside this tile (its
-                    // first slot); c_lo used its first slot only if it starts
-                    // exactly at the tile's first unit
-                    const bool lo_first = part.begin(c_lo) == tile * nkb;
+                if (early) {
+                    // every other contributor has arrived, so nobody else
+                    // touches the counter during this launch
+                    if (etid == 0) counters[c_lo] = 0u;
+                } else {
+                    // publish, count, and let the last contributor finish
+                    epilogue_bar();
+                    if (etid == 0) {
+                        const uint32_t old = arrive_acq_rel(&counters[c_lo]);
+                        const bool is_last = old == static_cast<uint32_t>(c_hi - c_lo);
+                        if (is_last) atomicExch(&counters[c_lo], 0u);
+                        *last_flag = is_last ? 1 : 0;
+                    }
+                    epilogue_bar();
+                    if (*last_flag) {
 #pragma unroll 1
-                    for (int h = 0; h < NT / 16; ++h) {
-                        float acc[16];
+                        for (int h = 0; h < NT / 16 && h * 16 < m_rows; ++h) {
+                            float acc[16];
 #pragma unroll
-                        for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
-                        // contributors in CTA order (the result does not depend on
-                        // which CTA arrives last), kFixupBatch at a time
-                        for (int64_t cb = c_lo; cb <= c_hi; cb += kFixupBatch) {
-                            float4 v[kFixupBatch][4];
+                            for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
+                            // contributors in CTA order, kFixupBatch at a time
+                            for (int64_t cb = c_lo; cb <= c_hi; cb += kFixupBatch) {
+                                float4 v[kFixupBatch][4];
 #pragma unroll
-                            for (int e = 0; e < kFixupBatch; ++e) {
-                                const int64_t cc = cb + e;
-                                if (cc <= c_hi) {
-                                    const int64_t cs = 2 * cc + ((cc > c_lo || lo_first) ? 0 : 1);
-                                    const float4* src = reinterpret_cast<const float4*>(
-                                        slots + cs * ws_slot_floats() + r * kMaxNT + h * 16);
+                                for (int e = 0; e < kFixupBatch; ++e) {
+                                    const int64_t cc = cb + e;
 #pragma unroll
-                                    for (int q = 0; q < 4; ++q) v[e][q] = __ldcg(src + q);
-                                } else {
+                                    for (int q = 0; q < 4; ++q)
+                                        v[e][q] = (cc <= c_hi && h * 16 + 4 * q < m_rows)
+                                                      ? __ldcg(slot_of(cc) + h * 4 + q)
+                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                                }
 #pragma unroll
-                                    for (int q = 0; q < 4; ++q) v[e][q] = make_float4(0.f, 0.f, 0.f, 0.f);
+                                for (int e = 0; e < kFixupBatch; ++e) {
+                                    if (cb + e > c_hi) break;
+#pragma unroll
+                                    for (int q = 0; q < 4; ++q) {
+                                        acc[4 * q] += v[e][q].x;
+                                        acc[4 * q + 1] += v[e][q].y;
+                                        acc[4 * q + 2] += v[e][q].z;
+                                        acc[4 * q + 3] += v[e][q].w;
+                                    }
                                 }
                             }
+                            if (col < n) {
 #pragma unroll
-                            for (int e = 0; e < kFixupBatch; ++e) {
-#pragma unroll
-                                for (int q = 0; q < 4; ++q) {
-                                    acc[4 * q] += v[e][q].x;
-                                    acc[4 * q + 1] += v[e][q].y;
-                                    acc[4 * q + 2] += v[e][q].z;
-                                    acc[4 * q + 3] += v[e][q].w;
-                                }
+                                for (int q = 0; q < 16; ++q)
+                                    if (h * 16 + q < m_rows)
+                                        y[static_cast<int64_t>(h * 16 + q) * n + col] =
+                                            round_out<kBf16>(fmaf(acc[q], sc, b));
                             }
-                        }
-                        if (col < n) {
-#pragma unroll
-                            for (int q = 0; q < 16; ++q)
-                                if (h * 16 + q < m_rows)
-                                    y[static_cast<int64_t>(h * 16 + q) * n + col] =
-                                        round_out<kBf16>(fmaf(acc[q], sc, b));
                         }
                     }
                 }
+                // last_flag is rewritten at the next split segment
                 epilogue_bar();
             }
         }
     } else {
-        // ------------------------------- dequantising warpgroups (9-20) --
+        // ------------------------------- dequantising warpgroups (8-19) --
         const int group = (warp - kFirstDequantWarp) >> 2;
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
-        const uint32_t a_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + group * kAColsPerSlot;
-        int j = 0;  // this lane's units so far
-        for (int it = group; it < iters; it += kLanes, ++j) {
-            const int s = j % kCS;
-            if (!mbar_wait_warp(cfull(group, s), static_cast<uint32_t>((j / kCS) & 1), abort_flag)) {
+        const uint32_t a_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        int s = 0;         // == j % kCS
+        uint32_t ph = 0;   // == (j / kCS) & 1
+        for (int j = 0, it = group; it < iters; it += kLanes, ++j) {
+            if (!mbar_wait_warp(cfull(group, s), ph, abort_flag)) {
                 record_error(kErrWaitTma, abort_flag, cfull(group, s), bar0);
                 break;
             }
@@ -560,16 +651,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 8; ++q) cw[q] = *reinterpret_cast<const uint4*>(row + ((q ^ (r & 7)) << 4));
             __syncwarp();
             if (lane == 0) mbar_arrive(cempty(group, s));
-            // the first half is converted while the lane's previous MMAs may
-            // still be reading the A slot
+            if (++s == kCS) {
+                s = 0;
+                ph ^= 1u;
+            }
+            // the first half is converted while the MMAs may still read the slot
             uint32_t v0[4][8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) dequant16<kBf16>(cw[q], v0[q]);
-            if (!mbar_wait_warp(aempty(group), static_cast<uint32_t>((j & 1) ^ 1), abort_flag)) {
-                record_error(kErrWaitMma, abort_flag, aempty(group), bar0);
+            // A slot of unit it = group + 3j: it % 6 = group + 3 (j % 2)
+            const int r = group + kLanes * (j & 1);
+            if (!mbar_wait_warp(afree(r), static_cast<uint32_t>(((j >> 1) & 1) ^ 1), abort_flag)) {
+                record_error(kErrWaitMma, abort_flag, afree(r), bar0);
                 break;
             }
             tc_fence_after();
+            const uint32_t a_addr = a_lane + r * kAColsPerSlot;
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_st_x8(a_addr + q * 8, v0[q]);
 #pragma unroll
@@ -581,12 +678,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(afull(group));
+            if (lane == 0) mbar_arrive(aready(r));
         }
     }
 
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
