@@ -54,10 +54,12 @@ static size_t skinny_ws(void) {
     return fp8w::skinny_workspace_size(sms);
 }
 
+// m == 1 runs the GEMV unless its x does not fit in shared memory.
+static bool use_gemv(int64_t m, int64_t k) { return m == 1 && fp8w::gemv_supports(k); }
+
 size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k) {
     (void)n;
-    (void)k;
-    return m == 1 ? 0 : skinny_ws();
+    return use_gemv(m, k) ? 0 : skinny_ws();
 }
 
 fp8w_status fp8w_linear_ex(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
@@ -66,8 +68,8 @@ fp8w_status fp8w_linear_ex(const void* x, int act_dtype, int64_t m, int64_t k, c
     fp8w_status st = check_linear(x, act_dtype, m, k, codes, scales, bias, n, y);
     if (st != FP8W_OK) return st;
     int kernel = config ? config->kernel : FP8W_KERNEL_AUTO;
-    if (kernel == FP8W_KERNEL_AUTO) kernel = (m == 1) ? FP8W_KERNEL_GEMV : FP8W_KERNEL_SKINNY;
-    if (kernel == FP8W_KERNEL_GEMV && m != 1) return FP8W_ERR_CONFIG;
+    if (kernel == FP8W_KERNEL_AUTO) kernel = use_gemv(m, k) ? FP8W_KERNEL_GEMV : FP8W_KERNEL_SKINNY;
+    if (kernel == FP8W_KERNEL_GEMV && !use_gemv(m, k)) return FP8W_ERR_CONFIG;
     if (kernel != FP8W_KERNEL_GEMV && kernel != FP8W_KERNEL_SKINNY) return FP8W_ERR_CONFIG;
     const int ctas = config ? config->ctas : 0;
     if (ctas < 0 || (ctas != 0 && kernel == FP8W_KERNEL_GEMV)) return FP8W_ERR_CONFIG;
@@ -99,7 +101,7 @@ fp8w_status fp8w_linear_noalloc(const void* x, int act_dtype, int64_t m, int64_t
     if (st != FP8W_OK) return st;
     fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, scales, bias, y};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (m == 1) return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear_noalloc gemv launch");
+    if (use_gemv(m, k)) return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear_noalloc gemv launch");
     const size_t need = skinny_ws();
     if (need == 0) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear_noalloc device query");
     if (need > fp8w::static_scratch_bytes()) return FP8W_ERR_SCRATCH;

@@ -21,8 +21,9 @@ struct LinearArgs {
 cudaError_t launch_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes, float* scales,
                             cudaStream_t st);
 
-// K2: m == 1.
+// K2: m == 1, k <= 32768 (gemv_supports).
 cudaError_t launch_gemv(const LinearArgs& a, cudaStream_t st);
+bool gemv_supports(int64_t k);
 
 // K3: any m (32-row slabs, one launch each); needs a workspace of
 // skinny_workspace_size(sms) bytes, zero-filled before its first use.

@@ -1,26 +1,34 @@
 // gemv.cu -- kernel K2: the M = 1 linear layer (GEMV) on CUDA cores.
 //
 // Page "kadirnar/kernel-agent fp8-weights", section "Dequantise in
-// registers": the codes are streamed once past L1, each pair is converted
-// to f16x2 by the hardware e4m3x2 conversion (exact) and widened to fp32,
-// fp32 FMA against x, a shuffle reduction, scale (and bias) applied once per
-// output in the epilogue.
+// registers": the codes are streamed once past L1, converted in registers
+// (exactly), multiplied by x with fp32 accumulation, reduced across a warp
+// with shuffles, and scale (and bias) are applied once per output in the
+// epilogue.
 //
 // GB300 layout of the work:
 //  * Persistent grid, one CTA per SM; CTA c owns the contiguous rows
 //    [c*N/P, (c+1)*N/P), so every SM streams the same bytes (+-1 row).
-//  * The last warp moves R whole rows per stage (R*K contiguous bytes) with
-//    one 1-D TMA bulk copy into a shared-memory ring of ~160 KB, so ~160 KB
-//    per SM is in flight without occupying registers.
-//  * 16 compute warps (512 threads).  A row's 16-code chunks are spread over
-//    T_row threads (G = 512 / T_row row groups work on different rows);
-//    each thread keeps its chunks of x in fp32 registers for the whole
-//    kernel, so after start-up the codes are the only HBM stream.
-//  * Per stage, each group reduces its rows with a transposing shuffle tree
-//    and shared memory; one thread per row applies scale and bias.
+//  * The last warp moves a slot of R whole rows (R*K contiguous bytes, up
+//    to 64 KB) per 1-D TMA bulk copy into a ring of slots.  A bulk copy costs
+//    the SM's TMA unit a fixed ~0.27 us whatever its size (measured: 4 KB
+//    copies stream 15 GB/s per SM, 64 KB copies 218 GB/s), so copies are
+//    large.
+//  * The CTA's rows are dealt round-robin to the 16 compute warps; a warp
+//    computes its row whole (lane l takes 16-code chunks l, l+32, ...), so
+//    no reduction crosses warps.  Every warp waits for every slot in order
+//    and arrives once on its "empty" barrier after its rows there (none, if
+//    the slot has fewer rows than warps): a warp whose next row lay several
+//    slots ahead would otherwise wait on a slot a full ring cycle early and
+//    pass on the previous phase of the same parity.
+//  * x is staged once in shared memory (as 16-bit values), and so are the
+//    CTA's scales and bias: after start-up the codes are the only stream.
+//  * Codes are converted exactly by the hardware e4m3x2 -> f16x2 conversion
+//    and widened to fp32, x is widened from its 16-bit pair, and each product
+//    is an fp32 FMA.
+//  * A row's partial sums are reduced with a shuffle tree; one lane applies
+//    fmaf(acc, scale, bias) and rounds once.
 // HBM bytes per output channel: K (codes) + 4 (scale) + 4 (bias) + 2 (y).
-// K > 16384 (a row longer than a stage) runs the chunked variant at the end
-// of this file.
 #include <mutex>
 
 #include "fp8w_device.cuh"
@@ -30,89 +38,22 @@ namespace fp8w {
 
 static __device__ int g_gemv_error;
 
-constexpr int kGemvComputeThreads = 512;
-constexpr int kGemvThreads = kGemvComputeThreads + 32;
-constexpr int kGemvRingBytes = 160 * 1024;
-constexpr int kGemvMaxRowsPerStage = 32;
-constexpr int kGemvMaxStages = 16;
-constexpr int kGemvMaxK = 16384;
+constexpr int kGemvWarps = 16;                       // compute warps
+constexpr int kGemvThreads = 32 * (kGemvWarps + 1);  // + the producer warp
+constexpr int kGemvMaxSlots = 8;
+constexpr uint32_t kGemvSlotTarget = 64 * 1024;      // bytes per bulk copy, up to
+constexpr int kGemvStagedRows = 2048;                // rows whose scale and bias are staged
+constexpr uint32_t kGemvSmemBudget = 224 * 1024;
+// Largest K the GEMV takes: x (2 bytes a value) and two 64 KB slots fit
+// beside the staged scales.
+constexpr int64_t kGemvMaxK = 32768;
 
-// Reduce R per-thread values across a warp.  On return, lane l holds the
-// warp total of row l / (32 / R) if l % (32 / R) == 0.
-template <int R>
-__device__ __forceinline__ float warp_reduce_rows(float (&p)[R]) {
-    const int lane = threadIdx.x & 31;
-    float v[R];
-#pragma unroll
-    for (int i = 0; i < R; ++i) v[i] = p[i];
-    int count = R;
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-        if (count > 1) {
-            const bool upper = (lane & off) != 0;
-            const int half = count / 2;
-#pragma unroll
-            for (int i = 0; i < R / 2; ++i) {
-                if (i < half) {
-                    const float send = upper ? v[i] : v[i + half];
-                    const float keep = upper ? v[i + half] : v[i];
-                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-                }
-            }
-            count = half;
-        } else {
-            v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
-        }
-    }
-    return v[0];
-}
-
-// x chunk (16 activations) -> fp32 registers.
-template <bool kBf16>
-__device__ __forceinline__ void load_x_chunk(const uint16_t* x, int64_t chunk, float (&xr)[16]) {
-    const uint4* p = reinterpret_cast<const uint4*>(x + chunk * 16);
-    const uint4 a = __ldg(p), b = __ldg(p + 1);
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        if constexpr (kBf16) {
-            xr[2 * i] = bf16_lo_to_f32(w[i]);
-            xr[2 * i + 1] = bf16_hi_to_f32(w[i]);
-        } else {
-            xr[2 * i] = f16_lo_to_f32(w[i]);
-            xr[2 * i + 1] = f16_hi_to_f32(w[i]);
-        }
-    }
-}
-
-// f16x2 -> two fp32 (halves selected in the register, no extraction).
-__device__ __forceinline__ void f16x2_to_f32x2(uint32_t h, float& lo, float& hi) {
-    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(h));
-}
-
-// acc += sum over 16 codes of x * e4m3(code).
-__device__ __forceinline__ float dot16(const uint4 c, const float (&xr)[16], float acc) {
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t h01, h23;
-        e4m3x4_to_f16x2(w[q], h01, h23);
-        float a, b, c2, d;
-        f16x2_to_f32x2(h01, a, b);
-        f16x2_to_f32x2(h23, c2, d);
-        acc = fmaf(xr[4 * q + 0], a, acc);
-        acc = fmaf(xr[4 * q + 1], b, acc);
-        acc = fmaf(xr[4 * q + 2], c2, acc);
-        acc = fmaf(xr[4 * q + 3], d, acc);
-    }
-    return acc;
-}
-
-__device__ __forceinline__ void compute_bar() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kGemvComputeThreads) : "memory");
-}
+struct GemvGeom {
+    int rows;         // rows per slot (R)
+    int slots;        // slots in the ring (S)
+    uint32_t slot_bytes;
+    uint32_t ring_bytes;
+};
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t pol) {
     asm volatile(
@@ -121,70 +62,101 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
-struct GemvGeom {
-    int rows_per_stage;  // R
-    int stages;          // S
-    int t_row;           // threads per row
-    int groups;          // 512 / t_row
-    uint32_t stage_bytes;
-};
+// f16x2 -> two fp32 (the halves selected in the register, no extraction).
+__device__ __forceinline__ void f16x2_to_f32x2(uint32_t h, float& lo, float& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h));
+}
 
-// C = chunks per thread, RPG = rows per group per stage (R / groups).
-template <int C, int RPG, bool kBf16>
+// One 16-code chunk against its 16 activations (8 packed 16-bit pairs),
+// into two accumulators for instruction-level parallelism.
+template <bool kBf16>
+__device__ __forceinline__ void dot_chunk(const uint4 c, const uint4 xa, const uint4 xb, float& a0, float& a1) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+    const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t h01, h23;
+        e4m3x4_to_f16x2(w[q], h01, h23);
+        float v0, v1, v2, v3;
+        f16x2_to_f32x2(h01, v0, v1);
+        f16x2_to_f32x2(h23, v2, v3);
+        float x0, x1, x2, x3;
+        if constexpr (kBf16) {
+            x0 = bf16_lo_to_f32(xw[2 * q]);
+            x1 = bf16_hi_to_f32(xw[2 * q]);
+            x2 = bf16_lo_to_f32(xw[2 * q + 1]);
+            x3 = bf16_hi_to_f32(xw[2 * q + 1]);
+        } else {
+            f16x2_to_f32x2(xw[2 * q], x0, x1);
+            f16x2_to_f32x2(xw[2 * q + 1], x2, x3);
+        }
+        a0 = fmaf(x0, v0, a0);
+        a1 = fmaf(x1, v1, a1);
+        a0 = fmaf(x2, v2, a0);
+        a1 = fmaf(x3, v3, a1);
+    }
+}
+
+template <bool kBf16>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes, const float* __restrict__ scales,
                 const float* __restrict__ bias, uint16_t* __restrict__ y, int64_t n, int64_t k, GemvGeom geo) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const uint32_t ring = smem_u32(smem);
-    const uint32_t bar_full = ring + kGemvRingBytes;                 // [S]
-    const uint32_t bar_empty = bar_full + 8 * kGemvMaxStages;       // [S]
-    float* red = reinterpret_cast<float*>(smem + kGemvRingBytes + 16 * kGemvMaxStages);  // [R][16 warps]
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kGemvMaxRowsPerStage * 16);
-    // written only by compute threads before a compute barrier, so they all
-    // read the same value after it and leave the loop together
-    volatile int* cmp_abort = abort_flag + 1;
+    const int S = geo.slots, R = geo.rows;
+    // layout: ring | x [k] | scales, bias [kGemvStagedRows] | full, empty [kGemvMaxSlots] | abort flag
+    const uint32_t x_bytes = static_cast<uint32_t>(((k * 2 + 127) / 128) * 128);
+    uint16_t* xs = reinterpret_cast<uint16_t*>(smem + geo.ring_bytes);
+    float* sc_s = reinterpret_cast<float*>(smem + geo.ring_bytes + x_bytes);
+    float* bi_s = sc_s + kGemvStagedRows;
+    const uint32_t bar_full = smem_u32(bi_s + kGemvStagedRows);
+    const uint32_t bar_empty = bar_full + 8 * kGemvMaxSlots;
+    auto full = [&](int s) { return bar_full + 8u * s; };
+    auto empty = [&](int s) { return bar_empty + 8u * s; };
+    volatile int* abort_flag =
+        reinterpret_cast<volatile int*>(smem + geo.ring_bytes + x_bytes + 8 * kGemvStagedRows + 16 * kGemvMaxSlots);
 
-    const int S = geo.stages, R = geo.rows_per_stage;
     const int64_t P = gridDim.x;
     const int64_t row0 = blockIdx.x * n / P, row1 = (blockIdx.x + 1) * n / P;
-    const int64_t nst = (row1 - row0 + R - 1) / R;
-    const int warp = threadIdx.x >> 5;
-    const int nwarps_compute = kGemvComputeThreads / 32;
+    const int64_t nrows = row1 - row0;
+    const int64_t nslots = (nrows + R - 1) / R;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
-            mbar_init(bar_empty + 8 * s, nwarps_compute);
+    if (warp == kGemvWarps) {
+        for (int i = lane; i < S; i += 32) {
+            mbar_init(full(i), 1);
+            mbar_init(empty(i), kGemvWarps);  // one arrival per compute warp
         }
-        *abort_flag = 0;
-        *cmp_abort = 0;
+        if (lane == 0) *abort_flag = 0;
         fence_mbar_init();
     }
     __syncthreads();
-    // the next kernel in the stream may start its prologue; it waits for
-    // this grid before touching global memory
+    // the next kernel in the stream may start its set-up; it waits for this
+    // grid before touching global memory
     pdl_launch_dependents();
 
-    if (warp == nwarps_compute) {
+    if (warp == kGemvWarps) {
         // ---------------------------------------------------- producer --
-        if ((threadIdx.x & 31) == 0) {
+        if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             pdl_wait();  // the codes may come from the previous kernel
             int64_t issued = 0;
             int s = 0;
-            uint32_t ph = 0;  // stage slot and its phase, advanced without division
-            for (int64_t st = 0; st < nst; ++st) {
-                if (!mbar_wait(bar_empty + 8 * s, ph ^ 1u, abort_flag)) {
+            uint32_t ph = 0;
+            for (int64_t sl = 0; sl < nslots; ++sl) {
+                if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) {
                     *abort_flag = 1;
                     atomicCAS(&g_gemv_error, 0, kErrWaitSlot);
                     break;
                 }
-                const int64_t r0 = row0 + st * R;
+                const int64_t r0 = row0 + sl * R;
                 const int64_t rows = (row1 - r0) < R ? (row1 - r0) : R;
                 const uint32_t bytes = static_cast<uint32_t>(rows * k);
-                mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
-                bulk_load(ring + s * geo.stage_bytes, codes + r0 * k, bytes, bar_full + 8 * s, pol);
+                mbar_arrive_expect_tx(full(s), bytes);
+                bulk_load(ring + s * geo.slot_bytes, codes + r0 * k, bytes, full(s), pol);
                 ++issued;
                 if (++s == S) {
                     s = 0;
@@ -192,8 +164,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                 }
             }
             if (*abort_flag) {
-                for (int64_t st = (issued > S ? issued - S : 0); st < issued; ++st)
-                    if (!mbar_wait_drain(bar_full + 8 * (st % S), static_cast<uint32_t>((st / S) & 1)))
+                // let the copies in flight land before the CTA exits
+                for (int64_t j = (issued > S ? issued - S : 0); j < issued; ++j)
+                    if (!mbar_wait_drain(full(static_cast<int>(j % S)), static_cast<uint32_t>((j / S) & 1)))
                         atomicCAS(&g_gemv_error, 0, kErrWaitDrain);
             }
         }
@@ -201,125 +174,102 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
 
     // -------------------------------------------------------- compute --
-    const int t = threadIdx.x;
-    const int g = t / geo.t_row, tr = t % geo.t_row;
-    const int lane = t & 31;
+    pdl_wait();  // x, scales and bias may come from the previous kernel, y may still be read by it
     const int64_t nchunks = k >> 4;
-    pdl_wait();  // x, scales and bias may come from the previous kernel, and y may still be read by it
-    float xr[C][16];
-#pragma unroll
-    for (int j = 0; j < C; ++j) {
-        const int64_t ch = tr + static_cast<int64_t>(geo.t_row) * j;
-        if (ch < nchunks) {
-            load_x_chunk<kBf16>(x, ch, xr[j]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 16; ++e) xr[j][e] = 0.0f;
+    {
+        const uint4* xg = reinterpret_cast<const uint4*>(x);
+        uint4* xd = reinterpret_cast<uint4*>(xs);
+        for (int64_t i = threadIdx.x; i < nchunks * 2; i += 32 * kGemvWarps) xd[i] = __ldg(xg + i);
+    }
+    const bool staged = nrows <= kGemvStagedRows;
+    if (staged) {
+        for (int64_t i = threadIdx.x; i < nrows; i += 32 * kGemvWarps) {
+            sc_s[i] = scales[row0 + i];
+            bi_s[i] = bias ? bias[row0 + i] : 0.0f;
         }
     }
-    const int warps_per_row = geo.t_row >> 5;
-    const int warp_in_group = (t % geo.t_row) >> 5;
+    // the staged x, scales and bias are visible to every compute warp
+    asm volatile("bar.sync %0, %1;" ::"n"(1), "n"(32 * kGemvWarps) : "memory");
+
+    const uint4* xv = reinterpret_cast<const uint4*>(xs);
     int s = 0;
     uint32_t ph = 0;
-    for (int64_t st = 0; st < nst; ++st) {
-        const int64_t r0 = row0 + st * R;
-        // the epilogue threads fetch their row's scale and bias before the
-        // stage's data arrives, off the critical path
-        float sc = 0.0f, b = 0.0f;
-        if (t < R && r0 + t < row1) {
-            sc = scales[r0 + t];
-            b = bias ? bias[r0 + t] : 0.0f;
+    for (int64_t sl = 0; sl < nslots; ++sl) {
+        if (!mbar_wait_warp(full(s), ph, abort_flag)) {
+            if (lane == 0) {
+                *abort_flag = 1;
+                atomicCAS(&g_gemv_error, 0, kErrWaitTma);
+            }
+            break;
         }
-        if (!mbar_wait_warp(bar_full + 8 * s, ph, abort_flag)) {
-            *cmp_abort = 1;
-            *abort_flag = 1;
-            atomicCAS(&g_gemv_error, 0, kErrWaitTma);
-        }
-        compute_bar();
-        if (*cmp_abort) break;
-        const uint8_t* stage = smem + s * geo.stage_bytes;
-        float p[RPG];
-#pragma unroll
-        for (int i = 0; i < RPG; ++i) {
-            p[i] = 0.0f;
-            const int rr = g + i * geo.groups;  // row within the stage
-            if (r0 + rr < row1) {
-                const uint8_t* rowp = stage + static_cast<int64_t>(rr) * k;
-#pragma unroll
-                for (int j = 0; j < C; ++j) {
-                    const int64_t ch = tr + static_cast<int64_t>(geo.t_row) * j;
-                    if (ch < nchunks) p[i] = dot16(*reinterpret_cast<const uint4*>(rowp + ch * 16), xr[j], p[i]);
+        const int64_t base = sl * R;  // CTA-local index of the slot's first row
+        const int rows = static_cast<int>((nrows - base) < R ? (nrows - base) : R);
+        // rows i = base + r with i % kGemvWarps == warp
+        for (int r = static_cast<int>((warp - base % kGemvWarps + kGemvWarps) % kGemvWarps); r < rows;
+             r += kGemvWarps) {
+            const int64_t i = base + r;
+            const int64_t row = row0 + i;
+            float sc = 0.0f, bi = 0.0f;
+            if (lane == 0) {
+                if (staged) {
+                    sc = sc_s[i];
+                    bi = bi_s[i];
+                } else {
+                    sc = scales[row];
+                    bi = bias ? bias[row] : 0.0f;
                 }
             }
+            const uint8_t* rowp = smem + s * geo.slot_bytes + static_cast<int64_t>(r) * k;
+            float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll 4
+            for (int64_t ch = lane; ch < nchunks; ch += 32)
+                dot_chunk<kBf16>(*reinterpret_cast<const uint4*>(rowp + ch * 16), xv[2 * ch], xv[2 * ch + 1], a0, a1);
+            float acc = a0 + a1;
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (lane == 0) y[row] = round_out<kBf16>(fmaf(acc, sc, bi));
         }
+        // this warp has read its rows of the slot
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+        if (lane == 0) mbar_arrive(empty(s));
         if (++s == S) {
             s = 0;
             ph ^= 1u;
         }
-        const float wsum = warp_reduce_rows<RPG>(p);
-        constexpr int kStride = 32 / RPG;
-        if ((lane % kStride) == 0) red[(g + (lane / kStride) * geo.groups) * 16 + warp_in_group] = wsum;
-        compute_bar();
-        if (t < R) {
-            const int64_t row = r0 + t;
-            if (row < row1) {
-                float acc = 0.0f;
-                for (int w = 0; w < warps_per_row; ++w) acc += red[t * 16 + w];
-                y[row] = round_out<kBf16>(fmaf(acc, sc, b));
-            }
-        }
-        // red is rewritten only after the next stage's first compute_bar
     }
 }
 
-// ------------------------------------------------ long rows (K > 16384) --
-// Rows longer than a stage: one warp-contiguous pass per row, x re-read
-// from L2 per row (correct, not tuned).
+static uint32_t gemv_fixed_bytes(int64_t k) {
+    return static_cast<uint32_t>(((k * 2 + 127) / 128) * 128) + 8 * kGemvStagedRows + 16 * kGemvMaxSlots + 16 + 128;
+}
+
 template <bool kBf16>
-__global__ void __launch_bounds__(256) gemv_long_kernel(const uint16_t* __restrict__ x,
-                                                        const uint8_t* __restrict__ codes,
-                                                        const float* __restrict__ scales,
-                                                        const float* __restrict__ bias, uint16_t* __restrict__ y,
-                                                        int64_t n, int64_t k) {
-    __shared__ float red[8];
-    const int64_t nchunks = k >> 4;
-    for (int64_t row = blockIdx.x; row < n; row += gridDim.x) {
-        float acc = 0.0f;
-        for (int64_t ch = threadIdx.x; ch < nchunks; ch += 256) {
-            float xr[16];
-            load_x_chunk<kBf16>(x, ch, xr);
-            acc = dot16(ldg_stream_v4(codes + row * k + ch * 16), xr, acc);
-        }
-        float v[1] = {acc};
-        const float wsum = warp_reduce_rows<1>(v);
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = wsum;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float s = 0.0f;
-            for (int w = 0; w < 8; ++w) s += red[w];
-            const float b = bias ? bias[row] : 0.0f;
-            y[row] = round_out<kBf16>(fmaf(s, scales[row], b));
-        }
-        __syncthreads();
-    }
-}
+static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
+    int sms = 0;
+    cudaError_t e = device_sm_count(sms);
+    if (e != cudaSuccess) return e;
+    if (a.k > kGemvMaxK) return cudaErrorNotSupported;
+    GemvGeom geo;
+    // a slot holds whole rows, up to kGemvSlotTarget bytes
+    int64_t rows = kGemvSlotTarget / a.k;
+    if (rows < 1) rows = 1;
+    geo.rows = static_cast<int>(rows);
+    geo.slot_bytes = static_cast<uint32_t>(((rows * a.k + 127) / 128) * 128);
+    int64_t slots = (kGemvSmemBudget - gemv_fixed_bytes(a.k)) / geo.slot_bytes;
+    if (slots > kGemvMaxSlots) slots = kGemvMaxSlots;
+    if (slots < 2) return cudaErrorNotSupported;
+    geo.slots = static_cast<int>(slots);
+    geo.ring_bytes = geo.slots * geo.slot_bytes;
+    const uint32_t smem = geo.ring_bytes + gemv_fixed_bytes(a.k);
 
-static constexpr uint32_t gemv_smem_bytes() {
-    return kGemvRingBytes + 16 * kGemvMaxStages + kGemvMaxRowsPerStage * 16 * 4 + 16 + 128;  // + flags, align
-}
-
-template <int C, int RPG, bool kBf16>
-static cudaError_t launch_cfg(const LinearArgs& a, const GemvGeom& geo, int sms, cudaStream_t st) {
-    auto kern = gemv_kernel<C, RPG, kBf16>;
+    auto kern = gemv_kernel<kBf16>;
     static std::once_flag attr_once[64];
     int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, gemv_smem_bytes());
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvSmemBudget);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t grid = a.n < sms ? a.n : sms;
@@ -330,7 +280,7 @@ static cudaError_t launch_cfg(const LinearArgs& a, const GemvGeom& geo, int sms,
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kGemvThreads);
-    cfg.dynamicSmemBytes = gemv_smem_bytes();
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -338,43 +288,7 @@ static cudaError_t launch_cfg(const LinearArgs& a, const GemvGeom& geo, int sms,
                               static_cast<uint16_t*>(a.y), a.n, a.k, geo);
 }
 
-template <bool kBf16>
-static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
-    int sms = 0;
-    cudaError_t e = device_sm_count(sms);
-    if (e != cudaSuccess) return e;
-    if (a.k > kGemvMaxK) {
-        const int64_t grid = a.n < 4 * sms ? a.n : 4 * sms;
-        gemv_long_kernel<kBf16><<<static_cast<unsigned>(grid), 256, 0, st>>>(
-            static_cast<const uint16_t*>(a.x), a.codes, a.scales, a.bias, static_cast<uint16_t*>(a.y), a.n, a.k);
-        return cudaGetLastError();
-    }
-    const int64_t nchunks = a.k / 16;
-    GemvGeom geo;
-    geo.t_row = static_cast<int>(nchunks >= kGemvComputeThreads ? kGemvComputeThreads : ((nchunks + 31) / 32) * 32);
-    // t_row must divide 512: round up to 32, 64, 128, 256 or 512
-    int tr = 32;
-    while (tr < geo.t_row) tr *= 2;
-    geo.t_row = tr;
-    geo.groups = kGemvComputeThreads / geo.t_row;
-    // ~16 KB per stage: rows = groups x (1, 2 or 4), at most 32
-    int64_t target = 16384 / a.k;
-    if (target > kGemvMaxRowsPerStage) target = kGemvMaxRowsPerStage;
-    int rpg_sel = 1;
-    while (rpg_sel < 4 && static_cast<int64_t>(geo.groups) * rpg_sel * 2 <= target) rpg_sel *= 2;
-    const int rows = geo.groups * rpg_sel;
-    geo.rows_per_stage = rows;
-    geo.stage_bytes = static_cast<uint32_t>(((rows * a.k + 127) / 128) * 128);
-    geo.stages = static_cast<int>(kGemvRingBytes / geo.stage_bytes);
-    if (geo.stages > kGemvMaxStages) geo.stages = kGemvMaxStages;
-    const int rpg = rows / geo.groups;
-    const int c = static_cast<int>((nchunks + geo.t_row - 1) / geo.t_row);
-    if (c == 1 && rpg == 1) return launch_cfg<1, 1, kBf16>(a, geo, sms, st);
-    if (c == 1 && rpg == 2) return launch_cfg<1, 2, kBf16>(a, geo, sms, st);
-    if (c == 1 && rpg == 4) return launch_cfg<1, 4, kBf16>(a, geo, sms, st);
-    if (c == 2 && rpg == 1) return launch_cfg<2, 1, kBf16>(a, geo, sms, st);
-    return cudaErrorNotSupported;
-}
+bool gemv_supports(int64_t k) { return k <= kGemvMaxK; }
 
 cudaError_t launch_gemv(const LinearArgs& a, cudaStream_t st) {
     return a.act == 1 ? launch_dt<true>(a, st) : launch_dt<false>(a, st);

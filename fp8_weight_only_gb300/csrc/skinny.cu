@@ -15,10 +15,11 @@
 //    count (stream-K).  A tile that straddles CTAs is finished by the last
 //    contributor: partial fp32 tiles go to a caller-provided workspace and
 //    are summed in CTA order (deterministic); nothing waits on another CTA.
-//    A CTA runs the partial piece at the end of its range first, so by the
-//    time it finishes the piece at the start of its range the other
-//    contributors are usually done, and it sums their partials straight
-//    from its registers without publishing its own.
+//    A CTA takes its units in order, so the piece at the start of its range
+//    (the end of a tile another CTA began) is done first and published
+//    early; the CTA holding the start of that tile finishes it last and, as
+//    every other contributor has arrived by then, sums their partials
+//    straight from its registers without publishing its own.
 //  * Warp 0 streams each unit's 128 x 128 code tile with TMA (128-byte
 //    swizzle; rows past N and k past K read as zeros) into the code ring of
 //    one of three dequantising warpgroups (units are dealt round-robin);
@@ -154,27 +155,20 @@ struct Partition {
     }
 };
 
-// Walks a CTA's units in processing order without divisions: (tile, kb) of
-// the current unit; after the moved piece [t_last*nkb, u1) it jumps to u0.
+// Walks a CTA's units in order without divisions: (tile, kb) of the current
+// unit.
 struct UnitCursor {
-    int it, len0;
+    int it;
     int tile, kb, nkb;
-    int tile0, kb0;  // position of u0
     __device__ __forceinline__ void next() {
         ++it;
-        if (it == len0) {
-            tile = tile0;
-            kb = kb0;
-        } else if (++kb == nkb) {
+        if (++kb == nkb) {
             kb = 0;
             ++tile;
         }
     }
-    // units left in the current tile within the current piece
-    __device__ __forceinline__ int seg_left(int iters) const {
-        const int piece_end = it < len0 ? len0 : iters;
-        return min(nkb - kb, piece_end - it);
-    }
+    // units left in the current tile within the CTA's range
+    __device__ __forceinline__ int seg_left(int iters) const { return min(nkb - kb, iters - it); }
 };
 
 template <bool kBf16>
@@ -245,21 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t c = blockIdx.x;
     const int64_t u0 = part.begin(c), u1 = part.begin(c + 1);
     const int iters = static_cast<int>(u1 - u0);
-    // Processing order: when the range ends inside a tile, that partial
-    // piece [t_last*nkb, u1) runs first, then the rest from u0.
-    const int64_t t_first = u0 / nkb, t_last = (u1 - 1) / nkb;
+    const int64_t t_first = u0 / nkb;
     const int kb_first = static_cast<int>(u0 - t_first * nkb);
-    const bool moved = t_last > t_first && (u1 % nkb) != 0;
-    const int len0 = moved ? static_cast<int>(u1 - t_last * nkb) : 0;
     auto cursor0 = [=]() {
         UnitCursor cu;
         cu.it = 0;
-        cu.len0 = len0;
         cu.nkb = static_cast<int>(nkb);
-        cu.tile0 = static_cast<int>(t_first);
-        cu.kb0 = kb_first;
-        cu.tile = moved ? static_cast<int>(t_last) : static_cast<int>(t_first);
-        cu.kb = moved ? 0 : kb_first;
+        cu.tile = static_cast<int>(t_first);
+        cu.kb = kb_first;
         return cu;
     };
 
@@ -476,12 +463,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jj = 0; jj < seg_len; ++jj) cu.next();
             const int d = seg & 1;
             int64_t c_lo = 0, c_hi = 0;
+            bool all_in = false;
             if (!whole) {
                 c_lo = part.owner(tile * nkb);
                 c_hi = part.owner((tile + 1) * nkb - 1);
                 // every other contributor already arrived: this CTA finishes
-                // the tile from its registers (checked while the MMAs run)
-                if (etid == 0) *last_flag = ld_acquire_gpu(&counters[c_lo]) == static_cast<uint32_t>(c_hi - c_lo);
+                // the tile from its registers (tested while the MMAs run, and
+                // again once the accumulator is ready)
+                if (etid == 0) all_in = ld_acquire_gpu(&counters[c_lo]) == static_cast<uint32_t>(c_hi - c_lo);
             }
             bool ok = true;
             for (int w = 0; w < kMmaWarps; ++w)
@@ -489,6 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) {
                 if (lane == 0) *ep_abort = 1;
                 record_error(kErrWaitMma, abort_flag);
+            }
+            if (!whole && etid == 0) {
+                if (!all_in) all_in = ld_acquire_gpu(&counters[c_lo]) == static_cast<uint32_t>(c_hi - c_lo);
+                *last_flag = all_in ? 1 : 0;
             }
             // the four epilogue warps leave together (ep_abort is written only
             // by them, before this barrier), so their named barriers stay matched

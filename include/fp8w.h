@@ -104,8 +104,9 @@ FP8W_API fp8w_status fp8w_quantize(const float *w, int64_t n, int64_t k,
  *   1 <= m <= FP8W_MAX_DIM, 1 <= n <= FP8W_MAX_DIM, 16 <= k <= FP8W_MAX_K,
  *   k % 16 == 0.  x and y must not overlap codes, scales, bias or workspace.
  *
- * m == 1 runs the GEMV kernel; m >= 2 the tensor-core kernel, one launch per
- * 32 rows of x (m > 32 re-streams the weight per slab: correct, not tuned).
+ * m == 1 with k <= 32768 runs the GEMV kernel; everything else the
+ * tensor-core kernel, one launch per 32 rows of x (m > 32 re-streams the
+ * weight per slab: correct, not tuned).
  */
 FP8W_API fp8w_status fp8w_linear(const void *x, int act_dtype, int64_t m, int64_t k,
                         const uint8_t *codes, const float *scales,
@@ -113,7 +114,7 @@ FP8W_API fp8w_status fp8w_linear(const void *x, int act_dtype, int64_t m, int64_
                         void *workspace, size_t workspace_bytes, void *stream);
 
 /* Workspace bytes fp8w_linear needs for this shape on the current device
- * (0 when the GEMV kernel is used). */
+ * (0 when the GEMV kernel is used: m == 1 and k <= 32768). */
 FP8W_API size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k);
 
 /* Explicit kernel choice, for tests and tuning; fp8w_linear uses
@@ -121,7 +122,7 @@ FP8W_API size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k);
 enum { FP8W_KERNEL_AUTO = 0, FP8W_KERNEL_GEMV = 1, FP8W_KERNEL_SKINNY = 2 };
 
 typedef struct fp8w_linear_config {
-    int kernel;   /* FP8W_KERNEL_*; GEMV requires m == 1 */
+    int kernel;   /* FP8W_KERNEL_*; GEMV requires m == 1 and k <= 32768 */
     int ctas;     /* tensor-core kernel only: CTAs of its persistent grid,
                      1..number of SMs, or 0 to choose from the shape; must be
                      0 for the GEMV kernel */

@@ -76,6 +76,11 @@ def test_gemv_rejects_a_grid_size():
     assert _lin(m=1, k=256, cfg=fw.LinearConfig(fw.KERNEL_GEMV, 8)) == 6
 
 
+def test_gemv_rejects_rows_longer_than_it_stages():
+    # x of a GEMV row lives in shared memory: k <= 32768
+    assert _lin(m=1, k=32768 + 16, cfg=fw.LinearConfig(fw.KERNEL_GEMV)) == 6
+
+
 @pytest.mark.parametrize("ws,ws_bytes", [(None, 0), (None, 1 << 30), (ctypes.c_void_p(0x600010), 1 << 30)])
 def test_tensor_core_path_rejects_missing_or_misaligned_workspace(ws, ws_bytes):
     # NULL or non-256-byte-aligned workspace is refused before any CUDA call
