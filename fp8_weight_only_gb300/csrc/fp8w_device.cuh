@@ -207,6 +207,15 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     return v;
 }
 
+// 16-byte shared-memory load by 32-bit shared address (a plain pointer into
+// dynamic shared memory can be compiled to a generic load, which goes
+// through the L1/texture path and waits like a global one).
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
 // ------------------------------------------------------------------ TMA --
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {

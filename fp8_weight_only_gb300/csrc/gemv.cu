@@ -14,9 +14,11 @@
 //    the SM's TMA unit a fixed ~0.27 us whatever its size (measured: 4 KB
 //    copies stream 15 GB/s per SM, 64 KB copies 218 GB/s), so copies are
 //    large.
-//  * The CTA's rows are dealt round-robin to the 16 compute warps; a warp
-//    computes its row whole (lane l takes 16-code chunks l, l+32, ...), so
-//    no reduction crosses warps.  Every warp waits for every slot in order
+//  * The CTA's rows are dealt round-robin to groups of G compute warps (16
+//    warps; G = 1 when a slot holds many rows, more for long rows, so that
+//    two slots keep every warp busy); lane l of the group's warp w takes the
+//    16-code chunks (32w + l) + 32G*j of its rows, and a group of several
+//    warps reduces through shared memory.  Every warp waits for every slot in order
 //    and arrives once on its "empty" barrier after its rows there (none, if
 //    the slot has fewer rows than warps): a warp whose next row lay several
 //    slots ahead would otherwise wait on a slot a full ring cycle early and
@@ -24,8 +26,10 @@
 //  * x is staged once in shared memory (as 16-bit values), and so are the
 //    CTA's scales and bias: after start-up the codes are the only stream.
 //  * Codes are converted exactly by the hardware e4m3x2 -> f16x2 conversion
-//    and widened to fp32, x is widened from its 16-bit pair, and each product
-//    is an fp32 FMA.
+//    and widened to fp32; x is widened from its 16-bit pair straight into a
+//    register pair, and products go two at a time through the packed
+//    fma.rn.f32x2.  For rows up to 8192 codes a warp computes two rows at
+//    once, so each widened x serves both: about 2.5 instructions a code.
 //  * A row's partial sums are reduced with a shuffle tree; one lane applies
 //    fmaf(acc, scale, bias) and rounds once.
 // HBM bytes per output channel: K (codes) + 4 (scale) + 4 (bias) + 2 (y).
@@ -51,6 +55,7 @@ constexpr int64_t kGemvMaxK = 32768;
 struct GemvGeom {
     int rows;         // rows per slot (R)
     int slots;        // slots in the ring (S)
+    int g;            // warps per row group (1, 2, 4, 8 or 16)
     uint32_t slot_bytes;
     uint32_t ring_bytes;
 };
@@ -69,37 +74,56 @@ __device__ __forceinline__ void f16x2_to_f32x2(uint32_t h, float& lo, float& hi)
         : "r"(h));
 }
 
-// One 16-code chunk against its 16 activations (8 packed 16-bit pairs),
-// into two accumulators for instruction-level parallelism.
+// Two fp32 values in one 64-bit register pair (low word = first).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+// acc2 += a2 * b2, lane-wise on fp32 pairs (one packed FMA).
+__device__ __forceinline__ void ffma2(uint64_t& acc2, uint64_t a2, uint64_t b2) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2) : "l"(a2), "l"(b2));
+}
+// A 16-bit pair of x widened to an fp32 pair.
 template <bool kBf16>
-__device__ __forceinline__ void dot_chunk(const uint4 c, const uint4 xa, const uint4 xb, float& a0, float& a1) {
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+__device__ __forceinline__ uint64_t widen_x(uint32_t w) {
+    if constexpr (kBf16) {
+        return static_cast<uint64_t>(w << 16) | (static_cast<uint64_t>(w & 0xFFFF0000u) << 32);
+    } else {
+        float lo, hi;
+        f16x2_to_f32x2(w, lo, hi);
+        return pack2(lo, hi);
+    }
+}
+// Four codes (one word) widened to two fp32 pairs, exactly.
+__device__ __forceinline__ void widen_codes(uint32_t w, uint64_t& p01, uint64_t& p23) {
+    uint32_t h01, h23;
+    e4m3x4_to_f16x2(w, h01, h23);
+    float v0, v1, v2, v3;
+    f16x2_to_f32x2(h01, v0, v1);
+    f16x2_to_f32x2(h23, v2, v3);
+    p01 = pack2(v0, v1);
+    p23 = pack2(v2, v3);
+}
+
+// RP rows' 16-code chunks against the same 16 activations: acc[r] is a pair
+// of partial sums (even, odd positions) of row r.
+template <int RP, bool kBf16>
+__device__ __forceinline__ void dot_chunk(const uint4 (&c)[RP], const uint4 xa, const uint4 xb, uint64_t (&acc)[RP]) {
     const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-        uint32_t h01, h23;
-        e4m3x4_to_f16x2(w[q], h01, h23);
-        float v0, v1, v2, v3;
-        f16x2_to_f32x2(h01, v0, v1);
-        f16x2_to_f32x2(h23, v2, v3);
-        float x0, x1, x2, x3;
-        if constexpr (kBf16) {
-            x0 = bf16_lo_to_f32(xw[2 * q]);
-            x1 = bf16_hi_to_f32(xw[2 * q]);
-            x2 = bf16_lo_to_f32(xw[2 * q + 1]);
-            x3 = bf16_hi_to_f32(xw[2 * q + 1]);
-        } else {
-            f16x2_to_f32x2(xw[2 * q], x0, x1);
-            f16x2_to_f32x2(xw[2 * q + 1], x2, x3);
+        const uint64_t x01 = widen_x<kBf16>(xw[2 * q]), x23 = widen_x<kBf16>(xw[2 * q + 1]);
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+            const uint32_t w = q == 0 ? c[r].x : q == 1 ? c[r].y : q == 2 ? c[r].z : c[r].w;
+            uint64_t p01, p23;
+            widen_codes(w, p01, p23);
+            ffma2(acc[r], x01, p01);
+            ffma2(acc[r], x23, p23);
         }
-        a0 = fmaf(x0, v0, a0);
-        a1 = fmaf(x1, v1, a1);
-        a0 = fmaf(x2, v2, a0);
-        a1 = fmaf(x3, v3, a1);
     }
 }
 
-template <bool kBf16>
+template <int RP, bool kBf16>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes, const float* __restrict__ scales,
                 const float* __restrict__ bias, uint16_t* __restrict__ y, int64_t n, int64_t k, GemvGeom geo) {
@@ -107,7 +131,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const uint32_t ring = smem_u32(smem);
     const int S = geo.slots, R = geo.rows;
-    // layout: ring | x [k] | scales, bias [kGemvStagedRows] | full, empty [kGemvMaxSlots] | abort flag
+    // layout: ring | x [k] | scales, bias [kGemvStagedRows] | full, empty [kGemvMaxSlots] |
+    // group partial sums [kGemvWarps][2][kGemvWarps][RP] | abort flag
     const uint32_t x_bytes = static_cast<uint32_t>(((k * 2 + 127) / 128) * 128);
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + geo.ring_bytes);
     float* sc_s = reinterpret_cast<float*>(smem + geo.ring_bytes + x_bytes);
@@ -116,8 +141,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     const uint32_t bar_empty = bar_full + 8 * kGemvMaxSlots;
     auto full = [&](int s) { return bar_full + 8u * s; };
     auto empty = [&](int s) { return bar_empty + 8u * s; };
-    volatile int* abort_flag =
-        reinterpret_cast<volatile int*>(smem + geo.ring_bytes + x_bytes + 8 * kGemvStagedRows + 16 * kGemvMaxSlots);
+    float* red = reinterpret_cast<float*>(smem + geo.ring_bytes + x_bytes + 8 * kGemvStagedRows + 16 * kGemvMaxSlots);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kGemvWarps * 2 * kGemvWarps * RP);
+    const int G = geo.g, groups = kGemvWarps / G;
 
     const int64_t P = gridDim.x;
     const int64_t row0 = blockIdx.x * n / P, row1 = (blockIdx.x + 1) * n / P;
@@ -189,45 +215,77 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         }
     }
     // the staged x, scales and bias are visible to every compute warp
-    asm volatile("bar.sync %0, %1;" ::"n"(1), "n"(32 * kGemvWarps) : "memory");
+    asm volatile("bar.sync %0, %1;" ::"n"(15), "n"(32 * kGemvWarps) : "memory");  // ids 1..8: row groups
 
-    const uint4* xv = reinterpret_cast<const uint4*>(xs);
+    const uint32_t xv = smem_u32(xs);
+    const int grp = warp / G, wg = warp % G;
     int s = 0;
     uint32_t ph = 0;
+    int parity = 0;
     for (int64_t sl = 0; sl < nslots; ++sl) {
-        if (!mbar_wait_warp(full(s), ph, abort_flag)) {
-            if (lane == 0) {
-                *abort_flag = 1;
-                atomicCAS(&g_gemv_error, 0, kErrWaitTma);
-            }
-            break;
+        bool ok = mbar_wait_warp(full(s), ph, abort_flag);
+        if (!ok && lane == 0) {
+            *abort_flag = 1;
+            atomicCAS(&g_gemv_error, 0, kErrWaitTma);
         }
+        // a group of several warps leaves together, so none is left waiting
+        // at the group's barrier below
+        if (G > 1) ok = !bar_red_or(1 + grp, 32 * G, !ok);
+        if (!ok) break;
         const int64_t base = sl * R;  // CTA-local index of the slot's first row
         const int rows = static_cast<int>((nrows - base) < R ? (nrows - base) : R);
-        // rows i = base + r with i % kGemvWarps == warp
-        for (int r = static_cast<int>((warp - base % kGemvWarps + kGemvWarps) % kGemvWarps); r < rows;
-             r += kGemvWarps) {
-            const int64_t i = base + r;
-            const int64_t row = row0 + i;
-            float sc = 0.0f, bi = 0.0f;
-            if (lane == 0) {
-                if (staged) {
-                    sc = sc_s[i];
-                    bi = bi_s[i];
-                } else {
-                    sc = scales[row];
-                    bi = bias ? bias[row] : 0.0f;
-                }
-            }
-            const uint8_t* rowp = smem + s * geo.slot_bytes + static_cast<int64_t>(r) * k;
-            float a0 = 0.0f, a1 = 0.0f;
-#pragma unroll 4
-            for (int64_t ch = lane; ch < nchunks; ch += 32)
-                dot_chunk<kBf16>(*reinterpret_cast<const uint4*>(rowp + ch * 16), xv[2 * ch], xv[2 * ch + 1], a0, a1);
-            float acc = a0 + a1;
+        // items of RP consecutive rows, item index (base / RP + r / RP) dealt
+        // round-robin: this group takes the items with index % groups == grp
+        const int64_t gbase = base / RP;
+        for (int r = static_cast<int>((grp - gbase % groups + groups) % groups) * RP; r < rows; r += groups * RP) {
+            const int nr = rows - r < RP ? rows - r : RP;  // rows in this item (the slot's last may be short)
+            const uint32_t rowp = ring + s * geo.slot_bytes + static_cast<uint32_t>(r * k);
+            uint64_t acc[RP];
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-            if (lane == 0) y[row] = round_out<kBf16>(fmaf(acc, sc, bi));
+            for (int q = 0; q < RP; ++q) acc[q] = 0ull;
+#pragma unroll 2
+            for (int64_t ch = wg * 32 + lane; ch < nchunks; ch += 32 * G) {
+                uint4 cw[RP];
+#pragma unroll
+                for (int q = 0; q < RP; ++q)
+                    cw[q] = q < nr ? lds128(rowp + static_cast<uint32_t>(q * k + ch * 16)) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t xa = xv + static_cast<uint32_t>(ch * 32);
+                dot_chunk<RP, kBf16>(cw, lds128(xa), lds128(xa + 16), acc);
+            }
+            float sum[RP];
+#pragma unroll
+            for (int q = 0; q < RP; ++q) {
+                sum[q] = __uint_as_float(static_cast<uint32_t>(acc[q])) + __uint_as_float(static_cast<uint32_t>(acc[q] >> 32));
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) sum[q] += __shfl_xor_sync(0xffffffffu, sum[q], off);
+            }
+            if (G > 1) {
+                // the group's warps add their sums in a fixed order
+                float* rd = red + ((grp * 2 + parity) * kGemvWarps) * RP;
+                if (lane == 0)
+#pragma unroll
+                    for (int q = 0; q < RP; ++q) rd[wg * RP + q] = sum[q];
+                asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(32 * G) : "memory");
+                if (wg == 0 && lane == 0)
+#pragma unroll
+                    for (int q = 0; q < RP; ++q) {
+                        float t = 0.0f;
+                        for (int w2 = 0; w2 < G; ++w2) t += rd[w2 * RP + q];
+                        sum[q] = t;
+                    }
+                // the other parity's sums are rewritten only after the next
+                // item's barrier, which warp 0 reaches after reading these
+                parity ^= 1;
+            }
+            if (wg == 0 && lane == 0)
+#pragma unroll
+                for (int q = 0; q < RP; ++q) {
+                    if (q >= nr) break;
+                    const int64_t i = base + r + q;
+                    const float sc = staged ? sc_s[i] : scales[row0 + i];
+                    const float bi = staged ? bi_s[i] : (bias ? bias[row0 + i] : 0.0f);
+                    y[row0 + i] = round_out<kBf16>(fmaf(sum[q], sc, bi));
+                }
         }
         // this warp has read its rows of the slot
         __syncwarp();
@@ -240,7 +298,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 }
 
 static uint32_t gemv_fixed_bytes(int64_t k) {
-    return static_cast<uint32_t>(((k * 2 + 127) / 128) * 128) + 8 * kGemvStagedRows + 16 * kGemvMaxSlots + 16 + 128;
+    return static_cast<uint32_t>(((k * 2 + 127) / 128) * 128) + 8 * kGemvStagedRows + 16 * kGemvMaxSlots +
+           4 * kGemvWarps * 2 * kGemvWarps * 2 + 16 + 128;
 }
 
 template <bool kBf16>
@@ -250,8 +309,11 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (a.k > kGemvMaxK) return cudaErrorNotSupported;
     GemvGeom geo;
-    // a slot holds whole rows, up to kGemvSlotTarget bytes
+    // a slot holds whole rows, up to kGemvSlotTarget bytes; rows up to 8192
+    // codes are computed in pairs, so their slots hold an even number
+    const int rp = a.k <= 8192 ? 2 : 1;
     int64_t rows = kGemvSlotTarget / a.k;
+    rows -= rows % rp;
     if (rows < 1) rows = 1;
     geo.rows = static_cast<int>(rows);
     geo.slot_bytes = static_cast<uint32_t>(((rows * a.k + 127) / 128) * 128);
@@ -260,16 +322,24 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     if (slots < 2) return cudaErrorNotSupported;
     geo.slots = static_cast<int>(slots);
     geo.ring_bytes = geo.slots * geo.slot_bytes;
+    // warps per row group: enough that two slots' items keep all warps busy
+    const int64_t items = (rows + rp - 1) / rp;
+    geo.g = 1;
+    while (geo.g < kGemvWarps && items * geo.g * 2 < kGemvWarps) geo.g *= 2;
     const uint32_t smem = geo.ring_bytes + gemv_fixed_bytes(a.k);
 
-    auto kern = gemv_kernel<kBf16>;
+    auto kern = rp == 2 ? gemv_kernel<2, kBf16> : gemv_kernel<1, kBf16>;
     static std::once_flag attr_once[64];
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvSmemBudget);
+        attr_err = cudaFuncSetAttribute(gemv_kernel<1, kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kGemvSmemBudget);
+        if (attr_err == cudaSuccess)
+            attr_err = cudaFuncSetAttribute(gemv_kernel<2, kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            kGemvSmemBudget);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int64_t grid = a.n < sms ? a.n : sms;

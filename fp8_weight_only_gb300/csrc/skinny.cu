@@ -638,10 +638,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 record_error(kErrWaitTma, abort_flag, cfull(group, s), bar0);
                 break;
             }
-            const uint8_t* row = smem + code_smem(group, s) + r * 128;
+            const uint32_t row = sbase + code_smem(group, s) + r * 128;
             uint4 cw[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) cw[q] = *reinterpret_cast<const uint4*>(row + ((q ^ (r & 7)) << 4));
+            for (int q = 0; q < 8; ++q) cw[q] = lds128(row + ((q ^ (r & 7)) << 4));
             __syncwarp();
             if (lane == 0) mbar_arrive(cempty(group, s));
             if (++s == kCS) {
