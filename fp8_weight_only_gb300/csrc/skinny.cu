@@ -9,12 +9,16 @@
 // mma.sync on sm_80..sm_120; this one is built for sm_103a:
 //
 //  * Persistent grid, at most one CTA per SM.  The work is the list of units
-//    (channel tile of 128, k-block of 128); CTA c takes the contiguous units
-//    [c*U/P, (c+1)*U/P).  P is the tile count when that nearly fills the GPU
-//    (every tile whole, nothing to combine), else a multiple of it or the SM
-//    count (stream-K).  A tile that straddles CTAs is finished by the last
-//    contributor: partial fp32 tiles go to a caller-provided workspace and
-//    are summed in CTA order (deterministic); nothing waits on another CTA.
+//    (channel tile of 128, k-block of 128).  Three launch shapes:
+//    - whole tiles, one CTA each, when the tile count nearly fills the GPU;
+//    - split: fewer tiles than SMs, each tile's k-blocks divided evenly over
+//      a thread-block cluster of 2, 4 or 8 CTAs, whose fp32 partials are
+//      summed through distributed shared memory at the end (each CTA adds
+//      up, in rank order, a slice of the tile's channels from every rank);
+//    - stream-K: more tiles than SMs; CTA c takes the contiguous units
+//      [c*U/P, (c+1)*U/P), and a tile that straddles CTAs is finished by the
+//      last contributor: partial fp32 tiles go to a caller-provided workspace
+//      and are summed in CTA order (deterministic); no CTA waits on another.
 //    A CTA takes its units in order, so the piece at the start of its range
 //    (the end of a tile another CTA began) is done first and published
 //    early; the CTA holding the start of that tile finishes it last and, as
@@ -206,7 +210,7 @@ template <int NT, bool kBf16>
 __global__ void __launch_bounds__(kThreads, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                   const float* __restrict__ scales, const float* __restrict__ bias, uint16_t* __restrict__ y,
-                  uint8_t* __restrict__ workspace, int m_rows, int m_row0, int64_t n, int64_t k) {
+                  uint8_t* __restrict__ workspace, int m_rows, int m_row0, int64_t n, int64_t k, int split) {
     using L = SkinnySmem<NT>;
     constexpr int kCS = L::kCodeSlots, kXS = L::kXSlots;
     extern __shared__ uint8_t smem_raw[];
@@ -237,7 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t nkb = (k + kBlockK - 1) / kBlockK;
     const Partition part{tiles * nkb, static_cast<int64_t>(gridDim.x), nkb};
     const int64_t c = blockIdx.x;
-    const int64_t u0 = part.begin(c), u1 = part.begin(c + 1);
+    // split launches: cluster c / split takes tile c / split, its rank c % split
+    // an even share of the k-blocks; otherwise the contiguous range of units
+    const int64_t u0 = split > 1 ? (c / split) * nkb + (c % split) * nkb / split : part.begin(c);
+    const int64_t u1 = split > 1 ? (c / split) * nkb + (c % split + 1) * nkb / split : part.begin(c + 1);
     const int iters = static_cast<int>(u1 - u0);
     const int64_t t_first = u0 / nkb;
     const int kb_first = static_cast<int>(u0 - t_first * nkb);
@@ -464,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int d = seg & 1;
             int64_t c_lo = 0, c_hi = 0;
             bool all_in = false;
-            if (!whole) {
+            if (!whole && split == 1) {
                 c_lo = part.owner(tile * nkb);
                 c_hi = part.owner((tile + 1) * nkb - 1);
                 // every other contributor already arrived: this CTA finishes
@@ -479,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) *ep_abort = 1;
                 record_error(kErrWaitMma, abort_flag);
             }
-            if (!whole && etid == 0) {
+            if (!whole && split == 1 && etid == 0) {
                 if (!all_in) all_in = ld_acquire_gpu(&counters[c_lo]) == static_cast<uint32_t>(c_hi - c_lo);
                 *last_flag = all_in ? 1 : 0;
             }
@@ -487,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // by them, before this barrier), so their named barriers stay matched
             epilogue_bar();
             if (*ep_abort) break;
-            const bool early = !whole && *last_flag;
+            const bool early = !whole && split == 1 && *last_flag;
             tc_fence_after();
             const int64_t col = tile * kTileN + r;
             const float sc = col < n ? scales[col] : 0.0f;
@@ -519,7 +526,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 16; ++q) acc[q] += __uint_as_float(v[q]);
                 }
-                if (whole || early) {
+                if (split > 1) {
+                    // this rank's partial tile, token-major, into the free code ring
+                    float* pt = reinterpret_cast<float*>(smem + L::kCodesOff);
+#pragma unroll
+                    for (int q = 0; q < 16; ++q)
+                        if (h * 16 + q < m_rows) pt[(h * 16 + q) * kTileN + r] = acc[q];
+                } else if (whole || early) {
                     if (early) {
                         // contributors in CTA order, this CTA's own partial from
                         // registers: the same sum the publishing path forms
@@ -566,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(dfree(d));
 
-            if (!whole) {
+            if (!whole && split == 1) {
                 if (early) {
                     // every other contributor has arrived, so nobody else
                     // touches the counter during this launch
@@ -676,6 +689,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     __syncthreads();
+    if (split > 1) {
+        // this rank adds up channels [ch0, ch0 + nch) of the tile over all
+        // ranks, in rank order, and writes y; split is a power of two, so a
+        // thread keeps one channel, whose scale and bias it fetches first
+        const bool red_thread = warp >= kFirstEpilogueWarp && warp < kFirstDequantWarp;
+        const int etid = threadIdx.x - 32 * kFirstEpilogueWarp;
+        const int nch = kTileN / split;
+        const int ch = static_cast<int>(c % split) * nch + (red_thread ? etid % nch : 0);
+        const int64_t col = (c / split) * kTileN + ch;
+        float sc = 0.0f, b = 0.0f;
+        if (red_thread && col < n) {
+            sc = scales[col];
+            b = bias ? bias[col] : 0.0f;
+        }
+        // every rank's partial tile is in its shared memory
+        cluster_sync_all();
+        if (red_thread && !*ep_abort && iters > 0) {
+            const uint32_t pt = sbase + L::kCodesOff;
+            if (col < n) {
+                for (int tok = etid / nch; tok < m_rows; tok += 128 / nch) {
+                    const uint32_t off = pt + static_cast<uint32_t>((tok * kTileN + ch) * 4);
+                    float v[8];
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr)
+                        if (rr < split) v[rr] = ld_shared_cluster_f32(mapa_shared(off, rr));
+                    float t = 0.0f;
+#pragma unroll
+                    for (int rr = 0; rr < 8; ++rr)
+                        if (rr < split) t += v[rr];
+                    y[static_cast<int64_t>(tok) * n + col] = round_out<kBf16>(fmaf(t, sc, b));
+                }
+            }
+        }
+        // no rank leaves while its partial may still be read
+        cluster_sync_all();
+    }
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -735,26 +784,32 @@ cudaError_t device_sm_count(int& sms) {
 // fills the GPU (no partial tiles, no fix-up); when it is well below the SM
 // count, each tile split evenly over s CTAs; otherwise stream-K over the SMs.
 // A split CTA gets at least kMinUnitsPerCta units, and P <= kMaxCtas.
-int64_t skinny_grid(int64_t n, int64_t k, int sms) {
+// Launch shape: the grid size, and the cluster size of a split launch (1 =
+// whole tiles or stream-K).
+struct SkinnyShape {
+    int64_t grid;
+    int split;
+};
+
+constexpr int kMaxSplit = 8;  // portable cluster size
+
+SkinnyShape skinny_shape(int64_t n, int64_t k, int sms) {
     const int64_t tiles = (n + kTileN - 1) / kTileN;
     const int64_t nkb = (k + kBlockK - 1) / kBlockK;
     const int64_t units = tiles * nkb;
     const int64_t cap = sms < kMaxCtas ? sms : kMaxCtas;
-    int64_t p;
-    if (tiles <= cap && 10 * tiles >= 7 * cap) {
-        p = tiles;
-    } else if (tiles < cap) {
-        int64_t split = cap / tiles;
-        const int64_t most = nkb / kMinUnitsPerCta;
-        if (split > most) split = most;
-        if (split < 1) split = 1;
-        p = tiles * split;
-    } else {
-        p = units / kMinUnitsPerCta;
-        if (p > cap) p = cap;
+    if (tiles <= cap && 10 * tiles >= 7 * cap) return {tiles, 1};
+    if (tiles < cap) {
+        // each tile over a cluster of split CTAs (a power of two), each CTA
+        // with at least kMinUnitsPerCta k-blocks
+        int split = 1;
+        while (split * 2 <= kMaxSplit && tiles * split * 2 <= cap && split * 2 * kMinUnitsPerCta <= nkb) split *= 2;
+        return {tiles * split, split};
     }
+    int64_t p = units / kMinUnitsPerCta;
+    if (p > cap) p = cap;
     if (p < 1) p = 1;
-    return p;
+    return {p, 1};
 }
 
 template <int NT, bool kBf16>
@@ -785,26 +840,30 @@ static cudaError_t launch_nt(const LinearArgs& a, void* workspace, int ctas, cud
     // every CTA gets at least one unit: the fix-up counts CTAs, so an empty
     // range inside a split tile would leave that tile unfinished
     const int64_t units = ((a.n + kTileN - 1) / kTileN) * ((a.k + kBlockK - 1) / kBlockK);
-    int64_t grid = ctas > 0 ? ctas : skinny_grid(a.n, a.k, sms);
-    if (grid > units) grid = units;
+    SkinnyShape shape = ctas > 0 ? SkinnyShape{ctas, 1} : skinny_shape(a.n, a.k, sms);
+    if (shape.grid > units) shape.grid = units;
     // programmatic dependent launch: this grid's prologue (barrier set-up,
     // TMEM allocation) overlaps the tail of the previous kernel in the
     // stream; every role waits for that kernel before touching global memory
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(shape.split);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.gridDim = dim3(static_cast<unsigned>(shape.grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = L::kAlloc;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = shape.split > 1 ? 2 : 1;
     uint16_t* yp = static_cast<uint16_t*>(a.y);
     for (int64_t m0 = 0; m0 < a.m; m0 += kMaxNT) {
         const int rows = static_cast<int>(a.m - m0 < kMaxNT ? a.m - m0 : kMaxNT);
         e = cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, a.scales, a.bias, yp + m0 * a.n,
-                               static_cast<uint8_t*>(workspace), rows, static_cast<int>(m0), a.n, a.k);
+                               static_cast<uint8_t*>(workspace), rows, static_cast<int>(m0), a.n, a.k, shape.split);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
