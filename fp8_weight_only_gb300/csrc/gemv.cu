@@ -23,13 +23,14 @@
 //    the slot has fewer rows than warps): a warp whose next row lay several
 //    slots ahead would otherwise wait on a slot a full ring cycle early and
 //    pass on the previous phase of the same parity.
-//  * x is staged once in shared memory (as 16-bit values), and so are the
-//    CTA's scales and bias: after start-up the codes are the only stream.
+//  * x is staged once in shared memory (widened to fp32 for rows up to 8192
+//    codes, as 16-bit values beyond), and so are the CTA's scales and bias:
+//    after start-up the codes are the only stream.
 //  * Codes are converted exactly by the hardware e4m3x2 -> f16x2 conversion
-//    and widened to fp32; x is widened from its 16-bit pair straight into a
-//    register pair, and products go two at a time through the packed
+//    and widened to fp32, and products go two at a time through the packed
 //    fma.rn.f32x2.  For rows up to 8192 codes a warp computes two rows at
-//    once, so each widened x serves both: about 2.5 instructions a code.
+//    once against fp32 x read straight from shared memory (about 2.4
+//    instructions a code); longer rows widen x from its 16-bit pairs.
 //  * A row's partial sums are reduced with a shuffle tree; one lane applies
 //    fmaf(acc, scale, bias) and rounds once.
 // HBM bytes per output channel: K (codes) + 4 (scale) + 4 (bias) + 2 (y).
@@ -46,7 +47,7 @@ constexpr int kGemvWarps = 16;                       // compute warps
 constexpr int kGemvThreads = 32 * (kGemvWarps + 1);  // + the producer warp
 constexpr int kGemvMaxSlots = 8;
 constexpr uint32_t kGemvSlotTarget = 64 * 1024;      // bytes per bulk copy, up to
-constexpr int kGemvStagedRows = 2048;                // rows whose scale and bias are staged
+constexpr int kGemvStagedRows = 2048;                // most rows whose scale and bias are staged
 constexpr uint32_t kGemvSmemBudget = 224 * 1024;
 // Largest K the GEMV takes: x (2 bytes a value) and two 64 KB slots fit
 // beside the staged scales.
@@ -56,6 +57,7 @@ struct GemvGeom {
     int rows;         // rows per slot (R)
     int slots;        // slots in the ring (S)
     int g;            // warps per row group (1, 2, 4, 8 or 16)
+    int staged;       // rows of scale and bias staged in shared memory (a multiple of 32)
     uint32_t slot_bytes;
     uint32_t ring_bytes;
 };
@@ -123,7 +125,28 @@ __device__ __forceinline__ void dot_chunk(const uint4 (&c)[RP], const uint4 xa, 
     }
 }
 
-template <int RP, bool kBf16>
+// RP rows' 16-code chunks against 16 fp32 activations (4 x 16 bytes).
+template <int RP>
+__device__ __forceinline__ void dot_chunk_f32(const uint4 (&c)[RP], const uint4 (&xf)[4], uint64_t (&acc)[RP]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const uint64_t x01 = static_cast<uint64_t>(q == 0 ? xf[0].x : q == 1 ? xf[1].x : q == 2 ? xf[2].x : xf[3].x) |
+                             (static_cast<uint64_t>(q == 0 ? xf[0].y : q == 1 ? xf[1].y : q == 2 ? xf[2].y : xf[3].y) << 32);
+        const uint64_t x23 = static_cast<uint64_t>(q == 0 ? xf[0].z : q == 1 ? xf[1].z : q == 2 ? xf[2].z : xf[3].z) |
+                             (static_cast<uint64_t>(q == 0 ? xf[0].w : q == 1 ? xf[1].w : q == 2 ? xf[2].w : xf[3].w) << 32);
+#pragma unroll
+        for (int r = 0; r < RP; ++r) {
+            const uint32_t w = q == 0 ? c[r].x : q == 1 ? c[r].y : q == 2 ? c[r].z : c[r].w;
+            uint64_t p01, p23;
+            widen_codes(w, p01, p23);
+            ffma2(acc[r], x01, p01);
+            ffma2(acc[r], x23, p23);
+        }
+    }
+}
+
+// kF32X: x is staged in shared memory as fp32 (else as 16-bit values).
+template <int RP, bool kBf16, bool kF32X>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes, const float* __restrict__ scales,
                 const float* __restrict__ bias, uint16_t* __restrict__ y, int64_t n, int64_t k, GemvGeom geo) {
@@ -131,17 +154,17 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const uint32_t ring = smem_u32(smem);
     const int S = geo.slots, R = geo.rows;
-    // layout: ring | x [k] | scales, bias [kGemvStagedRows] | full, empty [kGemvMaxSlots] |
+    // layout: ring | x [k] | scales, bias [geo.staged] | full, empty [kGemvMaxSlots] |
     // group partial sums [kGemvWarps][2][kGemvWarps][RP] | abort flag
-    const uint32_t x_bytes = static_cast<uint32_t>(((k * 2 + 127) / 128) * 128);
+    const uint32_t x_bytes = static_cast<uint32_t>(((k * (kF32X ? 4 : 2) + 127) / 128) * 128);
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + geo.ring_bytes);
     float* sc_s = reinterpret_cast<float*>(smem + geo.ring_bytes + x_bytes);
-    float* bi_s = sc_s + kGemvStagedRows;
-    const uint32_t bar_full = smem_u32(bi_s + kGemvStagedRows);
+    float* bi_s = sc_s + geo.staged;
+    const uint32_t bar_full = smem_u32(bi_s + geo.staged);
     const uint32_t bar_empty = bar_full + 8 * kGemvMaxSlots;
     auto full = [&](int s) { return bar_full + 8u * s; };
     auto empty = [&](int s) { return bar_empty + 8u * s; };
-    float* red = reinterpret_cast<float*>(smem + geo.ring_bytes + x_bytes + 8 * kGemvStagedRows + 16 * kGemvMaxSlots);
+    float* red = reinterpret_cast<float*>(smem + geo.ring_bytes + x_bytes + 8u * geo.staged + 16 * kGemvMaxSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kGemvWarps * 2 * kGemvWarps * RP);
     const int G = geo.g, groups = kGemvWarps / G;
 
@@ -202,12 +225,39 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     // -------------------------------------------------------- compute --
     pdl_wait();  // x, scales and bias may come from the previous kernel, y may still be read by it
     const int64_t nchunks = k >> 4;
+    // x is staged piece-major: the j-th 16-byte piece of every 16-activation
+    // chunk together, so the 32 lanes (32 consecutive chunks) read 32
+    // consecutive pieces, free of bank conflicts
     {
         const uint4* xg = reinterpret_cast<const uint4*>(x);
         uint4* xd = reinterpret_cast<uint4*>(xs);
-        for (int64_t i = threadIdx.x; i < nchunks * 2; i += 32 * kGemvWarps) xd[i] = __ldg(xg + i);
+        for (int64_t i = threadIdx.x; i < nchunks * 2; i += 32 * kGemvWarps) {
+            const uint4 v = __ldg(xg + i);
+            if constexpr (kF32X) {
+                // 8 activations -> 8 fp32
+                const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if constexpr (kBf16) {
+                        f[2 * e] = bf16_lo_to_f32(wv[e]);
+                        f[2 * e + 1] = bf16_hi_to_f32(wv[e]);
+                    } else {
+                        f16x2_to_f32x2(wv[e], f[2 * e], f[2 * e + 1]);
+                    }
+                }
+                // half h of chunk ch holds pieces 2h and 2h+1
+                const int64_t ch = i >> 1, pc = 2 * (i & 1);
+                xd[pc * nchunks + ch] =
+                    make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+                xd[(pc + 1) * nchunks + ch] =
+                    make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]), __float_as_uint(f[7]));
+            } else {
+                xd[(i & 1) * nchunks + (i >> 1)] = v;
+            }
+        }
     }
-    const bool staged = nrows <= kGemvStagedRows;
+    const bool staged = nrows <= geo.staged;
     if (staged) {
         for (int64_t i = threadIdx.x; i < nrows; i += 32 * kGemvWarps) {
             sc_s[i] = scales[row0 + i];
@@ -218,6 +268,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     asm volatile("bar.sync %0, %1;" ::"n"(15), "n"(32 * kGemvWarps) : "memory");  // ids 1..8: row groups
 
     const uint32_t xv = smem_u32(xs);
+    const uint32_t xpiece = static_cast<uint32_t>(nchunks * 16);  // bytes from one piece of x to the next
     const int grp = warp / G, wg = warp % G;
     int s = 0;
     uint32_t ph = 0;
@@ -243,14 +294,22 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             uint64_t acc[RP];
 #pragma unroll
             for (int q = 0; q < RP; ++q) acc[q] = 0ull;
-#pragma unroll 2
-            for (int64_t ch = wg * 32 + lane; ch < nchunks; ch += 32 * G) {
+            const int nch = static_cast<int>(nchunks);
+            const uint32_t kk = static_cast<uint32_t>(k);
+#pragma unroll 4
+            for (int ch = wg * 32 + lane; ch < nch; ch += 32 * G) {
                 uint4 cw[RP];
 #pragma unroll
                 for (int q = 0; q < RP; ++q)
-                    cw[q] = q < nr ? lds128(rowp + static_cast<uint32_t>(q * k + ch * 16)) : make_uint4(0u, 0u, 0u, 0u);
-                const uint32_t xa = xv + static_cast<uint32_t>(ch * 32);
-                dot_chunk<RP, kBf16>(cw, lds128(xa), lds128(xa + 16), acc);
+                    cw[q] = q < nr ? lds128(rowp + q * kk + static_cast<uint32_t>(ch) * 16u) : make_uint4(0u, 0u, 0u, 0u);
+                const uint32_t xa = xv + static_cast<uint32_t>(ch) * 16u;
+                if constexpr (kF32X) {
+                    const uint4 xf[4] = {lds128(xa), lds128(xa + xpiece), lds128(xa + 2 * xpiece),
+                                         lds128(xa + 3 * xpiece)};
+                    dot_chunk_f32<RP>(cw, xf, acc);
+                } else {
+                    dot_chunk<RP, kBf16>(cw, lds128(xa), lds128(xa + xpiece), acc);
+                }
             }
             float sum[RP];
 #pragma unroll
@@ -297,9 +356,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
 }
 
-static uint32_t gemv_fixed_bytes(int64_t k) {
-    return static_cast<uint32_t>(((k * 2 + 127) / 128) * 128) + 8 * kGemvStagedRows + 16 * kGemvMaxSlots +
-           4 * kGemvWarps * 2 * kGemvWarps * 2 + 16 + 128;
+static uint32_t gemv_fixed_bytes(int64_t k, bool f32x, int staged) {
+    return static_cast<uint32_t>(((k * (f32x ? 4 : 2) + 127) / 128) * 128) + 8u * staged +
+           16 * kGemvMaxSlots + 4 * kGemvWarps * 2 * kGemvWarps * 2 + 16 + 128;
 }
 
 template <bool kBf16>
@@ -309,6 +368,10 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (a.k > kGemvMaxK) return cudaErrorNotSupported;
     GemvGeom geo;
+    const int64_t grid = a.n < sms ? a.n : sms;
+    // scale and bias of a CTA's rows (at most ceil(n / grid)) are staged
+    const int64_t per_cta = (a.n + grid - 1) / grid;
+    geo.staged = static_cast<int>(per_cta > kGemvStagedRows ? kGemvStagedRows : (per_cta + 31) / 32 * 32);
     // a slot holds whole rows, up to kGemvSlotTarget bytes; rows up to 8192
     // codes are computed in pairs, so their slots hold an even number
     const int rp = a.k <= 8192 ? 2 : 1;
@@ -317,7 +380,7 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     if (rows < 1) rows = 1;
     geo.rows = static_cast<int>(rows);
     geo.slot_bytes = static_cast<uint32_t>(((rows * a.k + 127) / 128) * 128);
-    int64_t slots = (kGemvSmemBudget - gemv_fixed_bytes(a.k)) / geo.slot_bytes;
+    int64_t slots = (kGemvSmemBudget - gemv_fixed_bytes(a.k, rp == 2, geo.staged)) / geo.slot_bytes;
     if (slots > kGemvMaxSlots) slots = kGemvMaxSlots;
     if (slots < 2) return cudaErrorNotSupported;
     geo.slots = static_cast<int>(slots);
@@ -326,23 +389,23 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     const int64_t items = (rows + rp - 1) / rp;
     geo.g = 1;
     while (geo.g < kGemvWarps && items * geo.g * 2 < kGemvWarps) geo.g *= 2;
-    const uint32_t smem = geo.ring_bytes + gemv_fixed_bytes(a.k);
+    const uint32_t smem = geo.ring_bytes + gemv_fixed_bytes(a.k, rp == 2, geo.staged);
 
-    auto kern = rp == 2 ? gemv_kernel<2, kBf16> : gemv_kernel<1, kBf16>;
+    // rows up to 8192 codes: row pairs against fp32 x
+    auto kern = rp == 2 ? gemv_kernel<2, kBf16, true> : gemv_kernel<1, kBf16, false>;
     static std::once_flag attr_once[64];
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(gemv_kernel<1, kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(gemv_kernel<1, kBf16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kGemvSmemBudget);
         if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(gemv_kernel<2, kBf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            attr_err = cudaFuncSetAttribute(gemv_kernel<2, kBf16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             kGemvSmemBudget);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    const int64_t grid = a.n < sms ? a.n : sms;
     // programmatic dependent launch: set-up overlaps the previous kernel's tail
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -202,6 +202,57 @@ def test_tensor_core_partitions(m, n, k):
     assert_parity(y, ref, oracle.ACT_BF16, (m, n, k))
 
 
+@pytest.mark.parametrize("act", [oracle.ACT_BF16, oracle.ACT_F16])
+@pytest.mark.parametrize("n,k", [
+    (1, 512),        # one row: one CTA
+    (151, 512),      # fewer rows than SMs
+    (153, 1024),     # one CTA with two rows, the rest one
+    (1000, 2048),    # odd and even row counts per CTA
+    (4097, 4096),    # 27 rows a CTA: ragged last slot and row pair
+    (700, 14336),    # long rows: one row per item, rows split over warps
+    (96, 32768),     # the longest rows the GEMV takes
+])
+def test_gemv_shapes(n, k, act):
+    """The M = 1 kernel across slot sizes, row pairs and warp groups, with
+    odd row counts per CTA and both activation types."""
+    c, codes, scales = _case(300 + n + k + act, 1, n, k, act, with_bias=(n % 2 == 1))
+    ref = oracle.linear(c["x"], act, codes, scales, c["bias"], threads=oracle.host_cores())
+    y = gpu_linear(c["x"], act, codes, scales, c["bias"], kernel=fw.KERNEL_GEMV)
+    assert_parity(y, ref, act, (1, n, k))
+
+
+@pytest.mark.parametrize("kind", ["huge", "tiny", "subnormal", "spread", "zero", "one_big"])
+def test_gemv_activation_range(kind):
+    """The GEMV's result must not depend on where x's values sit in bf16's
+    range: huge, tiny, subnormal, widely spread, all zero, one outlier."""
+    n, k = 500, 4096
+    rng = np.random.default_rng(11)
+    # weights 2^20 larger keep y a normal number when x is tiny
+    c, codes, scales = _case(41, 1, n, k, oracle.ACT_BF16, with_bias=False,
+                             std=0.02 * (2.0 ** 20 if kind in ("tiny", "subnormal") else 1.0))
+    xf = rng.standard_normal((1, k))
+    if kind == "huge":
+        # the fp32 sum is in code units (|code| <= 448): it holds x up to ~2^110
+        xf *= 2.0 ** 100
+    elif kind == "tiny":
+        xf *= 2.0 ** -120
+    elif kind == "subnormal":
+        xf *= 2.0 ** -128          # bf16 subnormals and the smallest normals
+    elif kind == "spread":
+        xf *= 2.0 ** rng.integers(-40, 40, size=(1, k))
+    elif kind == "zero":
+        xf[:] = 0.0
+    elif kind == "one_big":
+        xf[0, 17] = 3.0e4
+    x = synthetic.to_bf16_bits(xf.astype(np.float32))
+    y = gpu_linear(x, oracle.ACT_BF16, codes, scales, None, kernel=fw.KERNEL_GEMV)
+    ref = oracle.linear(x, oracle.ACT_BF16, codes, scales, None)
+    if kind == "zero":
+        assert not y.any() or np.all((y & 0x7FFF) == 0)
+    else:
+        assert_parity(y, ref, oracle.ACT_BF16, kind)
+
+
 def test_workspace_left_ready_across_shapes():
     """Back-to-back calls of different shapes share one workspace: each call
     must leave the arrival counters at zero for the next."""
