@@ -23,6 +23,7 @@ CPU oracle on a bounded sample, and SM clocks sampled during the timed loop.
 """
 import argparse
 import ctypes
+import hashlib
 import json
 import os
 import subprocess
@@ -242,10 +243,79 @@ def enqueue_step(fw, mats, xs, ys, events=None, ev_list=None, stream_handle=None
     return launches
 
 
-def kernel_name(m):
+def kernel_name(m, k):
+    """The kernel (template instance, as ncu names it) that runs a call."""
     if m == 1:
-        return "fp8w::gemv_kernel<4,2,bf16>|<1,8,bf16>"
-    return "fp8w::skinny_kernel<%d,bf16>" % (16 if m <= 16 else 32)
+        # rows of up to 8192 codes: row pairs against fp32 x; longer rows one at a time
+        return "fp8w::gemv_kernel<2, 1, 1>" if k <= 8192 else "fp8w::gemv_kernel<1, 1, 0>"
+    return "fp8w::skinny_kernel<%d, 1>" % (16 if m <= 16 else 32)
+
+
+KERNEL_SOURCES = {"skinny_kernel": ["skinny.cu", "fp8w_device.cuh"], "gemv_kernel": ["gemv.cu", "fp8w_device.cuh"]}
+
+
+def kernel_source_hash(kernel):
+    """sha256 over the sources a kernel is built from (to tell whether a stored
+    ncu figure still describes the kernel as it is now)."""
+    base = kernel.split("::")[-1].split("<")[0]
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[base]:
+        with open(os.path.join(ROOT, "fp8_weight_only_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+TRAFFIC_COMMAND = ("ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum --clock-control none "
+                   "-k regex:'gemv_kernel|skinny_kernel' -c 21 --csv --log-file traffic.csv "
+                   "python bench.py --steps 2 --warmup 1 --no-cpu")
+
+
+def record_traffic(csv_path):
+    """Write profiles/dram_traffic_decode_stack.json from the CSV of
+    TRAFFIC_COMMAND: the first 21 linear launches (one eager step, every
+    call once, L2 flushed by ncu before each launch), DRAM bytes per launch
+    by kernel, with the source hash they were taken on."""
+    import csv
+    per = {}
+    with open(csv_path) as f:
+        rows = [r for r in csv.reader(f) if len(r) > 10]
+    hdr = rows[0]
+    ik, im, iv, iid = hdr.index("Kernel Name"), hdr.index("Metric Name"), hdr.index("Metric Value"), hdr.index("ID")
+    vals = {}
+    for r in rows[1:]:
+        name = r[ik].replace("void ", "", 1).split("(")[0].strip()
+        if "::" not in name:
+            name = "fp8w::" + name
+        vals.setdefault((r[iid], name), {})[r[im]] = float(r[iv].replace(",", ""))
+    for (_, name), m in vals.items():
+        d = per.setdefault(name, {"launches": 0, "bytes": 0.0})
+        d["launches"] += 1
+        d["bytes"] += m["dram__bytes_read.sum"] + m["dram__bytes_write.sum"]
+    out = {"command": TRAFFIC_COMMAND, "kernels": {}}
+    for name, d in per.items():
+        out["kernels"][name] = {"launches": d["launches"], "dram_bytes_per_launch": round(d["bytes"] / d["launches"]),
+                                "source_sha256": kernel_source_hash(name)}
+    with open(os.path.join(ROOT, "profiles", "dram_traffic_decode_stack.json"), "w") as f:
+        json.dump(out, f, indent=1)
+        f.write("\n")
+    print(json.dumps(out, indent=1))
+
+
+def stored_traffic(kernel):
+    """DRAM bytes per launch of `kernel` over the step's launches, from the
+    committed ncu summary, or (None, why) when absent or taken on other source."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic_decode_stack.json")
+    if not os.path.exists(p):
+        return None, "no stored ncu traffic"
+    with open(p) as f:
+        d = json.load(f)
+    short = kernel.split("::")[-1]
+    rec = next((v for kk, v in d.get("kernels", {}).items() if kk.split("::")[-1] == short), None)
+    if rec is None:
+        return None, "no stored ncu traffic for this kernel"
+    if rec.get("source_sha256") != kernel_source_hash(kernel):
+        return None, "kernel source changed since the stored ncu capture"
+    return rec["dram_bytes_per_launch"], "ncu dram__bytes_read.sum + dram__bytes_write.sum, " + d.get("command", "")
 
 
 def run_ours(args, torch, dist):
@@ -311,7 +381,12 @@ def run_ours(args, torch, dist):
             gi.replay()
             torch.cuda.synchronize()
             acc += [evs.elapsed_ms(ev_list[i], ev_list[i + 1]) for i in range(len(step_calls()))]
-        per_call = acc / reps
+        per_call_raw = acc / reps
+        # the events between launches keep consecutive kernels from
+        # overlapping (programmatic dependent launch), so the instrumented
+        # step is longer than the timed one: durations are scaled to the timed
+        # step, keeping each call's share
+        per_call = per_call_raw * (ms_step / float(per_call_raw.sum()))
         del gi
     except (OSError, RuntimeError) as e:  # pragma: no cover - reported in the JSON
         per_call = None
@@ -336,7 +411,7 @@ def run_ours(args, torch, dist):
         by_kernel = {}
         by_m = {}
         for (m, name, n, k), ms in zip(calls, per_call):
-            kn = kernel_name(m)
+            kn = kernel_name(m, k)
             d = by_kernel.setdefault(kn, {"ms": 0.0, "bytes": 0, "launches": 0})
             d["ms"] += ms
             d["bytes"] += call_bytes(m, n, k)
@@ -348,11 +423,15 @@ def run_ours(args, torch, dist):
         top = max(by_kernel, key=lambda kk: by_kernel[kk]["ms"])
         d = by_kernel[top]
         achieved = d["bytes"] / d["launches"] / (d["ms"] / d["launches"] / 1e3) / 1e9
+        traffic, traffic_src = stored_traffic(top)
         result["roofline"] = {"bound": "hbm", "kernel": top, "achieved": round(achieved, 1),
                               "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                              "traffic": None, "share": round(d["ms"] / total, 4),
-                              "note": "achieved = algorithmic bytes per launch / mean launch duration "
-                                      "(device events between launches in an instrumented graph replay); "
+                              "traffic": traffic, "traffic_source": traffic_src,
+                              "algorithmic_bytes_per_launch": round(d["bytes"] / d["launches"]),
+                              "share": round(d["ms"] / total, 4),
+                              "note": "achieved = algorithmic bytes per launch / mean launch duration; durations "
+                                      "from device events between the launches of an instrumented graph replay, "
+                                      "scaled so that the calls add up to the timed step (shares kept); "
                                       "peak is " + peak_src}
         result["kernels"] = {kk: {"share": round(v["ms"] / total, 4), "launches_per_step": v["launches"],
                                   "ms_per_step": round(v["ms"], 5),
@@ -363,6 +442,7 @@ def run_ours(args, torch, dist):
                            for m, v in by_m.items()}
         result["per_call_us"] = {"%s@M%d" % (name, m): round(ms * 1e3, 2)
                                  for (m, name, n, k), ms in zip(calls, per_call)}
+        result["instrumented_step_ms"] = round(float(per_call_raw.sum()), 5)
     else:
         result["roofline"] = {"bound": "hbm", "achieved": None, "peak": peak, "unit": "GB/s", "frac": None,
                               "traffic": None, "note": "instrumented replay failed: " + instr_err}
@@ -488,7 +568,12 @@ def main():
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--kernel", type=int, default=0, help="with --profile: 0 auto, 1 gemv, 2 tensor-core")
     ap.add_argument("--ctas", type=int, default=0, help="with --profile: tensor-core grid size (0 = from the shape)")
+    ap.add_argument("--record-traffic", default=None, metavar="CSV",
+                    help="write profiles/dram_traffic_decode_stack.json from an ncu CSV (see TRAFFIC_COMMAND)")
     args = ap.parse_args()
+    if args.record_traffic:
+        record_traffic(args.record_traffic)
+        return
     if args.profile:
         run_profile_case(args)
         return
