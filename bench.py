@@ -246,8 +246,8 @@ def enqueue_step(fw, mats, xs, ys, events=None, ev_list=None, stream_handle=None
 def kernel_name(m, k):
     """The kernel (template instance, as ncu names it) that runs a call."""
     if m == 1:
-        # rows of up to 8192 codes: row pairs against fp32 x; longer rows one at a time
-        return "fp8w::gemv_kernel<2, 1, 1>" if k <= 8192 else "fp8w::gemv_kernel<1, 1, 0>"
+        # row pairs against fp32 x up to 8192 codes a row, 16-bit x beyond
+        return "fp8w::gemv_kernel<2, 1, 1>" if k <= 8192 else "fp8w::gemv_kernel<2, 1, 0>"
     return "fp8w::skinny_kernel<%d, 1>" % (16 if m <= 16 else 32)
 
 

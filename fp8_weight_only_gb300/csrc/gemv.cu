@@ -28,9 +28,10 @@
 //    after start-up the codes are the only stream.
 //  * Codes are converted exactly by the hardware e4m3x2 -> f16x2 conversion
 //    and widened to fp32, and products go two at a time through the packed
-//    fma.rn.f32x2.  For rows up to 8192 codes a warp computes two rows at
-//    once against fp32 x read straight from shared memory (about 2.4
-//    instructions a code); longer rows widen x from its 16-bit pairs.
+//    fma.rn.f32x2.  A warp computes two rows at once, so each activation it
+//    reads serves both: x is read as fp32 straight from shared memory for
+//    rows up to 8192 codes (about 2.4 instructions a code), and widened from
+//    its 16-bit pairs for longer rows.
 //  * A row's partial sums are reduced with a shuffle tree; one lane applies
 //    fmaf(acc, scale, bias) and rounds once.
 // HBM bytes per output channel: K (codes) + 4 (scale) + 4 (bias) + 2 (y).
@@ -372,15 +373,17 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     // scale and bias of a CTA's rows (at most ceil(n / grid)) are staged
     const int64_t per_cta = (a.n + grid - 1) / grid;
     geo.staged = static_cast<int>(per_cta > kGemvStagedRows ? kGemvStagedRows : (per_cta + 31) / 32 * 32);
-    // a slot holds whole rows, up to kGemvSlotTarget bytes; rows up to 8192
-    // codes are computed in pairs, so their slots hold an even number
-    const int rp = a.k <= 8192 ? 2 : 1;
+    // a slot holds whole rows, up to kGemvSlotTarget bytes; rows are computed
+    // in pairs, so slots hold an even number (x is staged as fp32 for rows up
+    // to 8192 codes, as 16-bit values beyond)
+    const int rp = 2;
+    const bool f32x = a.k <= 8192;
     int64_t rows = kGemvSlotTarget / a.k;
     rows -= rows % rp;
-    if (rows < 1) rows = 1;
+    if (rows < rp) rows = rp;
     geo.rows = static_cast<int>(rows);
     geo.slot_bytes = static_cast<uint32_t>(((rows * a.k + 127) / 128) * 128);
-    int64_t slots = (kGemvSmemBudget - gemv_fixed_bytes(a.k, rp == 2, geo.staged)) / geo.slot_bytes;
+    int64_t slots = (kGemvSmemBudget - gemv_fixed_bytes(a.k, f32x, geo.staged)) / geo.slot_bytes;
     if (slots > kGemvMaxSlots) slots = kGemvMaxSlots;
     if (slots < 2) return cudaErrorNotSupported;
     geo.slots = static_cast<int>(slots);
@@ -389,17 +392,16 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     const int64_t items = (rows + rp - 1) / rp;
     geo.g = 1;
     while (geo.g < kGemvWarps && items * geo.g * 2 < kGemvWarps) geo.g *= 2;
-    const uint32_t smem = geo.ring_bytes + gemv_fixed_bytes(a.k, rp == 2, geo.staged);
+    const uint32_t smem = geo.ring_bytes + gemv_fixed_bytes(a.k, f32x, geo.staged);
 
-    // rows up to 8192 codes: row pairs against fp32 x
-    auto kern = rp == 2 ? gemv_kernel<2, kBf16, true> : gemv_kernel<1, kBf16, false>;
+    auto kern = f32x ? gemv_kernel<2, kBf16, true> : gemv_kernel<2, kBf16, false>;
     static std::once_flag attr_once[64];
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(gemv_kernel<1, kBf16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(gemv_kernel<2, kBf16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kGemvSmemBudget);
         if (attr_err == cudaSuccess)
             attr_err = cudaFuncSetAttribute(gemv_kernel<2, kBf16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
