@@ -318,6 +318,63 @@ def stored_traffic(kernel):
     return rec["dram_bytes_per_launch"], "ncu dram__bytes_read.sum + dram__bytes_write.sum, " + d.get("command", "")
 
 
+FUSED_GROUPS = (("qkv", ("q", "k", "v")), ("o", ("o",)), ("gate_up", ("gate", "up")), ("down", ("down",)))
+
+
+def run_fused(torch, fw, mats, xs, dev, s, steps, warmup, peak):
+    """The decode stack with q/k/v and gate/up fused: one call over the
+    concatenated rows of each group, on one shared x (the first member's), as
+    a decode layer runs them; 4 calls per M instead of 7.  Same weights, same
+    two replicas alternating between the M passes, same graph replay."""
+    fmats = {}
+    for gname, members in FUSED_GROUPS:
+        reps = [torch.cat([mats[nm]["codes"][r] for nm in members]) for r in range(len(mats["q"]["codes"]))]
+        fmats[gname] = {"codes": reps, "scales": torch.cat([mats[nm]["scales"] for nm in members]),
+                        "bias": torch.cat([mats[nm]["bias"] for nm in members]),
+                        "n": sum(mats[nm]["n"] for nm in members), "k": mats[members[0]]["k"], "x_of": members[0]}
+    calls = [(m, g) for m in synthetic.DECODE_STACK_M for (g, _) in FUSED_GROUPS]
+    ys = {(m, g): torch.empty((m, fmats[g]["n"]), dtype=torch.bfloat16, device=dev) for (m, g) in calls}
+
+    def step():
+        for (m, g) in calls:
+            f = fmats[g]
+            rep = synthetic.DECODE_STACK_M.index(m) % len(f["codes"])
+            fw.linear(xs[(m, f["x_of"])], f["codes"][rep], f["scales"], f["bias"], out=ys[(m, g)])
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=s):
+        step()
+    for _ in range(warmup):
+        gr.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for _ in range(steps):
+            gr.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    nbytes = sum(call_bytes(m, fmats[g]["n"], fmats[g]["k"]) for (m, g) in calls)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    # the fused calls give the parts' outputs (the GEMV bit for bit)
+    x = xs[(1, "q")]
+    yq = torch.empty((1, mats["q"]["n"]), dtype=torch.bfloat16, device=dev)
+    fw.linear(x, mats["q"]["codes"][0], mats["q"]["scales"], mats["q"]["bias"], out=yq)
+    yf = torch.empty((1, fmats["qkv"]["n"]), dtype=torch.bfloat16, device=dev)
+    fw.linear(x, fmats["qkv"]["codes"][0], fmats["qkv"]["scales"], fmats["qkv"]["bias"], out=yf)
+    torch.cuda.synchronize()
+    assert torch.equal(yf[:, :mats["q"]["n"]], yq)
+    del gr
+    return {"value": round(gbs, 2), "unit": "GB/s", "ms_per_step": round(ms, 5), "frac_of_hbm_peak": round(gbs / peak, 4),
+            "calls_per_step": len(calls), "bytes_per_step": nbytes, "steps": steps,
+            "note": "q/k/v and gate/up fused into one call each (concatenated weight rows, one shared x), "
+                    "o and down alone; M = 1, 8, 32; same weights, replicas and graph replay as the main step"}
+
+
 def run_ours(args, torch, dist):
     import fp8_weight_only_gb300 as fw
     ws, rank, local = dist_env()
@@ -446,6 +503,8 @@ def run_ours(args, torch, dist):
     else:
         result["roofline"] = {"bound": "hbm", "achieved": None, "peak": peak, "unit": "GB/s", "frac": None,
                               "traffic": None, "note": "instrumented replay failed: " + instr_err}
+
+    result["fused_stack"] = run_fused(torch, fw, mats, xs, dev, s, min(args.steps, 500), args.warmup, peak)
 
     # quantiser throughput on the seven matrices (load-time step)
     qcodes = {name: torch.empty_like(mats[name]["codes"][0]) for name in wdev}

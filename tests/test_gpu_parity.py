@@ -397,3 +397,49 @@ def test_m1_tensor_core_path_matches_gemv_tolerance():
     yt = gpu_linear(case["x"], 1, codes, scales, case["bias"], kernel=fw.KERNEL_SKINNY)
     c = compare(yt, yg, 1)
     assert c["rel_l2"] <= 2e-3 and c["min_cosine"] >= 0.9999, c
+
+
+# ------------------------------------------------------ fused decode stack --
+
+FUSED = {"qkv": ("q", "k", "v"), "gate_up": ("gate", "up")}
+
+
+@pytest.mark.parametrize("group", list(FUSED))
+def test_fused_weights_quantise_as_their_parts(group):
+    """q/k/v (and gate/up) fused into one weight of concatenated rows: the
+    quantiser is row-wise, so the fused codes and scales are the parts'
+    codes and scales, bit for bit."""
+    ws = [synthetic.case("decode_stack", 1, name)["w"] for name in FUSED[group]]
+    fused_codes, fused_scales = gpu_quantize(np.concatenate(ws))
+    parts = [gpu_quantize(w) for w in ws]
+    assert np.array_equal(fused_codes, np.concatenate([p[0] for p in parts]))
+    assert np.array_equal(fused_scales, np.concatenate([p[1] for p in parts]))
+
+
+@pytest.mark.parametrize("m", synthetic.DECODE_STACK_M)
+@pytest.mark.parametrize("group", list(FUSED))
+def test_fused_linear_matches_its_parts(group, m):
+    """One call over the fused weight and the parts' calls on the same x.
+    At M = 1 every row's sum runs in the same order in both launches, so the
+    outputs are bit-identical; at M = 8 and 32 the tensor-core kernel splits
+    the fused tiles differently, so both are held to the oracle on sampled
+    channels."""
+    cases = [synthetic.case("decode_stack", m, name) for name in FUSED[group]]
+    x = cases[0]["x"]
+    q = [oracle.quantize(c["w"]) for c in cases]
+    codes = np.concatenate([c for c, _ in q])
+    scales = np.concatenate([s for _, s in q])
+    bias = np.concatenate([c["bias"] for c in cases])
+    y = gpu_linear(x, oracle.ACT_BF16, codes, scales, bias)
+    parts = np.concatenate([gpu_linear(x, oracle.ACT_BF16, cq, sq, c["bias"]) for (cq, sq), c in zip(q, cases)],
+                           axis=1)
+    if m == 1:
+        assert np.array_equal(y, parts)
+    n = codes.shape[0]
+    rng = np.random.default_rng(n + m)
+    bounds = np.cumsum([0] + [c["n"] for c in cases])
+    cols = np.unique(np.concatenate([rng.choice(n, size=256, replace=False), bounds[1:-1] - 1, bounds[1:-1],
+                                     [0, n - 1]]))
+    ref = oracle.linear(x, oracle.ACT_BF16, codes[cols], scales[cols], bias[cols], threads=oracle.host_cores())
+    assert_parity(y[:, cols], ref, oracle.ACT_BF16, (group, m))
+    assert_parity(parts[:, cols], ref, oracle.ACT_BF16, (group, m, "parts"))
