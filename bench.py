@@ -72,6 +72,23 @@ def peaks():
 
 # ------------------------------------------------------------ dist helpers --
 
+def job_time_ms(ms_local, dist, device):
+    """The job's timed-region length: the maximum over ranks of each rank's
+    own (every rank timed the same K steps between barriers)."""
+    if dist is None:
+        return ms_local
+    import torch
+    t = torch.tensor([ms_local], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(bytes_per_step, n_ranks, steps, ms_total):
+    """Whole-job throughput in GB/s: the bytes all ranks processed over the
+    job's time (weak scaling: every rank runs the full step)."""
+    return bytes_per_step * n_ranks * steps / (ms_total / 1e3) / 1e9
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -412,14 +429,10 @@ def run_ours(args, torch, dist):
     if dist is not None:
         dist.barrier()
     clocks = sampler.stop()
-    ms_total = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = job_time_ms(e0.elapsed_time(e1), dist, dev)
     ms_step = ms_total / args.steps
     n_ranks = ws
-    value = step_bytes() * n_ranks * args.steps / (ms_total / 1e3) / 1e9
+    value = job_value(step_bytes(), n_ranks, args.steps, ms_total)
 
     # instrumented replay: external events between the launches inside a graph
     per_call = None
