@@ -109,11 +109,17 @@ struct SkinnySmem {
     static constexpr uint32_t kBarOff = kXOff + kXSlots * kXStageBytes;
     // per warpgroup: cfull, cempty [kCodeSlots]
     static constexpr uint32_t kBarsPerLane = 2 * kCodeSlots;
-    // then: aready, afree [6]; xfull, xempty [kXSlots]; dfree [2];
-    // dready [MMA warp][2]; drain [MMA warp]
+    // then: aready [6]; udone [kDoneSlots]; xfull [kXSlots]; dfree [2];
+    // dready [MMA warp][2]; drain [MMA warp].  udone(u % kDoneSlots) completes
+    // a phase when unit u's MMAs are done: it frees the unit's A slot (for
+    // unit u + 6) and its activation slot (for unit u + kXSlots) with one
+    // commit; kDoneSlots is a multiple of both ring sizes, so each waiter
+    // finds the phase of the unit it waits for.
     static constexpr int kASlotsAll = kLanes * kASlots;
+    static constexpr int kDoneSlots = NT == 16 ? 12 : 24;
+    static_assert(kDoneSlots % kASlotsAll == 0 && kDoneSlots % kXSlots == 0, "unit-done ring");
     static constexpr uint32_t kLaneBars = kLanes * kBarsPerLane;
-    static constexpr uint32_t kNumBars = kLaneBars + 2 * kASlotsAll + 2 * kXSlots + 2 + 3 * kMmaWarps;
+    static constexpr uint32_t kNumBars = kLaneBars + kASlotsAll + kDoneSlots + kXSlots + 2 + 3 * kMmaWarps;
     // tmem base, abort flag, last-contributor flag, epilogue abort flag
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
     static constexpr uint32_t kBytes = kMiscOff + 16;
@@ -125,7 +131,7 @@ struct SkinnySmem {
         if (i < kLaneBars) return (i % kBarsPerLane) >= static_cast<uint32_t>(kCodeSlots) ? 4u : 1u;
         const uint32_t gi = i - kLaneBars;
         if (gi < static_cast<uint32_t>(kASlotsAll)) return 4u;  // aready
-        const uint32_t di = static_cast<uint32_t>(2 * kASlotsAll + 2 * kXSlots);
+        const uint32_t di = static_cast<uint32_t>(kASlotsAll + kDoneSlots + kXSlots);
         return (gi == di || gi == di + 1) ? 4u : 1u;            // dfree
     }
 };
@@ -222,13 +228,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto cempty = [&](int g, int s) { return lbar(g, kCS + s); };
     constexpr int kAS = L::kASlotsAll;
     auto gbar = [&](int i) { return bar0 + 8u * (L::kLaneBars + i); };
+    constexpr int kDone = L::kDoneSlots;
     auto aready = [&](int r) { return gbar(r); };
-    auto afree = [&](int r) { return gbar(kAS + r); };
-    auto xfull = [&](int s) { return gbar(2 * kAS + s); };
-    auto xempty = [&](int s) { return gbar(2 * kAS + kXS + s); };
-    auto dfree = [&](int d) { return gbar(2 * kAS + 2 * kXS + d); };
-    auto dready = [&](int w, int d) { return gbar(2 * kAS + 2 * kXS + 2 + 2 * w + d); };
-    auto drain = [&](int w) { return gbar(2 * kAS + 2 * kXS + 2 + 2 * kMmaWarps + w); };
+    auto udone = [&](int i) { return gbar(kAS + i); };
+    auto xfull = [&](int s) { return gbar(kAS + kDone + s); };
+    auto dfree = [&](int d) { return gbar(kAS + kDone + kXS + d); };
+    auto dready = [&](int w, int d) { return gbar(kAS + kDone + kXS + 2 + 2 * w + d); };
+    auto drain = [&](int w) { return gbar(kAS + kDone + kXS + 2 + 2 * kMmaWarps + w); };
+    // unit v's MMAs are done (v < 0: nothing to wait for)
+    auto done_bar = [&](int v) { return udone(v % kDone); };
+    auto done_parity = [&](int v) { return static_cast<uint32_t>((v / kDone) & 1); };
     auto code_smem = [&](int g, int s) { return L::kCodesOff + (g * kCS + s) * kCodeStageBytes; };
     auto x_smem = [&](int s) { return L::kXOff + s * L::kXStageBytes; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
@@ -261,13 +270,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // others; each then arrives at the start-up barrier without waiting and
     // begins streaming, while the other warps wait there for both.
     if (warp <= kXWarp) {
-        const uint32_t xb0 = static_cast<uint32_t>(L::kLaneBars + 2 * kAS);  // xfull, xempty: [xb0, xb1)
-        const uint32_t xb1 = xb0 + static_cast<uint32_t>(2 * kXS);
+        // warp 1 sets up udone and xfull, [xb0, xb1): it is the first to wait on udone
+        const uint32_t xb0 = static_cast<uint32_t>(L::kLaneBars + kAS);
+        const uint32_t xb1 = xb0 + static_cast<uint32_t>(kDone + kXS);
         if (warp == 0) {
             for (uint32_t i = lane; i < L::kNumBars; i += 32)
                 if (i < xb0 || i >= xb1) mbar_init(bar0 + 8 * i, L::arrivals(i));
         } else {
             for (uint32_t i = xb0 + lane; i < xb1; i += 32) mbar_init(bar0 + 8 * i, L::arrivals(i));
+            __syncwarp();
         }
         if (lane == 0) {
             *abort_flag = 0;  // written by both producer warps before either can raise it
@@ -345,8 +356,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t ph = 0;
             int issued = 0;
             for (int it = 0; it < iters; ++it, cu.next()) {
-                if (!mbar_wait(xempty(s), ph ^ 1u, abort_flag)) {
-                    record_error(kErrWaitSlot, abort_flag, xempty(s), bar0);
+                // the slot's previous unit (it - kXS) must be done
+                if (it >= kXS && !mbar_wait(done_bar(it - kXS), done_parity(it - kXS), abort_flag)) {
+                    record_error(kErrWaitSlot, abort_flag, done_bar(it - kXS), bar0);
                     break;
                 }
                 const int32_t kk = cu.kb * kBlockK;
@@ -412,8 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t b_desc = smem_desc_sw128_kmajor(xs + (q >> 2) * L::kXBoxBytes + (q & 3) * 32);
                     mma_f16_ts_warp(d_tmem, a_tmem + q * 8, b_desc, idesc, mine_in_seg || q > 0);
                 }
-                tc_commit_warp(afree(ra));
-                tc_commit_warp(xempty(rx));
+                tc_commit_warp(done_bar(it));  // frees the unit's A and activation slots
                 mine_in_seg = true;
                 ra = ran;
                 rx = rxn;
@@ -667,8 +678,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int q = 0; q < 4; ++q) dequant16<kBf16>(cw[q], v0[q]);
             // A slot of unit it = group + 3j: it % 6 = group + 3 (j % 2)
             const int r = group + kLanes * (j & 1);
-            if (!mbar_wait_warp(afree(r), static_cast<uint32_t>(((j >> 1) & 1) ^ 1), abort_flag)) {
-                record_error(kErrWaitMma, abort_flag, afree(r), bar0);
+            // the A slot's previous unit (it - 6) must be done
+            if (it >= kAS && !mbar_wait_warp(done_bar(it - kAS), done_parity(it - kAS), abort_flag)) {
+                record_error(kErrWaitMma, abort_flag, done_bar(it - kAS), bar0);
                 break;
             }
             tc_fence_after();
