@@ -545,6 +545,27 @@ def run_ours(args, torch, dist):
     for name in wdev:
         assert torch.equal(qcodes[name], mats[name]["codes"][0])
 
+    # dequantiser throughput on the seven matrices (bf16 out, the pages' fallback weight)
+    dq = {name: torch.empty((mats[name]["n"], mats[name]["k"]), dtype=torch.bfloat16, device=dev) for name in wdev}
+    with torch.cuda.stream(s):
+        for name in wdev:
+            fw.dequantize(mats[name]["codes"][0], mats[name]["scales"], out=dq[name])
+        torch.cuda.synchronize()
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        d0.record(s)
+        for r in range(qreps):
+            for name in wdev:
+                fw.dequantize(mats[name]["codes"][r % len(mats[name]["codes"])], mats[name]["scales"], out=dq[name])
+        d1.record(s)
+    torch.cuda.synchronize()
+    dbytes = sum(3 * n * k + 4 * n for (_, n, k) in synthetic.DECODE_STACK)
+    dms = d0.elapsed_time(d1) / qreps
+    result["dequantize"] = {"gbs": round(dbytes / (dms / 1e3) / 1e9, 1), "ms_per_pass": round(dms, 4),
+                            "frac": round(dbytes / (dms / 1e3) / 1e9 / peak, 4), "bytes_per_pass": dbytes,
+                            "note": "7 matrices to bf16, 1 B read + 2 B written per element + 4 B/row, eager launches"}
+    del dq
+
     # end to end through the Python API: pinned host x in, pinned host y out
     hx = {key: t.cpu().pin_memory() for key, t in xs.items()}
     hy = {key: torch.empty(t.shape, dtype=t.dtype).pin_memory() for key, t in ys.items()}

@@ -16,12 +16,13 @@ LIB_PATH = os.path.join(HERE, "libfp8w.so")
 
 FP8W_BF16 = 1
 FP8W_F16 = 2
+FP8W_F32 = 3
 KERNEL_AUTO, KERNEL_GEMV, KERNEL_SKINNY = 0, 1, 2
 
 SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_workspace_size", "fp8w_linear_ex",
            "fp8w_status_string", "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version",
-           "fp8w_linear_noalloc")
-ABI_VERSION = 2
+           "fp8w_linear_noalloc", "fp8w_dequantize")
+ABI_VERSION = 3
 
 
 class Fp8wError(RuntimeError):
@@ -48,6 +49,8 @@ def lib():
         c, P = ctypes, ctypes.c_void_p
         L.fp8w_quantize.restype = c.c_int
         L.fp8w_quantize.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
+        L.fp8w_dequantize.restype = c.c_int
+        L.fp8w_dequantize.argtypes = [P, P, c.c_int64, c.c_int64, c.c_int, P, P]
         L.fp8w_linear.restype = c.c_int
         L.fp8w_linear.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P, c.c_size_t, P]
         L.fp8w_linear_workspace_size.restype = c.c_size_t
@@ -108,6 +111,27 @@ def quantize(w, codes=None, scales=None):
         scales = torch.empty((n,), dtype=torch.float32, device=w.device)
     _check(lib().fp8w_quantize(_ptr(w), n, k, _ptr(codes), _ptr(scales), _stream(w)))
     return codes, scales
+
+
+def dequantize(codes, scales, dtype=None, out=None):
+    """W'[N, K] = e4m3(codes) * scales[:, None], rounded once to `dtype`
+    (torch.float32, bfloat16 or float16; default bfloat16)."""
+    import torch
+    if dtype is None:
+        dtype = out.dtype if out is not None else torch.bfloat16
+    kind = {torch.float32: FP8W_F32, torch.bfloat16: FP8W_BF16, torch.float16: FP8W_F16}.get(dtype)
+    if kind is None:
+        raise TypeError("dequantize: dtype must be float32, bfloat16 or float16, got %s" % dtype)
+    for name, t, dt in (("codes", codes, torch.uint8), ("scales", scales, torch.float32)):
+        if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
+            raise TypeError("%s must be a contiguous %s CUDA tensor" % (name, dt))
+    n, k = codes.shape
+    if out is None:
+        out = torch.empty((n, k), dtype=dtype, device=codes.device)
+    elif out.shape != (n, k) or out.dtype != dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [N, K] tensor of the requested dtype")
+    _check(lib().fp8w_dequantize(_ptr(codes), _ptr(scales), n, k, kind, _ptr(out), _stream(codes)))
+    return out
 
 
 _workspaces = {}

@@ -48,6 +48,17 @@ fp8w_status fp8w_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes, 
                        "fp8w_quantize launch");
 }
 
+fp8w_status fp8w_dequantize(const uint8_t* codes, const float* scales, int64_t n, int64_t k, int out_dtype,
+                            void* w, void* stream) {
+    if (!codes || !scales || !w) return FP8W_ERR_NULL;
+    if (n < 1 || n > FP8W_MAX_DIM || !valid_k(k)) return FP8W_ERR_SHAPE;
+    if (out_dtype != FP8W_F32 && out_dtype != FP8W_BF16 && out_dtype != FP8W_F16) return FP8W_ERR_DTYPE;
+    if (!aligned(codes, 16) || !aligned(scales, 4) || !aligned(w, 16)) return FP8W_ERR_ALIGN;
+    const int kind = out_dtype == FP8W_BF16 ? 1 : out_dtype == FP8W_F16 ? 2 : 0;
+    return cuda_status(fp8w::launch_dequantize(codes, scales, n, k, kind, w, static_cast<cudaStream_t>(stream)),
+                       "fp8w_dequantize launch");
+}
+
 static size_t skinny_ws(void) {
     int sms = 0;
     if (fp8w::device_sm_count(sms) != cudaSuccess) return 0;

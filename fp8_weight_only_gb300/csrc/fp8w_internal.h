@@ -21,6 +21,10 @@ struct LinearArgs {
 cudaError_t launch_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes, float* scales,
                             cudaStream_t st);
 
+// The dequantised weight, rounded once to fp32 (out_dtype 0), bf16 (1) or fp16 (2).
+cudaError_t launch_dequantize(const uint8_t* codes, const float* scales, int64_t n, int64_t k, int out_dtype,
+                              void* w, cudaStream_t st);
+
 // K2: m == 1, k <= 32768 (gemv_supports).
 cudaError_t launch_gemv(const LinearArgs& a, cudaStream_t st);
 bool gemv_supports(int64_t k);

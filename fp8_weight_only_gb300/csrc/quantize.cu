@@ -111,4 +111,114 @@ cudaError_t launch_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ dequantise --
+// Page "kadirnar/kernel-agent fp8-weights", section "The contract" (the
+// fallback: the decoded codes times the row scale): w[n, k] = e4m3(q[n, k]) *
+// scale[n], rounded once to the output type.  The product of a 4-bit and a
+// 24-bit significand needs up to 28 bits, so it is carried as hi = fp32
+// product plus lo = its exact remainder (fmaf); a 16-bit result rounds hi
+// and lets lo decide when hi lies exactly on a rounding midpoint (no other
+// midpoint can lie between hi and the exact product: both are within half
+// an fp32 ulp, and every 16-bit midpoint is an fp32 number).  HBM bytes per
+// element: 1 read + 2 or 4 written.
+
+constexpr int kDequantThreads = 256;
+
+// bf16 nearest-even of hi + lo (|lo| <= half an ulp of hi).
+__device__ __forceinline__ uint16_t exact_to_bf16(float hi, float lo) {
+    const uint32_t t = __float_as_uint(hi);
+    const uint32_t mag = t & 0x7FFFFFFFu;
+    if (mag > 0x7F800000u) return static_cast<uint16_t>((t >> 16) | 0x0040u);  // NaN stays NaN
+    const uint32_t rem = t & 0xFFFFu;
+    // lo's sign towards hi's magnitude
+    const bool lo_up = (lo > 0.0f) == (hi > 0.0f) && lo != 0.0f;
+    const bool lo_dn = lo != 0.0f && !lo_up;
+    uint32_t r = t >> 16;
+    const bool up = rem > 0x8000u || (rem == 0x8000u && (lo_up || (!lo_dn && (r & 1u))));
+    return static_cast<uint16_t>(r + (up ? 1u : 0u));  // a carry moves into the exponent (inf at the top)
+}
+
+// fp16 nearest-even of hi + lo (|lo| <= half an ulp of hi).
+__device__ __forceinline__ uint16_t exact_to_f16(float hi, float lo) {
+    const float a = fabsf(hi);
+    const uint16_t sign = hi < 0.0f || (hi == 0.0f && signbit(hi)) ? 0x8000u : 0u;
+    if (!(a == a)) return 0x7E00u;  // NaN
+    const bool lo_up = lo != 0.0f && ((lo > 0.0f) == (hi > 0.0f));
+    const bool lo_dn = lo != 0.0f && !lo_up;
+    uint16_t m;  // magnitude bits
+    if (a > 65504.0f) {
+        // between the largest finite value and the overflow midpoint 65520
+        m = (a < 65520.0f || (a == 65520.0f && lo_dn)) ? 0x7BFFu : 0x7C00u;
+    } else {
+        const uint16_t dn = __half_as_ushort(__float2half_rd(a)), upb = __half_as_ushort(__float2half_ru(a));
+        if (dn == upb) {
+            m = dn;
+        } else {
+            const float mid = 0.5f * (__half2float(__ushort_as_half(dn)) + __half2float(__ushort_as_half(upb)));
+            if (a != mid) m = a < mid ? dn : upb;
+            else m = lo_up ? upb : lo_dn ? dn : ((dn & 1u) ? upb : dn);
+        }
+    }
+    return static_cast<uint16_t>(m | sign);
+}
+
+// OUT: 0 fp32, 1 bf16, 2 fp16.  Thread i of the grid-stride loop converts the
+// 16 codes of vector i (k % 16 == 0, so a vector lies in one row).
+template <int OUT>
+__global__ void __launch_bounds__(kDequantThreads) dequantize_kernel(const uint8_t* __restrict__ codes,
+                                                                      const float* __restrict__ scales, int64_t k,
+                                                                      int64_t nvec, void* __restrict__ out) {
+    const int64_t vpr = k >> 4;  // vectors per row
+    for (int64_t i = blockIdx.x * static_cast<int64_t>(kDequantThreads) + threadIdx.x; i < nvec;
+         i += static_cast<int64_t>(gridDim.x) * kDequantThreads) {
+        const float s = scales[i / vpr];
+        const uint4 cv = ldg_stream_v4(codes + i * 16);
+        const uint32_t w4[4] = {cv.x, cv.y, cv.z, cv.w};
+        uint32_t o[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t p01, p23;
+            e4m3x4_to_f16x2(w4[q], p01, p23);
+            const float c[4] = {f16_lo_to_f32(p01), f16_hi_to_f32(p01), f16_lo_to_f32(p23), f16_hi_to_f32(p23)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float hi = __fmul_rn(c[e], s);
+                if constexpr (OUT == 0) {
+                    o[4 * q + e] = __float_as_uint(hi);
+                } else {
+                    const float lo = fmaf(c[e], s, -hi);
+                    o[4 * q + e] = OUT == 1 ? exact_to_bf16(hi, lo) : exact_to_f16(hi, lo);
+                }
+            }
+        }
+        if constexpr (OUT == 0) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(out) + i * 16);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
+        } else {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + i * 16);
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+                dst[q] = make_uint4(o[8 * q] | (o[8 * q + 1] << 16), o[8 * q + 2] | (o[8 * q + 3] << 16),
+                                    o[8 * q + 4] | (o[8 * q + 5] << 16), o[8 * q + 6] | (o[8 * q + 7] << 16));
+        }
+    }
+}
+
+cudaError_t launch_dequantize(const uint8_t* codes, const float* scales, int64_t n, int64_t k, int out_dtype,
+                              void* w, cudaStream_t st) {
+    int sms = 0;
+    cudaError_t e = device_sm_count(sms);
+    if (e != cudaSuccess) return e;
+    const int64_t nvec = n * (k >> 4);
+    int64_t blocks = (nvec + kDequantThreads - 1) / kDequantThreads;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 CTAs of 256 threads per SM
+    if (blocks > cap) blocks = cap;
+    const unsigned g = static_cast<unsigned>(blocks);
+    if (out_dtype == 1) dequantize_kernel<1><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nvec, w);
+    else if (out_dtype == 2) dequantize_kernel<2><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nvec, w);
+    else dequantize_kernel<0><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nvec, w);
+    return cudaGetLastError();
+}
+
 }  // namespace fp8w

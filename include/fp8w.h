@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define FP8W_ABI_VERSION 2
+#define FP8W_ABI_VERSION 3
 
 #if defined(__GNUC__)
 #define FP8W_API __attribute__((visibility("default")))
@@ -60,8 +60,8 @@ typedef enum fp8w_status {
                                scratch than the library's static maximum */
 } fp8w_status;
 
-/* Activation / output dtypes. */
-enum { FP8W_BF16 = 1, FP8W_F16 = 2 };
+/* Activation / output dtypes (FP8W_F32: fp8w_dequantize's output only). */
+enum { FP8W_BF16 = 1, FP8W_F16 = 2, FP8W_F32 = 3 };
 
 /* Largest supported reduction length and row count. */
 #define FP8W_MAX_K 65536
@@ -83,6 +83,26 @@ enum { FP8W_BF16 = 1, FP8W_F16 = 2 };
  */
 FP8W_API fp8w_status fp8w_quantize(const float *w, int64_t n, int64_t k,
                           uint8_t *codes, float *scales, void *stream);
+
+/*
+ * fp8w_dequantize -- the dequantised weight, the pages' fallback form
+ * (page "kadirnar/kernel-agent fp8-weights", section "The contract": the
+ * codes decoded and multiplied by their row's scale).
+ *
+ *   codes  [n, k] e4m3 bytes, device, 16-byte aligned.
+ *   scales [n] fp32, device, 4-byte aligned.
+ *   out_dtype FP8W_F32, FP8W_BF16 or FP8W_F16.
+ *   w      [n, k] of out_dtype, device, 16-byte aligned (output).
+ *   1 <= n <= FP8W_MAX_DIM, 16 <= k <= FP8W_MAX_K, k % 16 == 0.
+ *
+ * w[r, c] = e4m3(codes[r, c]) * scales[r], the exact product rounded once to
+ * out_dtype (nearest even).  For bf16 the rounding is exact while the
+ * product is an fp32 normal number (|product| >= 2^-126); below that, a bf16
+ * tie may be broken to even where the exact value lies off it.  NaN codes
+ * give NaN.
+ */
+FP8W_API fp8w_status fp8w_dequantize(const uint8_t *codes, const float *scales, int64_t n,
+                            int64_t k, int out_dtype, void *w, void *stream);
 
 /*
  * fp8w_linear -- steps "stream codes", "decode", "contract", "epilogue" and

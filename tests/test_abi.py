@@ -116,3 +116,14 @@ def test_noalloc_entry_rejects_bad_arguments_on_the_host(kw, status):
     L = fw.lib()
     assert L.fp8w_linear_noalloc(a["x"], a["act"], a["m"], a["k"], a["codes"], a["scales"], a["bias"],
                                  a["n"], a["y"], None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, C16, 4, 64, 1, D16), 1), ((B16, None, 4, 64, 1, D16), 1), ((B16, C16, 4, 64, 1, None), 1),
+    ((B16, C16, 0, 64, 1, D16), 2), ((B16, C16, 4, 24, 1, D16), 2), ((B16, C16, 4, 65536 + 16, 1, D16), 2),
+    ((B16, C16, 4, 64, 0, D16), 4), ((B16, C16, 4, 64, 7, D16), 4),
+    ((ctypes.c_void_p(0x200004), C16, 4, 64, 1, D16), 3), ((B16, ctypes.c_void_p(0x300002), 4, 64, 1, D16), 3),
+    ((B16, C16, 4, 64, 3, ctypes.c_void_p(0x400008)), 3),
+])
+def test_dequantize_rejects_bad_arguments(args, status):
+    assert fw.lib().fp8w_dequantize(*args, None) == status

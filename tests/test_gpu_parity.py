@@ -443,3 +443,102 @@ def test_fused_linear_matches_its_parts(group, m):
     ref = oracle.linear(x, oracle.ACT_BF16, codes[cols], scales[cols], bias[cols], threads=oracle.host_cores())
     assert_parity(y[:, cols], ref, oracle.ACT_BF16, (group, m))
     assert_parity(parts[:, cols], ref, oracle.ACT_BF16, (group, m, "parts"))
+
+
+# ------------------------------------------------------------ dequantise --
+
+def _oracle_dequant_bits(codes, scales, dtype):
+    """The oracle's exact product rounded once to dtype, as raw bits."""
+    w = oracle.dequantize(codes, scales)
+    if dtype == torch.float32:
+        return w.astype(np.float32).view(np.uint32)
+    return (oracle.round_bf16(w) if dtype == torch.bfloat16 else oracle.round_f16(w)).reshape(w.shape)
+
+
+def _gpu_dequant_bits(codes, scales, dtype):
+    c = torch.from_numpy(np.ascontiguousarray(codes)).to(DEV)
+    s = torch.from_numpy(np.ascontiguousarray(scales)).to(DEV)
+    n, k = codes.shape
+    esize = 4 if dtype == torch.float32 else 2
+    buf = torch.full(((n * k + 2 * CANARY) * esize,), 0xA5, dtype=torch.uint8, device=DEV)
+    out = buf[CANARY * esize:(CANARY + n * k) * esize].view(dtype).view(n, k)
+    fw.dequantize(c, s, dtype=dtype, out=out)
+    torch.cuda.synchronize()
+    assert bool((buf[:CANARY * esize] == 0xA5).all()) and bool((buf[(CANARY + n * k) * esize:] == 0xA5).all())
+    raw = out.view(torch.int32 if esize == 4 else torch.int16).cpu().numpy()
+    return raw.view(np.uint32 if esize == 4 else np.uint16)
+
+
+DQ_TYPES = [torch.float32, torch.bfloat16, torch.float16]
+
+
+@pytest.mark.parametrize("dtype", DQ_TYPES)
+@pytest.mark.parametrize("n,k", [(1, 16), (37, 1040), (300, 4096), (1024, 14336)])
+def test_dequantize_bit_exact(n, k, dtype):
+    rng = np.random.default_rng(n + k)
+    codes = rng.integers(0, 256, size=(n, k), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3A               # NaN codes are tested apart
+    # scales over a wide range, fp16 outputs kept within fp16's range
+    hi_exp = 6 if dtype == torch.float16 else 60
+    scales = (2.0 ** rng.uniform(-30, hi_exp, size=n) * rng.uniform(1, 2, size=n)).astype(np.float32)
+    got = _gpu_dequant_bits(codes, scales, dtype)
+    want = _oracle_dequant_bits(codes, scales, dtype)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, (bad[:5], got[tuple(bad[0])], want[tuple(bad[0])])
+
+
+def _tie_cases(bits_fn, lo_range, hi_range, mask, tie, seed, rounds=20):
+    """(code, scale) pairs whose fp32 product lies exactly on a rounding
+    midpoint of the 16-bit type while the exact product does not: the case
+    where rounding the fp32 product again would round twice."""
+    t = oracle.e4m3_decode_table()
+    pos = np.array([b for b in range(1, 127) if np.isfinite(t[b])], dtype=np.uint8)
+    rng = np.random.default_rng(seed)
+    found_c, found_s = [], []
+    for _ in range(rounds):
+        s = rng.uniform(lo_range, hi_range, size=200_000).astype(np.float32)
+        c = rng.choice(pos, size=s.size)
+        p = t[c] * s.astype(np.float64)
+        hi = p.astype(np.float32)
+        sel = ((bits_fn(hi) & mask) == tie) & (hi.astype(np.float64) != p)
+        found_c.append(c[sel])
+        found_s.append(s[sel])
+    c = np.concatenate(found_c)
+    s = np.concatenate(found_s)
+    sign = (np.arange(c.size) % 2 * 0x80).astype(np.uint8)   # half of them negative
+    return np.repeat((c | sign)[:, None], 16, axis=1), s
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_dequantize_rounds_once_at_exact_midpoints(dtype):
+    if dtype == torch.bfloat16:
+        codes, scales = _tie_cases(lambda h: h.view(np.uint32), 1e-4, 1e-1, 0xFFFF, 0x8000, 21, rounds=60)
+    else:
+        # fp16 normal range: the 13 low mantissa bits of the fp32 midpoint are 1000000000000
+        codes, scales = _tie_cases(lambda h: h.view(np.uint32), 1e-2, 10.0, 0x1FFF, 0x1000, 22)
+        keep = np.abs(oracle.dequantize(codes[:, :1], scales)[:, 0]) >= 2.0 ** -14
+        codes, scales = codes[keep], scales[keep]
+    assert codes.shape[0] >= 50
+    got = _gpu_dequant_bits(codes, scales, dtype)
+    want = _oracle_dequant_bits(codes, scales, dtype)
+    assert np.array_equal(got, want)
+    # the cases matter: rounding the fp32 product again differs from the exact rounding in some
+    hi = (oracle.dequantize(codes, scales)).astype(np.float32).astype(np.float64)
+    twice = (oracle.round_bf16(hi) if dtype == torch.bfloat16 else oracle.round_f16(hi)).reshape(hi.shape)
+    assert np.count_nonzero(twice != want) > 0
+
+
+@pytest.mark.parametrize("dtype", DQ_TYPES)
+def test_dequantize_nan_codes_give_nan(dtype):
+    codes = np.tile(np.array([0x7F, 0xFF, 0x00, 0x80], np.uint8), (2, 4))
+    got = _gpu_dequant_bits(codes, np.float32([0.5, 3.0]), dtype)
+    vals = torch.from_numpy(got.view(np.int32 if dtype == torch.float32 else np.int16)).view(dtype).float().numpy()
+    assert np.isnan(vals[:, 0::4]).all() and np.isnan(vals[:, 1::4]).all()
+    assert (vals[:, 2::4] == 0).all() and (vals[:, 3::4] == 0).all()
+
+
+def test_dequantize_of_quantize_is_the_oracle_fallback_weight():
+    case = synthetic.case("decode_stack", 1, "k")
+    codes, scales = gpu_quantize(case["w"])
+    got = _gpu_dequant_bits(codes, scales, torch.float32)
+    assert np.array_equal(got, oracle.dequantize(codes, scales).astype(np.float32).view(np.uint32))
