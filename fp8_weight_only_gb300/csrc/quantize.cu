@@ -124,83 +124,133 @@ cudaError_t launch_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes
 
 constexpr int kDequantThreads = 256;
 
-// bf16 nearest-even of hi + lo (|lo| <= half an ulp of hi).
-__device__ __forceinline__ uint16_t exact_to_bf16(float hi, float lo) {
+// bf16 nearest-even of the exact product c * s, hi = fp32(c * s).  The
+// hardware rounds hi; only when hi sits exactly on a bf16 midpoint (its low
+// 16 bits are 0x8000) does the remainder lo = c * s - hi decide.
+__device__ __forceinline__ uint16_t exact_to_bf16(float hi, float c, float s) {
     const uint32_t t = __float_as_uint(hi);
-    const uint32_t mag = t & 0x7FFFFFFFu;
-    if (mag > 0x7F800000u) return static_cast<uint16_t>((t >> 16) | 0x0040u);  // NaN stays NaN
-    const uint32_t rem = t & 0xFFFFu;
-    // lo's sign towards hi's magnitude
-    const bool lo_up = (lo > 0.0f) == (hi > 0.0f) && lo != 0.0f;
-    const bool lo_dn = lo != 0.0f && !lo_up;
-    uint32_t r = t >> 16;
-    const bool up = rem > 0x8000u || (rem == 0x8000u && (lo_up || (!lo_dn && (r & 1u))));
-    return static_cast<uint16_t>(r + (up ? 1u : 0u));  // a carry moves into the exponent (inf at the top)
-}
-
-// fp16 nearest-even of hi + lo (|lo| <= half an ulp of hi).
-__device__ __forceinline__ uint16_t exact_to_f16(float hi, float lo) {
-    const float a = fabsf(hi);
-    const uint16_t sign = hi < 0.0f || (hi == 0.0f && signbit(hi)) ? 0x8000u : 0u;
-    if (!(a == a)) return 0x7E00u;  // NaN
-    const bool lo_up = lo != 0.0f && ((lo > 0.0f) == (hi > 0.0f));
-    const bool lo_dn = lo != 0.0f && !lo_up;
-    uint16_t m;  // magnitude bits
-    if (a > 65504.0f) {
-        // between the largest finite value and the overflow midpoint 65520
-        m = (a < 65520.0f || (a == 65520.0f && lo_dn)) ? 0x7BFFu : 0x7C00u;
-    } else {
-        const uint16_t dn = __half_as_ushort(__float2half_rd(a)), upb = __half_as_ushort(__float2half_ru(a));
-        if (dn == upb) {
-            m = dn;
-        } else {
-            const float mid = 0.5f * (__half2float(__ushort_as_half(dn)) + __half2float(__ushort_as_half(upb)));
-            if (a != mid) m = a < mid ? dn : upb;
-            else m = lo_up ? upb : lo_dn ? dn : ((dn & 1u) ? upb : dn);
-        }
+    uint16_t r = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+    if ((t & 0xFFFFu) == 0x8000u) {
+        const float lo = fmaf(c, s, -hi);
+        // on lo's side of the midpoint: away from zero when lo has hi's sign
+        if (lo != 0.0f) r = static_cast<uint16_t>((t >> 16) + (((__float_as_uint(lo) ^ t) >> 31) ^ 1u));
     }
-    return static_cast<uint16_t>(m | sign);
+    return r;
 }
 
-// OUT: 0 fp32, 1 bf16, 2 fp16.  Thread i of the grid-stride loop converts the
-// 16 codes of vector i (k % 16 == 0, so a vector lies in one row).
+// fp16 nearest-even of the exact product c * s, hi = fp32(c * s).  The
+// hardware rounds hi; only when hi may sit exactly on a midpoint (its 12 low
+// mantissa bits are zero, a necessary condition in fp16's normal and
+// subnormal ranges) and the remainder lo = c * s - hi is not zero does the
+// exact product need a look.
+__device__ __forceinline__ uint16_t exact_to_f16(float hi, float c, float s) {
+    const uint16_t r = __half_as_ushort(__float2half_rn(hi));
+    const uint32_t t = __float_as_uint(hi);
+    if ((t & 0xFFFu) != 0u || (t & 0x7FFFFFFFu) >= 0x7F800000u) return r;
+    const float lo = fmaf(c, s, -hi);
+    if (lo == 0.0f) return r;
+    const uint16_t sign = static_cast<uint16_t>(r & 0x8000u), rm = static_cast<uint16_t>(r & 0x7FFFu);
+    const float a = fabsf(hi);
+    float back, other;
+    uint16_t om;  // the other candidate's magnitude bits
+    if (rm == 0x7C00u) {  // rounded to inf: the candidates are 65504 and inf, the midpoint 65520
+        back = 65536.0f;
+        om = 0x7BFFu;
+        other = 65504.0f;
+    } else {
+        back = __half2float(__ushort_as_half(rm));
+        if (back == a) return r;  // hi itself is an fp16 value
+        om = static_cast<uint16_t>(a > back ? rm + 1u : rm - 1u);
+        other = om == 0x7C00u ? 65536.0f : __half2float(__ushort_as_half(om));
+    }
+    if (a != 0.5f * (back + other)) return r;  // not a midpoint: hi's rounding is the exact one
+    // on the midpoint: the exact product lies on lo's side (away from zero when lo has hi's sign)
+    const bool away = (lo > 0.0f) == (hi > 0.0f);
+    const uint16_t lower = back < other ? rm : om, upper = back < other ? om : rm;
+    return static_cast<uint16_t>(sign | (away ? upper : lower));
+}
+
+constexpr int kDequantUnroll = 4;  // chunks a thread has in flight
+
+// OUT: 0 fp32, 1 bf16, 2 fp16.  A chunk is C codes (8 for 16-bit outputs,
+// whose 16 bytes a lane stores at once, 4 for fp32), so a warp's loads and
+// stores are contiguous; k % 16 == 0, so a chunk lies in one row.  Thread t
+// converts the chunks t, t + P, t + 2P, ... (P = the grid's threads),
+// kDequantUnroll at a time with all their loads issued first; each of its
+// kDequantUnroll sequences tracks its row as it advances (one division per
+// sequence).
 template <int OUT>
 __global__ void __launch_bounds__(kDequantThreads) dequantize_kernel(const uint8_t* __restrict__ codes,
                                                                       const float* __restrict__ scales, int64_t k,
-                                                                      int64_t nvec, void* __restrict__ out) {
-    const int64_t vpr = k >> 4;  // vectors per row
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(kDequantThreads) + threadIdx.x; i < nvec;
-         i += static_cast<int64_t>(gridDim.x) * kDequantThreads) {
-        const float s = scales[i / vpr];
-        const uint4 cv = ldg_stream_v4(codes + i * 16);
-        const uint32_t w4[4] = {cv.x, cv.y, cv.z, cv.w};
-        uint32_t o[16];
+                                                                      int64_t nchunk, void* __restrict__ out) {
+    constexpr int U = kDequantUnroll;
+    constexpr int C = OUT == 0 ? 4 : 8;
+    const int64_t cpr = k / C;  // chunks per row
+    const int64_t P = static_cast<int64_t>(gridDim.x) * kDequantThreads;
+    const int64_t step = U * P;
+    const int64_t srow = step / cpr, scol = step - srow * cpr;
+    const int64_t i0 = blockIdx.x * static_cast<int64_t>(kDequantThreads) + threadIdx.x;
+    int64_t row[U], col[U];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            uint32_t p01, p23;
-            e4m3x4_to_f16x2(w4[q], p01, p23);
-            const float c[4] = {f16_lo_to_f32(p01), f16_hi_to_f32(p01), f16_lo_to_f32(p23), f16_hi_to_f32(p23)};
+    for (int u = 0; u < U; ++u) {
+        const int64_t v = i0 + u * P;
+        row[u] = v / cpr;
+        col[u] = v - row[u] * cpr;
+    }
+    for (int64_t i = i0; i < nchunk; i += step) {
+        uint32_t cw[U][C / 4];
+        float sc[U];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float hi = __fmul_rn(c[e], s);
-                if constexpr (OUT == 0) {
-                    o[4 * q + e] = __float_as_uint(hi);
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = i + u * P;
+            if (v < nchunk) {
+                if constexpr (C == 8) {
+                    const uint2 c2 = __ldcs(reinterpret_cast<const uint2*>(codes) + v);
+                    cw[u][0] = c2.x;
+                    cw[u][C / 4 - 1] = c2.y;
                 } else {
-                    const float lo = fmaf(c[e], s, -hi);
-                    o[4 * q + e] = OUT == 1 ? exact_to_bf16(hi, lo) : exact_to_f16(hi, lo);
+                    cw[u][0] = __ldcs(reinterpret_cast<const uint32_t*>(codes) + v);
                 }
+                sc[u] = scales[row[u]];
             }
         }
-        if constexpr (OUT == 0) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<float*>(out) + i * 16);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) dst[q] = make_uint4(o[4 * q], o[4 * q + 1], o[4 * q + 2], o[4 * q + 3]);
-        } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + i * 16);
+        for (int u = 0; u < U; ++u) {
+            const int64_t v = i + u * P;
+            if (v >= nchunk) break;
+            const float s = sc[u];
+            uint32_t o[C];
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
-                dst[q] = make_uint4(o[8 * q] | (o[8 * q + 1] << 16), o[8 * q + 2] | (o[8 * q + 3] << 16),
-                                    o[8 * q + 4] | (o[8 * q + 5] << 16), o[8 * q + 6] | (o[8 * q + 7] << 16));
+            for (int q = 0; q < C / 4; ++q) {
+                uint32_t p01, p23;
+                e4m3x4_to_f16x2(cw[u][q], p01, p23);
+                const float c[4] = {f16_lo_to_f32(p01), f16_hi_to_f32(p01), f16_lo_to_f32(p23), f16_hi_to_f32(p23)};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float hi = __fmul_rn(c[e], s);
+                    if constexpr (OUT == 0) {
+                        o[4 * q + e] = __float_as_uint(hi);
+                    } else {
+                        o[4 * q + e] = OUT == 1 ? exact_to_bf16(hi, c[e], s) : exact_to_f16(hi, c[e], s);
+                    }
+                }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out) + v;
+            if constexpr (OUT == 0) {
+                __stcs(dst, make_uint4(o[0], o[1], o[2], o[3]));
+            } else {
+                __stcs(dst, make_uint4(o[0] | (o[1] << 16), o[2] | (o[3] << 16), o[4] | (o[5] << 16),
+                                       o[6] | (o[7] << 16)));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            row[u] += srow;
+            col[u] += scol;
+            if (col[u] >= cpr) {
+                col[u] -= cpr;
+                ++row[u];
+            }
         }
     }
 }
@@ -210,14 +260,14 @@ cudaError_t launch_dequantize(const uint8_t* codes, const float* scales, int64_t
     int sms = 0;
     cudaError_t e = device_sm_count(sms);
     if (e != cudaSuccess) return e;
-    const int64_t nvec = n * (k >> 4);
-    int64_t blocks = (nvec + kDequantThreads - 1) / kDequantThreads;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;  // 8 CTAs of 256 threads per SM
+    const int64_t nchunk = n * (k / (out_dtype == 0 ? 4 : 8));
+    int64_t blocks = (nchunk + kDequantThreads * kDequantUnroll - 1) / (kDequantThreads * kDequantUnroll);
+    const int64_t cap = static_cast<int64_t>(sms) * 8;  // up to 8 CTAs of 256 threads per SM
     if (blocks > cap) blocks = cap;
     const unsigned g = static_cast<unsigned>(blocks);
-    if (out_dtype == 1) dequantize_kernel<1><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nvec, w);
-    else if (out_dtype == 2) dequantize_kernel<2><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nvec, w);
-    else dequantize_kernel<0><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nvec, w);
+    if (out_dtype == 1) dequantize_kernel<1><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nchunk, w);
+    else if (out_dtype == 2) dequantize_kernel<2><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nchunk, w);
+    else dequantize_kernel<0><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nchunk, w);
     return cudaGetLastError();
 }
 
