@@ -22,7 +22,7 @@ KERNEL_AUTO, KERNEL_GEMV, KERNEL_SKINNY = 0, 1, 2
 SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_workspace_size", "fp8w_linear_ex",
            "fp8w_status_string", "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version",
            "fp8w_linear_noalloc", "fp8w_dequantize")
-ABI_VERSION = 3
+ABI_VERSION = 4
 
 
 class Fp8wError(RuntimeError):

@@ -92,15 +92,18 @@ constexpr int kTmemCols = 512;              // one CTA per SM
 constexpr int kAColsPerSlot = kBlockK / 2;  // two 16-bit values per column
 constexpr int kDCol0 = kLanes * kASlots * kAColsPerSlot;  // 384: accumulators after the A slots
 constexpr uint32_t kCodeStageBytes = kTileN * kBlockK;  // 16 KB
-constexpr int kMaxNT = 32;
-static_assert(kDCol0 + kMmaWarps * 2 * kMaxNT <= kTmemCols, "TMEM columns");
+constexpr int kMaxNT = 64;
 
 template <int NT>
 struct SkinnySmem {
     // per warpgroup: freed as soon as read (9 tiles in flight per SM: deeper
     // rings on every SM make the HBM stream slower, not faster)
-    static constexpr int kCodeSlots = 3;
+    static constexpr int kCodeSlots = NT <= 32 ? 3 : 2;
     static constexpr int kXSlots = NT == 16 ? 12 : 8;  // activation ring (freed when the unit's MMAs are done)
+    // accumulator buffers per MMA warp: two (the epilogue drains one tile
+    // while the next accumulates) where TMEM has room, one for 64 tokens
+    static constexpr int kDBuf = NT <= 32 ? 2 : 1;
+    static_assert(kDCol0 + kMmaWarps * kDBuf * NT <= kTmemCols, "TMEM columns");
     static_assert(kXSlots % kMmaWarps == 0 && (kLanes * kASlots) % kMmaWarps == 0, "slots alternate between MMA warps");
     static constexpr uint32_t kXBoxBytes = NT * 128;          // 64 k x NT rows x 2 B
     static constexpr uint32_t kXStageBytes = 2 * kXBoxBytes;  // 128 k
@@ -398,9 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             failed = true;
         }
         for (int it = 0; it < iters && !failed; ++it) {
-            const int d = seg & 1;
+            const int d = seg % L::kDBuf;
             if (jj == 0 &&
-                !mbar_wait_warp(dfree(d), static_cast<uint32_t>(((seg >> 1) & 1) ^ 1), abort_flag)) {
+                !mbar_wait_warp(dfree(d), static_cast<uint32_t>(((seg / L::kDBuf) & 1) ^ 1), abort_flag)) {
                 // the epilogue has not drained this accumulator (two segments ago)
                 if (lane == 0) record_error(kErrWaitMma, abort_flag, dfree(d), bar0);
                 break;
@@ -418,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t xs = sbase + x_smem(rx);
                 const uint32_t a_tmem = tmem + ra * kAColsPerSlot;  // slot ra = (group ra % 3, A slot ra / 3)
-                const uint32_t d_tmem = tmem + kDCol0 + (w * 2 + d) * NT;
+                const uint32_t d_tmem = tmem + kDCol0 + (w * L::kDBuf + d) * NT;
 #pragma unroll
                 for (int q = 0; q < kBlockK / 16; ++q) {
                     const uint64_t b_desc = smem_desc_sw128_kmajor(xs + (q >> 2) * L::kXBoxBytes + (q & 3) * 32);
@@ -479,7 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int it0 = it;
             it += seg_len;
             for (int jj = 0; jj < seg_len; ++jj) cu.next();
-            const int d = seg & 1;
+            const int d = seg % L::kDBuf;
             int64_t c_lo = 0, c_hi = 0;
             bool all_in = false;
             if (!whole && split == 1) {
@@ -492,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bool ok = true;
             for (int w = 0; w < kMmaWarps; ++w)
-                ok = mbar_wait_warp(dready(w, d), static_cast<uint32_t>((seg >> 1) & 1), abort_flag) && ok;
+                ok = mbar_wait_warp(dready(w, d), static_cast<uint32_t>((seg / L::kDBuf) & 1), abort_flag) && ok;
             if (!ok) {
                 if (lane == 0) *ep_abort = 1;
                 record_error(kErrWaitMma, abort_flag);
@@ -532,7 +535,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int w = 0; w < kMmaWarps; ++w) {
                     if (seg_len < kMmaWarps && ((it0 + kMmaWarps - w) % kMmaWarps) >= seg_len) continue;
                     uint32_t v[16];
-                    tmem_ld_x16(lane_addr + kDCol0 + (w * 2 + d) * NT + h * 16, v);
+                    tmem_ld_x16(lane_addr + kDCol0 + (w * L::kDBuf + d) * NT + h * 16, v);
                     tmem_wait_ld();
 #pragma unroll
                     for (int q = 0; q < 16; ++q) acc[q] += __uint_as_float(v[q]);
@@ -872,8 +875,8 @@ static cudaError_t launch_nt(const LinearArgs& a, void* workspace, int ctas, cud
     cfg.attrs = attr;
     cfg.numAttrs = shape.split > 1 ? 2 : 1;
     uint16_t* yp = static_cast<uint16_t*>(a.y);
-    for (int64_t m0 = 0; m0 < a.m; m0 += kMaxNT) {
-        const int rows = static_cast<int>(a.m - m0 < kMaxNT ? a.m - m0 : kMaxNT);
+    for (int64_t m0 = 0; m0 < a.m; m0 += NT) {
+        const int rows = static_cast<int>(a.m - m0 < NT ? a.m - m0 : NT);
         e = cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, a.scales, a.bias, yp + m0 * a.n,
                                static_cast<uint8_t*>(workspace), rows, static_cast<int>(m0), a.n, a.k, shape.split);
         if (e != cudaSuccess) return e;
@@ -887,7 +890,11 @@ cudaError_t launch_skinny(const LinearArgs& a, void* workspace, int ctas, cudaSt
     const bool bf16 = a.act == 1;
     if (a.m <= 16)
         return bf16 ? launch_nt<16, true>(a, workspace, ctas, st) : launch_nt<16, false>(a, workspace, ctas, st);
-    return bf16 ? launch_nt<32, true>(a, workspace, ctas, st) : launch_nt<32, false>(a, workspace, ctas, st);
+    if (a.m <= 32)
+        return bf16 ? launch_nt<32, true>(a, workspace, ctas, st) : launch_nt<32, false>(a, workspace, ctas, st);
+    // 64 tokens a launch (slabs of 64 beyond): each weight tile is dequantised
+    // once for all of them
+    return bf16 ? launch_nt<64, true>(a, workspace, ctas, st) : launch_nt<64, false>(a, workspace, ctas, st);
 }
 
 // Library-owned scratch for fp8w_linear_noalloc: the workspace of a grid of

@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define FP8W_ABI_VERSION 3
+#define FP8W_ABI_VERSION 4
 
 #if defined(__GNUC__)
 #define FP8W_API __attribute__((visibility("default")))
@@ -125,8 +125,8 @@ FP8W_API fp8w_status fp8w_dequantize(const uint8_t *codes, const float *scales, 
  *   k % 16 == 0.  x and y must not overlap codes, scales, bias or workspace.
  *
  * m == 1 with k <= 32768 runs the GEMV kernel; everything else the
- * tensor-core kernel, one launch per 32 rows of x (m > 32 re-streams the
- * weight per slab: correct, not tuned).
+ * tensor-core kernel: one launch for m <= 64 (16, 32 or 64 token columns),
+ * one launch per 64 rows of x beyond (each re-streams the weight).
  */
 FP8W_API fp8w_status fp8w_linear(const void *x, int act_dtype, int64_t m, int64_t k,
                         const uint8_t *codes, const float *scales,
@@ -183,7 +183,7 @@ FP8W_API fp8w_status fp8w_linear_ex(const void *x, int act_dtype, int64_t m, int
  * return wrong results: keep them in one stream, or use fp8w_linear with a
  * workspace per stream.
  */
-#define FP8W_STATIC_SCRATCH_BYTES 5246976u
+#define FP8W_STATIC_SCRATCH_BYTES 10489856u
 FP8W_API fp8w_status fp8w_linear_noalloc(const void *x, int act_dtype, int64_t m, int64_t k,
                                 const uint8_t *codes, const float *scales,
                                 const float *bias, int64_t n, void *y, void *stream);

@@ -169,7 +169,7 @@ SHAPES = [  # (m, n, k): several tiles and ragged tails in n and k
     (1, 64, 20000 // 16 * 16), (1, 40, 65536),
     (2, 300, 1040), (3, 129, 4096), (4, 1024, 1024), (7, 257, 2064), (8, 640, 4096),
     (16, 300, 1040), (17, 300, 1040), (22, 4096, 1024), (31, 129, 256), (32, 1000, 4096),
-    (33, 300, 1040), (70, 260, 528), (2, 128, 16), (5, 513, 14336),
+    (33, 300, 1040), (70, 260, 528), (2, 128, 16), (5, 513, 14336), (64, 1000, 4096), (129, 300, 2064),
 ]
 
 
@@ -191,7 +191,7 @@ def test_linear_parity(m, n, k, act):
     (300, 14336),    # 3 tiles x 112 k-blocks: ~50 CTAs per tile
     (20000, 272),    # 157 tiles x 3 (ragged k): tiles straddling CTAs
 ])
-@pytest.mark.parametrize("m", [1, 2, 9, 32])
+@pytest.mark.parametrize("m", [1, 2, 9, 32, 48, 64])
 def test_tensor_core_partitions(m, n, k):
     """Stream-K partitions of every kind: whole tiles, tiles shared by two or
     by many CTAs (finished from the workspace by the last to arrive), fewer
@@ -268,7 +268,7 @@ def test_workspace_left_ready_across_shapes():
 
 @pytest.mark.parametrize("act", [oracle.ACT_BF16, oracle.ACT_F16])
 @pytest.mark.parametrize("kernel,m", [(fw.KERNEL_GEMV, 1), (fw.KERNEL_SKINNY, 1), (fw.KERNEL_SKINNY, 5),
-                                      (fw.KERNEL_SKINNY, 32)])
+                                      (fw.KERNEL_SKINNY, 32), (fw.KERNEL_SKINNY, 64)])
 def test_exact_cases_bit_identical(kernel, m, act):
     """Power-of-two scales, small-integer activations and weights whose codes
     lie in [1/8, 8] (plus the 448 that fixes the scale): every product and
