@@ -49,6 +49,11 @@ def _load():
         lib.oracle_linear.restype = c.c_int
         lib.oracle_linear.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P,
                                       c.c_int64, P, P, c.c_int]
+        lib.oracle_quantize_grouped.restype = None
+        lib.oracle_quantize_grouped.argtypes = [P, c.c_int64, c.c_int64, c.c_int64, P, P]
+        lib.oracle_linear_grouped.restype = c.c_int
+        lib.oracle_linear_grouped.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, c.c_int64, P,
+                                              c.c_int64, P, P, c.c_int]
         lib.oracle_fp8_error.restype = None
         lib.oracle_fp8_error.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
         lib.oracle_e4m3_encode_many.restype = None
@@ -158,6 +163,39 @@ def linear(x_bits, act: int, codes, scales, bias=None, threads: int = 1,
                                _ptr(bias), n, _ptr(y), _ptr(acc), int(threads))
     if rc != 0:
         raise RuntimeError("oracle.linear: thread start failed")
+    return (y, acc) if want_acc else y
+
+
+def quantize_grouped(w, group: int):
+    """W[N,K] fp32 -> (codes uint8 [N,K], scales fp32 [N, K/group]): one
+    scale per run of `group` weights of a row, each by the per-row rule."""
+    w = _c(w, np.float32)
+    n, k = w.shape
+    if group < 1 or k % group:
+        raise ValueError("oracle.quantize_grouped: k must be a multiple of group")
+    codes = np.empty((n, k), dtype=np.uint8)
+    scales = np.empty((n, k // group), dtype=np.float32)
+    _load().oracle_quantize_grouped(_ptr(w), n, k, group, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def linear_grouped(x_bits, act: int, codes, scales, group: int, bias=None, threads: int = 1,
+                   want_acc: bool = False):
+    """y[M,N] = round_act(sum_j scale[n,j] * sum_{k in group j} x[m,k] e4m3val(q[n,k]) + bias[n])."""
+    x_bits = _c(x_bits, np.uint16)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    bias = None if bias is None else _c(bias, np.float32)
+    m, k = x_bits.shape
+    n, k2 = codes.shape
+    if k != k2 or k % group or scales.shape != (n, k // group) or (bias is not None and bias.shape != (n,)):
+        raise ValueError("oracle.linear_grouped: shape mismatch")
+    y = np.empty((m, n), dtype=np.uint16)
+    acc = np.empty((m, n), dtype=np.float64) if want_acc else None
+    rc = _load().oracle_linear_grouped(_ptr(x_bits), act, m, k, _ptr(codes), _ptr(scales), group,
+                                       _ptr(bias), n, _ptr(y), _ptr(acc), int(threads))
+    if rc != 0:
+        raise RuntimeError("oracle.linear_grouped: thread start failed")
     return (y, acc) if want_acc else y
 
 

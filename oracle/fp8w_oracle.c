@@ -128,6 +128,27 @@ void oracle_quantize(const float *w, int64_t n, int64_t k, uint8_t *codes,
     }
 }
 
+/* Per-group scales along K: one scale per run of g weights of a row (page
+ * "B04 Precision & Quantization", section "Post-training quantization
+ * versus quantization-aware training", the granularity table's per-group
+ * row, g = 32/64/128).  Each group takes the per-channel rule on its own g
+ * weights: scale = fp32(amax/448), 1.0 if that is 0, codes = e4m3 of the
+ * fp32 quotient.  scales[n, k/g] row-major; k % g == 0.                   */
+void oracle_quantize_grouped(const float *w, int64_t n, int64_t k, int64_t g,
+                             uint8_t *codes, float *scales)
+{
+    int64_t r, j, i, ng = k / g;
+    for (r = 0; r < n; ++r) {
+        for (j = 0; j < ng; ++j) {
+            const float *seg = w + r * k + j * g;
+            float s = oracle_row_scale(seg, g);
+            scales[r * ng + j] = s;
+            for (i = 0; i < g; ++i)
+                codes[r * k + j * g + i] = oracle_e4m3_encode(seg[i] / s);
+        }
+    }
+}
+
 /* Dequantised weight in fp64: scale[n] * e4m3val(q[n,k]).  This is the
  * pages' fallback form q.float() * scale[:, None] ("The contract",
  * "Fallback").                                                              */
@@ -254,6 +275,7 @@ struct linear_job {
     uint16_t *y;
     double *yacc;
     int64_t n_begin, n_end;
+    int64_t group;  /* 0: one scale per row; else scales[n, k/group] */
 };
 
 static void linear_range(const struct linear_job *j)
@@ -263,9 +285,22 @@ static void linear_range(const struct linear_job *j)
         for (ni = j->n_begin; ni < j->n_end; ++ni) {
             const uint8_t *q = j->codes + ni * j->k;
             double acc = 0.0, out;
-            for (ki = 0; ki < j->k; ++ki)
-                acc += act_value(j->x, j->act, mi * j->k + ki) * oracle_e4m3_decode(q[ki]);
-            out = (double)j->scales[ni] * acc + (j->bias ? (double)j->bias[ni] : 0.0);
+            if (j->group == 0) {
+                for (ki = 0; ki < j->k; ++ki)
+                    acc += act_value(j->x, j->act, mi * j->k + ki) * oracle_e4m3_decode(q[ki]);
+                out = (double)j->scales[ni] * acc;
+            } else {
+                /* each group's sum times its scale, groups in k order */
+                int64_t gi, ng = j->k / j->group;
+                out = 0.0;
+                for (gi = 0; gi < ng; ++gi) {
+                    acc = 0.0;
+                    for (ki = gi * j->group; ki < (gi + 1) * j->group; ++ki)
+                        acc += act_value(j->x, j->act, mi * j->k + ki) * oracle_e4m3_decode(q[ki]);
+                    out += (double)j->scales[ni * ng + gi] * acc;
+                }
+            }
+            out += j->bias ? (double)j->bias[ni] : 0.0;
             if (j->yacc)
                 j->yacc[mi * j->n + ni] = out;
             if (j->y)
@@ -286,9 +321,10 @@ static void *linear_thread(void *arg)
  * fp64 value.  nthreads > 1 splits the output channels over POSIX threads;
  * each output is still one sequential sum, so the result does not depend
  * on the thread count.  Returns 0, or -1 if a thread could not start.     */
-int oracle_linear(const uint16_t *x, int act, int64_t m, int64_t k,
-                  const uint8_t *codes, const float *scales, const float *bias,
-                  int64_t n, uint16_t *y, double *yacc, int nthreads)
+static int linear_run(const uint16_t *x, int act, int64_t m, int64_t k,
+                      const uint8_t *codes, const float *scales, int64_t group,
+                      const float *bias, int64_t n, uint16_t *y, double *yacc,
+                      int nthreads)
 {
     struct linear_job *jobs;
     pthread_t *tids;
@@ -308,7 +344,7 @@ int oracle_linear(const uint16_t *x, int act, int64_t m, int64_t k,
         struct linear_job *j = &jobs[t];
         j->x = x; j->act = act; j->m = m; j->k = k; j->n = n;
         j->codes = codes; j->scales = scales; j->bias = bias;
-        j->y = y; j->yacc = yacc;
+        j->y = y; j->yacc = yacc; j->group = group;
         j->n_begin = n * t / nthreads;
         j->n_end = n * (t + 1) / nthreads;
     }
@@ -332,6 +368,24 @@ int oracle_linear(const uint16_t *x, int act, int64_t m, int64_t k,
     free(jobs);
     free(tids);
     return rc;
+}
+
+int oracle_linear(const uint16_t *x, int act, int64_t m, int64_t k,
+                  const uint8_t *codes, const float *scales, const float *bias,
+                  int64_t n, uint16_t *y, double *yacc, int nthreads)
+{
+    return linear_run(x, act, m, k, codes, scales, 0, bias, n, y, yacc, nthreads);
+}
+
+/* The same with per-group scales[n, k/g]:
+ * y[m,n] = RN_act( sum_j scale[n,j] * sum_{k in group j} x[m,k] q[n,k] + bias[n] ),
+ * fp64 throughout, one rounding.                                           */
+int oracle_linear_grouped(const uint16_t *x, int act, int64_t m, int64_t k,
+                          const uint8_t *codes, const float *scales, int64_t g,
+                          const float *bias, int64_t n, uint16_t *y, double *yacc,
+                          int nthreads)
+{
+    return linear_run(x, act, m, k, codes, scales, g, bias, n, y, yacc, nthreads);
 }
 
 /* ------------------------------------------------------------------------ */
