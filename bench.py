@@ -392,6 +392,48 @@ def run_fused(torch, fw, mats, xs, dev, s, steps, warmup, peak):
                     "o and down alone; M = 1, 8, 32; same weights, replicas and graph replay as the main step"}
 
 
+def run_grouped(torch, fw, dev, s, peak, launches=100):
+    """The M = 1 GEMV with per-group scales on the gate weight [14336 x 4096]:
+    per-launch time over graph-replayed back-to-back launches, weight
+    replicas (codes and scales) rotating so every read comes from HBM."""
+    c = synthetic.case("decode_stack", 1, "gate")
+    w = torch.from_numpy(c["w"]).to(dev)
+    x = torch.from_numpy(c["x"].view(np.int16)).to(dev).view(torch.bfloat16)
+    bias = torch.from_numpy(c["bias"]).to(dev)
+    n, k = w.shape
+    out = {}
+    for group in (128, 32):
+        codes, scales = fw.quantize(w, group=group)
+        nrep = max(3, -(-3 * 129 * 2 ** 20 // codes.numel()))
+        reps = [(codes, scales)] + [(codes.clone(), scales.clone()) for _ in range(nrep - 1)]
+        y = torch.empty((1, n), dtype=torch.bfloat16, device=dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            fw.linear(x, codes, scales, bias, out=y)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=s):
+                for i in range(launches):
+                    cd, sd = reps[i % nrep]
+                    fw.linear(x, cd, sd, bias, out=y)
+        g.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / launches
+        nbytes = n * k + 4 * n * (k // group) + 4 * n + 2 * k + 2 * n
+        out["g%d" % group] = {"us_per_launch": round(us, 3), "gbs": round(nbytes / us / 1e3, 1),
+                              "frac": round(nbytes / us / 1e3 / peak, 4), "bytes": nbytes}
+        del g, reps
+    out["note"] = ("gate [14336 x 4096], M = 1, bf16; bytes = codes + 4 B per group scale + bias + x + y; "
+                   "graph-replayed back-to-back launches")
+    return out
+
+
 def run_ours(args, torch, dist):
     import fp8_weight_only_gb300 as fw
     ws, rank, local = dist_env()
@@ -518,6 +560,8 @@ def run_ours(args, torch, dist):
                               "traffic": None, "note": "instrumented replay failed: " + instr_err}
 
     result["fused_stack"] = run_fused(torch, fw, mats, xs, dev, s, min(args.steps, 500), args.warmup, peak)
+
+    result["grouped_gemv"] = run_grouped(torch, fw, dev, s, peak)
 
     # quantiser throughput on the seven matrices (load-time step)
     qcodes = {name: torch.empty_like(mats[name]["codes"][0]) for name in wdev}

@@ -21,8 +21,8 @@ KERNEL_AUTO, KERNEL_GEMV, KERNEL_SKINNY = 0, 1, 2
 
 SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_workspace_size", "fp8w_linear_ex",
            "fp8w_status_string", "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version",
-           "fp8w_linear_noalloc", "fp8w_dequantize")
-ABI_VERSION = 4
+           "fp8w_linear_noalloc", "fp8w_dequantize", "fp8w_quantize_grouped", "fp8w_linear_grouped")
+ABI_VERSION = 5
 
 
 class Fp8wError(RuntimeError):
@@ -49,6 +49,10 @@ def lib():
         c, P = ctypes, ctypes.c_void_p
         L.fp8w_quantize.restype = c.c_int
         L.fp8w_quantize.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
+        L.fp8w_quantize_grouped.restype = c.c_int
+        L.fp8w_quantize_grouped.argtypes = [P, c.c_int64, c.c_int64, c.c_int, P, P, P]
+        L.fp8w_linear_grouped.restype = c.c_int
+        L.fp8w_linear_grouped.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, c.c_int, P, c.c_int64, P, P]
         L.fp8w_dequantize.restype = c.c_int
         L.fp8w_dequantize.argtypes = [P, P, c.c_int64, c.c_int64, c.c_int, P, P]
         L.fp8w_linear.restype = c.c_int
@@ -99,8 +103,10 @@ def _act(dtype):
     raise TypeError("activations must be bfloat16 or float16, got %s" % dtype)
 
 
-def quantize(w, codes=None, scales=None):
-    """W[N, K] fp32 (CUDA, contiguous) -> (codes uint8 [N, K], scales fp32 [N])."""
+def quantize(w, codes=None, scales=None, group=None):
+    """W[N, K] fp32 (CUDA, contiguous) -> (codes uint8 [N, K], scales fp32 [N]),
+    or with group (32, 64 or 128) scales fp32 [N, K / group], one per run of
+    `group` weights of a row."""
     import torch
     if w.dtype != torch.float32 or not w.is_cuda or w.dim() != 2 or not w.is_contiguous():
         raise TypeError("w must be a contiguous 2-D float32 CUDA tensor")
@@ -108,8 +114,12 @@ def quantize(w, codes=None, scales=None):
     if codes is None:
         codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
     if scales is None:
-        scales = torch.empty((n,), dtype=torch.float32, device=w.device)
-    _check(lib().fp8w_quantize(_ptr(w), n, k, _ptr(codes), _ptr(scales), _stream(w)))
+        shape = (n,) if group is None else (n, k // group)
+        scales = torch.empty(shape, dtype=torch.float32, device=w.device)
+    if group is None:
+        _check(lib().fp8w_quantize(_ptr(w), n, k, _ptr(codes), _ptr(scales), _stream(w)))
+    else:
+        _check(lib().fp8w_quantize_grouped(_ptr(w), n, k, int(group), _ptr(codes), _ptr(scales), _stream(w)))
     return codes, scales
 
 
@@ -170,6 +180,16 @@ def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_
             raise TypeError("%s must be a contiguous %s CUDA tensor" % (name, dt))
     m, k = x.shape
     n = codes.shape[0]
+    if scales.dim() == 2:
+        # per-group scales [N, K / group]: the GEMV's grouped form (M == 1)
+        if codes.dim() != 2 or codes.shape[1] != k or scales.shape[0] != n or k % scales.shape[1] or \
+                (bias is not None and bias.numel() != n):
+            raise ValueError("shape mismatch for per-group scales")
+        if out is None:
+            out = torch.empty((m, n), dtype=x.dtype, device=x.device)
+        _check(lib().fp8w_linear_grouped(_ptr(x), _act(x.dtype), m, k, _ptr(codes), _ptr(scales),
+                                         k // scales.shape[1], _ptr(bias), n, _ptr(out), _stream(x)))
+        return out
     if codes.dim() != 2 or codes.shape[1] != k or scales.numel() != n or \
             (bias is not None and bias.numel() != n):
         raise ValueError("shape mismatch: x %s, codes %s, scales %s, bias %s" % (

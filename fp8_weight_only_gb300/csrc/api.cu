@@ -48,6 +48,27 @@ fp8w_status fp8w_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes, 
                        "fp8w_quantize launch");
 }
 
+static bool valid_group(int group) { return group == 32 || group == 64 || group == 128; }
+
+fp8w_status fp8w_quantize_grouped(const float* w, int64_t n, int64_t k, int group, uint8_t* codes, float* scales,
+                                  void* stream) {
+    if (!w || !codes || !scales) return FP8W_ERR_NULL;
+    if (n < 1 || n > FP8W_MAX_DIM || !valid_k(k) || !valid_group(group) || k % group != 0) return FP8W_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 4)) return FP8W_ERR_ALIGN;
+    return cuda_status(fp8w::launch_quantize_grouped(w, n, k, group, codes, scales, static_cast<cudaStream_t>(stream)),
+                       "fp8w_quantize_grouped launch");
+}
+
+fp8w_status fp8w_linear_grouped(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
+                                const float* scales, int group, const float* bias, int64_t n, void* y, void* stream) {
+    fp8w_status st = check_linear(x, act_dtype, m, k, codes, scales, bias, n, y);
+    if (st != FP8W_OK) return st;
+    if (m != 1 || !valid_group(group) || k % (4 * group) != 0 || !fp8w::gemv_supports(k)) return FP8W_ERR_SHAPE;
+    if (!aligned(scales, 16)) return FP8W_ERR_ALIGN;
+    fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, scales, bias, y, group};
+    return cuda_status(fp8w::launch_gemv(a, static_cast<cudaStream_t>(stream)), "fp8w_linear_grouped launch");
+}
+
 fp8w_status fp8w_dequantize(const uint8_t* codes, const float* scales, int64_t n, int64_t k, int out_dtype,
                             void* w, void* stream) {
     if (!codes || !scales || !w) return FP8W_ERR_NULL;

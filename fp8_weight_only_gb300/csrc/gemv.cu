@@ -60,7 +60,10 @@ struct GemvGeom {
     int g;            // warps per row group (1, 2, 4, 8 or 16)
     int staged;       // rows of scale and bias staged in shared memory (a multiple of 32)
     uint32_t slot_bytes;
-    uint32_t ring_bytes;
+    uint32_t ring_bytes;   // code slots, then (per-group scales) scale slots
+    uint32_t sslot_bytes;  // per-group scales: a slot's rows of scales (0 otherwise)
+    int ngroups;           // per-group scales: groups a row (k / group)
+    int gshift;            // per-group scales: log2 of 16-code chunks a group
 };
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t pol) {
@@ -147,7 +150,13 @@ __device__ __forceinline__ void dot_chunk_f32(const uint4 (&c)[RP], const uint4 
 }
 
 // kF32X: x is staged in shared memory as fp32 (else as 16-bit values).
-template <int RP, bool kBf16, bool kF32X>
+// kGrouped: scales[n, k / group], one per run of `group` codes of a row (page
+// "B04 Precision & Quantization", section "Post-training quantization versus
+// quantization-aware training", the per-group row): the producer brings each
+// slot's rows of scales with its codes, and every 16-code chunk's partial
+// sums enter the row's sums times their group's scale (one packed FMA), so
+// the epilogue adds only the bias.
+template <int RP, bool kBf16, bool kF32X, bool kGrouped>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes, const float* __restrict__ scales,
                 const float* __restrict__ bias, uint16_t* __restrict__ y, int64_t n, int64_t k, GemvGeom geo) {
@@ -155,7 +164,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const uint32_t ring = smem_u32(smem);
     const int S = geo.slots, R = geo.rows;
-    // layout: ring | x [k] | scales, bias [geo.staged] | full, empty [kGemvMaxSlots] |
+    // layout: ring (codes [S], then group scales [S]) | x [k] | scales, bias [geo.staged] | full, empty [kGemvMaxSlots] |
     // group partial sums [kGemvWarps][2][kGemvWarps][RP] | abort flag
     const uint32_t x_bytes = static_cast<uint32_t>(((k * (kF32X ? 4 : 2) + 127) / 128) * 128);
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + geo.ring_bytes);
@@ -168,6 +177,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     float* red = reinterpret_cast<float*>(smem + geo.ring_bytes + x_bytes + 8u * geo.staged + 16 * kGemvMaxSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kGemvWarps * 2 * kGemvWarps * RP);
     const int G = geo.g, groups = kGemvWarps / G;
+    const uint32_t sring = ring + static_cast<uint32_t>(S) * geo.slot_bytes;  // group scale slots
 
     const int64_t P = gridDim.x;
     const int64_t row0 = blockIdx.x * n / P, row1 = (blockIdx.x + 1) * n / P;
@@ -205,7 +215,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                 const int64_t r0 = row0 + sl * R;
                 const int64_t rows = (row1 - r0) < R ? (row1 - r0) : R;
                 const uint32_t bytes = static_cast<uint32_t>(rows * k);
-                mbar_arrive_expect_tx(full(s), bytes);
+                if constexpr (kGrouped) {
+                    const uint32_t sbytes = static_cast<uint32_t>(rows * geo.ngroups * 4);
+                    mbar_arrive_expect_tx(full(s), bytes + sbytes);
+                    bulk_load(sring + s * geo.sslot_bytes, scales + r0 * geo.ngroups, sbytes, full(s), pol);
+                } else {
+                    mbar_arrive_expect_tx(full(s), bytes);
+                }
                 bulk_load(ring + s * geo.slot_bytes, codes + r0 * k, bytes, full(s), pol);
                 ++issued;
                 if (++s == S) {
@@ -261,7 +277,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     const bool staged = nrows <= geo.staged;
     if (staged) {
         for (int64_t i = threadIdx.x; i < nrows; i += 32 * kGemvWarps) {
-            sc_s[i] = scales[row0 + i];
+            if constexpr (!kGrouped) sc_s[i] = scales[row0 + i];
             bi_s[i] = bias ? bias[row0 + i] : 0.0f;
         }
     }
@@ -292,6 +308,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         for (int r = static_cast<int>((grp - gbase % groups + groups) % groups) * RP; r < rows; r += groups * RP) {
             const int nr = rows - r < RP ? rows - r : RP;  // rows in this item (the slot's last may be short)
             const uint32_t rowp = ring + s * geo.slot_bytes + static_cast<uint32_t>(r * k);
+            // per-group scales of the item's rows
+            const float* gsc = reinterpret_cast<const float*>(smem + (sring - ring) + s * geo.sslot_bytes) +
+                               static_cast<int64_t>(r) * geo.ngroups;
             uint64_t acc[RP];
 #pragma unroll
             for (int q = 0; q < RP; ++q) acc[q] = 0ull;
@@ -304,12 +323,23 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                 for (int q = 0; q < RP; ++q)
                     cw[q] = q < nr ? lds128(rowp + q * kk + static_cast<uint32_t>(ch) * 16u) : make_uint4(0u, 0u, 0u, 0u);
                 const uint32_t xa = xv + static_cast<uint32_t>(ch) * 16u;
+                uint64_t part[RP];
+#pragma unroll
+                for (int q = 0; q < RP; ++q) part[q] = 0ull;
+                uint64_t (&dst)[RP] = kGrouped ? part : acc;
                 if constexpr (kF32X) {
                     const uint4 xf[4] = {lds128(xa), lds128(xa + xpiece), lds128(xa + 2 * xpiece),
                                          lds128(xa + 3 * xpiece)};
-                    dot_chunk_f32<RP>(cw, xf, acc);
+                    dot_chunk_f32<RP>(cw, xf, dst);
                 } else {
-                    dot_chunk<RP, kBf16>(cw, lds128(xa), lds128(xa + xpiece), acc);
+                    dot_chunk<RP, kBf16>(cw, lds128(xa), lds128(xa + xpiece), dst);
+                }
+                if constexpr (kGrouped) {
+#pragma unroll
+                    for (int q = 0; q < RP; ++q) {
+                        const float g = gsc[q * geo.ngroups + (ch >> geo.gshift)];
+                        ffma2(acc[q], part[q], pack2(g, g));
+                    }
                 }
             }
             float sum[RP];
@@ -342,9 +372,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                 for (int q = 0; q < RP; ++q) {
                     if (q >= nr) break;
                     const int64_t i = base + r + q;
-                    const float sc = staged ? sc_s[i] : scales[row0 + i];
                     const float bi = staged ? bi_s[i] : (bias ? bias[row0 + i] : 0.0f);
-                    y[row0 + i] = round_out<kBf16>(fmaf(sum[q], sc, bi));
+                    if constexpr (kGrouped) {
+                        y[row0 + i] = round_out<kBf16>(sum[q] + bi);  // the scales are applied already
+                    } else {
+                        const float sc = staged ? sc_s[i] : scales[row0 + i];
+                        y[row0 + i] = round_out<kBf16>(fmaf(sum[q], sc, bi));
+                    }
                 }
         }
         // this warp has read its rows of the slot
@@ -364,6 +398,7 @@ static uint32_t gemv_fixed_bytes(int64_t k, bool f32x, int staged) {
 
 template <bool kBf16>
 static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
+    const bool grouped = a.group > 0;
     int sms = 0;
     cudaError_t e = device_sm_count(sms);
     if (e != cudaSuccess) return e;
@@ -383,29 +418,35 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     if (rows < rp) rows = rp;
     geo.rows = static_cast<int>(rows);
     geo.slot_bytes = static_cast<uint32_t>(((rows * a.k + 127) / 128) * 128);
-    int64_t slots = (kGemvSmemBudget - gemv_fixed_bytes(a.k, f32x, geo.staged)) / geo.slot_bytes;
+    // per-group scales: a slot's rows of scales beside its codes
+    geo.ngroups = grouped ? static_cast<int>(a.k / a.group) : 0;
+    geo.gshift = 0;
+    while (grouped && (16 << geo.gshift) < a.group) ++geo.gshift;
+    geo.sslot_bytes = static_cast<uint32_t>(((rows * geo.ngroups * 4 + 127) / 128) * 128);
+    int64_t slots = (kGemvSmemBudget - gemv_fixed_bytes(a.k, f32x, geo.staged)) / (geo.slot_bytes + geo.sslot_bytes);
     if (slots > kGemvMaxSlots) slots = kGemvMaxSlots;
     if (slots < 2) return cudaErrorNotSupported;
     geo.slots = static_cast<int>(slots);
-    geo.ring_bytes = geo.slots * geo.slot_bytes;
+    geo.ring_bytes = geo.slots * (geo.slot_bytes + geo.sslot_bytes);
     // warps per row group: enough that two slots' items keep all warps busy
     const int64_t items = (rows + rp - 1) / rp;
     geo.g = 1;
     while (geo.g < kGemvWarps && items * geo.g * 2 < kGemvWarps) geo.g *= 2;
     const uint32_t smem = geo.ring_bytes + gemv_fixed_bytes(a.k, f32x, geo.staged);
 
-    auto kern = f32x ? gemv_kernel<2, kBf16, true> : gemv_kernel<2, kBf16, false>;
+    auto kern = grouped ? (f32x ? gemv_kernel<2, kBf16, true, true> : gemv_kernel<2, kBf16, false, true>)
+                        : (f32x ? gemv_kernel<2, kBf16, true, false> : gemv_kernel<2, kBf16, false, false>);
     static std::once_flag attr_once[64];
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(gemv_kernel<2, kBf16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kGemvSmemBudget);
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(gemv_kernel<2, kBf16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            kGemvSmemBudget);
+        decltype(kern) all[4] = {gemv_kernel<2, kBf16, false, false>, gemv_kernel<2, kBf16, true, false>,
+                                 gemv_kernel<2, kBf16, false, true>, gemv_kernel<2, kBf16, true, true>};
+        for (auto f : all)
+            if (attr_err == cudaSuccess)
+                attr_err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvSmemBudget);
     });
     if (attr_err != cudaSuccess) return attr_err;
     // programmatic dependent launch: set-up overlaps the previous kernel's tail

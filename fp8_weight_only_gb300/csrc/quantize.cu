@@ -111,6 +111,54 @@ cudaError_t launch_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes
     return cudaGetLastError();
 }
 
+// ------------------------------------------------- per-group quantise --
+// One scale per run of `group` weights of a row (page "B04 Precision &
+// Quantization", section "Post-training quantization versus
+// quantization-aware training", the per-group row), each group by the
+// per-channel rule above.  A lane takes 4 weights; a group is GL = group / 4
+// consecutive lanes of one warp, whose amax is an exact shuffle maximum.
+// HBM bytes per element: 4 read + 1 written (+ 4 per group).
+template <int GL>
+__global__ void __launch_bounds__(kQuantThreads) quantize_grouped_kernel(const float* __restrict__ w, int64_t nf4,
+                                                                         int gshift, uint8_t* __restrict__ codes,
+                                                                         float* __restrict__ scales) {
+    const int lane = threadIdx.x & 31;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kQuantThreads;
+    // a warp-uniform loop: the shuffles below need every lane; nf4 is a
+    // multiple of GL, so a group is all in or all out
+    for (int64_t base = blockIdx.x * static_cast<int64_t>(kQuantThreads) + (threadIdx.x & ~31); base < nf4;
+         base += stride) {
+        const int64_t f = base + lane;
+        const bool in = f < nf4;
+        const float4 v = in ? ldg_stream_f4(w + f * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+        float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+        for (int off = GL / 2; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+        const float sc = scale_from_amax(a);
+        if (in) {
+            reinterpret_cast<uint32_t*>(codes)[f] = encode4(v, sc);
+            if ((lane & (GL - 1)) == 0) scales[(f * 4) >> gshift] = sc;
+        }
+    }
+}
+
+cudaError_t launch_quantize_grouped(const float* w, int64_t n, int64_t k, int group, uint8_t* codes, float* scales,
+                                    cudaStream_t st) {
+    int sms = 0;
+    cudaError_t e = device_sm_count(sms);
+    if (e != cudaSuccess) return e;
+    const int64_t nf4 = n * k / 4;
+    int64_t blocks = (nf4 + kQuantThreads - 1) / kQuantThreads;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    const unsigned g = static_cast<unsigned>(blocks);
+    const int gshift = group == 32 ? 5 : group == 64 ? 6 : 7;
+    if (group == 32) quantize_grouped_kernel<8><<<g, kQuantThreads, 0, st>>>(w, nf4, gshift, codes, scales);
+    else if (group == 64) quantize_grouped_kernel<16><<<g, kQuantThreads, 0, st>>>(w, nf4, gshift, codes, scales);
+    else quantize_grouped_kernel<32><<<g, kQuantThreads, 0, st>>>(w, nf4, gshift, codes, scales);
+    return cudaGetLastError();
+}
+
 // ------------------------------------------------------------ dequantise --
 // Page "kadirnar/kernel-agent fp8-weights", section "The contract" (the
 // fallback: the decoded codes times the row scale): w[n, k] = e4m3(q[n, k]) *

@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define FP8W_ABI_VERSION 4
+#define FP8W_ABI_VERSION 5
 
 #if defined(__GNUC__)
 #define FP8W_API __attribute__((visibility("default")))
@@ -83,6 +83,39 @@ enum { FP8W_BF16 = 1, FP8W_F16 = 2, FP8W_F32 = 3 };
  */
 FP8W_API fp8w_status fp8w_quantize(const float *w, int64_t n, int64_t k,
                           uint8_t *codes, float *scales, void *stream);
+
+/*
+ * fp8w_quantize_grouped -- the quantiser with one scale per run of `group`
+ * weights of a row instead of one per row (page "B04 Precision &
+ * Quantization", section "Post-training quantization versus
+ * quantization-aware training", the granularity table's per-group row).
+ *
+ *   w      [n, k] fp32, device, 16-byte aligned, finite.
+ *   group  32, 64 or 128; k % group == 0.
+ *   codes  [n, k] uint8, device, 16-byte aligned (output).
+ *   scales [n, k / group] fp32 row-major, device, 4-byte aligned (output).
+ *
+ * Each group takes fp8w_quantize's rule on its own weights: scale =
+ * fp32(amax / 448), 1.0 when that is 0; code = nearest-even e4m3 of the fp32
+ * quotient.
+ */
+FP8W_API fp8w_status fp8w_quantize_grouped(const float *w, int64_t n, int64_t k, int group,
+                                  uint8_t *codes, float *scales, void *stream);
+
+/*
+ * fp8w_linear_grouped -- fp8w_linear for codes with per-group scales:
+ *   y[0, r] = round_act( sum_j scales[r, j] * sum_{c in group j} x[0, c] * e4m3(codes[r, c]) + bias[r] ).
+ *
+ * The GEMV kernel (m == 1 only: any other m is FP8W_ERR_SHAPE, not built
+ * for the tensor-core kernel).  group 32, 64 or 128 with k % (4 * group) ==
+ * 0 and k <= 32768; scales [n, k / group] fp32, 16-byte aligned (each slot's
+ * rows of scales are bulk-copied beside its codes).  Other arguments as
+ * fp8w_linear; fp32 accumulation, each 16-code partial sum scaled by its
+ * group's scale, bias added once, one rounding.
+ */
+FP8W_API fp8w_status fp8w_linear_grouped(const void *x, int act_dtype, int64_t m, int64_t k,
+                                const uint8_t *codes, const float *scales, int group,
+                                const float *bias, int64_t n, void *y, void *stream);
 
 /*
  * fp8w_dequantize -- the dequantised weight, the pages' fallback form

@@ -127,3 +127,27 @@ def test_noalloc_entry_rejects_bad_arguments_on_the_host(kw, status):
 ])
 def test_dequantize_rejects_bad_arguments(args, status):
     assert fw.lib().fp8w_dequantize(*args, None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, 4, 128, 32, B16, C16), 1), ((A16, 4, 128, 32, None, C16), 1),
+    ((A16, 4, 128, 48, B16, C16), 2), ((A16, 4, 128, 256, B16, C16), 2), ((A16, 4, 96, 64, B16, C16), 2),
+    ((A16, 0, 128, 32, B16, C16), 2), ((ctypes.c_void_p(0x100004), 4, 128, 32, B16, C16), 3),
+])
+def test_quantize_grouped_rejects_bad_arguments(args, status):
+    assert fw.lib().fp8w_quantize_grouped(*args, None) == status
+
+
+def _lin_g(m=1, k=512, group=32, scales=C16, cfg=None):
+    return fw.lib().fp8w_linear_grouped(A16, 1, m, k, B16, scales, group, None, 8, D16, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(m=2), 2),                      # the grouped form is the GEMV: m == 1
+    (dict(group=16), 2), (dict(group=96), 2),
+    (dict(k=32 * 4 * 3 + 64, group=32), 2),   # k % (4 * group) != 0
+    (dict(k=65536, group=128), 2),       # beyond the GEMV's 32768
+    (dict(scales=ctypes.c_void_p(0x300004)), 3),   # scales are bulk-copied: 16-byte aligned
+])
+def test_linear_grouped_rejects_bad_arguments(kw, status):
+    assert _lin_g(**kw) == status

@@ -542,3 +542,64 @@ def test_dequantize_of_quantize_is_the_oracle_fallback_weight():
     codes, scales = gpu_quantize(case["w"])
     got = _gpu_dequant_bits(codes, scales, torch.float32)
     assert np.array_equal(got, oracle.dequantize(codes, scales).astype(np.float32).view(np.uint32))
+
+
+# ------------------------------------------------------ per-group scales --
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+@pytest.mark.parametrize("n,k,kind", [(1, 128, "normal"), (300, 4096, "t"), (77, 14336, "normal"),
+                                      (5, 1152, "zeros")])
+def test_quantize_grouped_bit_exact(n, k, kind, group):
+    if k % group:
+        pytest.skip("k not a multiple of the group")
+    if kind == "t":
+        w = synthetic.weight_outlier(31 + n, n, k)
+    else:
+        w = synthetic.weight_normal(37 + n, n, k, 0.02)
+    if kind == "zeros":
+        w[:, :group] = 0.0                               # a whole zero group: scale 1.0
+        w[1, group: 2 * group] = 1e-45                    # an underflowing group
+    wd = torch.from_numpy(w).to(DEV)
+    codes, scales = fw.quantize(wd, group=group)
+    torch.cuda.synchronize()
+    rc, rs = oracle.quantize_grouped(w, group)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
+@pytest.mark.parametrize("act", [oracle.ACT_BF16, oracle.ACT_F16])
+@pytest.mark.parametrize("n,k,group", [(1, 512, 32), (300, 4096, 32), (1000, 4096, 128), (257, 14336, 64),
+                                       (4097, 4096, 128), (153, 1024, 64), (64, 32768, 128)])
+def test_linear_grouped_parity(n, k, group, act):
+    c = synthetic.random_case(900 + n + k + group + act, 1, n, k, act=act, with_bias=(n % 2 == 1))
+    w = c["w"].copy()
+    w[:, ::97] *= 40.0                                    # outliers that per-group scales contain
+    codes, scales = oracle.quantize_grouped(w, group)
+    x = torch.from_numpy(c["x"].view(np.int16)).to(DEV).view(_dt(act))
+    cd = torch.from_numpy(codes).to(DEV)
+    sd = torch.from_numpy(scales).to(DEV)
+    bd = None if c["bias"] is None else torch.from_numpy(c["bias"]).to(DEV)
+    buf, y = _guarded(n, _dt(act), POISON16)
+    fw.linear(x, cd, sd, bd, out=y.view(1, n))
+    torch.cuda.synchronize()
+    _check_canaries(buf, n, POISON16)
+    assert fw.device_error() == 0
+    got = y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(1, n)
+    ref = oracle.linear_grouped(c["x"], act, codes, scales, group, c["bias"], threads=oracle.host_cores())
+    assert_parity(got, ref, act, (n, k, group))
+
+
+def test_linear_grouped_with_one_scale_per_group_equal_to_per_channel():
+    """Group scales all equal to the row's scale: the grouped GEMV must give
+    the per-channel GEMV's output (the same sums, scaled per chunk instead of
+    once: equal within the tolerance, and bit-equal for most outputs)."""
+    c, codes, scales = _case(17, 1, 500, 4096, oracle.ACT_BF16)
+    gs = np.repeat(scales[:, None], 4096 // 128, axis=1).astype(np.float32)
+    y1 = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"])
+    x = torch.from_numpy(c["x"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    yg = fw.linear(x, torch.from_numpy(codes).to(DEV), torch.from_numpy(gs).to(DEV),
+                   torch.from_numpy(c["bias"]).to(DEV))
+    torch.cuda.synchronize()
+    yg = yg.view(torch.int16).cpu().numpy().view(np.uint16)
+    cmp = compare(yg, y1, oracle.ACT_BF16)
+    assert cmp["rel_l2"] <= 1e-3 and cmp["bit_equal"] >= 0.95, cmp
