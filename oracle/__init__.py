@@ -54,6 +54,15 @@ def _load():
         lib.oracle_linear_grouped.restype = c.c_int
         lib.oracle_linear_grouped.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, c.c_int64, P,
                                               c.c_int64, P, P, c.c_int]
+        lib.oracle_e8m0_decode.restype = c.c_double
+        lib.oracle_e8m0_decode.argtypes = [c.c_uint8]
+        lib.oracle_mx_scale.restype = c.c_uint8
+        lib.oracle_mx_scale.argtypes = [P, c.c_int64]
+        lib.oracle_quantize_mx.restype = None
+        lib.oracle_quantize_mx.argtypes = [P, c.c_int64, c.c_int64, P, P]
+        lib.oracle_linear_mx.restype = c.c_int
+        lib.oracle_linear_mx.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P,
+                                         c.c_int64, P, P, c.c_int]
         lib.oracle_fp8_error.restype = None
         lib.oracle_fp8_error.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
         lib.oracle_e4m3_encode_many.restype = None
@@ -196,6 +205,52 @@ def linear_grouped(x_bits, act: int, codes, scales, group: int, bias=None, threa
                                        _ptr(bias), n, _ptr(y), _ptr(acc), int(threads))
     if rc != 0:
         raise RuntimeError("oracle.linear_grouped: thread start failed")
+    return (y, acc) if want_acc else y
+
+
+MX_BLOCK = 32
+
+
+def e8m0_decode(b: int) -> float:
+    """Value of one E8M0 byte: 2^(b - 127), NaN for 0xFF (page "11.
+    Inference with NVFP4/MXFP8", section "MXFP8-Style FP8")."""
+    return _load().oracle_e8m0_decode(int(b) & 0xFF)
+
+
+def mx_scale(block) -> int:
+    """E8M0 byte of one block of weights: the smallest 2^e >= amax/448."""
+    block = _c(block, np.float32)
+    return int(_load().oracle_mx_scale(_ptr(block), block.size))
+
+
+def quantize_mx(w):
+    """W[N,K] fp32 -> (codes uint8 [N,K], E8M0 scales uint8 [N, K/32])."""
+    w = _c(w, np.float32)
+    n, k = w.shape
+    if k % MX_BLOCK:
+        raise ValueError("oracle.quantize_mx: k must be a multiple of 32")
+    codes = np.empty((n, k), dtype=np.uint8)
+    scales = np.empty((n, k // MX_BLOCK), dtype=np.uint8)
+    _load().oracle_quantize_mx(_ptr(w), n, k, _ptr(codes), _ptr(scales))
+    return codes, scales
+
+
+def linear_mx(x_bits, act: int, codes, scales, bias=None, threads: int = 1, want_acc: bool = False):
+    """The per-group linear layer, g = 32, with scale[n, j] = e8m0val(scales[n, j])."""
+    x_bits = _c(x_bits, np.uint16)
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    bias = None if bias is None else _c(bias, np.float32)
+    m, k = x_bits.shape
+    n, k2 = codes.shape
+    if k != k2 or k % MX_BLOCK or scales.shape != (n, k // MX_BLOCK) or (bias is not None and bias.shape != (n,)):
+        raise ValueError("oracle.linear_mx: shape mismatch")
+    y = np.empty((m, n), dtype=np.uint16)
+    acc = np.empty((m, n), dtype=np.float64) if want_acc else None
+    rc = _load().oracle_linear_mx(_ptr(x_bits), act, m, k, _ptr(codes), _ptr(scales),
+                                  _ptr(bias), n, _ptr(y), _ptr(acc), int(threads))
+    if rc != 0:
+        raise RuntimeError("oracle.linear_mx: allocation or thread start failed")
     return (y, acc) if want_acc else y
 
 

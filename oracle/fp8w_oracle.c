@@ -149,6 +149,84 @@ void oracle_quantize_grouped(const float *w, int64_t n, int64_t k, int64_t g,
     }
 }
 
+/* ------------------------------------------------------------------------ */
+/* MX-style weight-only form: one E8M0 scale per 32 weights along K.  Page
+ * "11. Inference with NVFP4/MXFP8", section "MXFP8-Style FP8": e4m3 codes
+ * [N, K] and f8e8m0fnu scales [N, K/32], one scale per 32 values along K.
+ * E8M0 ("e8m0fnu") is an unsigned biased exponent byte b, worth 2^(b-127);
+ * 0xFF is NaN and there is no zero.
+ *
+ * The page fixes the storage, not how a block's scale is chosen.  Reading
+ * taken: the per-channel rule limited to powers of two, i.e. the smallest
+ * 2^e with 2^e >= amax/448, so that the block's largest weight maps to at
+ * most 448 and is never clipped; amax 0 takes 2^0 (the per-channel rule's
+ * 1.0); e is clamped to the format's [-127, 127]; an infinite amax has no
+ * such power and takes the NaN scale, with every code of its block the
+ * e4m3 NaN 0x7F.  Codes are e4m3(w / 2^e), one fp32 division as above.    */
+/* ------------------------------------------------------------------------ */
+
+#define ORACLE_MX_BLOCK 32
+
+double oracle_e8m0_decode(uint8_t b)
+{
+    if (b == 0xFF)
+        return NAN;
+    return ldexp(1.0, (int)b - 127);
+}
+
+/* The scale byte of a block of g weights: amax as in oracle_row_scale (NaN
+ * weights do not count), then the exponent by exact comparisons in fp64
+ * (448 * 2^e and amax are both exact there), from a first guess.          */
+uint8_t oracle_mx_scale(const float *blk, int64_t g)
+{
+    float amax = 0.0f;
+    int64_t i;
+    int e;
+    for (i = 0; i < g; ++i) {
+        float a = fabsf(blk[i]);
+        if (a > amax)
+            amax = a;
+    }
+    if (isinf(amax))
+        return 0xFF;
+    if (amax == 0.0f)
+        return 127;
+    e = ilogb((double)amax) - 8;
+    while (ldexp(448.0, e) < (double)amax)
+        ++e;
+    while (ldexp(448.0, e - 1) >= (double)amax)
+        --e;
+    if (e < -127)
+        e = -127;
+    if (e > 127)
+        e = 127;
+    return (uint8_t)(e + 127);
+}
+
+/* W[n,k] -> codes[n,k], scales[n, k/32] (E8M0 bytes); k % 32 == 0.        */
+void oracle_quantize_mx(const float *w, int64_t n, int64_t k, uint8_t *codes,
+                        uint8_t *scales)
+{
+    int64_t r, j, i, ng = k / ORACLE_MX_BLOCK;
+    for (r = 0; r < n; ++r) {
+        for (j = 0; j < ng; ++j) {
+            const float *seg = w + r * k + j * ORACLE_MX_BLOCK;
+            uint8_t *out = codes + r * k + j * ORACLE_MX_BLOCK;
+            uint8_t b = oracle_mx_scale(seg, ORACLE_MX_BLOCK);
+            scales[r * ng + j] = b;
+            if (b == 0xFF) {
+                memset(out, 0x7F, ORACLE_MX_BLOCK);
+                continue;
+            }
+            {
+                float s = (float)oracle_e8m0_decode(b);   /* exact, 2^-127 included */
+                for (i = 0; i < ORACLE_MX_BLOCK; ++i)
+                    out[i] = oracle_e4m3_encode(seg[i] / s);
+            }
+        }
+    }
+}
+
 /* Dequantised weight in fp64: scale[n] * e4m3val(q[n,k]).  This is the
  * pages' fallback form q.float() * scale[:, None] ("The contract",
  * "Fallback").                                                              */
@@ -386,6 +464,26 @@ int oracle_linear_grouped(const uint16_t *x, int act, int64_t m, int64_t k,
                           int nthreads)
 {
     return linear_run(x, act, m, k, codes, scales, g, bias, n, y, yacc, nthreads);
+}
+
+/* The MX-style form: the per-group linear layer with g = 32 and each scale
+ * the value of its E8M0 byte (exact in fp32, 2^-127 included; 0xFF is NaN).
+ * Returns 0, or -1 if memory or a thread could not be had.               */
+int oracle_linear_mx(const uint16_t *x, int act, int64_t m, int64_t k,
+                     const uint8_t *codes, const uint8_t *scales,
+                     const float *bias, int64_t n, uint16_t *y, double *yacc,
+                     int nthreads)
+{
+    int64_t i, ns = n * (k / ORACLE_MX_BLOCK);
+    int rc;
+    float *sf = (float *)malloc((size_t)(ns > 0 ? ns : 1) * sizeof *sf);
+    if (!sf)
+        return -1;
+    for (i = 0; i < ns; ++i)
+        sf[i] = (float)oracle_e8m0_decode(scales[i]);
+    rc = linear_run(x, act, m, k, codes, sf, ORACLE_MX_BLOCK, bias, n, y, yacc, nthreads);
+    free(sf);
+    return rc;
 }
 
 /* ------------------------------------------------------------------------ */
