@@ -393,7 +393,8 @@ def run_fused(torch, fw, mats, xs, dev, s, steps, warmup, peak):
 
 
 def run_grouped(torch, fw, dev, s, peak, launches=100):
-    """The M = 1 GEMV with per-group scales on the gate weight [14336 x 4096]:
+    """The M = 1 GEMV with per-group scales on the gate weight [14336 x 4096]
+    (fp32 scales per 128 and per 32, and the MX-style E8M0 byte per 32):
     per-launch time over graph-replayed back-to-back launches, weight
     replicas (codes and scales) rotating so every read comes from HBM."""
     c = synthetic.case("decode_stack", 1, "gate")
@@ -402,8 +403,8 @@ def run_grouped(torch, fw, dev, s, peak, launches=100):
     bias = torch.from_numpy(c["bias"]).to(dev)
     n, k = w.shape
     out = {}
-    for group in (128, 32):
-        codes, scales = fw.quantize(w, group=group)
+    for group in (128, 32, "mx"):
+        codes, scales = fw.quantize_mx(w) if group == "mx" else fw.quantize(w, group=group)
         nrep = max(3, -(-3 * 129 * 2 ** 20 // codes.numel()))
         reps = [(codes, scales)] + [(codes.clone(), scales.clone()) for _ in range(nrep - 1)]
         y = torch.empty((1, n), dtype=torch.bfloat16, device=dev)
@@ -425,11 +426,12 @@ def run_grouped(torch, fw, dev, s, peak, launches=100):
             e1.record(s)
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / launches
-        nbytes = n * k + 4 * n * (k // group) + 4 * n + 2 * k + 2 * n
-        out["g%d" % group] = {"us_per_launch": round(us, 3), "gbs": round(nbytes / us / 1e3, 1),
+        nbytes = n * k + scales.numel() * scales.element_size() + 4 * n + 2 * k + 2 * n
+        out[group if group == "mx" else "g%d" % group] = {"us_per_launch": round(us, 3), "gbs": round(nbytes / us / 1e3, 1),
                               "frac": round(nbytes / us / 1e3 / peak, 4), "bytes": nbytes}
         del g, reps
-    out["note"] = ("gate [14336 x 4096], M = 1, bf16; bytes = codes + 4 B per group scale + bias + x + y; "
+    out["note"] = ("gate [14336 x 4096], M = 1, bf16; bytes = codes + group scales (4 B, or 1 B for the E8M0 "
+                   "byte of mx) + bias + x + y; "
                    "graph-replayed back-to-back launches")
     return out
 

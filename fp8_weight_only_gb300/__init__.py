@@ -7,6 +7,8 @@ raised.
 
     codes, scales = quantize(w)                 # w: [N, K] fp32 CUDA tensor
     y = linear(x, codes, scales, bias)          # x: [M, K] bf16/fp16 CUDA tensor
+    codes, e8 = quantize_mx(w)                  # one E8M0 scale byte per 32 along K
+    y1 = linear(x1, codes, e8, bias)            # x1: [1, K]
 """
 import ctypes
 import os
@@ -21,8 +23,9 @@ KERNEL_AUTO, KERNEL_GEMV, KERNEL_SKINNY = 0, 1, 2
 
 SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_workspace_size", "fp8w_linear_ex",
            "fp8w_status_string", "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version",
-           "fp8w_linear_noalloc", "fp8w_dequantize", "fp8w_quantize_grouped", "fp8w_linear_grouped")
-ABI_VERSION = 5
+           "fp8w_linear_noalloc", "fp8w_dequantize", "fp8w_quantize_grouped", "fp8w_linear_grouped",
+           "fp8w_quantize_mx", "fp8w_linear_mx")
+ABI_VERSION = 6
 
 
 class Fp8wError(RuntimeError):
@@ -53,6 +56,10 @@ def lib():
         L.fp8w_quantize_grouped.argtypes = [P, c.c_int64, c.c_int64, c.c_int, P, P, P]
         L.fp8w_linear_grouped.restype = c.c_int
         L.fp8w_linear_grouped.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, c.c_int, P, c.c_int64, P, P]
+        L.fp8w_quantize_mx.restype = c.c_int
+        L.fp8w_quantize_mx.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
+        L.fp8w_linear_mx.restype = c.c_int
+        L.fp8w_linear_mx.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P]
         L.fp8w_dequantize.restype = c.c_int
         L.fp8w_dequantize.argtypes = [P, P, c.c_int64, c.c_int64, c.c_int, P, P]
         L.fp8w_linear.restype = c.c_int
@@ -123,6 +130,22 @@ def quantize(w, codes=None, scales=None, group=None):
     return codes, scales
 
 
+def quantize_mx(w, codes=None, scales=None):
+    """W[N, K] fp32 (CUDA, contiguous, K % 32 == 0) -> (codes uint8 [N, K],
+    scales uint8 [N, K / 32]): the MX-style form, one E8M0 byte (2^(b - 127))
+    per 32 weights along K."""
+    import torch
+    if w.dtype != torch.float32 or not w.is_cuda or w.dim() != 2 or not w.is_contiguous():
+        raise TypeError("w must be a contiguous 2-D float32 CUDA tensor")
+    n, k = w.shape
+    if codes is None:
+        codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
+    if scales is None:
+        scales = torch.empty((n, k // 32), dtype=torch.uint8, device=w.device)
+    _check(lib().fp8w_quantize_mx(_ptr(w), n, k, _ptr(codes), _ptr(scales), _stream(w)))
+    return codes, scales
+
+
 def dequantize(codes, scales, dtype=None, out=None):
     """W'[N, K] = e4m3(codes) * scales[:, None], rounded once to `dtype`
     (torch.float32, bfloat16 or float16; default bfloat16)."""
@@ -174,7 +197,9 @@ def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_
     import torch
     if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
         raise TypeError("x must be a contiguous 2-D CUDA tensor")
-    for name, t, dt in (("codes", codes, torch.uint8), ("scales", scales, torch.float32),
+    # E8M0 scale bytes [N, K / 32] (the MX-style form) or fp32 scales
+    mx = scales.dim() == 2 and scales.dtype == torch.uint8
+    for name, t, dt in (("codes", codes, torch.uint8), ("scales", scales, torch.uint8 if mx else torch.float32),
                         ("bias", bias, torch.float32)):
         if t is not None and (t.dtype != dt or not t.is_cuda or not t.is_contiguous()):
             raise TypeError("%s must be a contiguous %s CUDA tensor" % (name, dt))
@@ -183,12 +208,18 @@ def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_
     if scales.dim() == 2:
         # per-group scales [N, K / group]: the GEMV's grouped form (M == 1)
         if codes.dim() != 2 or codes.shape[1] != k or scales.shape[0] != n or k % scales.shape[1] or \
-                (bias is not None and bias.numel() != n):
+                (mx and scales.shape[1] * 32 != k) or (bias is not None and bias.numel() != n):
             raise ValueError("shape mismatch for per-group scales")
         if out is None:
             out = torch.empty((m, n), dtype=x.dtype, device=x.device)
-        _check(lib().fp8w_linear_grouped(_ptr(x), _act(x.dtype), m, k, _ptr(codes), _ptr(scales),
-                                         k // scales.shape[1], _ptr(bias), n, _ptr(out), _stream(x)))
+        elif out.shape != (m, n) or out.dtype != x.dtype or not out.is_contiguous():
+            raise ValueError("out must be a contiguous [M, N] tensor of x's dtype")
+        if mx:
+            _check(lib().fp8w_linear_mx(_ptr(x), _act(x.dtype), m, k, _ptr(codes), _ptr(scales),
+                                        _ptr(bias), n, _ptr(out), _stream(x)))
+        else:
+            _check(lib().fp8w_linear_grouped(_ptr(x), _act(x.dtype), m, k, _ptr(codes), _ptr(scales),
+                                             k // scales.shape[1], _ptr(bias), n, _ptr(out), _stream(x)))
         return out
     if codes.dim() != 2 or codes.shape[1] != k or scales.numel() != n or \
             (bias is not None and bias.numel() != n):

@@ -69,6 +69,26 @@ fp8w_status fp8w_linear_grouped(const void* x, int act_dtype, int64_t m, int64_t
     return cuda_status(fp8w::launch_gemv(a, static_cast<cudaStream_t>(stream)), "fp8w_linear_grouped launch");
 }
 
+fp8w_status fp8w_quantize_mx(const float* w, int64_t n, int64_t k, uint8_t* codes, uint8_t* scales, void* stream) {
+    if (!w || !codes || !scales) return FP8W_ERR_NULL;
+    if (n < 1 || n > FP8W_MAX_DIM || !valid_k(k) || k % 32 != 0) return FP8W_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(codes, 16)) return FP8W_ERR_ALIGN;
+    return cuda_status(fp8w::launch_quantize_mx(w, n, k, codes, scales, static_cast<cudaStream_t>(stream)),
+                       "fp8w_quantize_mx launch");
+}
+
+fp8w_status fp8w_linear_mx(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
+                           const uint8_t* scales, const float* bias, int64_t n, void* y, void* stream) {
+    const float* sp = reinterpret_cast<const float*>(scales);  // E8M0 bytes, passed through
+    fp8w_status st = check_linear(x, act_dtype, m, k, codes, sp, bias, n, y);
+    if (st != FP8W_OK) return st;
+    // a row's k / 32 scale bytes are bulk-copied with its codes: k % 512 == 0
+    if (m != 1 || k % 512 != 0 || !fp8w::gemv_supports(k)) return FP8W_ERR_SHAPE;
+    if (!aligned(scales, 16)) return FP8W_ERR_ALIGN;
+    fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, sp, bias, y, 32, true};
+    return cuda_status(fp8w::launch_gemv(a, static_cast<cudaStream_t>(stream)), "fp8w_linear_mx launch");
+}
+
 fp8w_status fp8w_dequantize(const uint8_t* codes, const float* scales, int64_t n, int64_t k, int out_dtype,
                             void* w, void* stream) {
     if (!codes || !scales || !w) return FP8W_ERR_NULL;

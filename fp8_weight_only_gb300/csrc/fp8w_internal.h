@@ -16,6 +16,7 @@ struct LinearArgs {
     const float* bias;  // may be null
     void* y;
     int64_t group = 0;  // 0: scales[n]; else scales[n, k / group] (GEMV only)
+    bool e8m0 = false;  // with group 32: scales are E8M0 bytes, not fp32
 };
 
 // K1: codes/scales from fp32 weights.
@@ -25,6 +26,10 @@ cudaError_t launch_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes
 // Per-group scales: scales[n, k / group], group 32, 64 or 128, k % group == 0.
 cudaError_t launch_quantize_grouped(const float* w, int64_t n, int64_t k, int group, uint8_t* codes, float* scales,
                                     cudaStream_t st);
+
+// MX-style: codes and E8M0 scales[n, k / 32], k % 32 == 0.
+cudaError_t launch_quantize_mx(const float* w, int64_t n, int64_t k, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t st);
 
 // The dequantised weight, rounded once to fp32 (out_dtype 0), bf16 (1) or fp16 (2).
 cudaError_t launch_dequantize(const uint8_t* codes, const float* scales, int64_t n, int64_t k, int out_dtype,

@@ -156,10 +156,17 @@ __device__ __forceinline__ void dot_chunk_f32(const uint4 (&c)[RP], const uint4 
 // slot's rows of scales with its codes, and every 16-code chunk's partial
 // sums enter the row's sums times their group's scale (one packed FMA), so
 // the epilogue adds only the bias.
-template <int RP, bool kBf16, bool kF32X, bool kGrouped>
+// kGS: 0 one fp32 scale a row; 1 fp32 scales per group (kGrouped); 2 the
+// MX-style form (page "11. Inference with NVFP4/MXFP8", section
+// "MXFP8-Style FP8"): one E8M0 byte per 32 codes, worth 2^(b - 127), which
+// scales the partials exactly like an fp32 group scale.
+template <int RP, bool kBf16, bool kF32X, int kGS>
 __global__ void __launch_bounds__(kGemvThreads, 1)
     gemv_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ codes, const float* __restrict__ scales,
                 const float* __restrict__ bias, uint16_t* __restrict__ y, int64_t n, int64_t k, GemvGeom geo) {
+    constexpr bool kGrouped = kGS != 0;
+    constexpr bool kE8 = kGS == 2;
+    constexpr int kScaleBytes = kE8 ? 1 : 4;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const uint32_t ring = smem_u32(smem);
@@ -216,9 +223,11 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                 const int64_t rows = (row1 - r0) < R ? (row1 - r0) : R;
                 const uint32_t bytes = static_cast<uint32_t>(rows * k);
                 if constexpr (kGrouped) {
-                    const uint32_t sbytes = static_cast<uint32_t>(rows * geo.ngroups * 4);
+                    const uint32_t sbytes = static_cast<uint32_t>(rows * geo.ngroups * kScaleBytes);
                     mbar_arrive_expect_tx(full(s), bytes + sbytes);
-                    bulk_load(sring + s * geo.sslot_bytes, scales + r0 * geo.ngroups, sbytes, full(s), pol);
+                    bulk_load(sring + s * geo.sslot_bytes,
+                              reinterpret_cast<const uint8_t*>(scales) + r0 * geo.ngroups * kScaleBytes, sbytes,
+                              full(s), pol);
                 } else {
                     mbar_arrive_expect_tx(full(s), bytes);
                 }
@@ -309,8 +318,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             const int nr = rows - r < RP ? rows - r : RP;  // rows in this item (the slot's last may be short)
             const uint32_t rowp = ring + s * geo.slot_bytes + static_cast<uint32_t>(r * k);
             // per-group scales of the item's rows
-            const float* gsc = reinterpret_cast<const float*>(smem + (sring - ring) + s * geo.sslot_bytes) +
-                               static_cast<int64_t>(r) * geo.ngroups;
+            const uint8_t* gsb = smem + (sring - ring) + s * geo.sslot_bytes +
+                                 static_cast<int64_t>(r) * geo.ngroups * kScaleBytes;
             uint64_t acc[RP];
 #pragma unroll
             for (int q = 0; q < RP; ++q) acc[q] = 0ull;
@@ -321,7 +330,8 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                 uint4 cw[RP];
 #pragma unroll
                 for (int q = 0; q < RP; ++q)
-                    cw[q] = q < nr ? lds128(rowp + q * kk + static_cast<uint32_t>(ch) * 16u) : make_uint4(0u, 0u, 0u, 0u);
+                    cw[q] = q < nr ? lds128(rowp + q * kk + static_cast<uint32_t>(ch) * 16u)
+                                   : make_uint4(0u, 0u, 0u, 0u);
                 const uint32_t xa = xv + static_cast<uint32_t>(ch) * 16u;
                 uint64_t part[RP];
 #pragma unroll
@@ -337,7 +347,18 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                 if constexpr (kGrouped) {
 #pragma unroll
                     for (int q = 0; q < RP; ++q) {
-                        const float g = gsc[q * geo.ngroups + (ch >> geo.gshift)];
+                        const int gi = q * geo.ngroups + (ch >> geo.gshift);
+                        float g;
+                        if constexpr (kE8) {
+                            // 2^(b - 127) is the fp32 pattern b << 23, except b = 0
+                            // (the subnormal 2^-127, 0x00400000) and b = 0xFF (NaN,
+                            // 0x7FC00000): both gain the bit 0x00400000, and they are
+                            // the two bytes with (b + 1) & 0xFE == 0
+                            const uint32_t b = gsb[gi];
+                            g = __uint_as_float((b << 23) | (((b + 1u) & 0xFEu) == 0u ? 0x00400000u : 0u));
+                        } else {
+                            g = reinterpret_cast<const float*>(gsb)[gi];
+                        }
                         ffma2(acc[q], part[q], pack2(g, g));
                     }
                 }
@@ -399,6 +420,7 @@ static uint32_t gemv_fixed_bytes(int64_t k, bool f32x, int staged) {
 template <bool kBf16>
 static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     const bool grouped = a.group > 0;
+    const int sbytes = a.e8m0 ? 1 : 4;
     int sms = 0;
     cudaError_t e = device_sm_count(sms);
     if (e != cudaSuccess) return e;
@@ -422,7 +444,7 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     geo.ngroups = grouped ? static_cast<int>(a.k / a.group) : 0;
     geo.gshift = 0;
     while (grouped && (16 << geo.gshift) < a.group) ++geo.gshift;
-    geo.sslot_bytes = static_cast<uint32_t>(((rows * geo.ngroups * 4 + 127) / 128) * 128);
+    geo.sslot_bytes = static_cast<uint32_t>(((rows * geo.ngroups * sbytes + 127) / 128) * 128);
     int64_t slots = (kGemvSmemBudget - gemv_fixed_bytes(a.k, f32x, geo.staged)) / (geo.slot_bytes + geo.sslot_bytes);
     if (slots > kGemvMaxSlots) slots = kGemvMaxSlots;
     if (slots < 2) return cudaErrorNotSupported;
@@ -434,16 +456,17 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     while (geo.g < kGemvWarps && items * geo.g * 2 < kGemvWarps) geo.g *= 2;
     const uint32_t smem = geo.ring_bytes + gemv_fixed_bytes(a.k, f32x, geo.staged);
 
-    auto kern = grouped ? (f32x ? gemv_kernel<2, kBf16, true, true> : gemv_kernel<2, kBf16, false, true>)
-                        : (f32x ? gemv_kernel<2, kBf16, true, false> : gemv_kernel<2, kBf16, false, false>);
+    const int kind = !grouped ? 0 : a.e8m0 ? 2 : 1;
+    decltype(&gemv_kernel<2, kBf16, false, 0>) all[6] = {
+        gemv_kernel<2, kBf16, false, 0>, gemv_kernel<2, kBf16, true, 0>, gemv_kernel<2, kBf16, false, 1>,
+        gemv_kernel<2, kBf16, true, 1>,  gemv_kernel<2, kBf16, false, 2>, gemv_kernel<2, kBf16, true, 2>};
+    auto kern = all[2 * kind + (f32x ? 1 : 0)];
     static std::once_flag attr_once[64];
     int dev = 0;
     e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once[dev & 63], [&] {
-        decltype(kern) all[4] = {gemv_kernel<2, kBf16, false, false>, gemv_kernel<2, kBf16, true, false>,
-                                 gemv_kernel<2, kBf16, false, true>, gemv_kernel<2, kBf16, true, true>};
         for (auto f : all)
             if (attr_err == cudaSuccess)
                 attr_err = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemvSmemBudget);

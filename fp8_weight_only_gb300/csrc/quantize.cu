@@ -118,10 +118,36 @@ cudaError_t launch_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes
 // per-channel rule above.  A lane takes 4 weights; a group is GL = group / 4
 // consecutive lanes of one warp, whose amax is an exact shuffle maximum.
 // HBM bytes per element: 4 read + 1 written (+ 4 per group).
-template <int GL>
+//
+// kMx: the MX-style form (page "11. Inference with NVFP4/MXFP8", section
+// "MXFP8-Style FP8"): group 32 and an E8M0 byte per group, the smallest
+// power of two 2^e >= amax / 448, e clamped to [-127, 127]; an all-zero
+// group takes 2^0 and an infinite amax the NaN byte 0xFF with NaN codes.
+
+// E8M0 byte of a group's amax (non-negative, NaN already dropped by fmaxf
+// unless every weight was NaN).  With amax = (1 + f) 2^E, amax / 448 =
+// (1 + f) / 1.75 * 2^(E - 8), a number in (2^(E - 9), 2^(E - 8)] while
+// 1 + f <= 1.75 (mantissa field <= 0x600000), else in (2^(E - 8), 2^(E - 7)):
+// an integer decision on the bits, no rounding involved.
+__device__ __forceinline__ uint32_t mx_scale_byte(float amax) {
+    const uint32_t u = __float_as_uint(amax);
+    if (u == 0u || u > 0x7F800000u) return 127u;  // zero (or an all-NaN group, as a zero amax)
+    if (u == 0x7F800000u) return 255u;            // infinite
+    if (u < 0x00800000u) return 0u;               // subnormal: far below 448 * 2^-127
+    const int e = static_cast<int>(u >> 23) - 135 + ((u & 0x7FFFFFu) > 0x600000u ? 1 : 0);
+    return e < -127 ? 0u : static_cast<uint32_t>(e + 127);
+}
+
+// The fp32 value of an E8M0 byte below 0xFF: 2^(b - 127) (b = 0 is the
+// subnormal 2^-127).
+__device__ __forceinline__ float mx_scale_value(uint32_t b) {
+    return __uint_as_float(b == 0u ? 0x00400000u : b << 23);
+}
+
+template <int GL, bool kMx>
 __global__ void __launch_bounds__(kQuantThreads) quantize_grouped_kernel(const float* __restrict__ w, int64_t nf4,
                                                                          int gshift, uint8_t* __restrict__ codes,
-                                                                         float* __restrict__ scales) {
+                                                                         void* __restrict__ scales) {
     const int lane = threadIdx.x & 31;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kQuantThreads;
     // a warp-uniform loop: the shuffles below need every lane; nf4 is a
@@ -134,12 +160,26 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_grouped_kernel(const f
         float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 #pragma unroll
         for (int off = GL / 2; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-        const float sc = scale_from_amax(a);
-        if (in) {
-            reinterpret_cast<uint32_t*>(codes)[f] = encode4(v, sc);
-            if ((lane & (GL - 1)) == 0) scales[(f * 4) >> gshift] = sc;
+        if constexpr (kMx) {
+            const uint32_t b = mx_scale_byte(a);
+            if (in) {
+                reinterpret_cast<uint32_t*>(codes)[f] = b == 255u ? 0x7F7F7F7Fu : encode4(v, mx_scale_value(b));
+                if ((lane & (GL - 1)) == 0) static_cast<uint8_t*>(scales)[(f * 4) >> gshift] = static_cast<uint8_t>(b);
+            }
+        } else {
+            const float sc = scale_from_amax(a);
+            if (in) {
+                reinterpret_cast<uint32_t*>(codes)[f] = encode4(v, sc);
+                if ((lane & (GL - 1)) == 0) static_cast<float*>(scales)[(f * 4) >> gshift] = sc;
+            }
         }
     }
+}
+
+static unsigned grouped_grid(int64_t nf4, int sms) {
+    int64_t blocks = (nf4 + kQuantThreads - 1) / kQuantThreads;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    return static_cast<unsigned>(blocks > cap ? cap : blocks);
 }
 
 cudaError_t launch_quantize_grouped(const float* w, int64_t n, int64_t k, int group, uint8_t* codes, float* scales,
@@ -148,14 +188,21 @@ cudaError_t launch_quantize_grouped(const float* w, int64_t n, int64_t k, int gr
     cudaError_t e = device_sm_count(sms);
     if (e != cudaSuccess) return e;
     const int64_t nf4 = n * k / 4;
-    int64_t blocks = (nf4 + kQuantThreads - 1) / kQuantThreads;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;
-    if (blocks > cap) blocks = cap;
-    const unsigned g = static_cast<unsigned>(blocks);
+    const unsigned g = grouped_grid(nf4, sms);
     const int gshift = group == 32 ? 5 : group == 64 ? 6 : 7;
-    if (group == 32) quantize_grouped_kernel<8><<<g, kQuantThreads, 0, st>>>(w, nf4, gshift, codes, scales);
-    else if (group == 64) quantize_grouped_kernel<16><<<g, kQuantThreads, 0, st>>>(w, nf4, gshift, codes, scales);
-    else quantize_grouped_kernel<32><<<g, kQuantThreads, 0, st>>>(w, nf4, gshift, codes, scales);
+    if (group == 32) quantize_grouped_kernel<8, false><<<g, kQuantThreads, 0, st>>>(w, nf4, gshift, codes, scales);
+    else if (group == 64) quantize_grouped_kernel<16, false><<<g, kQuantThreads, 0, st>>>(w, nf4, gshift, codes, scales);
+    else quantize_grouped_kernel<32, false><<<g, kQuantThreads, 0, st>>>(w, nf4, gshift, codes, scales);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_mx(const float* w, int64_t n, int64_t k, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t st) {
+    int sms = 0;
+    cudaError_t e = device_sm_count(sms);
+    if (e != cudaSuccess) return e;
+    const int64_t nf4 = n * k / 4;
+    quantize_grouped_kernel<8, true><<<grouped_grid(nf4, sms), kQuantThreads, 0, st>>>(w, nf4, 5, codes, scales);
     return cudaGetLastError();
 }
 

@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define FP8W_ABI_VERSION 5
+#define FP8W_ABI_VERSION 6
 
 #if defined(__GNUC__)
 #define FP8W_API __attribute__((visibility("default")))
@@ -116,6 +116,38 @@ FP8W_API fp8w_status fp8w_quantize_grouped(const float *w, int64_t n, int64_t k,
 FP8W_API fp8w_status fp8w_linear_grouped(const void *x, int act_dtype, int64_t m, int64_t k,
                                 const uint8_t *codes, const float *scales, int group,
                                 const float *bias, int64_t n, void *y, void *stream);
+
+/*
+ * fp8w_quantize_mx -- the MX-style weight-only quantiser (page "11.
+ * Inference with NVFP4/MXFP8", section "MXFP8-Style FP8": e4m3 codes
+ * [n, k] and one E8M0 ("f8e8m0fnu") scale byte per 32 codes along k).
+ *
+ *   w      [n, k] fp32, device, 16-byte aligned; k % 32 == 0.
+ *   codes  [n, k] uint8, device, 16-byte aligned (output).
+ *   scales [n, k / 32] uint8 row-major, device, any alignment (output).
+ *
+ * A byte b stands for 2^(b - 127) (0xFF is NaN).  Each block of 32 takes
+ * the smallest power of two 2^e >= amax / 448, e clamped to [-127, 127], so
+ * its largest weight is never clipped; an all-zero block takes 2^0.  Codes
+ * are the nearest-even e4m3 of fp32(w / 2^e).  A block with an infinite
+ * weight gets the NaN byte 0xFF and NaN codes (0x7F).
+ */
+FP8W_API fp8w_status fp8w_quantize_mx(const float *w, int64_t n, int64_t k,
+                             uint8_t *codes, uint8_t *scales, void *stream);
+
+/*
+ * fp8w_linear_mx -- fp8w_linear_grouped with group 32 and E8M0 scale bytes:
+ *   y[0, r] = round_act( sum_j 2^(scales[r, j] - 127) * sum_{c in block j} x[0, c] * e4m3(codes[r, c]) + bias[r] ).
+ *
+ * The GEMV kernel: m == 1, k % 512 == 0 and k <= 32768 (otherwise
+ * FP8W_ERR_SHAPE); scales [n, k / 32] uint8, 16-byte aligned (a slot's rows
+ * of scale bytes are bulk-copied beside its codes).  Other arguments as
+ * fp8w_linear.  The scales are powers of two, so scaling a partial sum adds
+ * no rounding (short of over- or underflow); bias added once, one rounding.
+ */
+FP8W_API fp8w_status fp8w_linear_mx(const void *x, int act_dtype, int64_t m, int64_t k,
+                           const uint8_t *codes, const uint8_t *scales,
+                           const float *bias, int64_t n, void *y, void *stream);
 
 /*
  * fp8w_dequantize -- the dequantised weight, the pages' fallback form

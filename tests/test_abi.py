@@ -151,3 +151,32 @@ def _lin_g(m=1, k=512, group=32, scales=C16, cfg=None):
 ])
 def test_linear_grouped_rejects_bad_arguments(kw, status):
     assert _lin_g(**kw) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, 4, 128, B16, C16), 1), ((A16, 4, 128, None, C16), 1), ((A16, 4, 128, B16, None), 1),
+    ((A16, 4, 48, B16, C16), 2), ((A16, 0, 128, B16, C16), 2), ((A16, 4, 65536 + 32, B16, C16), 2),
+    ((ctypes.c_void_p(0x100004), 4, 128, B16, C16), 3), ((A16, 4, 128, ctypes.c_void_p(0x200008), C16), 3),
+])
+def test_quantize_mx_rejects_bad_arguments(args, status):
+    assert fw.lib().fp8w_quantize_mx(*args, None) == status
+
+
+def test_quantize_mx_takes_scale_bytes_at_any_alignment():
+    # a host check only: a misaligned scale pointer passes, a bad k still fails
+    assert fw.lib().fp8w_quantize_mx(A16, 4, 48, B16, ctypes.c_void_p(0x300001), None) == 2
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(scales=None), 1), (dict(x=None), 1),
+    (dict(m=2), 2),                            # the MX form is the GEMV: m == 1
+    (dict(k=256), 2), (dict(k=1024 + 256), 2),  # k % 512 != 0
+    (dict(k=32768 + 512), 2),                  # beyond the GEMV's 32768
+    (dict(act=3), 4),
+    (dict(scales=ctypes.c_void_p(0x300008)), 3),   # scale bytes are bulk-copied: 16-byte aligned
+])
+def test_linear_mx_rejects_bad_arguments(kw, status):
+    a = dict(x=A16, act=1, m=1, k=1024, codes=B16, scales=C16, bias=None, n=8, y=D16)
+    a.update(kw)
+    assert fw.lib().fp8w_linear_mx(a["x"], a["act"], a["m"], a["k"], a["codes"], a["scales"], a["bias"],
+                                   a["n"], a["y"], None) == status

@@ -589,6 +589,105 @@ def test_linear_grouped_parity(n, k, group, act):
     assert_parity(got, ref, act, (n, k, group))
 
 
+def _mx_weight(seed, n, k, kind):
+    if kind == "t":
+        w = synthetic.weight_outlier(seed, n, k)
+    else:
+        w = synthetic.weight_normal(seed, n, k, 0.02)
+    if kind == "range":
+        # blocks spread over the whole fp32 exponent range: clamped (2^-127),
+        # subnormal and near-FLT_MAX amaxes, and exact 448 * 2^e boundaries
+        rng = np.random.default_rng(seed)
+        ex = rng.integers(-149, 128, size=(n, k // 32)).astype(np.float64)
+        w = (w.reshape(n, k // 32, 32) / 0.1 * 2.0 ** ex[:, :, None]).astype(np.float32).reshape(n, k)
+        w[np.isinf(w)] = np.float32(3e38)
+        w[0, 0:32] = 0.0
+        if k >= 96:
+            w[0, 32] = np.float32(448.0 * 2.0 ** -20)
+            w[0, 64] = np.nextafter(np.float32(448.0 * 2.0 ** 5), np.float32(np.inf))
+    if kind == "inf":
+        w[n // 2, 40 % k] = np.inf
+        w[0, 3] = -np.inf
+    return w
+
+
+@pytest.mark.parametrize("kind", ["normal", "t", "range", "inf"])
+@pytest.mark.parametrize("n,k", [(1, 32), (7, 96), (300, 4096), (257, 14336), (33, 1056)])
+def test_quantize_mx_bit_exact(n, k, kind):
+    w = _mx_weight(41 + n + k, n, k, kind)
+    codes, scales = fw.quantize_mx(torch.from_numpy(w).to(DEV))
+    torch.cuda.synchronize()
+    rc, rs = oracle.quantize_mx(w)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+def test_quantize_mx_scale_byte_at_every_boundary():
+    """One block per amax 448 * 2^e and its two fp32 neighbours, e over the
+    whole range, plus tiny and huge amaxes: every byte as the oracle's."""
+    amax = []
+    for e in range(-140, 120):
+        v = np.float32(448.0 * 2.0 ** e)
+        if v == 0 or not np.isfinite(v):
+            continue
+        amax += [np.nextafter(v, np.float32(0)), v, np.nextafter(v, np.float32(np.inf))]
+    amax += [np.float32(1e-45), np.float32(1e-40), np.finfo(np.float32).max, np.float32(0)]
+    w = np.zeros((len(amax), 32), np.float32)
+    for i, a in enumerate(amax):
+        w[i, :] = a / np.float32(3)
+        w[i, i % 32] = -a
+    codes, scales = fw.quantize_mx(torch.from_numpy(w).to(DEV))
+    torch.cuda.synchronize()
+    rc, rs = oracle.quantize_mx(w)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+
+
+@pytest.mark.parametrize("act", [oracle.ACT_BF16, oracle.ACT_F16])
+@pytest.mark.parametrize("n,k", [(1, 512), (300, 4096), (1000, 4096), (257, 14336), (4097, 4096), (153, 1024),
+                                 (64, 32768), (14336, 4096)])
+def test_linear_mx_parity(n, k, act):
+    c = synthetic.random_case(700 + n + k + act, 1, n, k, act=act, with_bias=(n % 2 == 1))
+    w = c["w"].copy()
+    w[:, ::97] *= 40.0                                    # outliers that the blocks of 32 contain
+    codes, scales = oracle.quantize_mx(w)
+    x = torch.from_numpy(c["x"].view(np.int16)).to(DEV).view(_dt(act))
+    cd = torch.from_numpy(codes).to(DEV)
+    sd = torch.from_numpy(scales).to(DEV)
+    bd = None if c["bias"] is None else torch.from_numpy(c["bias"]).to(DEV)
+    buf, y = _guarded(n, _dt(act), POISON16)
+    fw.linear(x, cd, sd, bd, out=y.view(1, n))
+    torch.cuda.synchronize()
+    _check_canaries(buf, n, POISON16)
+    assert fw.device_error() == 0
+    got = y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(1, n)
+    ref = oracle.linear_mx(c["x"], act, codes, scales, c["bias"], threads=oracle.host_cores())
+    assert_parity(got, ref, act, (n, k, "mx"))
+
+
+def test_linear_mx_equals_the_grouped_linear_on_decoded_scales():
+    """The E8M0 bytes decode to exact fp32 powers of two: the MX GEMV and the
+    fp32 per-group GEMV at g = 32 do the same arithmetic, bit for bit,
+    including the 2^-127 and 2^127 ends and the NaN byte."""
+    n, k = 700, 4096
+    c = synthetic.random_case(5, 1, n, k, act=oracle.ACT_BF16, with_bias=True)
+    codes, scales = oracle.quantize_mx(c["w"])
+    scales[3, :4] = [0, 1, 254, 253]
+    scales[5, 7] = 255
+    dec = np.vectorize(oracle.e8m0_decode)(scales).astype(np.float32)
+    x = torch.from_numpy(c["x"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    cd = torch.from_numpy(codes).to(DEV)
+    bd = torch.from_numpy(c["bias"]).to(DEV)
+    y_mx = fw.linear(x, cd, torch.from_numpy(scales).to(DEV), bd)
+    y_g = fw.linear(x, cd, torch.from_numpy(dec).to(DEV), bd)
+    torch.cuda.synchronize()
+    a = y_mx.view(torch.int16).cpu().numpy()
+    b = y_g.view(torch.int16).cpu().numpy()
+    assert np.array_equal(a, b)
+    assert (int(a[0, 5]) & 0x7FFF) > 0x7F80              # the NaN byte's row is NaN
+    assert np.count_nonzero((a[0] & 0x7FFF) > 0x7F80) == 1 + int(((a[0, 3] & 0x7FFF) > 0x7F80))
+
+
 def test_linear_grouped_with_one_scale_per_group_equal_to_per_channel():
     """Group scales all equal to the row's scale: the grouped GEMV must give
     the per-channel GEMV's output (the same sums, scaled per chunk instead of
