@@ -149,6 +149,9 @@ __host__ __device__ constexpr size_t ws_slot_floats() { return static_cast<size_
 constexpr size_t skinny_workspace_bytes(int p) {
     return kWsCountersBytes + 2 * static_cast<size_t>(p) * ws_slot_floats() * 4;
 }
+// Tokens whose cluster partials one thread loads before adding them up.
+constexpr int kRedBatch = 4;
+
 // A split CTA takes at least this many units, so a small matrix is not cut
 // into more partial tiles than it has k-blocks to share.
 constexpr int64_t kMinUnitsPerCta = 4;
@@ -723,17 +726,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (red_thread && !*ep_abort && iters > 0) {
             const uint32_t pt = sbase + L::kCodesOff;
             if (col < n) {
-                for (int tok = etid / nch; tok < m_rows; tok += 128 / nch) {
-                    const uint32_t off = pt + static_cast<uint32_t>((tok * kTileN + ch) * 4);
-                    float v[8];
+                // kRedBatch tokens' loads from all ranks are issued before any
+                // sum, so their remote round trips overlap
+                const int tstep = 128 / nch;
+                for (int tok0 = etid / nch; tok0 < m_rows; tok0 += kRedBatch * tstep) {
+                    float v[kRedBatch][8];
 #pragma unroll
-                    for (int rr = 0; rr < 8; ++rr)
-                        if (rr < split) v[rr] = ld_shared_cluster_f32(mapa_shared(off, rr));
-                    float t = 0.0f;
+                    for (int e = 0; e < kRedBatch; ++e) {
+                        const int tok = tok0 + e * tstep;
+                        const uint32_t off = pt + static_cast<uint32_t>((tok * kTileN + ch) * 4);
 #pragma unroll
-                    for (int rr = 0; rr < 8; ++rr)
-                        if (rr < split) t += v[rr];
-                    y[static_cast<int64_t>(tok) * n + col] = round_out<kBf16>(fmaf(t, sc, b));
+                        for (int rr = 0; rr < 8; ++rr)
+                            if (rr < split && tok < m_rows) v[e][rr] = ld_shared_cluster_f32(mapa_shared(off, rr));
+                    }
+#pragma unroll
+                    for (int e = 0; e < kRedBatch; ++e) {
+                        const int tok = tok0 + e * tstep;
+                        if (tok >= m_rows) break;
+                        float t = 0.0f;
+#pragma unroll
+                        for (int rr = 0; rr < 8; ++rr)
+                            if (rr < split) t += v[e][rr];
+                        y[static_cast<int64_t>(tok) * n + col] = round_out<kBf16>(fmaf(t, sc, b));
+                    }
                 }
             }
         }
