@@ -8,7 +8,7 @@ raised.
     codes, scales = quantize(w)                 # w: [N, K] fp32 CUDA tensor
     y = linear(x, codes, scales, bias)          # x: [M, K] bf16/fp16 CUDA tensor
     codes, e8 = quantize_mx(w)                  # one E8M0 scale byte per 32 along K
-    y1 = linear(x1, codes, e8, bias)            # x1: [1, K]
+    y = linear(x, codes, e8, bias)              # bf16 x for M > 1
 """
 import ctypes
 import os
@@ -59,7 +59,7 @@ def lib():
         L.fp8w_quantize_mx.restype = c.c_int
         L.fp8w_quantize_mx.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
         L.fp8w_linear_mx.restype = c.c_int
-        L.fp8w_linear_mx.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P]
+        L.fp8w_linear_mx.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P, c.c_size_t, P]
         L.fp8w_dequantize.restype = c.c_int
         L.fp8w_dequantize.argtypes = [P, P, c.c_int64, c.c_int64, c.c_int, P, P]
         L.fp8w_linear.restype = c.c_int
@@ -215,8 +215,13 @@ def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_
         elif out.shape != (m, n) or out.dtype != x.dtype or not out.is_contiguous():
             raise ValueError("out must be a contiguous [M, N] tensor of x's dtype")
         if mx:
-            _check(lib().fp8w_linear_mx(_ptr(x), _act(x.dtype), m, k, _ptr(codes), _ptr(scales),
-                                        _ptr(bias), n, _ptr(out), _stream(x)))
+            L = lib()
+            need = 0 if (m == 1 and k % 512 == 0 and k <= 32768) else L.fp8w_linear_workspace_size(max(m, 2), n, k)
+            ws = None
+            if need:
+                ws = workspace_buffer if workspace_buffer is not None else workspace(x.device, need)
+            _check(L.fp8w_linear_mx(_ptr(x), _act(x.dtype), m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
+                                    _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(), _stream(x)))
         else:
             _check(lib().fp8w_linear_grouped(_ptr(x), _act(x.dtype), m, k, _ptr(codes), _ptr(scales),
                                              k // scales.shape[1], _ptr(bias), n, _ptr(out), _stream(x)))

@@ -48,6 +48,8 @@ fp8w_status fp8w_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes, 
                        "fp8w_quantize launch");
 }
 
+static size_t skinny_ws(void);
+
 static bool valid_group(int group) { return group == 32 || group == 64 || group == 128; }
 
 fp8w_status fp8w_quantize_grouped(const float* w, int64_t n, int64_t k, int group, uint8_t* codes, float* scales,
@@ -78,15 +80,27 @@ fp8w_status fp8w_quantize_mx(const float* w, int64_t n, int64_t k, uint8_t* code
 }
 
 fp8w_status fp8w_linear_mx(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
-                           const uint8_t* scales, const float* bias, int64_t n, void* y, void* stream) {
+                           const uint8_t* scales, const float* bias, int64_t n, void* y, void* workspace,
+                           size_t workspace_bytes, void* stream) {
     const float* sp = reinterpret_cast<const float*>(scales);  // E8M0 bytes, passed through
     fp8w_status st = check_linear(x, act_dtype, m, k, codes, sp, bias, n, y);
     if (st != FP8W_OK) return st;
-    // a row's k / 32 scale bytes are bulk-copied with its codes: k % 512 == 0
-    if (m != 1 || k % 512 != 0 || !fp8w::gemv_supports(k)) return FP8W_ERR_SHAPE;
+    // a unit's 128 codes take one 4-byte word of scale bytes a row
+    if (k % 128 != 0) return FP8W_ERR_SHAPE;
     if (!aligned(scales, 16)) return FP8W_ERR_ALIGN;
     fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, sp, bias, y, 32, true};
-    return cuda_status(fp8w::launch_gemv(a, static_cast<cudaStream_t>(stream)), "fp8w_linear_mx launch");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // m == 1: the GEMV, which bulk-copies a row's k / 32 scale bytes with its
+    // codes (16-byte pieces: k % 512 == 0)
+    if (m == 1 && k % 512 == 0 && fp8w::gemv_supports(k))
+        return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear_mx gemv launch");
+    // otherwise the tensor-core kernel, which folds the scales into bf16 weights
+    if (act_dtype != FP8W_BF16) return FP8W_ERR_DTYPE;
+    if (!workspace || !aligned(workspace, 256)) return FP8W_ERR_WORKSPACE;
+    const size_t need = skinny_ws();
+    if (need == 0) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear_mx device query");
+    if (workspace_bytes < need) return FP8W_ERR_WORKSPACE;
+    return cuda_status(fp8w::launch_skinny(a, workspace, 0, s), "fp8w_linear_mx tensor-core launch");
 }
 
 fp8w_status fp8w_dequantize(const uint8_t* codes, const float* scales, int64_t n, int64_t k, int out_dtype,

@@ -80,11 +80,19 @@ __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
 
 constexpr uint32_t kBf16x2Pow2_120 = 0x7B807B80u;  // bf16 2^120 in both halves
 
-__device__ __forceinline__ void e4m3x4_to_bf16x2(uint32_t w, uint32_t& p01, uint32_t& p23) {
+// Four e4m3 codes -> their values times mul / 2^120 as bf16 pairs: the byte
+// moves place the code's exponent and mantissa bits in a bf16, which reads
+// as value * 2^-120 exactly (e4m3 subnormals become bf16 subnormals); one
+// bf16 multiply by mul (2^120 restores the value) rounds the product once.
+__device__ __forceinline__ void e4m3x4_to_bf16x2_mul(uint32_t w, uint32_t& p01, uint32_t& p23, uint32_t mul) {
     const uint32_t lo = (w << 4) & 0xF0F0F0F0u;                         // E0 M2 M1 M0 0000
     const uint32_t hi = ((w >> 4) & 0x07070707u) | (w & 0x80808080u);  // S 0000 E3 E2 E1
-    p01 = bf16x2_mul(__byte_perm(lo, hi, 0x5140), kBf16x2Pow2_120);
-    p23 = bf16x2_mul(__byte_perm(lo, hi, 0x7362), kBf16x2Pow2_120);
+    p01 = bf16x2_mul(__byte_perm(lo, hi, 0x5140), mul);
+    p23 = bf16x2_mul(__byte_perm(lo, hi, 0x7362), mul);
+}
+
+__device__ __forceinline__ void e4m3x4_to_bf16x2(uint32_t w, uint32_t& p01, uint32_t& p23) {
+    e4m3x4_to_bf16x2_mul(w, p01, p23, kBf16x2Pow2_120);
 }
 
 // Two fp32 values -> two saturating, round-to-nearest-even e4m3 codes

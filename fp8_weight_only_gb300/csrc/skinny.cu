@@ -200,6 +200,28 @@ __device__ __forceinline__ void dequant16(const uint4 c, uint32_t (&out)[8]) {
     }
 }
 
+// MX-style scales (page "11. Inference with NVFP4/MXFP8", section
+// "MXFP8-Style FP8"): one E8M0 byte b per 32 codes, worth 2^e, e = b - 127.
+// It is folded into the dequantised weight, whose bf16 value * 2^e is exact
+// wherever it is a bf16 number (the codes have 4 significant bits).  The
+// first multiplier of a group is 2^(120 + e), a bf16 number for b <= 134
+// (0xFF gives NaN); a warp holding a byte in 135..254 multiplies by 2^120
+// and then by 2^e (b = 0: the subnormal 2^-127), which rounds the same
+// product once.
+__device__ __forceinline__ uint32_t mx_first_mul(uint32_t b, bool twice) {
+    const uint32_t h = b == 255u ? 0x7FC0u : twice ? 0x7B80u : (b + 120u) << 7;
+    return h | (h << 16);
+}
+__device__ __forceinline__ uint32_t mx_second_mul(uint32_t b) {
+    const uint32_t h = b == 255u ? 0x7FC0u : b == 0u ? 0x0040u : b << 7;
+    return h | (h << 16);
+}
+__device__ __forceinline__ void dequant16_mx(const uint4 c, uint32_t (&out)[8], uint32_t mul) {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) e4m3x4_to_bf16x2_mul(w[q], out[2 * q], out[2 * q + 1], mul);
+}
+
 // The recorded code is role * 1000 + 1 + the barrier's index in shared
 // memory (0 when no barrier applies), so a report names the wait that gave up.
 __device__ __forceinline__ void record_error(int code, volatile int* abort_flag, uint32_t bar = 0, uint32_t bar0 = 0) {
@@ -218,11 +240,16 @@ __device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t* counter) {
     return old;
 }
 
-template <int NT, bool kBf16>
+// kMx: the weight carries E8M0 scale bytes e8[n, k / 32] (bf16 activations,
+// k % 128 == 0) instead of per-row scales; they enter the dequantised
+// weight, and the epilogue adds only the bias.
+template <int NT, bool kBf16, bool kMx = false>
 __global__ void __launch_bounds__(kThreads, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
-                  const float* __restrict__ scales, const float* __restrict__ bias, uint16_t* __restrict__ y,
-                  uint8_t* __restrict__ workspace, int m_rows, int m_row0, int64_t n, int64_t k, int split) {
+                  const float* __restrict__ scales, const uint8_t* __restrict__ e8, const float* __restrict__ bias,
+                  uint16_t* __restrict__ y, uint8_t* __restrict__ workspace, int m_rows, int m_row0, int64_t n,
+                  int64_t k, int split) {
+    static_assert(!kMx || kBf16, "MX-style scales fold into bf16 weights only");
     using L = SkinnySmem<NT>;
     constexpr int kCS = L::kCodeSlots, kXS = L::kXSlots;
     extern __shared__ uint8_t smem_raw[];
@@ -514,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool early = !whole && split == 1 && *last_flag;
             tc_fence_after();
             const int64_t col = tile * kTileN + r;
-            const float sc = col < n ? scales[col] : 0.0f;
+            const float sc = kMx ? 1.0f : col < n ? scales[col] : 0.0f;
             const float b = (bias && col < n) ? bias[col] : 0.0f;
             const int64_t slot = 2 * c + (tile == t_first ? 0 : 1);
             float* mine = slots + slot * ws_slot_floats() + r * kMaxNT;
@@ -658,6 +685,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------- dequantising warpgroups (8-19) --
         const int group = (warp - kFirstDequantWarp) >> 2;
+        // MX: this thread's row's four scale bytes of a unit (one word), loaded
+        // a unit ahead; (mx_tile, mx_kb) is the unit after the current one
+        int64_t mx_tile = 0;
+        int mx_kb = 0;
+        uint32_t mx_next = 0x7F7F7F7Fu;
+        auto mx_load = [&](int64_t tile, int kb) -> uint32_t {
+            const int64_t row = tile * kTileN + (warp & 3) * 32 + lane;
+            // rows past n hold zero codes (the copy's fill): any scale does
+            return row < n ? __ldg(reinterpret_cast<const uint32_t*>(e8 + row * (k >> 5) + kb * 4)) : 0x7F7F7F7Fu;
+        };
+        if constexpr (kMx) {
+            pdl_wait();  // the scales may come from the previous kernel
+            const int64_t u = u0 + group;
+            mx_tile = u / nkb;
+            mx_kb = static_cast<int>(u - mx_tile * nkb);
+            if (group < iters) mx_next = mx_load(mx_tile, mx_kb);
+        }
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
         const uint32_t a_lane = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
@@ -667,6 +711,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!mbar_wait_warp(cfull(group, s), ph, abort_flag)) {
                 record_error(kErrWaitTma, abort_flag, cfull(group, s), bar0);
                 break;
+            }
+            uint32_t mx_word = 0u;
+            if constexpr (kMx) {
+                mx_word = mx_next;
+                mx_kb += kLanes;
+                while (mx_kb >= nkb) {
+                    mx_kb -= static_cast<int>(nkb);
+                    ++mx_tile;
+                }
+                if (it + kLanes < iters) mx_next = mx_load(mx_tile, mx_kb);
             }
             const uint32_t row = sbase + code_smem(group, s) + r * 128;
             uint4 cw[8];
@@ -680,8 +734,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // the first half is converted while the MMAs may still read the slot
             uint32_t v0[4][8];
+            uint32_t mul[4];
+            bool twice = false;
+            if constexpr (kMx) {
+                // a byte in 135..254 anywhere in the warp: two multiplies
+                twice = __any_sync(0xffffffffu,
+                                   (__vcmpgtu4(mx_word, 0x86868686u) & ~__vcmpeq4(mx_word, 0xFFFFFFFFu)) != 0u);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) dequant16<kBf16>(cw[q], v0[q]);
+                for (int g = 0; g < 4; ++g) mul[g] = mx_first_mul((mx_word >> (8 * g)) & 0xFFu, twice);
+            }
+            // the second multiply of a group's two chunks, when needed
+            auto mx_fix = [&](uint32_t (&v)[8], int q) {
+                if constexpr (kMx) {
+                    if (twice) {
+                        const uint32_t m2 = mx_second_mul((mx_word >> (8 * (q >> 1))) & 0xFFu);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) v[e] = bf16x2_mul(v[e], m2);
+                    }
+                }
+            };
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                if constexpr (kMx) {
+                    dequant16_mx(cw[q], v0[q], mul[q >> 1]);
+                    mx_fix(v0[q], q);
+                } else {
+                    dequant16<kBf16>(cw[q], v0[q]);
+                }
+            }
             // A slot of unit it = group + 3j: it % 6 = group + 3 (j % 2)
             const int r = group + kLanes * (j & 1);
             // the A slot's previous unit (it - 6) must be done
@@ -696,7 +776,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int q = 4; q < 8; ++q) {
                 uint32_t v[8];
-                dequant16<kBf16>(cw[q], v);
+                if constexpr (kMx) {
+                    dequant16_mx(cw[q], v, mul[q >> 1]);
+                    mx_fix(v, q);
+                } else {
+                    dequant16<kBf16>(cw[q], v);
+                }
                 tmem_st_x8(a_addr + q * 8, v);
             }
             tmem_wait_st();
@@ -718,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t col = (c / split) * kTileN + ch;
         float sc = 0.0f, b = 0.0f;
         if (red_thread && col < n) {
-            sc = scales[col];
+            sc = kMx ? 1.0f : scales[col];
             b = bias ? bias[col] : 0.0f;
         }
         // every rank's partial tile is in its shared memory
@@ -842,10 +927,10 @@ SkinnyShape skinny_shape(int64_t n, int64_t k, int sms) {
     return {p, 1};
 }
 
-template <int NT, bool kBf16>
+template <int NT, bool kBf16, bool kMx = false>
 static cudaError_t launch_nt(const LinearArgs& a, void* workspace, int ctas, cudaStream_t st) {
     using L = SkinnySmem<NT>;
-    auto kern = skinny_kernel<NT, kBf16>;
+    auto kern = skinny_kernel<NT, kBf16, kMx>;
     static std::once_flag attr_once[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -892,7 +977,9 @@ static cudaError_t launch_nt(const LinearArgs& a, void* workspace, int ctas, cud
     uint16_t* yp = static_cast<uint16_t*>(a.y);
     for (int64_t m0 = 0; m0 < a.m; m0 += NT) {
         const int rows = static_cast<int>(a.m - m0 < NT ? a.m - m0 : NT);
-        e = cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, a.scales, a.bias, yp + m0 * a.n,
+        const float* sc = kMx ? nullptr : a.scales;
+        const uint8_t* e8 = kMx ? reinterpret_cast<const uint8_t*>(a.scales) : nullptr;
+        e = cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, sc, e8, a.bias, yp + m0 * a.n,
                                static_cast<uint8_t*>(workspace), rows, static_cast<int>(m0), a.n, a.k, shape.split);
         if (e != cudaSuccess) return e;
     }
@@ -903,6 +990,13 @@ size_t skinny_workspace_size(int sms) { return skinny_workspace_bytes(sms < kMax
 
 cudaError_t launch_skinny(const LinearArgs& a, void* workspace, int ctas, cudaStream_t st) {
     const bool bf16 = a.act == 1;
+    if (a.e8m0) {
+        // MX-style scales: bf16 activations, k % 128 == 0 (checked by the caller)
+        if (!bf16 || a.group != 32 || a.k % 128 != 0) return cudaErrorInvalidValue;
+        if (a.m <= 16) return launch_nt<16, true, true>(a, workspace, ctas, st);
+        if (a.m <= 32) return launch_nt<32, true, true>(a, workspace, ctas, st);
+        return launch_nt<64, true, true>(a, workspace, ctas, st);
+    }
     if (a.m <= 16)
         return bf16 ? launch_nt<16, true>(a, workspace, ctas, st) : launch_nt<16, false>(a, workspace, ctas, st);
     if (a.m <= 32)

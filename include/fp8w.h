@@ -136,18 +136,28 @@ FP8W_API fp8w_status fp8w_quantize_mx(const float *w, int64_t n, int64_t k,
                              uint8_t *codes, uint8_t *scales, void *stream);
 
 /*
- * fp8w_linear_mx -- fp8w_linear_grouped with group 32 and E8M0 scale bytes:
- *   y[0, r] = round_act( sum_j 2^(scales[r, j] - 127) * sum_{c in block j} x[0, c] * e4m3(codes[r, c]) + bias[r] ).
+ * fp8w_linear_mx -- fp8w_linear for codes with E8M0 scale bytes (group 32):
+ *   y[i, r] = round_act( sum_j 2^(scales[r, j] - 127) * sum_{c in block j} x[i, c] * e4m3(codes[r, c]) + bias[r] ).
  *
- * The GEMV kernel: m == 1, k % 512 == 0 and k <= 32768 (otherwise
- * FP8W_ERR_SHAPE); scales [n, k / 32] uint8, 16-byte aligned (a slot's rows
- * of scale bytes are bulk-copied beside its codes).  Other arguments as
- * fp8w_linear.  The scales are powers of two, so scaling a partial sum adds
- * no rounding (short of over- or underflow); bias added once, one rounding.
+ *   scales [n, k / 32] uint8, device, 16-byte aligned; k % 128 == 0.
+ *   workspace, workspace_bytes: as fp8w_linear (fp8w_linear_workspace_size);
+ *           may be NULL / 0 when the GEMV runs.
+ *   Other arguments as fp8w_linear.
+ *
+ * m == 1 with k % 512 == 0 and k <= 32768 runs the GEMV: a slot's rows of
+ * scale bytes are bulk-copied beside its codes, and each 16-code fp32 partial
+ * sum is scaled by its block's power of two, which adds no rounding (short
+ * of over- or underflow); bias added once, one rounding.  Any other shape
+ * runs the tensor-core kernel, for bf16 activations only (FP8W_ERR_DTYPE for
+ * fp16): the scale is folded into the dequantised bf16 weight, e4m3(q) *
+ * 2^(b - 127), which is exact wherever that product is a bf16 number
+ * (anything but products below 2^-130 or beyond the bf16 range), then fp32
+ * accumulation, bias added once, one rounding.
  */
 FP8W_API fp8w_status fp8w_linear_mx(const void *x, int act_dtype, int64_t m, int64_t k,
                            const uint8_t *codes, const uint8_t *scales,
-                           const float *bias, int64_t n, void *y, void *stream);
+                           const float *bias, int64_t n, void *y,
+                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * fp8w_dequantize -- the dequantised weight, the pages' fallback form

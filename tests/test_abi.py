@@ -169,14 +169,17 @@ def test_quantize_mx_takes_scale_bytes_at_any_alignment():
 
 @pytest.mark.parametrize("kw,status", [
     (dict(scales=None), 1), (dict(x=None), 1),
-    (dict(m=2), 2),                            # the MX form is the GEMV: m == 1
-    (dict(k=256), 2), (dict(k=1024 + 256), 2),  # k % 512 != 0
-    (dict(k=32768 + 512), 2),                  # beyond the GEMV's 32768
+    (dict(k=256 + 64), 2), (dict(k=1024 + 16), 2),   # k % 128 != 0
+    (dict(k=65536 + 128), 2),                  # beyond FP8W_MAX_K
     (dict(act=3), 4),
-    (dict(scales=ctypes.c_void_p(0x300008)), 3),   # scale bytes are bulk-copied: 16-byte aligned
+    (dict(scales=ctypes.c_void_p(0x300008)), 3),   # scale bytes: 16-byte aligned
+    (dict(m=2, act=2), 4),                     # the tensor-core form folds the scales into bf16 weights
+    (dict(m=1, k=384, act=2), 4),              # m == 1 but k % 512 != 0: the tensor-core form too
+    (dict(m=2), 7), (dict(m=1, k=384), 7),     # tensor-core form without a workspace
+    (dict(m=2, ws=ctypes.c_void_p(0x600010), ws_bytes=1 << 30), 7),   # misaligned workspace
 ])
 def test_linear_mx_rejects_bad_arguments(kw, status):
-    a = dict(x=A16, act=1, m=1, k=1024, codes=B16, scales=C16, bias=None, n=8, y=D16)
+    a = dict(x=A16, act=1, m=1, k=1024, codes=B16, scales=C16, bias=None, n=8, y=D16, ws=None, ws_bytes=0)
     a.update(kw)
     assert fw.lib().fp8w_linear_mx(a["x"], a["act"], a["m"], a["k"], a["codes"], a["scales"], a["bias"],
-                                   a["n"], a["y"], None) == status
+                                   a["n"], a["y"], a["ws"], a["ws_bytes"], None) == status

@@ -688,6 +688,75 @@ def test_linear_mx_equals_the_grouped_linear_on_decoded_scales():
     assert np.count_nonzero((a[0] & 0x7FFF) > 0x7F80) == 1 + int(((a[0, 3] & 0x7FFF) > 0x7F80))
 
 
+MX_TC_SHAPES = [  # (m, n, k): the tensor-core form; whole tiles, cluster splits, stream-K, 64-token slabs
+    (1, 300, 384), (2, 300, 4096), (8, 4096, 4096), (9, 1024, 4096), (32, 14336, 4096), (17, 257, 640),
+    (8, 20480, 1024), (48, 1000, 1024), (64, 640, 14336), (70, 257, 640), (129, 130, 256),
+]
+
+
+def _mx_case(seed, m, n, k):
+    c = synthetic.random_case(seed, m, n, k, act=oracle.ACT_BF16, with_bias=(n % 2 == 1))
+    w = c["w"].copy()
+    w[:, ::97] *= 40.0
+    codes, scales = oracle.quantize_mx(w)
+    return c, codes, scales
+
+
+def _gpu_mx(c, codes, scales):
+    m, k = c["x"].shape
+    n = codes.shape[0]
+    x = torch.from_numpy(c["x"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    bd = None if c["bias"] is None else torch.from_numpy(c["bias"]).to(DEV)
+    buf, y = _guarded(m * n, torch.bfloat16, POISON16)
+    fw.linear(x, torch.from_numpy(codes).to(DEV), torch.from_numpy(scales).to(DEV), bd, out=y.view(m, n))
+    torch.cuda.synchronize()
+    _check_canaries(buf, m * n, POISON16)
+    assert fw.device_error() == 0
+    return y.view(torch.int16).cpu().numpy().view(np.uint16).reshape(m, n)
+
+
+@pytest.mark.parametrize("m,n,k", MX_TC_SHAPES)
+def test_linear_mx_tensor_core_parity(m, n, k):
+    c, codes, scales = _mx_case(300 + m + n + k, m, n, k)
+    got = _gpu_mx(c, codes, scales)
+    ref = oracle.linear_mx(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], threads=oracle.host_cores())
+    assert_parity(got, ref, oracle.ACT_BF16, (m, n, k, "mx"))
+
+
+@pytest.mark.parametrize("m,n,k,lo,hi", [
+    (8, 4096, 4096, 100, 134),      # one multiply
+    (32, 14336, 1024, 100, 134),
+    (8, 1000, 4096, 120, 141),      # rows with bytes 135..254: two multiplies in their warps
+    (48, 300, 1024, 130, 150),
+])
+def test_linear_mx_with_equal_blocks_is_the_per_channel_linear(m, n, k, lo, hi):
+    """Every block of a row with the same byte b: the MX result equals the
+    per-channel result with scale 2^(b - 127) bit for bit (a power of two
+    commutes with every rounding of the fp32 sums)."""
+    rng = np.random.default_rng(m + n + k + lo)
+    c = synthetic.random_case(31 + m + n, m, n, k, act=oracle.ACT_BF16, with_bias=True)
+    codes = rng.integers(0, 0x7E, size=(n, k), dtype=np.uint8) | rng.integers(0, 2, size=(n, k), dtype=np.uint8) << 7
+    b = rng.integers(lo, hi + 1, size=n).astype(np.uint8)
+    e8 = np.repeat(b[:, None], k // 32, axis=1)
+    per_row = np.float32(2.0) ** (b.astype(np.int32) - 127).astype(np.float32)
+    y_mx = _gpu_mx(c, codes, e8)
+    y_pc = gpu_linear(c["x"], oracle.ACT_BF16, codes, per_row, c["bias"], kernel=fw.KERNEL_SKINNY)
+    assert np.array_equal(y_mx, y_pc)
+
+
+def test_linear_mx_tensor_core_nan_byte_poisons_its_row_only():
+    m, n, k = 8, 640, 1024
+    c, codes, scales = _mx_case(77, m, n, k)
+    scales[5, 3] = 255
+    got = _gpu_mx(c, codes, scales)
+    nan = (got & 0x7FFF) > 0x7F80
+    assert nan[:, 5].all() and nan.sum() == m
+    ref = oracle.linear_mx(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], threads=oracle.host_cores())
+    keep = np.ones(n, bool)
+    keep[5] = False
+    assert_parity(got[:, keep], ref[:, keep], oracle.ACT_BF16, "nan row")
+
+
 def test_linear_grouped_with_one_scale_per_group_equal_to_per_channel():
     """Group scales all equal to the row's scale: the grouped GEMV must give
     the per-channel GEMV's output (the same sums, scaled per chunk instead of
