@@ -263,9 +263,10 @@ def enqueue_step(fw, mats, xs, ys, events=None, ev_list=None, stream_handle=None
 def kernel_name(m, k):
     """The kernel (template instance, as ncu names it) that runs a call."""
     if m == 1:
-        # row pairs against fp32 x up to 8192 codes a row, 16-bit x beyond
-        return "fp8w::gemv_kernel<2, 1, 1>" if k <= 8192 else "fp8w::gemv_kernel<2, 1, 0>"
-    return "fp8w::skinny_kernel<%d, 1>" % (16 if m <= 16 else 32)
+        # row pairs, bf16, fp32 x up to 8192 codes a row (16-bit x beyond), one scale a row
+        return "fp8w::gemv_kernel<2, 1, 1, 0>" if k <= 8192 else "fp8w::gemv_kernel<2, 1, 0, 0>"
+    # tokens a launch, bf16, per-row scales
+    return "fp8w::skinny_kernel<%d, 1, 0>" % (16 if m <= 16 else 32)
 
 
 KERNEL_SOURCES = {"skinny_kernel": ["skinny.cu", "fp8w_device.cuh"], "gemv_kernel": ["gemv.cu", "fp8w_device.cuh"]}

@@ -204,14 +204,9 @@ __device__ __forceinline__ void dequant16(const uint4 c, uint32_t (&out)[8]) {
 // "MXFP8-Style FP8"): one E8M0 byte b per 32 codes, worth 2^e, e = b - 127.
 // It is folded into the dequantised weight, whose bf16 value * 2^e is exact
 // wherever it is a bf16 number (the codes have 4 significant bits).  The
-// first multiplier of a group is 2^(120 + e), a bf16 number for b <= 134
-// (0xFF gives NaN); a warp holding a byte in 135..254 multiplies by 2^120
-// and then by 2^e (b = 0: the subnormal 2^-127), which rounds the same
-// product once.
-__device__ __forceinline__ uint32_t mx_first_mul(uint32_t b, bool twice) {
-    const uint32_t h = b == 255u ? 0x7FC0u : twice ? 0x7B80u : (b + 120u) << 7;
-    return h | (h << 16);
-}
+// multiplier of a group is 2^(120 + e), a bf16 number for b <= 134; a warp
+// holding a larger byte multiplies by 2^120 and then by 2^e (b = 0: the
+// subnormal 2^-127; 0xFF: NaN), which rounds the same product once.
 __device__ __forceinline__ uint32_t mx_second_mul(uint32_t b) {
     const uint32_t h = b == 255u ? 0x7FC0u : b == 0u ? 0x0040u : b << 7;
     return h | (h << 16);
@@ -737,11 +732,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t mul[4];
             bool twice = false;
             if constexpr (kMx) {
-                // a byte in 135..254 anywhere in the warp: two multiplies
-                twice = __any_sync(0xffffffffu,
-                                   (__vcmpgtu4(mx_word, 0x86868686u) & ~__vcmpeq4(mx_word, 0xFFFFFFFFu)) != 0u);
+                // a byte above 134 anywhere in the warp (0xFF included):
+                // two multiplies; otherwise the four 2^(120 + e) at once, the
+                // bytes b + 120 (no carry for b <= 134) as bf16 exponent
+                // fields in both halves
+                twice = __any_sync(0xffffffffu, __vcmpgtu4(mx_word, 0x86868686u) != 0u);
+                const uint32_t wb = __vadd4(mx_word, 0x78787878u);
 #pragma unroll
-                for (int g = 0; g < 4; ++g) mul[g] = mx_first_mul((mx_word >> (8 * g)) & 0xFFu, twice);
+                for (int g = 0; g < 4; ++g)
+                    mul[g] = twice ? kBf16x2Pow2_120 : __byte_perm(wb, 0u, 0x4040u + 0x0101u * g) << 7;
             }
             // the second multiply of a group's two chunks, when needed
             auto mx_fix = [&](uint32_t (&v)[8], int q) {
