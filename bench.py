@@ -192,16 +192,17 @@ class DriverEvents:
 # ------------------------------------------------------------- CPU baseline --
 
 CPU_STRIDE = 2  # the CPU sample takes every 2nd output channel of every call
+CPU_STRIDE_1T = 32  # the single-thread figure: every 32nd channel
 
 
-def cpu_sample(m_list=synthetic.DECODE_STACK_M):
-    """Inputs of the CPU sample: every call of the step, every CPU_STRIDE-th channel."""
+def cpu_sample(m_list=synthetic.DECODE_STACK_M, stride=CPU_STRIDE):
+    """Inputs of the CPU sample: every call of the step, every stride-th channel."""
     import oracle
     out = []
     for m in m_list:
         for (name, n, k) in synthetic.DECODE_STACK:
             c = synthetic.case("decode_stack", m, name)
-            cols = np.arange(0, n, CPU_STRIDE)
+            cols = np.arange(0, n, stride)
             codes, scales = oracle.quantize(c["w"][cols])
             out.append((c["x"], codes, scales, c["bias"][cols], m, len(cols), k))
     return out
@@ -217,10 +218,14 @@ def run_cpu(sample, threads):
     return nbytes / dt / 1e9, dt
 
 
+def ordinal(i):
+    return "%d%s" % (i, "th" if 10 <= i % 100 <= 20 else {1: "st", 2: "nd", 3: "rd"}.get(i % 10, "th"))
+
+
 def cpu_baseline_obj(gbs, dt, cores):
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": "the full step (21 calls, M=1,8,32) restricted to every %dth output channel; "
-                      "plain C fp64 oracle, %d threads; %.2f s" % (CPU_STRIDE, cores, dt)}
+            "sample": "the full step (21 calls, M=1,8,32) restricted to every %s output channel; "
+                      "plain C fp64 oracle, %d threads; %.2f s" % (ordinal(CPU_STRIDE), cores, dt)}
 
 
 # ------------------------------------------------------------------- ours --
@@ -437,6 +442,39 @@ def run_grouped(torch, fw, dev, s, peak, launches=100):
     return out
 
 
+def run_warm_l2(torch, fw, dev, s, launches=200):
+    """[22, 1024] x [1024, 4096] with fp16 activations (the pages' Triton
+    figure, 5.6 us with a warm L2 on an sm_120 GPU): the same buffers
+    replayed back to back, so the 4.2 MB weight stays in L2."""
+    c = synthetic.case("fp16_template")
+    w = torch.from_numpy(c["w"]).to(dev)
+    x = torch.from_numpy(c["x"].view(np.int16)).to(dev).view(torch.float16)
+    bias = torch.from_numpy(c["bias"]).to(dev)
+    codes, scales = fw.quantize(w)
+    y = torch.empty((c["m"], c["n"]), dtype=torch.float16, device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        fw.linear(x, codes, scales, bias, out=y)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(launches):
+                fw.linear(x, codes, scales, bias, out=y)
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / launches
+    del g
+    return {"us_per_launch": round(us, 3), "shape": "[22, 1024] x [1024, 4096], fp16",
+            "note": "same buffers, graph-replayed back-to-back launches (warm L2); context: the pages report "
+                    "5.6 us for this shape with a warm L2 on another GPU"}
+
+
 def run_ours(args, torch, dist):
     import fp8_weight_only_gb300 as fw
     ws, rank, local = dist_env()
@@ -465,9 +503,16 @@ def run_ours(args, torch, dist):
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # events at chunk boundaries inside the timed region give the spread of
+    # the per-step time across the run (recording an event costs nothing)
+    n_chunks = 5 if args.steps >= 5 else 1
+    bounds = [args.steps * i // n_chunks for i in range(n_chunks + 1)]
+    ce = [torch.cuda.Event(enable_timing=True) for _ in range(n_chunks - 1)]
     with torch.cuda.stream(s):
         e0.record(s)
-        for _ in range(args.steps):
+        for i in range(args.steps):
+            if 0 < i and i in bounds[1:-1]:
+                ce[bounds.index(i) - 1].record(s)
             g.replay()
         e1.record(s)
     torch.cuda.synchronize()
@@ -476,6 +521,8 @@ def run_ours(args, torch, dist):
     clocks = sampler.stop()
     ms_total = job_time_ms(e0.elapsed_time(e1), dist, dev)
     ms_step = ms_total / args.steps
+    marks = [e0] + ce + [e1]
+    chunk_ms = [marks[i].elapsed_time(marks[i + 1]) / (bounds[i + 1] - bounds[i]) for i in range(n_chunks)]
     n_ranks = ws
     value = job_value(step_bytes(), n_ranks, args.steps, ms_total)
 
@@ -519,7 +566,12 @@ def run_ours(args, torch, dist):
                                "alternate between the M passes",
                          "graph": "step captured in one CUDA graph", "parallelism": "replicas (dp%d)" % ws},
               "clocks": clocks, "gpu_launches": launches_per_step * args.steps,
-              "frac_of_hbm_peak": round(value / n_ranks / peak, 4), "peak_source": peak_src}
+              "frac_of_hbm_peak": round(value / n_ranks / peak, 4), "peak_source": peak_src,
+              "spread": {"chunks": n_chunks,
+                         "ms_per_step_p10": round(float(np.percentile(chunk_ms, 10)), 5),
+                         "ms_per_step_median": round(float(np.median(chunk_ms)), 5),
+                         "ms_per_step_p90": round(float(np.percentile(chunk_ms, 90)), 5),
+                         "note": "per-step time of each of the chunks the timed steps fall into (rank 0)"}}
 
     if per_call is not None:
         calls = step_calls()
@@ -565,6 +617,7 @@ def run_ours(args, torch, dist):
     result["fused_stack"] = run_fused(torch, fw, mats, xs, dev, s, min(args.steps, 500), args.warmup, peak)
 
     result["grouped_gemv"] = run_grouped(torch, fw, dev, s, peak)
+    result["warm_l2"] = run_warm_l2(torch, fw, dev, s)
 
     # quantiser throughput on the seven matrices (load-time step)
     qcodes = {name: torch.empty_like(mats[name]["codes"][0]) for name in wdev}
@@ -785,7 +838,7 @@ def main():
                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                "data": "synthetic",
                "config": {"workload": WORKLOAD, "M": list(synthetic.DECODE_STACK_M),
-                          "sample": "every %dth output channel of every call" % CPU_STRIDE},
+                          "sample": "every %s output channel of every call" % ordinal(CPU_STRIDE)},
                "cpu_baseline": cpu_baseline_obj(value, tot_s / args.steps, cores),
                "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(out))
@@ -804,6 +857,10 @@ def main():
         cores = oracle.host_cores()
         gbs, dt = run_cpu(cpu_sample(), cores)
         result["cpu_baseline"] = cpu_baseline_obj(gbs, dt, cores)
+        gbs1, dt1 = run_cpu(cpu_sample(stride=CPU_STRIDE_1T), 1)
+        result["cpu_baseline"]["single_thread"] = {
+            "value": round(gbs1, 4), "unit": "GB/s", "cores": 1, "seconds": round(dt1, 2),
+            "sample": "every %s output channel of every call, one thread" % ordinal(CPU_STRIDE_1T)}
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()

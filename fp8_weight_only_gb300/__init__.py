@@ -24,8 +24,8 @@ KERNEL_AUTO, KERNEL_GEMV, KERNEL_SKINNY = 0, 1, 2
 SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_workspace_size", "fp8w_linear_ex",
            "fp8w_status_string", "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version",
            "fp8w_linear_noalloc", "fp8w_dequantize", "fp8w_quantize_grouped", "fp8w_linear_grouped",
-           "fp8w_quantize_mx", "fp8w_linear_mx")
-ABI_VERSION = 6
+           "fp8w_quantize_mx", "fp8w_linear_mx", "fp8w_quantize_ex")
+ABI_VERSION = 7
 
 
 class Fp8wError(RuntimeError):
@@ -56,6 +56,8 @@ def lib():
         L.fp8w_quantize_grouped.argtypes = [P, c.c_int64, c.c_int64, c.c_int, P, P, P]
         L.fp8w_linear_grouped.restype = c.c_int
         L.fp8w_linear_grouped.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, c.c_int, P, c.c_int64, P, P]
+        L.fp8w_quantize_ex.restype = c.c_int
+        L.fp8w_quantize_ex.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P]
         L.fp8w_quantize_mx.restype = c.c_int
         L.fp8w_quantize_mx.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
         L.fp8w_linear_mx.restype = c.c_int
@@ -111,12 +113,15 @@ def _act(dtype):
 
 
 def quantize(w, codes=None, scales=None, group=None):
-    """W[N, K] fp32 (CUDA, contiguous) -> (codes uint8 [N, K], scales fp32 [N]),
-    or with group (32, 64 or 128) scales fp32 [N, K / group], one per run of
-    `group` weights of a row."""
+    """W[N, K] (CUDA, contiguous; fp32, or bf16/fp16 widened exactly) ->
+    (codes uint8 [N, K], scales fp32 [N]), or with group (32, 64 or 128; fp32
+    weights) scales fp32 [N, K / group], one per run of `group` weights of a row."""
     import torch
-    if w.dtype != torch.float32 or not w.is_cuda or w.dim() != 2 or not w.is_contiguous():
-        raise TypeError("w must be a contiguous 2-D float32 CUDA tensor")
+    wdt = {torch.float32: FP8W_F32, torch.bfloat16: FP8W_BF16, torch.float16: FP8W_F16}.get(w.dtype)
+    if wdt is None or not w.is_cuda or w.dim() != 2 or not w.is_contiguous():
+        raise TypeError("w must be a contiguous 2-D float32, bfloat16 or float16 CUDA tensor")
+    if wdt != FP8W_F32 and group is not None:
+        raise TypeError("per-group quantisation takes float32 weights")
     n, k = w.shape
     if codes is None:
         codes = torch.empty((n, k), dtype=torch.uint8, device=w.device)
@@ -124,7 +129,7 @@ def quantize(w, codes=None, scales=None, group=None):
         shape = (n,) if group is None else (n, k // group)
         scales = torch.empty(shape, dtype=torch.float32, device=w.device)
     if group is None:
-        _check(lib().fp8w_quantize(_ptr(w), n, k, _ptr(codes), _ptr(scales), _stream(w)))
+        _check(lib().fp8w_quantize_ex(_ptr(w), wdt, n, k, _ptr(codes), _ptr(scales), _stream(w)))
     else:
         _check(lib().fp8w_quantize_grouped(_ptr(w), n, k, int(group), _ptr(codes), _ptr(scales), _stream(w)))
     return codes, scales

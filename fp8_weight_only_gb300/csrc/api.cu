@@ -48,6 +48,18 @@ fp8w_status fp8w_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes, 
                        "fp8w_quantize launch");
 }
 
+fp8w_status fp8w_quantize_ex(const void* w, int w_dtype, int64_t n, int64_t k, uint8_t* codes, float* scales,
+                             void* stream) {
+    if (w_dtype == FP8W_F32) return fp8w_quantize(static_cast<const float*>(w), n, k, codes, scales, stream);
+    if (!w || !codes || !scales) return FP8W_ERR_NULL;
+    if (w_dtype != FP8W_BF16 && w_dtype != FP8W_F16) return FP8W_ERR_DTYPE;
+    if (n < 1 || n > FP8W_MAX_DIM || !valid_k(k)) return FP8W_ERR_SHAPE;
+    if (!aligned(w, 16) || !aligned(codes, 16) || !aligned(scales, 4)) return FP8W_ERR_ALIGN;
+    return cuda_status(fp8w::launch_quantize_16(static_cast<const uint16_t*>(w), w_dtype == FP8W_BF16, n, k, codes,
+                                                scales, static_cast<cudaStream_t>(stream)),
+                       "fp8w_quantize_ex launch");
+}
+
 static size_t skinny_ws(void);
 
 static bool valid_group(int group) { return group == 32 || group == 64 || group == 128; }

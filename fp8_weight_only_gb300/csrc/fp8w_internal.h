@@ -23,6 +23,10 @@ struct LinearArgs {
 cudaError_t launch_quantize(const float* w, int64_t n, int64_t k, uint8_t* codes, float* scales,
                             cudaStream_t st);
 
+// K1 for 16-bit weights (bf16 or fp16), widened exactly to fp32.
+cudaError_t launch_quantize_16(const uint16_t* w, bool bf16, int64_t n, int64_t k, uint8_t* codes, float* scales,
+                               cudaStream_t st);
+
 // Per-group scales: scales[n, k / group], group 32, 64 or 128, k % group == 0.
 cudaError_t launch_quantize_grouped(const float* w, int64_t n, int64_t k, int group, uint8_t* codes, float* scales,
                                     cudaStream_t st);

@@ -91,6 +91,58 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_rows_two_pass(const fl
     if (threadIdx.x == 0) scales[row] = s;
 }
 
+// 16-bit weights (bf16 or fp16) widened exactly to fp32, then the same rule.
+// One CTA per row; the second pass re-reads the row from L2.
+template <bool kBf16W>
+__device__ __forceinline__ void widen8(const uint4 v, float (&f)[8]) {
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        if constexpr (kBf16W) {
+            f[2 * e] = bf16_lo_to_f32(u[e]);
+            f[2 * e + 1] = bf16_hi_to_f32(u[e]);
+        } else {
+            f[2 * e] = f16_lo_to_f32(u[e]);
+            f[2 * e + 1] = f16_hi_to_f32(u[e]);
+        }
+    }
+}
+
+template <bool kBf16W>
+__global__ void __launch_bounds__(kQuantThreads) quantize_rows_16(const uint16_t* __restrict__ w, int64_t k,
+                                                                   uint8_t* __restrict__ codes,
+                                                                   float* __restrict__ scales) {
+    __shared__ float red[kQuantThreads / 32];
+    const int64_t row = blockIdx.x;
+    const uint4* src = reinterpret_cast<const uint4*>(w + row * k);
+    const int64_t n8 = k >> 3;
+    float amax = 0.0f;
+    for (int64_t c = threadIdx.x; c < n8; c += kQuantThreads) {
+        float f[8];
+        widen8<kBf16W>(src[c], f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(f[e]));
+    }
+    const float s = scale_from_amax(block_max_nonneg(amax, red));
+    uint2* dst = reinterpret_cast<uint2*>(codes + row * k);
+    for (int64_t c = threadIdx.x; c < n8; c += kQuantThreads) {
+        float f[8];
+        widen8<kBf16W>(src[c], f);
+        dst[c] = make_uint2(encode4(make_float4(f[0], f[1], f[2], f[3]), s),
+                            encode4(make_float4(f[4], f[5], f[6], f[7]), s));
+    }
+    if (threadIdx.x == 0) scales[row] = s;
+}
+
+cudaError_t launch_quantize_16(const uint16_t* w, bool bf16, int64_t n, int64_t k, uint8_t* codes, float* scales,
+                               cudaStream_t st) {
+    if (bf16)
+        quantize_rows_16<true><<<static_cast<unsigned>(n), kQuantThreads, 0, st>>>(w, k, codes, scales);
+    else
+        quantize_rows_16<false><<<static_cast<unsigned>(n), kQuantThreads, 0, st>>>(w, k, codes, scales);
+    return cudaGetLastError();
+}
+
 template <int VPT>
 static cudaError_t launch_reg(const float* w, int64_t n, int64_t k, uint8_t* codes, float* scales,
                               cudaStream_t st) {

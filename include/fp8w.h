@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define FP8W_ABI_VERSION 6
+#define FP8W_ABI_VERSION 7
 
 #if defined(__GNUC__)
 #define FP8W_API __attribute__((visibility("default")))
@@ -60,7 +60,8 @@ typedef enum fp8w_status {
                                scratch than the library's static maximum */
 } fp8w_status;
 
-/* Activation / output dtypes (FP8W_F32: fp8w_dequantize's output only). */
+/* Activation / output dtypes (FP8W_F32: fp8w_dequantize's output and
+ * fp8w_quantize_ex's weights only). */
 enum { FP8W_BF16 = 1, FP8W_F16 = 2, FP8W_F32 = 3 };
 
 /* Largest supported reduction length and row count. */
@@ -83,6 +84,17 @@ enum { FP8W_BF16 = 1, FP8W_F16 = 2, FP8W_F32 = 3 };
  */
 FP8W_API fp8w_status fp8w_quantize(const float *w, int64_t n, int64_t k,
                           uint8_t *codes, float *scales, void *stream);
+
+/*
+ * fp8w_quantize_ex -- fp8w_quantize for weights stored as fp32, bf16 or fp16
+ * (w_dtype FP8W_F32, FP8W_BF16 or FP8W_F16; any other is FP8W_ERR_DTYPE).
+ * A 16-bit weight is widened to fp32, which is exact, and then quantised by
+ * the same rule, so its codes and scales equal fp8w_quantize's on the
+ * widened matrix.  w is [n, k] of w_dtype, device, 16-byte aligned; other
+ * arguments and checks as fp8w_quantize.
+ */
+FP8W_API fp8w_status fp8w_quantize_ex(const void *w, int w_dtype, int64_t n, int64_t k,
+                             uint8_t *codes, float *scales, void *stream);
 
 /*
  * fp8w_quantize_grouped -- the quantiser with one scale per run of `group`

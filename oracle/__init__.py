@@ -117,6 +117,19 @@ def quantize(w):
     return codes, scales
 
 
+def widen_16(bits, act: int) -> np.ndarray:
+    """fp32 values of bf16 (act=1) or fp16 (act=2) bit patterns: exact, as
+    every bf16 and fp16 value is an fp32 value (page "B04 Precision &
+    Quantization", section 2, the bf16 and fp16 rows)."""
+    return act_values(bits, act).astype(np.float32)
+
+
+def quantize_16(w_bits, act: int):
+    """Weights stored as bf16 (act=1) or fp16 (act=2) bits: widened to fp32,
+    then the per-channel rule."""
+    return quantize(widen_16(w_bits, act))
+
+
 def dequantize(codes, scales) -> np.ndarray:
     """fp64 W' = scale[n] * e4m3val(codes[n,k])."""
     codes = _c(codes, np.uint8)

@@ -183,3 +183,14 @@ def test_linear_mx_rejects_bad_arguments(kw, status):
     a.update(kw)
     assert fw.lib().fp8w_linear_mx(a["x"], a["act"], a["m"], a["k"], a["codes"], a["scales"], a["bias"],
                                    a["n"], a["y"], a["ws"], a["ws_bytes"], None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, 1, 4, 64, B16, C16), 1), ((A16, 1, 4, 64, None, C16), 1), ((A16, 2, 4, 64, B16, None), 1),
+    ((A16, 0, 4, 64, B16, C16), 4), ((A16, 5, 4, 64, B16, C16), 4),
+    ((A16, 1, 0, 64, B16, C16), 2), ((A16, 2, 4, 24, B16, C16), 2), ((A16, 1, 4, 65536 + 16, B16, C16), 2),
+    ((ctypes.c_void_p(0x100008), 1, 4, 64, B16, C16), 3), ((A16, 2, 4, 64, ctypes.c_void_p(0x200004), C16), 3),
+    ((A16, 3, 4, 24, B16, C16), 2),              # FP8W_F32: fp8w_quantize's checks
+])
+def test_quantize_ex_rejects_bad_arguments(args, status):
+    assert fw.lib().fp8w_quantize_ex(*args, None) == status

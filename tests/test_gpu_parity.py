@@ -84,6 +84,26 @@ def gpu_linear(x_bits, act, codes, scales, bias, kernel=fw.KERNEL_AUTO):
 
 # --------------------------------------------------------------- quantise --
 
+@pytest.mark.parametrize("act", [oracle.ACT_BF16, oracle.ACT_F16])
+@pytest.mark.parametrize("n,k", [(1, 16), (33, 1040), (300, 4096), (7, 14336), (5, 65536)])
+def test_quantize_16_bit_weights_bit_exact(n, k, act):
+    """bf16 / fp16 weights: codes and scales equal the fp32 quantiser's on
+    the exactly widened matrix."""
+    rng = np.random.default_rng(n + k + act)
+    w = (rng.standard_normal((n, k)) * 0.02).astype(np.float32)
+    w[:, ::113] *= 300.0
+    if n > 2:
+        w[1] = 0.0                                        # zero row: scale 1.0
+        w[2] *= 1e-4                                      # fp16 subnormals
+    bits = synthetic.to_f16_bits(w) if act == oracle.ACT_F16 else synthetic.to_bf16_bits(w)
+    wd = torch.from_numpy(bits.view(np.int16)).to(DEV).view(_dt(act))
+    codes, scales = fw.quantize(wd)
+    torch.cuda.synchronize()
+    rc, rs = oracle.quantize_16(bits, act)
+    assert np.array_equal(codes.cpu().numpy(), rc)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), rs.view(np.uint32))
+
+
 @pytest.mark.parametrize("shape,seed,kind", [
     ((1, 16), 1, "normal"), ((3, 48), 2, "normal"), ((129, 1040), 3, "t"),
     ((1024, 1024), 4, "normal"), ((300, 4096), 5, "t"), ((77, 14336), 6, "normal"),
@@ -397,6 +417,37 @@ def test_m1_tensor_core_path_matches_gemv_tolerance():
     yt = gpu_linear(case["x"], 1, codes, scales, case["bias"], kernel=fw.KERNEL_SKINNY)
     c = compare(yt, yg, 1)
     assert c["rel_l2"] <= 2e-3 and c["min_cosine"] >= 0.9999, c
+
+
+@pytest.mark.parametrize("m,matrix", [(1, "gate"), (32, "gate"), (8, "down"), (1, "down"), (32, "k")])
+def test_full_size_outputs_within_the_quantisation_bound(m, matrix):
+    """At the bench's sizes and launch configuration, with GPU-quantised
+    weights, every sampled output lies within the e4m3 bound of the
+    UNQUANTISED product x . W^T + b: half an e4m3 step a weight (2^-4 of |w|,
+    or 2^-10 * scale below the normal range), widened by the fp32
+    accumulation (k * 2^-22 of sum |x w|, generous for any summation order)
+    and the one rounding to bf16 (2^-8 of |y|).  That worst case is loose at
+    large k, so the aggregate is also held to the statistical level of
+    independent, centred e4m3 rounding errors: rel_l2 about 0.0255 (a
+    doubled scale gives 1.0, a permuted channel 1.4).  A check against the
+    mathematics rather than the oracle."""
+    case = synthetic.case("decode_stack", m, matrix)
+    codes, scales = gpu_quantize(case["w"])
+    y = gpu_linear(case["x"], case["act"], codes, scales, case["bias"])
+    n, k = case["n"], case["k"]
+    cols = np.random.default_rng(m + n).choice(n, size=256, replace=False)
+    x = oracle.act_values(case["x"], case["act"])
+    w = case["w"][cols].astype(np.float64)
+    y_true = x @ w.T + case["bias"][cols].astype(np.float64)
+    yv = oracle.act_values(y[:, cols], case["act"])
+    ax, aw = np.abs(x), np.abs(w)
+    quant = ax @ (2.0 ** -4 * aw * (1 + 2.0 ** -20)).T + ax.sum(1)[:, None] * 2.0 ** -10 * scales[cols].astype(np.float64)
+    accum = k * 2.0 ** -22 * (ax @ (aw * (1 + 2.0 ** -4)).T)
+    bound = (quant + accum) * (1 + 2.0 ** -8) + 2.0 ** -8 * np.abs(y_true) + 1e-30
+    err = np.abs(yv - y_true)
+    assert np.all(err <= bound), float(np.max(err / bound))
+    rel = np.linalg.norm(yv - y_true) / np.linalg.norm(y_true)
+    assert 0.015 <= rel <= 0.04, rel
 
 
 # ------------------------------------------------------ fused decode stack --

@@ -149,3 +149,18 @@ def test_activation_decoders():
     mine = oracle.act_values(b, oracle.ACT_BF16)
     fin = np.isfinite(bf)
     assert np.array_equal(mine[fin], bf[fin])
+
+
+def test_widening_16_bit_weights_is_exact_for_every_pattern():
+    """Every fp16 and bf16 pattern widens to the fp32 value numpy's float16
+    conversion and the bf16 closed form (the pattern as the top half of an
+    fp32) give; NaNs stay NaN."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f16 = oracle.widen_16(bits, oracle.ACT_F16)
+    ref16 = bits.view(np.float16).astype(np.float32)
+    nan = np.isnan(ref16)
+    assert np.array_equal(np.isnan(f16), nan) and np.array_equal(f16[~nan].view(np.uint32), ref16[~nan].view(np.uint32))
+    b16 = oracle.widen_16(bits, oracle.ACT_BF16)
+    refb = (bits.astype(np.uint32) << 16).view(np.float32)
+    nan = np.isnan(refb)
+    assert np.array_equal(np.isnan(b16), nan) and np.array_equal(b16[~nan].view(np.uint32), refb[~nan].view(np.uint32))
