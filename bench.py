@@ -567,6 +567,7 @@ def run_ours(args, torch, dist):
                          "graph": "step captured in one CUDA graph", "parallelism": "replicas (dp%d)" % ws},
               "clocks": clocks, "gpu_launches": launches_per_step * args.steps,
               "frac_of_hbm_peak": round(value / n_ranks / peak, 4), "peak_source": peak_src,
+              "tflops": round(step_flops() * n_ranks / (ms_step / 1e3) / 1e12, 2),
               "spread": {"chunks": n_chunks,
                          "ms_per_step_p10": round(float(np.percentile(chunk_ms, 10)), 5),
                          "ms_per_step_median": round(float(np.median(chunk_ms)), 5),

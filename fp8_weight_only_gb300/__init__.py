@@ -13,6 +13,8 @@ raised.
 import ctypes
 import os
 
+from .fp8w_file import Fp8wFileError, load as load_fp8w, save as save_fp8w  # noqa: F401  (the .fp8w file)
+
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libfp8w.so")
 
