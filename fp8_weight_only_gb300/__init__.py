@@ -26,8 +26,9 @@ KERNEL_AUTO, KERNEL_GEMV, KERNEL_SKINNY = 0, 1, 2
 SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_workspace_size", "fp8w_linear_ex",
            "fp8w_status_string", "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version",
            "fp8w_linear_noalloc", "fp8w_dequantize", "fp8w_quantize_grouped", "fp8w_linear_grouped",
-           "fp8w_quantize_mx", "fp8w_linear_mx", "fp8w_quantize_ex")
-ABI_VERSION = 7
+           "fp8w_quantize_mx", "fp8w_linear_mx", "fp8w_quantize_ex", "fp8w_dequantize_grouped",
+           "fp8w_dequantize_mx")
+ABI_VERSION = 8
 
 
 class Fp8wError(RuntimeError):
@@ -64,6 +65,10 @@ def lib():
         L.fp8w_quantize_mx.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
         L.fp8w_linear_mx.restype = c.c_int
         L.fp8w_linear_mx.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P, c.c_size_t, P]
+        L.fp8w_dequantize_grouped.restype = c.c_int
+        L.fp8w_dequantize_grouped.argtypes = [P, P, c.c_int, c.c_int64, c.c_int64, c.c_int, P, P]
+        L.fp8w_dequantize_mx.restype = c.c_int
+        L.fp8w_dequantize_mx.argtypes = [P, P, c.c_int64, c.c_int64, c.c_int, P, P]
         L.fp8w_dequantize.restype = c.c_int
         L.fp8w_dequantize.argtypes = [P, P, c.c_int64, c.c_int64, c.c_int, P, P]
         L.fp8w_linear.restype = c.c_int
@@ -155,14 +160,16 @@ def quantize_mx(w, codes=None, scales=None):
 
 def dequantize(codes, scales, dtype=None, out=None):
     """W'[N, K] = e4m3(codes) * scales[:, None], rounded once to `dtype`
-    (torch.float32, bfloat16 or float16; default bfloat16)."""
+    (torch.float32, bfloat16 or float16; default bfloat16).  scales may also
+    be per-group fp32 [N, K / group] or E8M0 uint8 [N, K / 32]."""
     import torch
     if dtype is None:
         dtype = out.dtype if out is not None else torch.bfloat16
     kind = {torch.float32: FP8W_F32, torch.bfloat16: FP8W_BF16, torch.float16: FP8W_F16}.get(dtype)
     if kind is None:
         raise TypeError("dequantize: dtype must be float32, bfloat16 or float16, got %s" % dtype)
-    for name, t, dt in (("codes", codes, torch.uint8), ("scales", scales, torch.float32)):
+    mx = scales.dim() == 2 and scales.dtype == torch.uint8
+    for name, t, dt in (("codes", codes, torch.uint8), ("scales", scales, torch.uint8 if mx else torch.float32)):
         if t.dtype != dt or not t.is_cuda or not t.is_contiguous():
             raise TypeError("%s must be a contiguous %s CUDA tensor" % (name, dt))
     n, k = codes.shape
@@ -170,6 +177,15 @@ def dequantize(codes, scales, dtype=None, out=None):
         out = torch.empty((n, k), dtype=dtype, device=codes.device)
     elif out.shape != (n, k) or out.dtype != dtype or not out.is_contiguous():
         raise ValueError("out must be a contiguous [N, K] tensor of the requested dtype")
+    if scales.dim() == 2:
+        if scales.shape[0] != n or scales.shape[1] == 0 or k % scales.shape[1] or (mx and scales.shape[1] * 32 != k):
+            raise ValueError("shape mismatch for per-group scales")
+        if mx:
+            _check(lib().fp8w_dequantize_mx(_ptr(codes), _ptr(scales), n, k, kind, _ptr(out), _stream(codes)))
+        else:
+            _check(lib().fp8w_dequantize_grouped(_ptr(codes), _ptr(scales), k // scales.shape[1], n, k, kind,
+                                                 _ptr(out), _stream(codes)))
+        return out
     _check(lib().fp8w_dequantize(_ptr(codes), _ptr(scales), n, k, kind, _ptr(out), _stream(codes)))
     return out
 

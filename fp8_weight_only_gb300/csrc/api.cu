@@ -126,6 +126,28 @@ fp8w_status fp8w_dequantize(const uint8_t* codes, const float* scales, int64_t n
                        "fp8w_dequantize launch");
 }
 
+static fp8w_status dequant_grouped(const uint8_t* codes, const void* scales, bool e8m0, int group, int64_t n,
+                                   int64_t k, int out_dtype, void* w, void* stream, const char* what) {
+    if (!codes || !scales || !w) return FP8W_ERR_NULL;
+    if (n < 1 || n > FP8W_MAX_DIM || !valid_k(k) || !valid_group(group) || k % group != 0) return FP8W_ERR_SHAPE;
+    if (out_dtype != FP8W_F32 && out_dtype != FP8W_BF16 && out_dtype != FP8W_F16) return FP8W_ERR_DTYPE;
+    if (!aligned(codes, 16) || !aligned(scales, e8m0 ? 1 : 4) || !aligned(w, 16)) return FP8W_ERR_ALIGN;
+    const int kind = out_dtype == FP8W_BF16 ? 1 : out_dtype == FP8W_F16 ? 2 : 0;
+    return cuda_status(fp8w::launch_dequantize_grouped(codes, scales, e8m0, group, n, k, kind, w,
+                                                       static_cast<cudaStream_t>(stream)),
+                       what);
+}
+
+fp8w_status fp8w_dequantize_grouped(const uint8_t* codes, const float* scales, int group, int64_t n, int64_t k,
+                                    int out_dtype, void* w, void* stream) {
+    return dequant_grouped(codes, scales, false, group, n, k, out_dtype, w, stream, "fp8w_dequantize_grouped launch");
+}
+
+fp8w_status fp8w_dequantize_mx(const uint8_t* codes, const uint8_t* scales, int64_t n, int64_t k, int out_dtype,
+                               void* w, void* stream) {
+    return dequant_grouped(codes, scales, true, 32, n, k, out_dtype, w, stream, "fp8w_dequantize_mx launch");
+}
+
 static size_t skinny_ws(void) {
     int sms = 0;
     if (fp8w::device_sm_count(sms) != cudaSuccess) return 0;

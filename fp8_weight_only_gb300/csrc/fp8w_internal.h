@@ -39,6 +39,11 @@ cudaError_t launch_quantize_mx(const float* w, int64_t n, int64_t k, uint8_t* co
 cudaError_t launch_dequantize(const uint8_t* codes, const float* scales, int64_t n, int64_t k, int out_dtype,
                               void* w, cudaStream_t st);
 
+// The same with per-group scales: fp32 scales[n, k / group] (group 32, 64 or
+// 128), or E8M0 bytes[n, k / 32] (e8m0, group 32).
+cudaError_t launch_dequantize_grouped(const uint8_t* codes, const void* scales, bool e8m0, int group, int64_t n,
+                                      int64_t k, int out_dtype, void* w, cudaStream_t st);
+
 // K2: m == 1, k <= 32768 (gemv_supports).
 cudaError_t launch_gemv(const LinearArgs& a, cudaStream_t st);
 bool gemv_supports(int64_t k);

@@ -326,10 +326,17 @@ constexpr int kDequantUnroll = 4;  // chunks a thread has in flight
 // kDequantUnroll at a time with all their loads issued first; each of its
 // kDequantUnroll sequences tracks its row as it advances (one division per
 // sequence).
-template <int OUT>
+// SK: 0 one fp32 scale a row; 1 fp32 scales[n, k / g] per group (page "B04
+// Precision & Quantization", the per-group row); 2 E8M0 bytes[n, k / 32]
+// (page "11. Inference with NVFP4/MXFP8", section "MXFP8-Style FP8"), each
+// 2^(b - 127), whose product with a code is exact in fp32 (the smallest,
+// 2^-9 * 2^-127, is an fp32 subnormal), so lo is 0 there.  A chunk lies in
+// one group (g >= 32, chunks of 8 or 4 aligned).
+template <int OUT, int SK>
 __global__ void __launch_bounds__(kDequantThreads) dequantize_kernel(const uint8_t* __restrict__ codes,
-                                                                      const float* __restrict__ scales, int64_t k,
-                                                                      int64_t nchunk, void* __restrict__ out) {
+                                                                      const void* __restrict__ scales, int64_t k,
+                                                                      int64_t nchunk, int gshift,
+                                                                      void* __restrict__ out) {
     constexpr int U = kDequantUnroll;
     constexpr int C = OUT == 0 ? 4 : 8;
     const int64_t cpr = k / C;  // chunks per row
@@ -358,7 +365,17 @@ __global__ void __launch_bounds__(kDequantThreads) dequantize_kernel(const uint8
                 } else {
                     cw[u][0] = __ldcs(reinterpret_cast<const uint32_t*>(codes) + v);
                 }
-                sc[u] = scales[row[u]];
+                if constexpr (SK == 0) {
+                    sc[u] = static_cast<const float*>(scales)[row[u]];
+                } else {
+                    const int64_t gi = row[u] * (k >> gshift) + ((col[u] * C) >> gshift);
+                    if constexpr (SK == 1) {
+                        sc[u] = static_cast<const float*>(scales)[gi];
+                    } else {
+                        const uint32_t b = static_cast<const uint8_t*>(scales)[gi];
+                        sc[u] = __uint_as_float(b == 0u ? 0x00400000u : b == 255u ? 0x7FFFFFFFu : b << 23);
+                    }
+                }
             }
         }
 #pragma unroll
@@ -402,8 +419,9 @@ __global__ void __launch_bounds__(kDequantThreads) dequantize_kernel(const uint8
     }
 }
 
-cudaError_t launch_dequantize(const uint8_t* codes, const float* scales, int64_t n, int64_t k, int out_dtype,
-                              void* w, cudaStream_t st) {
+template <int SK>
+static cudaError_t launch_dq(const uint8_t* codes, const void* scales, int64_t n, int64_t k, int gshift,
+                             int out_dtype, void* w, cudaStream_t st) {
     int sms = 0;
     cudaError_t e = device_sm_count(sms);
     if (e != cudaSuccess) return e;
@@ -412,10 +430,25 @@ cudaError_t launch_dequantize(const uint8_t* codes, const float* scales, int64_t
     const int64_t cap = static_cast<int64_t>(sms) * 8;  // up to 8 CTAs of 256 threads per SM
     if (blocks > cap) blocks = cap;
     const unsigned g = static_cast<unsigned>(blocks);
-    if (out_dtype == 1) dequantize_kernel<1><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nchunk, w);
-    else if (out_dtype == 2) dequantize_kernel<2><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nchunk, w);
-    else dequantize_kernel<0><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nchunk, w);
+    if (out_dtype == 1)
+        dequantize_kernel<1, SK><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nchunk, gshift, w);
+    else if (out_dtype == 2)
+        dequantize_kernel<2, SK><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nchunk, gshift, w);
+    else
+        dequantize_kernel<0, SK><<<g, kDequantThreads, 0, st>>>(codes, scales, k, nchunk, gshift, w);
     return cudaGetLastError();
+}
+
+cudaError_t launch_dequantize(const uint8_t* codes, const float* scales, int64_t n, int64_t k, int out_dtype,
+                              void* w, cudaStream_t st) {
+    return launch_dq<0>(codes, scales, n, k, 0, out_dtype, w, st);
+}
+
+cudaError_t launch_dequantize_grouped(const uint8_t* codes, const void* scales, bool e8m0, int group, int64_t n,
+                                      int64_t k, int out_dtype, void* w, cudaStream_t st) {
+    const int gshift = group == 32 ? 5 : group == 64 ? 6 : 7;
+    return e8m0 ? launch_dq<2>(codes, scales, n, k, 5, out_dtype, w, st)
+                : launch_dq<1>(codes, scales, n, k, gshift, out_dtype, w, st);
 }
 
 }  // namespace fp8w

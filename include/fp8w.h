@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define FP8W_ABI_VERSION 7
+#define FP8W_ABI_VERSION 8
 
 #if defined(__GNUC__)
 #define FP8W_API __attribute__((visibility("default")))
@@ -190,6 +190,22 @@ FP8W_API fp8w_status fp8w_linear_mx(const void *x, int act_dtype, int64_t m, int
  */
 FP8W_API fp8w_status fp8w_dequantize(const uint8_t *codes, const float *scales, int64_t n,
                             int64_t k, int out_dtype, void *w, void *stream);
+
+/*
+ * fp8w_dequantize_grouped / fp8w_dequantize_mx -- fp8w_dequantize for codes
+ * with per-group fp32 scales [n, k / group] (group 32, 64 or 128, k % group
+ * == 0; 4-byte aligned) or E8M0 scale bytes [n, k / 32] (each 2^(b - 127),
+ * 0xFF NaN; any alignment).  w[r, c] is the exact product of the decoded
+ * code and its group's scale, rounded once to out_dtype.  An E8M0 product is
+ * exact in fp32 (the smallest is 2^-136), so every output type gets the one
+ * rounding of the exact value; fp32 group scales have fp8w_dequantize's bf16
+ * limit below 2^-126.  Other arguments, checks and errors as
+ * fp8w_dequantize.
+ */
+FP8W_API fp8w_status fp8w_dequantize_grouped(const uint8_t *codes, const float *scales, int group,
+                                    int64_t n, int64_t k, int out_dtype, void *w, void *stream);
+FP8W_API fp8w_status fp8w_dequantize_mx(const uint8_t *codes, const uint8_t *scales, int64_t n,
+                               int64_t k, int out_dtype, void *w, void *stream);
 
 /*
  * fp8w_linear -- steps "stream codes", "decode", "contract", "epilogue" and

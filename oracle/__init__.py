@@ -63,6 +63,10 @@ def _load():
         lib.oracle_linear_mx.restype = c.c_int
         lib.oracle_linear_mx.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P,
                                          c.c_int64, P, P, c.c_int]
+        lib.oracle_dequantize_grouped.restype = None
+        lib.oracle_dequantize_grouped.argtypes = [P, P, c.c_int64, c.c_int64, c.c_int64, P]
+        lib.oracle_dequantize_mx.restype = None
+        lib.oracle_dequantize_mx.argtypes = [P, P, c.c_int64, c.c_int64, P]
         lib.oracle_fp8_error.restype = None
         lib.oracle_fp8_error.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
         lib.oracle_e4m3_encode_many.restype = None
@@ -265,6 +269,30 @@ def linear_mx(x_bits, act: int, codes, scales, bias=None, threads: int = 1, want
     if rc != 0:
         raise RuntimeError("oracle.linear_mx: allocation or thread start failed")
     return (y, acc) if want_acc else y
+
+
+def dequantize_grouped(codes, scales, group: int) -> np.ndarray:
+    """fp64 W'[n, k] = scales[n, k // group] * e4m3val(codes[n, k])."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.float32)
+    n, k = codes.shape
+    if k % group or scales.shape != (n, k // group):
+        raise ValueError("oracle.dequantize_grouped: shape mismatch")
+    out = np.empty((n, k), dtype=np.float64)
+    _load().oracle_dequantize_grouped(_ptr(codes), _ptr(scales), n, k, group, _ptr(out))
+    return out
+
+
+def dequantize_mx(codes, scales) -> np.ndarray:
+    """fp64 W'[n, k] = e8m0val(scales[n, k // 32]) * e4m3val(codes[n, k])."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    n, k = codes.shape
+    if k % MX_BLOCK or scales.shape != (n, k // MX_BLOCK):
+        raise ValueError("oracle.dequantize_mx: shape mismatch")
+    out = np.empty((n, k), dtype=np.float64)
+    _load().oracle_dequantize_mx(_ptr(codes), _ptr(scales), n, k, _ptr(out))
+    return out
 
 
 def fp8_error(w, codes, scales) -> dict:

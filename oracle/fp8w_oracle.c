@@ -239,6 +239,28 @@ void oracle_dequantize(const uint8_t *codes, const float *scales, int64_t n,
             wq[r * k + i] = (double)scales[r] * oracle_e4m3_decode(codes[r * k + i]);
 }
 
+/* The same with per-group scales[n, k/g] (one per run of g codes of a row)
+ * and with E8M0 scale bytes[n, k/32] (each worth 2^(b-127), 0xFF NaN):
+ * scale times decoded code, exact in fp64.                                 */
+void oracle_dequantize_grouped(const uint8_t *codes, const float *scales,
+                               int64_t n, int64_t k, int64_t g, double *wq)
+{
+    int64_t r, i, ng = k / g;
+    for (r = 0; r < n; ++r)
+        for (i = 0; i < k; ++i)
+            wq[r * k + i] = (double)scales[r * ng + i / g] * oracle_e4m3_decode(codes[r * k + i]);
+}
+
+void oracle_dequantize_mx(const uint8_t *codes, const uint8_t *scales, int64_t n,
+                          int64_t k, double *wq)
+{
+    int64_t r, i, ng = k / ORACLE_MX_BLOCK;
+    for (r = 0; r < n; ++r)
+        for (i = 0; i < k; ++i)
+            wq[r * k + i] = oracle_e8m0_decode(scales[r * ng + i / ORACLE_MX_BLOCK]) *
+                            oracle_e4m3_decode(codes[r * k + i]);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Activation formats: bf16 (8 exponent, 7 mantissa bits, the top half of an
  * fp32) and fp16 (5 exponent bits, bias 15, 10 mantissa bits).  Page "B04",

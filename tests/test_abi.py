@@ -194,3 +194,24 @@ def test_linear_mx_rejects_bad_arguments(kw, status):
 ])
 def test_quantize_ex_rejects_bad_arguments(args, status):
     assert fw.lib().fp8w_quantize_ex(*args, None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, C16, 32, 4, 64, 1, D16), 1), ((B16, None, 32, 4, 64, 1, D16), 1), ((B16, C16, 32, 4, 64, 1, None), 1),
+    ((B16, C16, 48, 4, 96, 1, D16), 2), ((B16, C16, 128, 4, 192, 1, D16), 2), ((B16, C16, 32, 0, 64, 1, D16), 2),
+    ((B16, C16, 32, 4, 64, 7, D16), 4),
+    ((ctypes.c_void_p(0x200004), C16, 32, 4, 64, 1, D16), 3), ((B16, ctypes.c_void_p(0x300002), 32, 4, 64, 1, D16), 3),
+    ((B16, C16, 32, 4, 64, 3, ctypes.c_void_p(0x400008)), 3),
+])
+def test_dequantize_grouped_rejects_bad_arguments(args, status):
+    assert fw.lib().fp8w_dequantize_grouped(*args, None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((None, C16, 4, 64, 1, D16), 1), ((B16, None, 4, 64, 1, D16), 1),
+    ((B16, C16, 4, 48, 1, D16), 2), ((B16, C16, 4, 64, 0, D16), 4),
+    ((ctypes.c_void_p(0x200004), C16, 4, 64, 1, D16), 3),
+    ((B16, ctypes.c_void_p(0x300001), 4, 48, 1, D16), 2),   # scale bytes: any alignment, the shape still checked
+])
+def test_dequantize_mx_rejects_bad_arguments(args, status):
+    assert fw.lib().fp8w_dequantize_mx(*args, None) == status

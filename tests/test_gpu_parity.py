@@ -588,6 +588,43 @@ def test_dequantize_nan_codes_give_nan(dtype):
     assert (vals[:, 2::4] == 0).all() and (vals[:, 3::4] == 0).all()
 
 
+@pytest.mark.parametrize("dtype", DQ_TYPES)
+@pytest.mark.parametrize("form", ["g32", "g64", "g128", "mx"])
+@pytest.mark.parametrize("n,k", [(3, 128), (77, 1024), (300, 4096)])
+def test_dequantize_grouped_and_mx_bit_exact(n, k, form, dtype):
+    rng = np.random.default_rng(n + k + len(form))
+    codes = rng.integers(0, 256, size=(n, k), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x3A
+    if form == "mx":
+        lo, hi = (100, 140) if dtype == torch.float16 else (1, 250)
+        scales = rng.integers(lo, hi, size=(n, k // 32), dtype=np.uint8)
+        if dtype != torch.float16:
+            scales[0, :2] = [0, 254]                      # 2^-127 and 2^127 (products overflow to inf)
+        want_w = oracle.dequantize_mx(codes, scales)
+    else:
+        g = int(form[1:])
+        hi_exp = 6 if dtype == torch.float16 else 60
+        scales = (2.0 ** rng.uniform(-30, hi_exp, size=(n, k // g)) * rng.uniform(1, 2, size=(n, k // g))).astype(np.float32)
+        want_w = oracle.dequantize_grouped(codes, scales, g)
+    got = _gpu_dequant_bits(codes, scales, dtype)
+    if dtype == torch.float32:
+        with np.errstate(over="ignore"):                   # products beyond fp32 round to inf, as intended
+            want = want_w.astype(np.float32).view(np.uint32)
+    else:
+        want = (oracle.round_bf16(want_w) if dtype == torch.bfloat16 else oracle.round_f16(want_w)).reshape(want_w.shape)
+    bad = np.argwhere(got != want)
+    assert bad.size == 0, (bad[:5], got[tuple(bad[0])], want[tuple(bad[0])])
+
+
+def test_dequantize_mx_of_quantize_mx_is_the_oracle_weight():
+    case = synthetic.case("decode_stack", 1, "k")
+    w = torch.from_numpy(case["w"]).to(DEV)
+    codes, e8 = fw.quantize_mx(w)
+    c, s = codes.cpu().numpy(), e8.cpu().numpy()
+    got = _gpu_dequant_bits(c, s, torch.float32)
+    assert np.array_equal(got, oracle.dequantize_mx(c, s).astype(np.float32).view(np.uint32))
+
+
 def test_dequantize_of_quantize_is_the_oracle_fallback_weight():
     case = synthetic.case("decode_stack", 1, "k")
     codes, scales = gpu_quantize(case["w"])
