@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(HERE, "libfp8w.so")
 FP8W_BF16 = 1
 FP8W_F16 = 2
 FP8W_F32 = 3
-KERNEL_AUTO, KERNEL_GEMV, KERNEL_SKINNY = 0, 1, 2
+KERNEL_AUTO, KERNEL_GEMV, KERNEL_SKINNY, KERNEL_PREFILL = 0, 1, 2, 3
 
 SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_workspace_size", "fp8w_linear_ex",
            "fp8w_status_string", "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version",

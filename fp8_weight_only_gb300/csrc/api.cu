@@ -154,8 +154,10 @@ static size_t skinny_ws(void) {
     return fp8w::skinny_workspace_size(sms);
 }
 
-// m == 1 runs the GEMV unless its x does not fit in shared memory.
+// m == 1 runs the GEMV unless its x does not fit in shared memory; m > 64
+// the prefill GEMM.
 static bool use_gemv(int64_t m, int64_t k) { return m == 1 && fp8w::gemv_supports(k); }
+static bool use_prefill(int64_t m) { return m > 64; }
 
 size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k) {
     (void)n;
@@ -168,14 +170,17 @@ fp8w_status fp8w_linear_ex(const void* x, int act_dtype, int64_t m, int64_t k, c
     fp8w_status st = check_linear(x, act_dtype, m, k, codes, scales, bias, n, y);
     if (st != FP8W_OK) return st;
     int kernel = config ? config->kernel : FP8W_KERNEL_AUTO;
-    if (kernel == FP8W_KERNEL_AUTO) kernel = use_gemv(m, k) ? FP8W_KERNEL_GEMV : FP8W_KERNEL_SKINNY;
+    if (kernel == FP8W_KERNEL_AUTO)
+        kernel = use_gemv(m, k) ? FP8W_KERNEL_GEMV : use_prefill(m) ? FP8W_KERNEL_PREFILL : FP8W_KERNEL_SKINNY;
     if (kernel == FP8W_KERNEL_GEMV && !use_gemv(m, k)) return FP8W_ERR_CONFIG;
-    if (kernel != FP8W_KERNEL_GEMV && kernel != FP8W_KERNEL_SKINNY) return FP8W_ERR_CONFIG;
+    if (kernel != FP8W_KERNEL_GEMV && kernel != FP8W_KERNEL_SKINNY && kernel != FP8W_KERNEL_PREFILL)
+        return FP8W_ERR_CONFIG;
     const int ctas = config ? config->ctas : 0;
-    if (ctas < 0 || (ctas != 0 && kernel == FP8W_KERNEL_GEMV)) return FP8W_ERR_CONFIG;
+    if (ctas < 0 || (ctas != 0 && kernel != FP8W_KERNEL_SKINNY)) return FP8W_ERR_CONFIG;
     fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, scales, bias, y};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (kernel == FP8W_KERNEL_GEMV) return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear gemv launch");
+    if (kernel == FP8W_KERNEL_PREFILL) return cuda_status(fp8w::launch_prefill(a, s), "fp8w_linear prefill launch");
     if (!workspace || !aligned(workspace, 256)) return FP8W_ERR_WORKSPACE;
     const size_t need = skinny_ws();
     if (need == 0) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear device query");
@@ -202,6 +207,7 @@ fp8w_status fp8w_linear_noalloc(const void* x, int act_dtype, int64_t m, int64_t
     fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, scales, bias, y};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (use_gemv(m, k)) return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear_noalloc gemv launch");
+    if (use_prefill(m)) return cuda_status(fp8w::launch_prefill(a, s), "fp8w_linear_noalloc prefill launch");
     const size_t need = skinny_ws();
     if (need == 0) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear_noalloc device query");
     if (need > fp8w::static_scratch_bytes()) return FP8W_ERR_SCRATCH;
@@ -234,7 +240,8 @@ int fp8w_device_error(void) {
     if (cudaDeviceSynchronize() != cudaSuccess) return -1;
     const int a = fp8w::read_skinny_device_error();
     const int b = fp8w::read_gemv_device_error();
-    return a ? a : b;
+    const int c = fp8w::read_prefill_device_error();
+    return a ? a : b ? b : c;
 }
 
 int fp8w_abi_version(void) { return FP8W_ABI_VERSION; }

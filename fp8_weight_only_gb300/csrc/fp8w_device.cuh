@@ -325,6 +325,31 @@ __device__ __forceinline__ void mma_f16_ts_warp(uint32_t d_tmem, uint32_t a_tmem
         : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem], both operands by descriptor (M = 128, N
+// and types from the instruction descriptor, K = 16), issued by one elected
+// lane of a converged warp.
+__device__ __forceinline__ void mma_f16_ss_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                bool accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate ? 1u : 0u)
+        : "memory");
+}
+
+// Shared-memory writes of this thread become visible to the async proxy
+// (the tensor core's operand reads) once a barrier orders them after this.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // tcgen05.commit from the lane elect.sync picks, i.e. the lane that issued
 // the MMAs above (a commit tracks its own thread's operations only).
 __device__ __forceinline__ void tc_commit_warp(uint32_t bar) {

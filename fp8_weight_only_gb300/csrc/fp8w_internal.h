@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace fp8w {
@@ -59,6 +60,14 @@ size_t skinny_workspace_size(int sms);
 cudaError_t static_scratch(void** ptr, cudaStream_t st);
 size_t static_scratch_bytes();
 cudaError_t device_sm_count(int& sms);
+// 2-D tiled tensor map with 128-byte swizzle: `inner` x `outer` elements,
+// rows of `row_bytes`, boxes of box_inner x box_outer.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+
+// K4: m > 64 (prefill shapes), per-row scales; one launch, no workspace.
+cudaError_t launch_prefill(const LinearArgs& a, cudaStream_t st);
+int read_prefill_device_error();
 
 // Kernel-recorded wait failures (0 = none); reading clears them.
 int read_skinny_device_error();

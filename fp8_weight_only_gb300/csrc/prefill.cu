@@ -1,0 +1,405 @@
+// prefill.cu -- kernel K4: the linear layer for many tokens (m > 64) as one
+// tcgen05 GEMM with both operands in shared memory.
+//
+// Page "kadirnar/kernel-agent fp8-weights", section "The contract":
+// y[m, n] = round(scale[n] * sum_k x[m, k] * e4m3(q[n, k]) + bias[n]), fp32
+// accumulation, one rounding.  For prefill shapes the work is compute-bound,
+// so each weight tile is dequantised into shared memory once and multiplied
+// by a wide token tile, instead of re-streaming the weight for every 64
+// tokens as the skinny kernel (K3) would.
+//
+// A CTA (one per SM, persistent) walks output tiles of 128 weight rows x BN
+// tokens (BN = 128 or 256); the tiles of one weight block are adjacent in
+// the walk, so CTAs that run together share it through L2.  K advances in
+// blocks of 64 (one 128-byte swizzle atom of 16-bit values a row).
+//   warp 0      code tiles (128 rows x 128 codes, 16 KB, TMA, 128-byte
+//               swizzle) into their ring
+//   warp 2      x tiles (BN tokens x 64) into theirs, independently
+//   warp 1      MMA issue: per k-block four tcgen05.mma (M = 128, N = BN,
+//               K = 16), A and B by shared-memory descriptor, D in TMEM
+//               (two accumulators, so the epilogue drains one tile while
+//               the next accumulates)
+//   warps 4-7   epilogue: TMEM -> fmaf(acc, scale, bias) -> bf16/fp16 -> y
+//   warps 8-15  two dequantising warpgroups: warpgroup h converts the k-blocks
+//               with h = (index in the tile) % 2, one weight row a thread,
+//               e4m3 -> bf16/fp16 exactly (value * 2^-120 by byte moves, then
+//               * 2^120, or the hardware e4m3 -> f16 conversion), written in
+//               the 128-byte swizzled K-major layout the descriptor reads
+// Every wait is bounded; a CTA that gives up records a code, raises its abort
+// flag, lets its copies and MMAs land and frees TMEM.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "fp8w_device.cuh"
+#include "fp8w_internal.h"
+
+namespace fp8w {
+
+static __device__ int g_prefill_error;
+
+namespace {
+
+constexpr int kPM = 128;                          // weight rows a tile (MMA M, TMEM lanes)
+constexpr int kPK = 64;                           // k of an A or x stage
+constexpr int kPCodeK = 128;                      // k of a code stage (two k-blocks)
+constexpr uint32_t kPCodeBytes = kPM * kPCodeK;   // 16 KB
+constexpr uint32_t kPABytes = kPM * kPK * 2;      // 16 KB
+constexpr int kPThreads = 512;
+constexpr int kPMmaWarp = 1, kPXWarp = 2, kPFirstEpiWarp = 4, kPFirstDqWarp = 8;
+constexpr int kPBarTmem = 1;                      // named barrier: MMA warp + epilogue warps
+
+// Ring depths: the code ring is the deepest, since each CTA streams its
+// weight rows from HBM with about a microsecond of copy latency to cover;
+// x tiles come from L2.  Both fill 224 KB of shared memory.
+template <int BN>
+struct PrefillSmem {
+    static constexpr int kPCS = BN == 128 ? 6 : 4;  // code stages (16 KB)
+    static constexpr int kPAS = 4;                  // dequantised A stages (16 KB)
+    static constexpr int kPXS = BN == 128 ? 4 : 3;  // x stages (BN x 64 x 2 B)
+    static constexpr uint32_t kXBytes = BN * kPK * 2;
+    static constexpr uint32_t kCodesOff = 0;
+    static constexpr uint32_t kAOff = kCodesOff + kPCS * kPCodeBytes;
+    static constexpr uint32_t kXOff = kAOff + kPAS * kPABytes;
+    static constexpr uint32_t kBarOff = kXOff + kPXS * kXBytes;
+    // cfull, cempty [kPCS] | afull, aempty [kPAS] | xfull, xempty [kPXS] | dfull, dempty [2] | drain
+    static constexpr uint32_t kNumBars = 2 * kPCS + 2 * kPAS + 2 * kPXS + 4 + 1;
+    static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
+    static constexpr uint32_t kBytes = kMiscOff + 16;
+    static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
+    static_assert(kAlloc <= 227 * 1024, "shared memory");
+    static constexpr uint32_t kTmemCols = 2 * BN;
+    static_assert(kTmemCols <= 512, "TMEM columns");
+};
+
+__device__ __forceinline__ void prefill_error(int code, volatile int* abort_flag) {
+    *abort_flag = 1;
+    atomicCAS(&g_prefill_error, 0, 4000 + code);
+}
+
+}  // namespace
+
+template <int BN, bool kBf16>
+__global__ void __launch_bounds__(kPThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
+                   const float* __restrict__ scales, const float* __restrict__ bias, uint16_t* __restrict__ y,
+                   int64_t m, int64_t n, int64_t k) {
+    using L = PrefillSmem<BN>;
+    constexpr int kPCS = L::kPCS, kPAS = L::kPAS, kPXS = L::kPXS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = sbase + L::kBarOff;
+    auto cfull = [&](int s) { return bar0 + 8u * s; };
+    auto cempty = [&](int s) { return bar0 + 8u * (kPCS + s); };
+    auto afull = [&](int s) { return bar0 + 8u * (2 * kPCS + s); };
+    auto aempty = [&](int s) { return bar0 + 8u * (2 * kPCS + kPAS + s); };
+    auto xfull = [&](int s) { return bar0 + 8u * (2 * kPCS + 2 * kPAS + s); };
+    auto xempty = [&](int s) { return bar0 + 8u * (2 * kPCS + 2 * kPAS + kPXS + s); };
+    auto dfull = [&](int d) { return bar0 + 8u * (2 * kPCS + 2 * kPAS + 2 * kPXS + d); };
+    auto dempty = [&](int d) { return bar0 + 8u * (2 * kPCS + 2 * kPAS + 2 * kPXS + 2 + d); };
+    const uint32_t drain = bar0 + 8u * (2 * kPCS + 2 * kPAS + 2 * kPXS + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t token_tiles = (m + BN - 1) / BN;
+    const int64_t tiles = ((n + kPM - 1) / kPM) * token_tiles;
+    const int nkb = static_cast<int>((k + kPK - 1) / kPK);          // k-blocks a tile
+    const int ncs = static_cast<int>((k + kPCodeK - 1) / kPCodeK);  // code stages a tile
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int s = 0; s < kPCS; ++s) {
+                mbar_init(cfull(s), 1);
+                mbar_init(cempty(s), 8);  // the eight dequantising warps
+            }
+            for (int s = 0; s < kPAS; ++s) {
+                mbar_init(afull(s), 4);   // the four warps of one warpgroup
+                mbar_init(aempty(s), 1);  // MMA commit
+            }
+            for (int s = 0; s < kPXS; ++s) {
+                mbar_init(xfull(s), 1);
+                mbar_init(xempty(s), 1);
+            }
+            for (int d = 0; d < 2; ++d) {
+                mbar_init(dfull(d), 1);
+                mbar_init(dempty(d), 4);  // the four epilogue warps
+            }
+            mbar_init(drain, 1);
+            *abort_flag = 0;
+            tma_prefetch_desc(&map_codes);
+            tma_prefetch_desc(&map_x);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+
+    uint32_t tmem = 0;
+    if (warp == kPMmaWarp || (warp >= kPFirstEpiWarp && warp < kPFirstDqWarp)) {
+        if (warp == kPMmaWarp) {
+            tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        asm volatile("bar.sync %0, %1;" ::"n"(kPBarTmem), "n"(32 * 5) : "memory");
+        tc_fence_after();
+        tmem = *tmem_slot;
+    }
+
+    if (warp == 0) {
+        // --------------------------------------------------- code producer --
+        if (lane == 0) {
+            const uint64_t pol_codes = policy_evict_first();
+            pdl_wait();
+            int64_t cs_n = 0;  // code stages issued
+            for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+                const int64_t cb = t / token_tiles;
+                bool ok = true;
+                for (int cs = 0; cs < ncs; ++cs) {
+                    const int s = static_cast<int>(cs_n % kPCS);
+                    if (!mbar_wait(cempty(s), static_cast<uint32_t>((cs_n / kPCS) & 1) ^ 1u, abort_flag)) {
+                        prefill_error(kErrWaitSlot, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(cfull(s), kPCodeBytes);
+                    tma_load_2d(sbase + L::kCodesOff + s * kPCodeBytes, &map_codes, cs * kPCodeK,
+                                static_cast<int32_t>(cb * kPM), cfull(s), pol_codes);
+                    ++cs_n;
+                }
+                if (!ok) break;
+            }
+            if (*abort_flag) {
+                // let the copies still in flight land before the CTA exits
+                for (int64_t i = (cs_n > kPCS ? cs_n - kPCS : 0); i < cs_n; ++i)
+                    if (!mbar_wait_drain(cfull(static_cast<int>(i % kPCS)), static_cast<uint32_t>((i / kPCS) & 1)))
+                        atomicCAS(&g_prefill_error, 0, 4000 + kErrWaitDrain);
+            }
+        }
+    } else if (warp == kPXWarp) {
+        // ------------------------------------------------------ x producer --
+        if (lane == 0) {
+            const uint64_t pol_x = policy_evict_last();
+            pdl_wait();  // x may come from the previous kernel
+            int64_t kb_n = 0;  // k-blocks issued
+            for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+                const int64_t cb = t / token_tiles, tb = t - cb * token_tiles;
+                bool ok = true;
+                for (int j = 0; j < nkb; ++j) {
+                    const int xs = static_cast<int>(kb_n % kPXS);
+                    if (!mbar_wait(xempty(xs), static_cast<uint32_t>((kb_n / kPXS) & 1) ^ 1u, abort_flag)) {
+                        prefill_error(kErrWaitSlot, abort_flag);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(xfull(xs), L::kXBytes);
+                    tma_load_2d(sbase + L::kXOff + xs * L::kXBytes, &map_x, j * kPK, static_cast<int32_t>(tb * BN),
+                                xfull(xs), pol_x);
+                    ++kb_n;
+                }
+                if (!ok) break;
+            }
+            if (*abort_flag) {
+                for (int64_t i = (kb_n > kPXS ? kb_n - kPXS : 0); i < kb_n; ++i)
+                    if (!mbar_wait_drain(xfull(static_cast<int>(i % kPXS)), static_cast<uint32_t>((i / kPXS) & 1)))
+                        atomicCAS(&g_prefill_error, 0, 4000 + kErrWaitDrain);
+            }
+        }
+    } else if (warp == kPMmaWarp) {
+        // ------------------------------------------------------ MMA issue --
+        constexpr uint32_t idesc = idesc_f16(kBf16, BN);
+        int64_t kb_n = 0;
+        int tile_n = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++tile_n) {
+            const int d = tile_n & 1;
+            if (!mbar_wait_warp(dempty(d), static_cast<uint32_t>((tile_n >> 1) & 1) ^ 1u, abort_flag)) {
+                if (lane == 0) prefill_error(kErrWaitMma, abort_flag);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + static_cast<uint32_t>(d * BN);
+            for (int j = 0; j < nkb; ++j, ++kb_n) {
+                const int as = static_cast<int>(kb_n % kPAS), xs = static_cast<int>(kb_n % kPXS);
+                if (!mbar_wait_warp(afull(as), static_cast<uint32_t>((kb_n / kPAS) & 1), abort_flag) ||
+                    !mbar_wait_warp(xfull(xs), static_cast<uint32_t>((kb_n / kPXS) & 1), abort_flag)) {
+                    if (lane == 0) prefill_error(kErrWaitDequant, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = sbase + L::kAOff + as * kPABytes;
+                const uint32_t x_addr = sbase + L::kXOff + xs * L::kXBytes;
+#pragma unroll
+                for (int kk = 0; kk < kPK / 16; ++kk)
+                    mma_f16_ss_warp(d_tmem, smem_desc_sw128_kmajor(a_addr + kk * 32),
+                                    smem_desc_sw128_kmajor(x_addr + kk * 32), idesc, j > 0 || kk > 0);
+                // both stages are free once these MMAs have read them
+                tc_commit_warp(aempty(as));
+                tc_commit_warp(xempty(xs));
+                __syncwarp();
+            }
+            if (!ok) break;
+            tc_commit_warp(dfull(d));
+            __syncwarp();
+        }
+        // every MMA issued above completes before TMEM is released
+        tc_commit_warp(drain);
+        if (!mbar_wait_drain(drain, 0) && lane == 0) atomicCAS(&g_prefill_error, 0, 4000 + kErrWaitDrain);
+        __syncwarp();
+    } else if (warp >= kPFirstEpiWarp && warp < kPFirstDqWarp) {
+        // ------------------------------------------------------- epilogue --
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;  // weight row within the tile == TMEM lane
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+        pdl_wait();  // y may still be read by the previous kernel
+        int tile_n = 0;
+        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++tile_n) {
+            const int64_t cb = t / token_tiles, tb = t - cb * token_tiles;
+            const int d = tile_n & 1;
+            if (!mbar_wait_warp(dfull(d), static_cast<uint32_t>((tile_n >> 1) & 1), abort_flag)) {
+                if (lane == 0) prefill_error(kErrWaitMma, abort_flag);
+                break;
+            }
+            tc_fence_after();
+            const int64_t col = cb * kPM + r;
+            const float sc = col < n ? scales[col] : 0.0f;
+            const float b = (bias && col < n) ? bias[col] : 0.0f;
+            const int64_t tok0 = tb * BN;
+            const int ntok = static_cast<int>(m - tok0 < BN ? m - tok0 : BN);
+            for (int c0 = 0; c0 < ntok; c0 += 16) {
+                uint32_t v[16];
+                tmem_ld_x16(lane_addr + static_cast<uint32_t>(d * BN + c0), v);
+                tmem_wait_ld();
+                if (col < n) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (c0 + i < ntok)
+                            y[(tok0 + c0 + i) * n + col] = round_out<kBf16>(fmaf(__uint_as_float(v[i]), sc, b));
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dempty(d));
+        }
+    } else if (warp >= kPFirstDqWarp) {
+        // ---------------------------------------------------- dequantising --
+        const int h = (warp - kPFirstDqWarp) >> 2;  // warpgroup: k-blocks with j % 2 == h
+        const int r = (warp & 3) * 32 + lane;       // weight row of the tile
+        const uint32_t swz = static_cast<uint32_t>(r & 7);
+        int64_t cs_n = 0, kb_base = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, kb_base += nkb) {
+            for (int cs = 0; cs < ncs; ++cs, ++cs_n) {
+                const int s = static_cast<int>(cs_n % kPCS);
+                if (!mbar_wait_warp(cfull(s), static_cast<uint32_t>((cs_n / kPCS) & 1), abort_flag)) {
+                    if (lane == 0) prefill_error(kErrWaitTma, abort_flag);
+                    ok = false;
+                    break;
+                }
+                const int j = 2 * cs + h;
+                const bool mine = j < nkb;
+                // this warpgroup's half of the row: chunks 4h .. 4h + 3 (64 codes)
+                uint4 cw[4];
+                const uint32_t row = sbase + L::kCodesOff + s * kPCodeBytes + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    cw[q] = mine ? lds128(row + (((4u * h + q) ^ swz) << 4)) : make_uint4(0u, 0u, 0u, 0u);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(cempty(s));
+                if (!mine) continue;
+                const int64_t kb = kb_base + j;
+                const int as = static_cast<int>(kb % kPAS);
+                if (!mbar_wait_warp(aempty(as), static_cast<uint32_t>((kb / kPAS) & 1) ^ 1u, abort_flag)) {
+                    if (lane == 0) prefill_error(kErrWaitMma, abort_flag);
+                    ok = false;
+                    break;
+                }
+                const uint32_t arow = sbase + L::kAOff + as * kPABytes + static_cast<uint32_t>(r) * 128u;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t v[8];
+                    const uint32_t w4[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if constexpr (kBf16) {
+                            e4m3x4_to_bf16x2(w4[e], v[2 * e], v[2 * e + 1]);
+                        } else {
+                            e4m3x4_to_f16x2(w4[e], v[2 * e], v[2 * e + 1]);
+                        }
+                    }
+                    // 16 values = logical chunks 2q and 2q + 1 of the A row
+                    sts128(arow + (((2u * q) ^ swz) << 4), v[0], v[1], v[2], v[3]);
+                    sts128(arow + (((2u * q + 1u) ^ swz) << 4), v[4], v[5], v[6], v[7]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(afull(as));
+            }
+        }
+    }
+
+    __syncthreads();
+    if (warp == kPMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+template <int BN, bool kBf16>
+static cudaError_t launch_bn(const LinearArgs& a, cudaStream_t st) {
+    using L = PrefillSmem<BN>;
+    auto kern = prefill_kernel<BN, kBf16>;
+    static std::once_flag attr_once[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once[dev & 63], [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    int sms = 0;
+    e = device_sm_count(sms);
+    if (e != cudaSuccess) return e;
+    CUtensorMap map_codes, map_x;
+    if (!encode_2d(&map_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, static_cast<uint64_t>(a.k),
+                   static_cast<uint64_t>(a.n), static_cast<uint64_t>(a.k), kPCodeK, kPM))
+        return cudaErrorInvalidValue;
+    if (!encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_UINT16, a.x, static_cast<uint64_t>(a.k),
+                   static_cast<uint64_t>(a.m), static_cast<uint64_t>(a.k) * 2, kPK, BN))
+        return cudaErrorInvalidValue;
+    const int64_t tiles = ((a.n + kPM - 1) / kPM) * ((a.m + BN - 1) / BN);
+    const int64_t grid = tiles < sms ? tiles : sms;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kPThreads);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, a.scales, a.bias, static_cast<uint16_t*>(a.y), a.m,
+                              a.n, a.k);
+}
+
+cudaError_t launch_prefill(const LinearArgs& a, cudaStream_t st) {
+    const bool bf16 = a.act == 1;
+    // 128-token tiles up to 128 tokens, 256 beyond
+    if (a.m <= 128) return bf16 ? launch_bn<128, true>(a, st) : launch_bn<128, false>(a, st);
+    return bf16 ? launch_bn<256, true>(a, st) : launch_bn<256, false>(a, st);
+}
+
+int read_prefill_device_error() {
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_prefill_error, sizeof v) != cudaSuccess) return -1;
+    if (v != 0 && cudaMemcpyToSymbol(g_prefill_error, &zero, sizeof zero) != cudaSuccess) return -1;
+    return v;
+}
+
+}  // namespace fp8w

@@ -865,7 +865,7 @@ static EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                       uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
     EncodeTiledFn fn = get_encode_fn();
     if (!fn) return false;

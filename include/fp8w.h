@@ -227,9 +227,11 @@ FP8W_API fp8w_status fp8w_dequantize_mx(const uint8_t *codes, const uint8_t *sca
  *   1 <= m <= FP8W_MAX_DIM, 1 <= n <= FP8W_MAX_DIM, 16 <= k <= FP8W_MAX_K,
  *   k % 16 == 0.  x and y must not overlap codes, scales, bias or workspace.
  *
- * m == 1 with k <= 32768 runs the GEMV kernel; everything else the
- * tensor-core kernel: one launch for m <= 64 (16, 32 or 64 token columns),
- * one launch per 64 rows of x beyond (each re-streams the weight).
+ * m == 1 with k <= 32768 runs the GEMV kernel; 2 <= m <= 64 the
+ * tensor-core kernel for few tokens (one launch of 16, 32 or 64 token
+ * columns); m > 64 the prefill GEMM, which dequantises each 128-row weight
+ * tile into shared memory once and multiplies it by 128- or 256-token tiles
+ * (one launch; it uses no workspace).
  */
 FP8W_API fp8w_status fp8w_linear(const void *x, int act_dtype, int64_t m, int64_t k,
                         const uint8_t *codes, const float *scales,
@@ -242,13 +244,13 @@ FP8W_API size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k);
 
 /* Explicit kernel choice, for tests and tuning; fp8w_linear uses
  * FP8W_KERNEL_AUTO. */
-enum { FP8W_KERNEL_AUTO = 0, FP8W_KERNEL_GEMV = 1, FP8W_KERNEL_SKINNY = 2 };
+enum { FP8W_KERNEL_AUTO = 0, FP8W_KERNEL_GEMV = 1, FP8W_KERNEL_SKINNY = 2, FP8W_KERNEL_PREFILL = 3 };
 
 typedef struct fp8w_linear_config {
     int kernel;   /* FP8W_KERNEL_*; GEMV requires m == 1 and k <= 32768 */
-    int ctas;     /* tensor-core kernel only: CTAs of its persistent grid,
+    int ctas;     /* FP8W_KERNEL_SKINNY only: CTAs of its persistent grid,
                      1..number of SMs, or 0 to choose from the shape; must be
-                     0 for the GEMV kernel */
+                     0 for the other kernels */
     int reserved[6];  /* must be 0 */
 } fp8w_linear_config;
 

@@ -67,6 +67,7 @@ def test_linear_rejects_bad_arguments(kw, status):
     fw.LinearConfig(7),                        # unknown kernel
     fw.LinearConfig(-1),
     fw.LinearConfig(fw.KERNEL_SKINNY, -3),     # negative grid size
+    fw.LinearConfig(fw.KERNEL_PREFILL, 8),     # the prefill GEMM takes no grid size
 ])
 def test_linear_rejects_bad_config(cfg):
     assert _lin(m=2, k=256, cfg=cfg) == 6

@@ -288,7 +288,8 @@ def test_workspace_left_ready_across_shapes():
 
 @pytest.mark.parametrize("act", [oracle.ACT_BF16, oracle.ACT_F16])
 @pytest.mark.parametrize("kernel,m", [(fw.KERNEL_GEMV, 1), (fw.KERNEL_SKINNY, 1), (fw.KERNEL_SKINNY, 5),
-                                      (fw.KERNEL_SKINNY, 32), (fw.KERNEL_SKINNY, 64)])
+                                      (fw.KERNEL_SKINNY, 32), (fw.KERNEL_SKINNY, 64), (fw.KERNEL_PREFILL, 2),
+                                      (fw.KERNEL_PREFILL, 65), (fw.KERNEL_PREFILL, 200), (fw.KERNEL_PREFILL, 300)])
 def test_exact_cases_bit_identical(kernel, m, act):
     """Power-of-two scales, small-integer activations and weights whose codes
     lie in [1/8, 8] (plus the 448 that fixes the scale): every product and
@@ -312,6 +313,55 @@ def test_exact_cases_bit_identical(kernel, m, act):
     assert np.array_equal(y, ref)
 
 
+# ------------------------------------------------------- prefill GEMM (K4) --
+
+PREFILL_SHAPES = [  # (m, n, k): 128- and 256-token tiles, ragged m, n and k (k % 128 == 16, 64, 112)
+    (65, 300, 1040), (100, 129, 4096), (128, 1000, 512), (129, 257, 2064), (200, 640, 4096),
+    (256, 130, 1008), (300, 1024, 1024), (513, 300, 256), (777, 64, 2000),
+]
+
+
+@pytest.mark.parametrize("act", [oracle.ACT_BF16, oracle.ACT_F16])
+@pytest.mark.parametrize("m,n,k", PREFILL_SHAPES)
+def test_prefill_parity(m, n, k, act):
+    c, codes, scales = _case(7000 + m + n + k + act, m, n, k, act, with_bias=(m % 2 == 1))
+    y = gpu_linear(c["x"], act, codes, scales, c["bias"])          # m > 64: the prefill GEMM
+    ref = oracle.linear(c["x"], act, codes, scales, c["bias"], threads=oracle.host_cores())
+    assert_parity(y, ref, act, (m, n, k))
+
+
+@pytest.mark.parametrize("m", [512, 2048])
+def test_prefill_full_gate_sampled(m):
+    """The gate weight [14336 x 4096] at prefill sizes, in the launch shape a
+    caller gets: sampled channels against the oracle."""
+    base = synthetic.case("decode_stack", 1, "gate")
+    rng = np.random.default_rng(m)
+    x = synthetic.to_bf16_bits(rng.standard_normal((m, 4096)).astype(np.float32))
+    case = dict(base, m=m, x=x)
+    _sampled_parity(case, n_sample=128)
+
+
+def test_prefill_agrees_with_the_skinny_kernel():
+    c, codes, scales = _case(41, 200, 1000, 4096, oracle.ACT_BF16)
+    yp = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], kernel=fw.KERNEL_PREFILL)
+    ys = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], kernel=fw.KERNEL_SKINNY)
+    cmp = compare(yp, ys, oracle.ACT_BF16)
+    assert cmp["rel_l2"] <= 2e-3 and cmp["min_cosine"] >= 0.9999 and cmp["bit_equal"] >= 0.9, cmp
+
+
+def test_prefill_without_workspace_through_the_no_alloc_entry():
+    c, codes, scales = _case(43, 150, 300, 1024, oracle.ACT_BF16)
+    x = torch.from_numpy(c["x"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    y = torch.empty((150, 300), dtype=torch.bfloat16, device=DEV)
+    cd, sd, bd = (torch.from_numpy(v).to(DEV) for v in (codes, scales, c["bias"]))
+    st = fw.lib().fp8w_linear_noalloc(x.data_ptr(), 1, 150, 1024, cd.data_ptr(), sd.data_ptr(), bd.data_ptr(), 300,
+                                      y.data_ptr(), None)
+    assert st == 0
+    torch.cuda.synchronize()
+    got = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert_parity(got, oracle.linear(c["x"], 1, codes, scales, c["bias"], threads=oracle.host_cores()), 1, "noalloc")
+
+
 def test_one_hot_reads_every_code():
     """x = e_j reads column j of the quantised weight: y[n] = RN(scale[n] * e4m3(q[n, j])),
     with scale a power of two so the product is exact; column j holds all 254
@@ -326,7 +376,7 @@ def test_one_hot_reads_every_code():
     assert np.all(scales == 1.0)
     for act in (oracle.ACT_BF16, oracle.ACT_F16):
         to_bits = synthetic.to_f16_bits if act == oracle.ACT_F16 else synthetic.to_bf16_bits
-        for m, kern in ((1, fw.KERNEL_GEMV), (1, fw.KERNEL_SKINNY), (3, fw.KERNEL_SKINNY)):
+        for m, kern in ((1, fw.KERNEL_GEMV), (1, fw.KERNEL_SKINNY), (3, fw.KERNEL_SKINNY), (70, fw.KERNEL_PREFILL)):
             xf = np.zeros((m, k), dtype=np.float32)
             xf[:, 5] = 1.0
             y = gpu_linear(to_bits(xf), act, codes, scales, None, kernel=kern)
