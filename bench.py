@@ -475,6 +475,52 @@ def run_warm_l2(torch, fw, dev, s, launches=200):
                     "5.6 us for this shape with a warm L2 on another GPU"}
 
 
+def bf16_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    return 1900.0, "fallback"
+
+
+def run_prefill(torch, fw, dev, s, m=2048, launches=10):
+    """The prefill GEMM on the gate weight [14336 x 4096] at m tokens (bf16):
+    graph-replayed back-to-back launches; a compute-bound shape, so TFLOP/s
+    against the measured bf16 tensor peak."""
+    c = synthetic.case("decode_stack", 1, "gate")
+    w = torch.from_numpy(c["w"]).to(dev)
+    bias = torch.from_numpy(c["bias"]).to(dev)
+    n, k = w.shape
+    codes, scales = fw.quantize(w)
+    del w
+    x = torch.from_numpy(synthetic.to_bf16_bits(np.random.default_rng(m).standard_normal((m, k)).astype(np.float32))
+                         .view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        fw.linear(x, codes, scales, bias, out=y)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(launches):
+                fw.linear(x, codes, scales, bias, out=y)
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        g.replay()
+        e1.record(s)
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / launches
+    del g
+    tf = 2.0 * m * n * k / us / 1e6
+    peak, src = bf16_peak()
+    return {"shape": "[%d, 4096] x gate [14336 x 4096], bf16" % m, "us_per_launch": round(us, 2),
+            "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peak, 4), "peak_source": src,
+            "kernel": "fp8w::prefill_kernel<256, 1>"}
+
+
 def run_ours(args, torch, dist):
     import fp8_weight_only_gb300 as fw
     ws, rank, local = dist_env()
@@ -619,6 +665,7 @@ def run_ours(args, torch, dist):
 
     result["grouped_gemv"] = run_grouped(torch, fw, dev, s, peak)
     result["warm_l2"] = run_warm_l2(torch, fw, dev, s)
+    result["prefill"] = run_prefill(torch, fw, dev, s)
 
     # quantiser throughput on the seven matrices (load-time step)
     qcodes = {name: torch.empty_like(mats[name]["codes"][0]) for name in wdev}
