@@ -851,7 +851,7 @@ def main():
                     help="profiling case: quantise one decode-stack matrix and run fp8w_linear --reps times "
                          "(three weight replicas, so every read comes from HBM); prints per-launch times")
     ap.add_argument("--reps", type=int, default=4)
-    ap.add_argument("--kernel", type=int, default=0, help="with --profile: 0 auto, 1 gemv, 2 tensor-core")
+    ap.add_argument("--kernel", type=int, default=0, help="with --profile: 0 auto, 1 gemv, 2 tensor-core (few tokens), 3 prefill GEMM")
     ap.add_argument("--ctas", type=int, default=0, help="with --profile: tensor-core grid size (0 = from the shape)")
     ap.add_argument("--record-traffic", default=None, metavar="CSV",
                     help="write profiles/dram_traffic_decode_stack.json from an ncu CSV (see TRAFFIC_COMMAND)")
