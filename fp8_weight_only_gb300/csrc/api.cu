@@ -61,6 +61,8 @@ fp8w_status fp8w_quantize_ex(const void* w, int w_dtype, int64_t n, int64_t k, u
 }
 
 static size_t skinny_ws(void);
+// m > 64 runs the prefill GEMM.
+static bool use_prefill(int64_t m) { return m > 64; }
 
 static bool valid_group(int group) { return group == 32 || group == 64 || group == 128; }
 
@@ -112,6 +114,7 @@ fp8w_status fp8w_linear_mx(const void* x, int act_dtype, int64_t m, int64_t k, c
     const size_t need = skinny_ws();
     if (need == 0) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear_mx device query");
     if (workspace_bytes < need) return FP8W_ERR_WORKSPACE;
+    if (use_prefill(m)) return cuda_status(fp8w::launch_prefill(a, s), "fp8w_linear_mx prefill launch");
     return cuda_status(fp8w::launch_skinny(a, workspace, 0, s), "fp8w_linear_mx tensor-core launch");
 }
 
@@ -154,10 +157,8 @@ static size_t skinny_ws(void) {
     return fp8w::skinny_workspace_size(sms);
 }
 
-// m == 1 runs the GEMV unless its x does not fit in shared memory; m > 64
-// the prefill GEMM.
+// m == 1 runs the GEMV unless its x does not fit in shared memory.
 static bool use_gemv(int64_t m, int64_t k) { return m == 1 && fp8w::gemv_supports(k); }
-static bool use_prefill(int64_t m) { return m > 64; }
 
 size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k) {
     (void)n;

@@ -91,6 +91,21 @@ __device__ __forceinline__ void e4m3x4_to_bf16x2_mul(uint32_t w, uint32_t& p01, 
     p23 = bf16x2_mul(__byte_perm(lo, hi, 0x7362), mul);
 }
 
+// MX-style scales folded into a dequantised bf16 weight: an E8M0 byte b is
+// worth 2^e, e = b - 127.  With the byte moves above (value * 2^-120), one
+// multiply by 2^(120 + e) gives value * 2^e rounded once; that multiplier is
+// a bf16 number for b <= 134.  Larger bytes take 2^120 first and then this
+// second factor, 2^e itself as bf16 pairs (b = 0: the subnormal 2^-127; 0xFF:
+// NaN), which rounds the same product once.
+__device__ __forceinline__ uint32_t mx_first_mul(uint32_t b) {
+    const uint32_t h = (b + 120u) << 7;
+    return h | (h << 16);
+}
+__device__ __forceinline__ uint32_t mx_second_mul(uint32_t b) {
+    const uint32_t h = b == 255u ? 0x7FC0u : b == 0u ? 0x0040u : b << 7;
+    return h | (h << 16);
+}
+
 __device__ __forceinline__ void e4m3x4_to_bf16x2(uint32_t w, uint32_t& p01, uint32_t& p23) {
     e4m3x4_to_bf16x2_mul(w, p01, p23, kBf16x2Pow2_120);
 }

@@ -80,11 +80,16 @@ __device__ __forceinline__ void prefill_error(int code, volatile int* abort_flag
 
 }  // namespace
 
-template <int BN, bool kBf16>
+// kMx: E8M0 scale bytes e8[n, k / 32] instead of per-row scales (page "11.
+// Inference with NVFP4/MXFP8", section "MXFP8-Style FP8"; bf16 only, k % 128
+// == 0): each 32-code group's power of two is folded into the dequantised
+// weight, exactly, and the epilogue adds only the bias.
+template <int BN, bool kBf16, bool kMx>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
-                   const float* __restrict__ scales, const float* __restrict__ bias, uint16_t* __restrict__ y,
-                   int64_t m, int64_t n, int64_t k) {
+                   const float* __restrict__ scales, const uint8_t* __restrict__ e8, const float* __restrict__ bias,
+                   uint16_t* __restrict__ y, int64_t m, int64_t n, int64_t k) {
+    static_assert(!kMx || kBf16, "MX-style scales fold into bf16 weights only");
     using L = PrefillSmem<BN>;
     constexpr int kPCS = L::kPCS, kPAS = L::kPAS, kPXS = L::kPXS;
     extern __shared__ uint8_t smem_raw[];
@@ -266,7 +271,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
             tc_fence_after();
             const int64_t col = cb * kPM + r;
-            const float sc = col < n ? scales[col] : 0.0f;
+            const float sc = kMx ? 1.0f : col < n ? scales[col] : 0.0f;
             const float b = (bias && col < n) ? bias[col] : 0.0f;
             const int64_t tok0 = tb * BN;
             const int ntok = static_cast<int>(m - tok0 < BN ? m - tok0 : BN);
@@ -290,6 +295,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int h = (warp - kPFirstDqWarp) >> 2;  // warpgroup: k-blocks with j % 2 == h
         const int r = (warp & 3) * 32 + lane;       // weight row of the tile
         const uint32_t swz = static_cast<uint32_t>(r & 7);
+        // MX: the row's two scale bytes of this warpgroup's k-blocks, loaded
+        // one of them ahead; (mx_t, mx_j) is the one after the current
+        uint32_t mx_next = 0x7F7Fu;
+        int64_t mx_t = blockIdx.x;
+        int mx_j = h;
+        auto mx_load = [&]() -> uint32_t {
+            const int64_t wrow = (mx_t / token_tiles) * kPM + r;
+            return wrow < n ? static_cast<uint32_t>(__ldg(reinterpret_cast<const uint16_t*>(e8 + wrow * (k >> 5)) + mx_j))
+                            : 0x7F7Fu;  // rows past n hold zero codes: any scale does
+        };
+        auto mx_step = [&]() {
+            if (mx_t < tiles && mx_j < nkb) mx_next = mx_load();
+            mx_j += 2;
+            if (mx_j >= nkb) {
+                mx_j = h;
+                mx_t += gridDim.x;
+            }
+        };
+        if constexpr (kMx) {
+            pdl_wait();  // the scales may come from the previous kernel
+            mx_step();
+        }
         int64_t cs_n = 0, kb_base = 0;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x, kb_base += nkb) {
@@ -319,16 +346,38 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     break;
                 }
                 const uint32_t arow = sbase + L::kAOff + as * kPABytes + static_cast<uint32_t>(r) * 128u;
+                // MX: the k-block's two groups (chunks 0-1 and 2-3); a byte above
+                // 134 anywhere in the warp takes two multiplies
+                uint32_t mx_word = 0u, mul[2] = {kBf16x2Pow2_120, kBf16x2Pow2_120};
+                bool twice = false;
+                if constexpr (kMx) {
+                    mx_word = mx_next;
+                    mx_step();
+                    twice = __any_sync(0xffffffffu, (mx_word & 0xFFu) > 134u || (mx_word >> 8) > 134u);
+                    if (!twice) {
+                        mul[0] = mx_first_mul(mx_word & 0xFFu);
+                        mul[1] = mx_first_mul(mx_word >> 8);
+                    }
+                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     uint32_t v[8];
                     const uint32_t w4[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        if constexpr (kBf16) {
+                        if constexpr (kMx) {
+                            e4m3x4_to_bf16x2_mul(w4[e], v[2 * e], v[2 * e + 1], mul[q >> 1]);
+                        } else if constexpr (kBf16) {
                             e4m3x4_to_bf16x2(w4[e], v[2 * e], v[2 * e + 1]);
                         } else {
                             e4m3x4_to_f16x2(w4[e], v[2 * e], v[2 * e + 1]);
+                        }
+                    }
+                    if constexpr (kMx) {
+                        if (twice) {
+                            const uint32_t m2 = mx_second_mul((mx_word >> (8 * (q >> 1))) & 0xFFu);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) v[e] = bf16x2_mul(v[e], m2);
                         }
                     }
                     // 16 values = logical chunks 2q and 2q + 1 of the A row
@@ -349,10 +398,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     }
 }
 
-template <int BN, bool kBf16>
+template <int BN, bool kBf16, bool kMx = false>
 static cudaError_t launch_bn(const LinearArgs& a, cudaStream_t st) {
     using L = PrefillSmem<BN>;
-    auto kern = prefill_kernel<BN, kBf16>;
+    auto kern = prefill_kernel<BN, kBf16, kMx>;
     static std::once_flag attr_once[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -384,12 +433,19 @@ static cudaError_t launch_bn(const LinearArgs& a, cudaStream_t st) {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, a.scales, a.bias, static_cast<uint16_t*>(a.y), a.m,
-                              a.n, a.k);
+    const float* sc = kMx ? nullptr : a.scales;
+    const uint8_t* e8 = kMx ? reinterpret_cast<const uint8_t*>(a.scales) : nullptr;
+    return cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, sc, e8, a.bias, static_cast<uint16_t*>(a.y), a.m, a.n,
+                              a.k);
 }
 
 cudaError_t launch_prefill(const LinearArgs& a, cudaStream_t st) {
     const bool bf16 = a.act == 1;
+    if (a.e8m0) {
+        // MX-style scales: bf16 activations, k % 128 == 0 (checked by the caller)
+        if (!bf16 || a.group != 32 || a.k % 128 != 0) return cudaErrorInvalidValue;
+        return a.m <= 128 ? launch_bn<128, true, true>(a, st) : launch_bn<256, true, true>(a, st);
+    }
     // 128-token tiles up to 128 tokens, 256 beyond
     if (a.m <= 128) return bf16 ? launch_bn<128, true>(a, st) : launch_bn<128, false>(a, st);
     return bf16 ? launch_bn<256, true>(a, st) : launch_bn<256, false>(a, st);

@@ -207,10 +207,6 @@ __device__ __forceinline__ void dequant16(const uint4 c, uint32_t (&out)[8]) {
 // multiplier of a group is 2^(120 + e), a bf16 number for b <= 134; a warp
 // holding a larger byte multiplies by 2^120 and then by 2^e (b = 0: the
 // subnormal 2^-127; 0xFF: NaN), which rounds the same product once.
-__device__ __forceinline__ uint32_t mx_second_mul(uint32_t b) {
-    const uint32_t h = b == 255u ? 0x7FC0u : b == 0u ? 0x0040u : b << 7;
-    return h | (h << 16);
-}
 __device__ __forceinline__ void dequant16_mx(const uint4 c, uint32_t (&out)[8], uint32_t mul) {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll

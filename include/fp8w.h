@@ -160,8 +160,9 @@ FP8W_API fp8w_status fp8w_quantize_mx(const float *w, int64_t n, int64_t k,
  * scale bytes are bulk-copied beside its codes, and each 16-code fp32 partial
  * sum is scaled by its block's power of two, which adds no rounding (short
  * of over- or underflow); bias added once, one rounding.  Any other shape
- * runs the tensor-core kernel, for bf16 activations only (FP8W_ERR_DTYPE for
- * fp16): the scale is folded into the dequantised bf16 weight, e4m3(q) *
+ * runs a tensor-core kernel (the skinny one up to m = 64, the prefill GEMM
+ * beyond), for bf16 activations only (FP8W_ERR_DTYPE for fp16): the scale is
+ * folded into the dequantised bf16 weight, e4m3(q) *
  * 2^(b - 127), which is exact wherever that product is a bf16 number
  * (anything but products below 2^-130 or beyond the bf16 range), then fp32
  * accumulation, bias added once, one rounding.

@@ -826,9 +826,10 @@ def test_linear_mx_equals_the_grouped_linear_on_decoded_scales():
     assert np.count_nonzero((a[0] & 0x7FFF) > 0x7F80) == 1 + int(((a[0, 3] & 0x7FFF) > 0x7F80))
 
 
-MX_TC_SHAPES = [  # (m, n, k): the tensor-core form; whole tiles, cluster splits, stream-K, 64-token slabs
+MX_TC_SHAPES = [  # (m, n, k): the tensor-core form (whole tiles, cluster splits, stream-K) and, beyond 64
     (1, 300, 384), (2, 300, 4096), (8, 4096, 4096), (9, 1024, 4096), (32, 14336, 4096), (17, 257, 640),
-    (8, 20480, 1024), (48, 1000, 1024), (64, 640, 14336), (70, 257, 640), (129, 130, 256),
+    (8, 20480, 1024), (48, 1000, 1024), (64, 640, 14336), (70, 257, 640), (129, 130, 256),   # tokens, the prefill GEMM
+    (200, 1000, 4096), (513, 300, 1024),
 ]
 
 
@@ -866,6 +867,8 @@ def test_linear_mx_tensor_core_parity(m, n, k):
     (32, 14336, 1024, 100, 134),
     (8, 1000, 4096, 120, 141),      # rows with bytes 135..254: two multiplies in their warps
     (48, 300, 1024, 130, 150),
+    (100, 640, 1024, 100, 134),     # the prefill GEMM, one and two multiplies
+    (300, 1000, 512, 120, 141),
 ])
 def test_linear_mx_with_equal_blocks_is_the_per_channel_linear(m, n, k, lo, hi):
     """Every block of a row with the same byte b: the MX result equals the
@@ -878,7 +881,8 @@ def test_linear_mx_with_equal_blocks_is_the_per_channel_linear(m, n, k, lo, hi):
     e8 = np.repeat(b[:, None], k // 32, axis=1)
     per_row = np.float32(2.0) ** (b.astype(np.int32) - 127).astype(np.float32)
     y_mx = _gpu_mx(c, codes, e8)
-    y_pc = gpu_linear(c["x"], oracle.ACT_BF16, codes, per_row, c["bias"], kernel=fw.KERNEL_SKINNY)
+    kern = fw.KERNEL_PREFILL if m > 64 else fw.KERNEL_SKINNY
+    y_pc = gpu_linear(c["x"], oracle.ACT_BF16, codes, per_row, c["bias"], kernel=kern)
     assert np.array_equal(y_mx, y_pc)
 
 
