@@ -781,11 +781,78 @@ def run_ours(args, torch, dist):
     ycheck = torch.cat([ys[key].reshape(-1) for key in keys_y]).cpu()
     assert torch.equal(hypack, ycheck)
     del ge
-    result["e2e"] = {"value": round(step_bytes() * n_ranks * args.steps / e2e_s / 1e9, 2), "unit": "GB/s",
+
+    # the same steps as a serving loop pipelines them: two sets of device
+    # buffers; step i+1's inputs are copied in and step i's outputs copied out
+    # on their own streams while step i computes, ordered by events
+    xpk = [xpack, torch.empty_like(xpack)]
+    ypk = [ypack, torch.empty_like(ypack)]
+    hyk = [hypack, torch.empty_like(hypack).pin_memory()]
+    gsteps = []
+    for b in range(2):
+        xvb = {key: xpk[b][xoff[key]:xoff[key] + xs[key].numel()].view(xs[key].shape) for key in keys_x}
+        yvb = {key: ypk[b][yoff[key]:yoff[key] + ys[key].numel()].view(ys[key].shape) for key in keys_y}
+        gb = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gb, stream=s):
+            enqueue_step(fw, mats, xvb, yvb)
+        gsteps.append(gb)
+    cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
+    step_i = [0]
+
+    def pipelined_step():
+        b = step_i[0] % 2
+        step_i[0] += 1
+        with torch.cuda.stream(cin):
+            cin.wait_event(comp_done[b])          # the step two back has read these inputs
+            xpk[b].copy_(hxpack, non_blocking=True)
+            in_done[b].record(cin)
+        s.wait_event(in_done[b])
+        s.wait_event(out_done[b])                 # the step two back's outputs are out
+        gsteps[b].replay()
+        comp_done[b].record(s)
+        with torch.cuda.stream(cout):
+            cout.wait_event(comp_done[b])
+            hyk[b].copy_(ypk[b], non_blocking=True)
+            out_done[b].record(cout)
+
+    def wall_pipelined(nsteps):
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(s):
+            for _ in range(nsteps):
+                pipelined_step()
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        if dist is not None:
+            t = torch.tensor([dt], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        return dt
+
+    with torch.cuda.stream(s):
+        for _ in range(max(2, args.warmup)):
+            pipelined_step()
+    torch.cuda.synchronize()
+    pipe_s = wall_pipelined(args.steps)
+    assert torch.equal(hyk[(step_i[0] - 1) % 2], ycheck)
+    del gsteps
+    result["e2e"] = {"value": round(step_bytes() * n_ranks * args.steps / pipe_s / 1e9, 2), "unit": "GB/s",
                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                     "ms_per_step": round(e2e_s / args.steps * 1e3, 4),
-                     "note": "fp8w.linear calls of the step plus one pinned-host copy of all its inputs in and one "
-                             "of all its outputs back, captured in a CUDA graph and replayed; host wall clock"}
+                     "ms_per_step": round(pipe_s / args.steps * 1e3, 4),
+                     "note": "fp8w.linear calls of each step plus one pinned-host copy of all its inputs in and one "
+                             "of all its outputs back, every step; the step captured in a CUDA graph, its copies on "
+                             "their own streams so that they overlap the neighbouring steps' compute (two buffer "
+                             "sets, event-ordered); host wall clock"}
+    result["e2e_serial"] = {"value": round(step_bytes() * n_ranks * args.steps / e2e_s / 1e9, 2), "unit": "GB/s",
+                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                            "ms_per_step": round(e2e_s / args.steps * 1e3, 4),
+                            "note": "the same, with the copies and the step in one graph on one stream, one after "
+                                    "another; host wall clock"}
     result["e2e_eager"] = {"value": round(step_bytes() * n_ranks * args.steps / eager_s / 1e9, 2), "unit": "GB/s",
                            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                            "ms_per_step": round(eager_s / args.steps * 1e3, 4),
