@@ -318,6 +318,7 @@ def test_exact_cases_bit_identical(kernel, m, act):
 PREFILL_SHAPES = [  # (m, n, k): 128- and 256-token tiles, ragged m, n and k (k % 128 == 16, 64, 112)
     (65, 300, 1040), (100, 129, 4096), (128, 1000, 512), (129, 257, 2064), (200, 640, 4096),
     (256, 130, 1008), (300, 1024, 1024), (513, 300, 256), (777, 64, 2000),
+    (100, 50, 16), (70, 200, 64), (300, 33, 48), (66, 1, 16),   # k below one code stage, one row
 ]
 
 
@@ -339,6 +340,15 @@ def test_prefill_full_gate_sampled(m):
     x = synthetic.to_bf16_bits(rng.standard_normal((m, 4096)).astype(np.float32))
     case = dict(base, m=m, x=x)
     _sampled_parity(case, n_sample=128)
+
+
+@pytest.mark.parametrize("m", [1, 2, 17])
+def test_prefill_kernel_at_few_tokens(m):
+    """The prefill GEMM chosen explicitly for a handful of tokens (a mostly
+    empty 128-token tile)."""
+    c, codes, scales = _case(61 + m, m, 300, 1040, oracle.ACT_BF16)
+    y = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], kernel=fw.KERNEL_PREFILL)
+    assert_parity(y, oracle.linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"]), oracle.ACT_BF16, m)
 
 
 def test_prefill_agrees_with_the_skinny_kernel():
@@ -829,7 +839,7 @@ def test_linear_mx_equals_the_grouped_linear_on_decoded_scales():
 MX_TC_SHAPES = [  # (m, n, k): the tensor-core form (whole tiles, cluster splits, stream-K) and, beyond 64
     (1, 300, 384), (2, 300, 4096), (8, 4096, 4096), (9, 1024, 4096), (32, 14336, 4096), (17, 257, 640),
     (8, 20480, 1024), (48, 1000, 1024), (64, 640, 14336), (70, 257, 640), (129, 130, 256),   # tokens, the prefill GEMM
-    (200, 1000, 4096), (513, 300, 1024),
+    (200, 1000, 4096), (513, 300, 1024), (90, 64, 128), (65, 300, 384),
 ]
 
 
