@@ -313,6 +313,16 @@ def test_exact_cases_bit_identical(kernel, m, act):
     assert np.array_equal(y, ref)
 
 
+@pytest.mark.parametrize("m,n,k", [(8, 14300, 1024), (32, 13700, 512), (8, 14600, 512), (16, 14336, 272)])
+def test_whole_tile_launches(m, n, k):
+    """Whole-tile launches (108 to 115 tiles of 128 rows, one a CTA) with a
+    ragged last tile or a ragged k."""
+    c, codes, scales = _case(900 + m + n + k, m, n, k, oracle.ACT_BF16)
+    y = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"])
+    ref = oracle.linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], threads=oracle.host_cores())
+    assert_parity(y, ref, oracle.ACT_BF16, (m, n, k))
+
+
 # ------------------------------------------------------- prefill GEMM (K4) --
 
 PREFILL_SHAPES = [  # (m, n, k): 128- and 256-token tiles, ragged m, n and k (k % 128 == 16, 64, 112)
