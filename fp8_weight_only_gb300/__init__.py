@@ -28,7 +28,7 @@ SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_workspace_size", "fp8w_l
            "fp8w_linear_noalloc", "fp8w_dequantize", "fp8w_quantize_grouped", "fp8w_linear_grouped",
            "fp8w_quantize_mx", "fp8w_linear_mx", "fp8w_quantize_ex", "fp8w_dequantize_grouped",
            "fp8w_dequantize_mx")
-ABI_VERSION = 8
+ABI_VERSION = 9
 
 
 class Fp8wError(RuntimeError):
@@ -239,7 +239,9 @@ def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_
             raise ValueError("out must be a contiguous [M, N] tensor of x's dtype")
         if mx:
             L = lib()
-            need = 0 if (m == 1 and k % 512 == 0 and k <= 32768) else L.fp8w_linear_workspace_size(max(m, 2), n, k)
+            # the GEMV and the prefill GEMM need no workspace
+            need = 0 if (m == 1 and k % 512 == 0 and k <= 32768) or m > 64 else \
+                L.fp8w_linear_workspace_size(max(m, 2), n, k)
             ws = None
             if need:
                 ws = workspace_buffer if workspace_buffer is not None else workspace(x.device, need)
@@ -261,7 +263,7 @@ def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_
     act = _act(x.dtype)
     L = lib()
     stream = _stream(x)
-    need = L.fp8w_linear_workspace_size(max(m, 2) if kernel == KERNEL_SKINNY else m, n, k)
+    need = L.fp8w_linear_workspace_size(min(max(m, 2), 64) if kernel == KERNEL_SKINNY else m, n, k)
     ws = None
     if need:
         ws = workspace_buffer if workspace_buffer is not None else workspace(x.device, need)

@@ -108,13 +108,14 @@ fp8w_status fp8w_linear_mx(const void* x, int act_dtype, int64_t m, int64_t k, c
     // codes (16-byte pieces: k % 512 == 0)
     if (m == 1 && k % 512 == 0 && fp8w::gemv_supports(k))
         return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear_mx gemv launch");
-    // otherwise the tensor-core kernel, which folds the scales into bf16 weights
+    // otherwise a tensor-core kernel, which folds the scales into bf16 weights:
+    // the prefill GEMM beyond 64 tokens (no workspace), the skinny kernel below
     if (act_dtype != FP8W_BF16) return FP8W_ERR_DTYPE;
+    if (use_prefill(m)) return cuda_status(fp8w::launch_prefill(a, s), "fp8w_linear_mx prefill launch");
     if (!workspace || !aligned(workspace, 256)) return FP8W_ERR_WORKSPACE;
     const size_t need = skinny_ws();
     if (need == 0) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear_mx device query");
     if (workspace_bytes < need) return FP8W_ERR_WORKSPACE;
-    if (use_prefill(m)) return cuda_status(fp8w::launch_prefill(a, s), "fp8w_linear_mx prefill launch");
     return cuda_status(fp8w::launch_skinny(a, workspace, 0, s), "fp8w_linear_mx tensor-core launch");
 }
 
@@ -162,7 +163,7 @@ static bool use_gemv(int64_t m, int64_t k) { return m == 1 && fp8w::gemv_support
 
 size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k) {
     (void)n;
-    return use_gemv(m, k) ? 0 : skinny_ws();
+    return use_gemv(m, k) || use_prefill(m) ? 0 : skinny_ws();
 }
 
 fp8w_status fp8w_linear_ex(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,

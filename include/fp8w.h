@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define FP8W_ABI_VERSION 8
+#define FP8W_ABI_VERSION 9
 
 #if defined(__GNUC__)
 #define FP8W_API __attribute__((visibility("default")))
@@ -153,7 +153,7 @@ FP8W_API fp8w_status fp8w_quantize_mx(const float *w, int64_t n, int64_t k,
  *
  *   scales [n, k / 32] uint8, device, 16-byte aligned; k % 128 == 0.
  *   workspace, workspace_bytes: as fp8w_linear (fp8w_linear_workspace_size);
- *           may be NULL / 0 when the GEMV runs.
+ *           may be NULL / 0 when the GEMV or the prefill GEMM (m > 64) runs.
  *   Other arguments as fp8w_linear.
  *
  * m == 1 with k % 512 == 0 and k <= 32768 runs the GEMV: a slot's rows of
@@ -239,8 +239,10 @@ FP8W_API fp8w_status fp8w_linear(const void *x, int act_dtype, int64_t m, int64_
                         const float *bias, int64_t n, void *y,
                         void *workspace, size_t workspace_bytes, void *stream);
 
-/* Workspace bytes fp8w_linear needs for this shape on the current device
- * (0 when the GEMV kernel is used: m == 1 and k <= 32768). */
+/* Workspace bytes fp8w_linear needs for this shape on the current device:
+ * 0 when the GEMV kernel (m == 1, k <= 32768) or the prefill GEMM (m > 64)
+ * runs.  FP8W_KERNEL_SKINNY chosen explicitly needs the size of the m == 2
+ * shape at m == 1 and of the m == 64 shape beyond 64. */
 FP8W_API size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k);
 
 /* Explicit kernel choice, for tests and tuning; fp8w_linear uses
@@ -256,7 +258,8 @@ typedef struct fp8w_linear_config {
 } fp8w_linear_config;
 
 /* fp8w_linear with an explicit configuration (NULL = automatic).  The
- * tensor-core kernel at m == 1 needs the workspace of the m == 2 shape. */
+ * skinny tensor-core kernel at m == 1 needs the workspace of the m == 2
+ * shape, and beyond 64 tokens that of the m == 64 shape. */
 FP8W_API fp8w_status fp8w_linear_ex(const void *x, int act_dtype, int64_t m, int64_t k,
                            const uint8_t *codes, const float *scales,
                            const float *bias, int64_t n, void *y,

@@ -361,6 +361,27 @@ def test_prefill_kernel_at_few_tokens(m):
     assert_parity(y, oracle.linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"]), oracle.ACT_BF16, m)
 
 
+def test_prefill_needs_no_workspace_and_captures_in_a_graph():
+    """m > 64 needs no workspace, so a first call can be captured in a CUDA
+    graph with nothing allocated before it."""
+    L = fw.lib()
+    assert L.fp8w_linear_workspace_size(65, 300, 1024) == 0 and L.fp8w_linear_workspace_size(64, 300, 1024) > 0
+    c, codes, scales = _case(47, 100, 300, 1024, oracle.ACT_BF16)
+    x = torch.from_numpy(c["x"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    cd, sd, bd = (torch.from_numpy(v).to(DEV) for v in (codes, scales, c["bias"]))
+    y = torch.empty((100, 300), dtype=torch.bfloat16, device=DEV)
+    fw.linear(x, cd, sd, bd, out=torch.empty_like(y))     # eager first launch (function attributes)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream(device=DEV)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        fw.linear(x, cd, sd, bd, out=y, workspace_buffer=None)
+    g.replay()
+    torch.cuda.synchronize()
+    got = y.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert_parity(got, oracle.linear(c["x"], 1, codes, scales, c["bias"], threads=oracle.host_cores()), 1, "graph")
+
+
 def test_prefill_agrees_with_the_skinny_kernel():
     c, codes, scales = _case(41, 200, 1000, 4096, oracle.ACT_BF16)
     yp = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], kernel=fw.KERNEL_PREFILL)
