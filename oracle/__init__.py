@@ -296,7 +296,8 @@ def dequantize_mx(codes, scales) -> np.ndarray:
 
 
 def fp8_error(w, codes, scales) -> dict:
-    """Weight report: rel_l2, worst_channel_rel_l2, underflow, crest."""
+    """Weight report: rel_l2, worst_channel_rel_l2, underflow, crest.  Parity
+    unpinned: the pages name these fields without defining them."""
     w = _c(w, np.float32)
     codes = _c(codes, np.uint8)
     scales = _c(scales, np.float32)

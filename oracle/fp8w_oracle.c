@@ -18,6 +18,12 @@
  *
  * Build: plain C11, no fast-math, no FMA contraction (-ffp-contract=off), so
  * every float operation below is one IEEE operation on both x86-64 and Arm.
+ *
+ * Pins: every function here is checked by the test suite against values the
+ * pages print, closed forms, exact rationals or brute force, except
+ * oracle_fp8_error, whose fields the pages name without defining: parity
+ * unpinned (its definitions are readings; only a hand-computed case and
+ * zero error on representable weights check it).
  */
 #include <math.h>
 #include <pthread.h>
