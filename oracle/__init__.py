@@ -67,6 +67,8 @@ def _load():
         lib.oracle_dequantize_grouped.argtypes = [P, P, c.c_int64, c.c_int64, c.c_int64, P]
         lib.oracle_dequantize_mx.restype = None
         lib.oracle_dequantize_mx.argtypes = [P, P, c.c_int64, c.c_int64, P]
+        lib.oracle_linear_w8a8.restype = c.c_int
+        lib.oracle_linear_w8a8.argtypes = [P, P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P]
         lib.oracle_fp8_error.restype = None
         lib.oracle_fp8_error.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
         lib.oracle_e4m3_encode_many.restype = None
@@ -293,6 +295,31 @@ def dequantize_mx(codes, scales) -> np.ndarray:
     out = np.empty((n, k), dtype=np.float64)
     _load().oracle_dequantize_mx(_ptr(codes), _ptr(scales), n, k, _ptr(out))
     return out
+
+
+def quantize_act(x_bits, act: int):
+    """W8A8 activation quantisation (page "tensormux Write an FP8 kernel",
+    per-token scales): each row of the bf16/fp16 activations, widened
+    exactly to fp32, by the per-row rule -> (codes uint8 [M, K], scales fp32 [M])."""
+    return quantize_16(x_bits, act)
+
+
+def linear_w8a8(qx, sx, act: int, qw, sw, bias=None, want_acc: bool = False):
+    """y[M,N] = round_act(sx[m] * sw[n] * sum_k e4m3val(qx[m,k]) e4m3val(qw[n,k]) + bias[n]), fp64."""
+    qx = _c(qx, np.uint8)
+    sx = _c(sx, np.float32)
+    qw = _c(qw, np.uint8)
+    sw = _c(sw, np.float32)
+    bias = None if bias is None else _c(bias, np.float32)
+    m, k = qx.shape
+    n, k2 = qw.shape
+    if k != k2 or sx.shape != (m,) or sw.shape != (n,) or (bias is not None and bias.shape != (n,)):
+        raise ValueError("oracle.linear_w8a8: shape mismatch")
+    y = np.empty((m, n), dtype=np.uint16)
+    acc = np.empty((m, n), dtype=np.float64) if want_acc else None
+    _load().oracle_linear_w8a8(_ptr(qx), _ptr(sx), act, m, k, _ptr(qw), _ptr(sw), _ptr(bias), n, _ptr(y),
+                               _ptr(acc))
+    return (y, acc) if want_acc else y
 
 
 def fp8_error(w, codes, scales) -> dict:

@@ -515,6 +515,37 @@ int oracle_linear_mx(const uint16_t *x, int act, int64_t m, int64_t k,
 }
 
 /* ------------------------------------------------------------------------ */
+/* W8A8: activations quantised too (page "tensormux Write an FP8 kernel",
+ * steps 2-4 and its epilogue: per-token activation scales, per-channel
+ * weight scales, both amax / 448, and the accumulator multiplied by both;
+ * page "kadirnar/kernel-agent fp8-weights" calls this a different target
+ * from weight-only).  Activation codes qx[m, k] and scales sx[m] come from
+ * the per-row rule above applied to the activations widened to fp32.
+ *   y[m,n] = RN_out( sx[m] * sw[n] * sum_k e4m3(qx[m,k]) e4m3(qw[n,k]) + bias[n] )
+ * in fp64 (every product and the k-ascending sum exact to fp64 rounding),
+ * one rounding to the output type (bf16 or fp16).                         */
+/* ------------------------------------------------------------------------ */
+int oracle_linear_w8a8(const uint8_t *qx, const float *sx, int act, int64_t m,
+                       int64_t k, const uint8_t *qw, const float *sw,
+                       const float *bias, int64_t n, uint16_t *y, double *yacc)
+{
+    int64_t mi, ni, ki;
+    for (mi = 0; mi < m; ++mi) {
+        for (ni = 0; ni < n; ++ni) {
+            double acc = 0.0, out;
+            for (ki = 0; ki < k; ++ki)
+                acc += oracle_e4m3_decode(qx[mi * k + ki]) * oracle_e4m3_decode(qw[ni * k + ki]);
+            out = (double)sx[mi] * (double)sw[ni] * acc + (bias ? (double)bias[ni] : 0.0);
+            if (yacc)
+                yacc[mi * n + ni] = out;
+            if (y)
+                y[mi * n + ni] = act == ORACLE_ACT_F16 ? oracle_round_f16(out) : oracle_round_bf16(out);
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Weight error report, the fields of fp8_error(weight, q, scale) named on
  * page "kadirnar/kernel-agent fp8-weights", "The contract".  The page names
  * the fields but prints no definitions; the readings used here:
