@@ -323,8 +323,8 @@ def linear_w8a8(qx, sx, act: int, qw, sw, bias=None, want_acc: bool = False):
 
 
 def fp8_error(w, codes, scales) -> dict:
-    """Weight report: rel_l2, worst_channel_rel_l2, underflow, crest.  Parity
-    unpinned: the pages name these fields without defining them."""
+    """Weight report: rel_l2, worst_channel_rel_l2, underflow, crest (the
+    readings are in the C source; the pages name the fields only)."""
     w = _c(w, np.float32)
     codes = _c(codes, np.uint8)
     scales = _c(scales, np.float32)

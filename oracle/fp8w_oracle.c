@@ -20,10 +20,12 @@
  * every float operation below is one IEEE operation on both x86-64 and Arm.
  *
  * Pins: every function here is checked by the test suite against values the
- * pages print, closed forms, exact rationals or brute force, except
- * oracle_fp8_error, whose fields the pages name without defining: parity
- * unpinned (its definitions are readings; only a hand-computed case and
- * zero error on representable weights check it).
+ * pages print, closed forms, exact rationals, invariants or brute force.
+ * oracle_fp8_error's fields are named by the pages without definitions; its
+ * readings are pinned by closed forms (crest of a one-spike row sqrt(k), of
+ * a constant row 1; weights below half the smallest e4m3 step all
+ * underflow; the error of a known tie) and invariances (power-of-two
+ * rescaling, duplicated and permuted rows).
  */
 #include <math.h>
 #include <pthread.h>

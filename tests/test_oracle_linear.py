@@ -176,29 +176,3 @@ def test_bias_none_equals_bias_zero_and_threads_do_not_matter():
     b = oracle.linear(c["x"], oracle.ACT_BF16, codes, scales, np.zeros(50, np.float32))
     d = oracle.linear(c["x"], oracle.ACT_BF16, codes, scales, None, threads=4)
     assert np.array_equal(a, b) and np.array_equal(a, d)
-
-
-# ------------------------------------------------------------ fp8 report --
-
-def test_fp8_error_hand_case():
-    w = np.array([[448.0, 1.0625], [448.0, 2.0 ** -11], [0.0, 0.0]], dtype=np.float32)
-    codes, scales = oracle.quantize(w)
-    assert list(codes[0]) == [0x7E, 0x38] and list(codes[1]) == [0x7E, 0x00]
-    r = oracle.fp8_error(w, codes, scales)
-    e0 = 0.0625 / np.sqrt(448.0 ** 2 + 1.0625 ** 2)
-    e1 = 2.0 ** -11 / np.sqrt(448.0 ** 2 + 2.0 ** -22)
-    assert np.isclose(r["worst_channel_rel_l2"], max(e0, e1), rtol=1e-12)
-    assert np.isclose(r["rel_l2"], np.sqrt(0.0625 ** 2 + 2.0 ** -22) /
-                      np.sqrt(2 * 448.0 ** 2 + 1.0625 ** 2 + 2.0 ** -22), rtol=1e-12)
-    assert r["underflow"] == 1 / 4
-    assert np.isclose(r["crest"], 448.0 / np.sqrt(2.0 ** -22 / 2 + 448.0 ** 2 / 2), rtol=1e-12)
-
-
-def test_fp8_error_zero_on_representable_weights():
-    t = oracle.e4m3_decode_table()[:0x7F]
-    rng = np.random.default_rng(71)
-    w = (rng.choice(t, size=(16, 40)) * 0.125).astype(np.float32)
-    w[:, 0] = 448 * 0.125
-    codes, scales = oracle.quantize(w)
-    r = oracle.fp8_error(w, codes, scales)
-    assert r["rel_l2"] == 0.0 and r["worst_channel_rel_l2"] == 0.0
