@@ -9,6 +9,8 @@ raised.
     y = linear(x, codes, scales, bias)          # x: [M, K] bf16/fp16 CUDA tensor
     codes, e8 = quantize_mx(w)                  # one E8M0 scale byte per 32 along K
     y = linear(x, codes, e8, bias)              # bf16 x for M > 1
+    qx, sx = quantize_act(x)                    # W8A8: per-token e4m3 activations
+    y = linear_w8a8(qx, sx, codes, scales, bias, out_dtype=torch.bfloat16)
 """
 import ctypes
 import os
@@ -27,8 +29,9 @@ SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_workspace_size", "fp8w_l
            "fp8w_status_string", "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version",
            "fp8w_linear_noalloc", "fp8w_dequantize", "fp8w_quantize_grouped", "fp8w_linear_grouped",
            "fp8w_quantize_mx", "fp8w_linear_mx", "fp8w_quantize_ex", "fp8w_dequantize_grouped",
-           "fp8w_dequantize_mx")
-ABI_VERSION = 9
+           "fp8w_dequantize_mx", "fp8w_quantize_act", "fp8w_linear_w8a8")
+ABI_VERSION = 10
+FLAG_WEIGHTS_READY = 1
 
 
 class Fp8wError(RuntimeError):
@@ -38,7 +41,8 @@ class Fp8wError(RuntimeError):
 
 
 class LinearConfig(ctypes.Structure):
-    _fields_ = [("kernel", ctypes.c_int), ("ctas", ctypes.c_int), ("reserved", ctypes.c_int * 6)]
+    _fields_ = [("kernel", ctypes.c_int), ("ctas", ctypes.c_int), ("flags", ctypes.c_int),
+                ("reserved", ctypes.c_int * 5)]
 
 
 _lib = None
@@ -80,6 +84,10 @@ def lib():
                                      c.POINTER(LinearConfig), P]
         L.fp8w_linear_noalloc.restype = c.c_int
         L.fp8w_linear_noalloc.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P]
+        L.fp8w_quantize_act.restype = c.c_int
+        L.fp8w_quantize_act.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P]
+        L.fp8w_linear_w8a8.restype = c.c_int
+        L.fp8w_linear_w8a8.argtypes = [P, P, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, c.c_int, c.c_int, P]
         L.fp8w_status_string.restype = c.c_char_p
         L.fp8w_status_string.argtypes = [c.c_int]
         L.fp8w_last_cuda_error.restype = c.c_char_p
@@ -212,11 +220,15 @@ def workspace(device, nbytes):
     return ws
 
 
-def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_buffer=None, ctas=0):
+def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_buffer=None, ctas=0,
+           weights_ready=False):
     """y[M, N] = round(scale[n] * sum_k x[m, k] * e4m3(codes[n, k]) + bias[n]).
 
     kernel and ctas (the tensor-core kernel's grid size, 0 = from the shape)
-    override the automatic launch choice, for tests and tuning."""
+    override the automatic launch choice, for tests and tuning.
+    weights_ready: every write to codes and scales has completed before this
+    call (FP8W_FLAG_WEIGHTS_READY): the kernels stream the codes without
+    waiting for the preceding kernel in the stream.  Per-row scales only."""
     import torch
     if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
         raise TypeError("x must be a contiguous 2-D CUDA tensor")
@@ -268,14 +280,55 @@ def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_
     if need:
         ws = workspace_buffer if workspace_buffer is not None else workspace(x.device, need)
     ws_ptr, ws_bytes = (_ptr(ws), ws.numel()) if ws is not None else (None, 0)
-    if kernel == KERNEL_AUTO and ctas == 0:
+    if kernel == KERNEL_AUTO and ctas == 0 and not weights_ready:
         st = L.fp8w_linear(_ptr(x), act, m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
                            _ptr(out), ws_ptr, ws_bytes, stream)
     else:
-        cfg = LinearConfig(kernel, ctas)
+        cfg = LinearConfig(kernel, ctas, FLAG_WEIGHTS_READY if weights_ready else 0)
         st = L.fp8w_linear_ex(_ptr(x), act, m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
                               _ptr(out), ws_ptr, ws_bytes, ctypes.byref(cfg), stream)
     _check(st)
+    return out
+
+
+def quantize_act(x, codes=None, scales=None):
+    """W8A8 activation quantisation: x[M, K] bf16/fp16 (CUDA, contiguous) ->
+    (codes uint8 [M, K], scales fp32 [M]), the per-row rule on every token."""
+    import torch
+    if x.dim() != 2 or not x.is_cuda or not x.is_contiguous():
+        raise TypeError("x must be a contiguous 2-D CUDA tensor")
+    m, k = x.shape
+    if codes is None:
+        codes = torch.empty((m, k), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((m,), dtype=torch.float32, device=x.device)
+    _check(lib().fp8w_quantize_act(_ptr(x), _act(x.dtype), m, k, _ptr(codes), _ptr(scales), _stream(x)))
+    return codes, scales
+
+
+def linear_w8a8(x_codes, x_scales, codes, scales, bias=None, out=None, out_dtype=None, weights_ready=False):
+    """W8A8: y[M, N] = round(x_scales[m] * scales[n] * sum_k e4m3(x_codes[m, k]) e4m3(codes[n, k]) + bias[n]),
+    out_dtype torch.bfloat16 (default) or torch.float16."""
+    import torch
+    for name, t, dt in (("x_codes", x_codes, torch.uint8), ("x_scales", x_scales, torch.float32),
+                        ("codes", codes, torch.uint8), ("scales", scales, torch.float32),
+                        ("bias", bias, torch.float32)):
+        if t is not None and (t.dtype != dt or not t.is_cuda or not t.is_contiguous()):
+            raise TypeError("%s must be a contiguous %s CUDA tensor" % (name, dt))
+    m, k = x_codes.shape
+    n = codes.shape[0]
+    if codes.dim() != 2 or codes.shape[1] != k or x_scales.numel() != m or scales.numel() != n or \
+            (bias is not None and bias.numel() != n):
+        raise ValueError("shape mismatch for W8A8")
+    if out_dtype is None:
+        out_dtype = out.dtype if out is not None else torch.bfloat16
+    if out is None:
+        out = torch.empty((m, n), dtype=out_dtype, device=codes.device)
+    elif out.shape != (m, n) or out.dtype != out_dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [M, N] tensor of out_dtype")
+    _check(lib().fp8w_linear_w8a8(_ptr(x_codes), _ptr(x_scales), m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
+                                  _ptr(out), _act(out_dtype), FLAG_WEIGHTS_READY if weights_ready else 0,
+                                  _stream(codes)))
     return out
 
 

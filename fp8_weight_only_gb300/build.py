@@ -14,7 +14,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libfp8w.so")
-SOURCES = ["api.cu", "quantize.cu", "gemv.cu", "skinny.cu", "prefill.cu"]
+SOURCES = ["api.cu", "quantize.cu", "gemv.cu", "skinny.cu", "prefill.cu", "w8a8.cu"]
 HEADERS = ["fp8w_device.cuh", "fp8w_internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

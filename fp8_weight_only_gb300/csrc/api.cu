@@ -179,7 +179,13 @@ fp8w_status fp8w_linear_ex(const void* x, int act_dtype, int64_t m, int64_t k, c
         return FP8W_ERR_CONFIG;
     const int ctas = config ? config->ctas : 0;
     if (ctas < 0 || (ctas != 0 && kernel != FP8W_KERNEL_SKINNY)) return FP8W_ERR_CONFIG;
+    const int flags = config ? config->flags : 0;
+    if (flags & ~FP8W_FLAG_WEIGHTS_READY) return FP8W_ERR_CONFIG;
+    if (config)
+        for (int r : config->reserved)
+            if (r != 0) return FP8W_ERR_CONFIG;
     fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, scales, bias, y};
+    a.early = (flags & FP8W_FLAG_WEIGHTS_READY) != 0;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (kernel == FP8W_KERNEL_GEMV) return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear gemv launch");
     if (kernel == FP8W_KERNEL_PREFILL) return cuda_status(fp8w::launch_prefill(a, s), "fp8w_linear prefill launch");
@@ -219,6 +225,27 @@ fp8w_status fp8w_linear_noalloc(const void* x, int act_dtype, int64_t m, int64_t
     return cuda_status(fp8w::launch_skinny(a, scratch, 0, s), "fp8w_linear_noalloc tensor-core launch");
 }
 
+fp8w_status fp8w_quantize_act(const void* x, int act_dtype, int64_t m, int64_t k, uint8_t* x_codes, float* x_scales,
+                              void* stream) {
+    if (act_dtype != FP8W_BF16 && act_dtype != FP8W_F16) return FP8W_ERR_DTYPE;
+    return fp8w_quantize_ex(x, act_dtype, m, k, x_codes, x_scales, stream);
+}
+
+fp8w_status fp8w_linear_w8a8(const uint8_t* x_codes, const float* x_scales, int64_t m, int64_t k,
+                             const uint8_t* w_codes, const float* w_scales, const float* bias, int64_t n, void* y,
+                             int out_dtype, int flags, void* stream) {
+    if (!x_codes || !x_scales || !w_codes || !w_scales || !y) return FP8W_ERR_NULL;
+    if (out_dtype != FP8W_BF16 && out_dtype != FP8W_F16) return FP8W_ERR_DTYPE;
+    if (m < 1 || n < 1 || m > FP8W_MAX_DIM || n > FP8W_MAX_DIM || !valid_k(k)) return FP8W_ERR_SHAPE;
+    if (!aligned(x_codes, 16) || !aligned(w_codes, 16) || !aligned(x_scales, 4) || !aligned(w_scales, 4) ||
+        (bias && !aligned(bias, 4)) || !aligned(y, 2))
+        return FP8W_ERR_ALIGN;
+    if (flags & ~FP8W_FLAG_WEIGHTS_READY) return FP8W_ERR_CONFIG;
+    fp8w::W8A8Args a{x_codes, x_scales, m, k, n, w_codes, w_scales, bias, y, out_dtype,
+                     (flags & FP8W_FLAG_WEIGHTS_READY) != 0};
+    return cuda_status(fp8w::launch_w8a8(a, static_cast<cudaStream_t>(stream)), "fp8w_linear_w8a8 launch");
+}
+
 const char* fp8w_status_string(int status) {
     switch (status) {
         case FP8W_OK: return "ok";
@@ -243,7 +270,8 @@ int fp8w_device_error(void) {
     const int a = fp8w::read_skinny_device_error();
     const int b = fp8w::read_gemv_device_error();
     const int c = fp8w::read_prefill_device_error();
-    return a ? a : b ? b : c;
+    const int d = fp8w::read_w8a8_device_error();
+    return a ? a : b ? b : c ? c : d;
 }
 
 int fp8w_abi_version(void) { return FP8W_ABI_VERSION; }

@@ -18,6 +18,8 @@ struct LinearArgs {
     void* y;
     int64_t group = 0;  // 0: scales[n]; else scales[n, k / group] (GEMV only)
     bool e8m0 = false;  // with group 32: scales are E8M0 bytes, not fp32
+    bool early = false; // the weights were complete before the preceding kernel
+                        // started: their copies may begin before it finishes
 };
 
 // K1: codes/scales from fp32 weights.
@@ -68,6 +70,25 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
 // K4: m > 64 (prefill shapes), per-row scales; one launch, no workspace.
 cudaError_t launch_prefill(const LinearArgs& a, cudaStream_t st);
 int read_prefill_device_error();
+
+// K5: W8A8, e4m3 activation codes x_codes[m, k] with per-token scales
+// x_scales[m] times e4m3 weight codes w_codes[n, k] with per-channel scales
+// w_scales[n]; y[m, n] in bf16 (out 1) or fp16 (out 2).  early: the weights
+// were complete before the preceding kernel started (their copies may begin
+// before it finishes).
+struct W8A8Args {
+    const uint8_t* x_codes;
+    const float* x_scales;
+    int64_t m, k, n;
+    const uint8_t* w_codes;
+    const float* w_scales;
+    const float* bias;  // may be null
+    void* y;
+    int out;
+    bool early;
+};
+cudaError_t launch_w8a8(const W8A8Args& a, cudaStream_t st);
+int read_w8a8_device_error();
 
 // Kernel-recorded wait failures (0 = none); reading clears them.
 int read_skinny_device_error();

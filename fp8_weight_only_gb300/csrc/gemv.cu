@@ -64,6 +64,8 @@ struct GemvGeom {
     uint32_t sslot_bytes;  // per-group scales: a slot's rows of scales (0 otherwise)
     int ngroups;           // per-group scales: groups a row (k / group)
     int gshift;            // per-group scales: log2 of 16-code chunks a group
+    int early;             // the weights were complete before the preceding
+                           // kernel started: stream them without waiting for it
 };
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint64_t pol) {
@@ -209,7 +211,9 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         // ---------------------------------------------------- producer --
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            pdl_wait();  // the codes may come from the previous kernel
+            // the codes (and group scales) may come from the previous kernel,
+            // unless the caller states that they were complete before it
+            if (!geo.early) pdl_wait();
             int64_t issued = 0;
             int s = 0;
             uint32_t ph = 0;
@@ -454,6 +458,7 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     const int64_t items = (rows + rp - 1) / rp;
     geo.g = 1;
     while (geo.g < kGemvWarps && items * geo.g * 2 < kGemvWarps) geo.g *= 2;
+    geo.early = a.early ? 1 : 0;
     const uint32_t smem = geo.ring_bytes + gemv_fixed_bytes(a.k, f32x, geo.staged);
 
     const int kind = !grouped ? 0 : a.e8m0 ? 2 : 1;

@@ -88,7 +88,7 @@ template <int BN, bool kBf16, bool kMx>
 __global__ void __launch_bounds__(kPThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                    const float* __restrict__ scales, const uint8_t* __restrict__ e8, const float* __restrict__ bias,
-                   uint16_t* __restrict__ y, int64_t m, int64_t n, int64_t k) {
+                   uint16_t* __restrict__ y, int64_t m, int64_t n, int64_t k, int early) {
     static_assert(!kMx || kBf16, "MX-style scales fold into bf16 weights only");
     using L = PrefillSmem<BN>;
     constexpr int kPCS = L::kPCS, kPAS = L::kPAS, kPXS = L::kPXS;
@@ -158,7 +158,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // --------------------------------------------------- code producer --
         if (lane == 0) {
             const uint64_t pol_codes = policy_evict_first();
-            pdl_wait();
+            // the codes may come from the previous kernel, unless the caller
+            // states that they were complete before it started
+            if (!early) pdl_wait();
             int64_t cs_n = 0;  // code stages issued
             for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
                 const int64_t cb = t / token_tiles;
@@ -314,7 +316,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             }
         };
         if constexpr (kMx) {
-            pdl_wait();  // the scales may come from the previous kernel
+            if (!early) pdl_wait();  // the scales may come from the previous kernel
             mx_step();
         }
         int64_t cs_n = 0, kb_base = 0;
@@ -436,7 +438,7 @@ static cudaError_t launch_bn(const LinearArgs& a, cudaStream_t st) {
     const float* sc = kMx ? nullptr : a.scales;
     const uint8_t* e8 = kMx ? reinterpret_cast<const uint8_t*>(a.scales) : nullptr;
     return cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, sc, e8, a.bias, static_cast<uint16_t*>(a.y), a.m, a.n,
-                              a.k);
+                              a.k, a.early ? 1 : 0);
 }
 
 cudaError_t launch_prefill(const LinearArgs& a, cudaStream_t st) {

@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                   const float* __restrict__ scales, const uint8_t* __restrict__ e8, const float* __restrict__ bias,
                   uint16_t* __restrict__ y, uint8_t* __restrict__ workspace, int m_rows, int m_row0, int64_t n,
-                  int64_t k, int split) {
+                  int64_t k, int split, int early) {
     static_assert(!kMx || kBf16, "MX-style scales fold into bf16 weights only");
     using L = SkinnySmem<NT>;
     constexpr int kCS = L::kCodeSlots, kXS = L::kXSlots;
@@ -335,7 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ----------------------------------------------- code-tile producer --
         if (lane == 0) {
             const uint64_t pol_stream = policy_evict_first();
-            pdl_wait();
+            // the codes may come from the previous kernel, unless the caller
+            // states that they were complete before it started
+            if (!early) pdl_wait();
             UnitCursor cu = cursor0();
             int g = 0, j = 0;  // warpgroup of the unit, and its index within the group
             int s = 0;         // == j % kCS
@@ -687,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             return row < n ? __ldg(reinterpret_cast<const uint32_t*>(e8 + row * (k >> 5) + kb * 4)) : 0x7F7F7F7Fu;
         };
         if constexpr (kMx) {
-            pdl_wait();  // the scales may come from the previous kernel
+            if (!early) pdl_wait();  // the scales may come from the previous kernel
             const int64_t u = u0 + group;
             mx_tile = u / nkb;
             mx_kb = static_cast<int>(u - mx_tile * nkb);
@@ -975,7 +977,8 @@ static cudaError_t launch_nt(const LinearArgs& a, void* workspace, int ctas, cud
         const float* sc = kMx ? nullptr : a.scales;
         const uint8_t* e8 = kMx ? reinterpret_cast<const uint8_t*>(a.scales) : nullptr;
         e = cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, sc, e8, a.bias, yp + m0 * a.n,
-                               static_cast<uint8_t*>(workspace), rows, static_cast<int>(m0), a.n, a.k, shape.split);
+                               static_cast<uint8_t*>(workspace), rows, static_cast<int>(m0), a.n, a.k, shape.split,
+                               a.early ? 1 : 0);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

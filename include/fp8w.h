@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define FP8W_ABI_VERSION 9
+#define FP8W_ABI_VERSION 10
 
 #if defined(__GNUC__)
 #define FP8W_API __attribute__((visibility("default")))
@@ -249,12 +249,25 @@ FP8W_API size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k);
  * FP8W_KERNEL_AUTO. */
 enum { FP8W_KERNEL_AUTO = 0, FP8W_KERNEL_GEMV = 1, FP8W_KERNEL_SKINNY = 2, FP8W_KERNEL_PREFILL = 3 };
 
+/*
+ * FP8W_FLAG_WEIGHTS_READY (fp8w_linear_config.flags, fp8w_linear_w8a8's
+ * flags): every write to the weight operands (codes and scales) completed
+ * before this call was enqueued -- no kernel or copy that writes them is
+ * still pending on any stream, as with weights quantised at load time and
+ * followed by a synchronisation.  The linear kernels then start streaming
+ * the codes while the preceding kernel in the stream is still finishing,
+ * instead of first waiting for it; x, bias and y are still ordered after
+ * that kernel.  Without the flag every global access waits for it.
+ */
+#define FP8W_FLAG_WEIGHTS_READY 1
+
 typedef struct fp8w_linear_config {
     int kernel;   /* FP8W_KERNEL_*; GEMV requires m == 1 and k <= 32768 */
     int ctas;     /* FP8W_KERNEL_SKINNY only: CTAs of its persistent grid,
                      1..number of SMs, or 0 to choose from the shape; must be
                      0 for the other kernels */
-    int reserved[6];  /* must be 0 */
+    int flags;    /* 0 or FP8W_FLAG_WEIGHTS_READY */
+    int reserved[5];  /* must be 0 */
 } fp8w_linear_config;
 
 /* fp8w_linear with an explicit configuration (NULL = automatic).  The
@@ -296,6 +309,59 @@ FP8W_API fp8w_status fp8w_linear_ex(const void *x, int act_dtype, int64_t m, int
 FP8W_API fp8w_status fp8w_linear_noalloc(const void *x, int act_dtype, int64_t m, int64_t k,
                                 const uint8_t *codes, const float *scales,
                                 const float *bias, int64_t n, void *y, void *stream);
+
+/*
+ * W8A8: the activations are quantised too (page "tensormux Write an FP8
+ * kernel", "Required reasoning process", steps 2, 4 and 5: per-token
+ * activation scales and per-channel weight scales, both amax / 448, a
+ * saturating e4m3 conversion, and an epilogue that multiplies the fp32
+ * accumulator by both scales; page "kadirnar/kernel-agent fp8-weights",
+ * section "Tensor cores and libraries on sm_120", names the e4m3 x e4m3
+ * tensor-core MMA as this separate target).  Two calls: fp8w_quantize_act
+ * once per activation matrix, then fp8w_linear_w8a8 for every weight that
+ * reads it.  The caller owns the activation codes and scales in between.
+ */
+
+/*
+ * fp8w_quantize_act -- per-token activation codes and scales: row i of x,
+ * widened exactly to fp32, takes fp8w_quantize's rule:
+ *   x_scales[i]   = fp32(amax_k |x[i, k]| / 448), 1.0 when that is 0
+ *   x_codes[i, k] = nearest-even, saturated e4m3 of fp32(x[i, k] / x_scales[i])
+ *   x        [m, k] bf16 or fp16 bits (act_dtype), device, 16-byte aligned.
+ *   x_codes  [m, k] uint8, device, 16-byte aligned (output).
+ *   x_scales [m] fp32, device, 4-byte aligned (output).
+ *   1 <= m <= FP8W_MAX_DIM, 16 <= k <= FP8W_MAX_K, k % 16 == 0.
+ * It runs fp8w_quantize_ex's kernel: codes and scales equal that call's on
+ * the same matrix.  Errors as fp8w_quantize_ex (FP8W_ERR_DTYPE for any
+ * act_dtype but FP8W_BF16 / FP8W_F16).
+ */
+FP8W_API fp8w_status fp8w_quantize_act(const void *x, int act_dtype, int64_t m, int64_t k,
+                              uint8_t *x_codes, float *x_scales, void *stream);
+
+/*
+ * fp8w_linear_w8a8 --
+ *   y[i, r] = round_out( x_scales[i] * w_scales[r]
+ *                        * sum_c e4m3(x_codes[i, c]) * e4m3(w_codes[r, c]) + bias[r] )
+ * on the tensor cores (tcgen05.mma kind::f8f6f4: every product of two e4m3
+ * values is exact, fp32 accumulation); in fp32 the accumulator is multiplied
+ * by x_scales[i], then fused-multiplied by w_scales[r] with bias[r] added,
+ * and rounded once to out_dtype.
+ *   x_codes  [m, k] uint8 from fp8w_quantize_act, device, 16-byte aligned.
+ *   x_scales [m] fp32, device, 4-byte aligned.
+ *   w_codes  [n, k] uint8 from fp8w_quantize, device, 16-byte aligned.
+ *   w_scales [n] fp32, device, 4-byte aligned.
+ *   bias     [n] fp32, device, 4-byte aligned, or NULL for no bias.
+ *   y        [m, n] of out_dtype (FP8W_BF16 or FP8W_F16), device, 2-byte
+ *            aligned (output); it must not overlap the inputs.
+ *   flags    0 or FP8W_FLAG_WEIGHTS_READY (for w_codes and w_scales).
+ *   1 <= m, n <= FP8W_MAX_DIM, 16 <= k <= FP8W_MAX_K, k % 16 == 0.
+ * One launch, no workspace.  Errors: FP8W_ERR_NULL, FP8W_ERR_SHAPE,
+ * FP8W_ERR_ALIGN, FP8W_ERR_DTYPE (out_dtype), FP8W_ERR_CONFIG (unknown
+ * flags), FP8W_ERR_CUDA.
+ */
+FP8W_API fp8w_status fp8w_linear_w8a8(const uint8_t *x_codes, const float *x_scales, int64_t m, int64_t k,
+                             const uint8_t *w_codes, const float *w_scales, const float *bias, int64_t n,
+                             void *y, int out_dtype, int flags, void *stream);
 
 /* Human-readable name of a status code (static string). */
 FP8W_API const char *fp8w_status_string(int status);

@@ -954,3 +954,25 @@ def test_linear_grouped_with_one_scale_per_group_equal_to_per_channel():
     yg = yg.view(torch.int16).cpu().numpy().view(np.uint16)
     cmp = compare(yg, y1, oracle.ACT_BF16)
     assert cmp["rel_l2"] <= 1e-3 and cmp["bit_equal"] >= 0.95, cmp
+
+
+# ------------------------------------------------------ weights-ready flag --
+
+@pytest.mark.parametrize("m,n,k", [(1, 4096, 4096), (1, 300, 14336), (8, 3000, 1024), (40, 640, 2048),
+                                   (96, 1000, 512)])
+def test_weights_ready_flag_gives_the_same_bits(m, n, k):
+    """FP8W_FLAG_WEIGHTS_READY only moves the code stream ahead of the
+    dependency wait: GEMV, tensor-core kernel and prefill GEMM give the same
+    bits with and without it, also right after the kernel that quantised the
+    weights (the flag's precondition then holds after a synchronisation)."""
+    c = synthetic.random_case(5100 + m, m, n, k)
+    w = torch.from_numpy(c["w"]).to(DEV)
+    codes, scales = fw.quantize(w)
+    torch.cuda.synchronize()
+    bias = torch.from_numpy(c["bias"]).to(DEV)
+    x = torch.from_numpy(c["x"].view(np.int16)).to(DEV).view(torch.bfloat16)
+    a = fw.linear(x, codes, scales, bias)
+    b = fw.linear(x, codes, scales, bias, weights_ready=True)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert fw.device_error() == 0
