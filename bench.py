@@ -885,15 +885,15 @@ def run_profile_case(args):
     x = torch.from_numpy(c["x"].view(np.int16)).to(dev).view(torch.bfloat16)
     y = torch.empty((m, c["n"]), dtype=torch.bfloat16, device=dev)
     for i in range(3):
-        fw.linear(x, reps[i % nrep], scales, bias, out=y, kernel=args.kernel, ctas=args.ctas)
+        fw.linear(x, reps[i % nrep], scales, bias, out=y, kernel=args.kernel, cluster=args.cluster, tiles=args.tiles)
     torch.cuda.synchronize()
-    out = {"case": args.profile, "kernel": args.kernel, "ctas": args.ctas, "bytes": call_bytes(m, c["n"], c["k"])}
+    out = {"case": args.profile, "kernel": args.kernel, "cluster": args.cluster, "tiles": args.tiles, "bytes": call_bytes(m, c["n"], c["k"])}
     if args.reps > 3:
         s = torch.cuda.Stream()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             for i in range(args.reps):
-                fw.linear(x, reps[i % nrep], scales, bias, out=y, kernel=args.kernel, ctas=args.ctas)
+                fw.linear(x, reps[i % nrep], scales, bias, out=y, kernel=args.kernel, cluster=args.cluster, tiles=args.tiles)
         g.replay()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -921,7 +921,8 @@ def main():
                          "(three weight replicas, so every read comes from HBM); prints per-launch times")
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--kernel", type=int, default=0, help="with --profile: 0 auto, 1 gemv, 2 tensor-core (few tokens), 3 prefill GEMM")
-    ap.add_argument("--ctas", type=int, default=0, help="with --profile: tensor-core grid size (0 = from the shape)")
+    ap.add_argument("--cluster", type=int, default=0, help="with --profile: tensor-core CTAs per cluster (0 = from the shape)")
+    ap.add_argument("--tiles", type=int, default=0, help="with --profile and --cluster: 128-channel tiles a cluster shares")
     ap.add_argument("--record-traffic", default=None, metavar="CSV",
                     help="write profiles/dram_traffic_decode_stack.json from an ncu CSV (see TRAFFIC_COMMAND)")
     args = ap.parse_args()

@@ -25,12 +25,12 @@ FP8W_F16 = 2
 FP8W_F32 = 3
 KERNEL_AUTO, KERNEL_GEMV, KERNEL_SKINNY, KERNEL_PREFILL = 0, 1, 2, 3
 
-SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_workspace_size", "fp8w_linear_ex",
+SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_ex",
            "fp8w_status_string", "fp8w_last_cuda_error", "fp8w_device_error", "fp8w_abi_version",
            "fp8w_linear_noalloc", "fp8w_dequantize", "fp8w_quantize_grouped", "fp8w_linear_grouped",
            "fp8w_quantize_mx", "fp8w_linear_mx", "fp8w_quantize_ex", "fp8w_dequantize_grouped",
            "fp8w_dequantize_mx", "fp8w_quantize_act", "fp8w_linear_w8a8")
-ABI_VERSION = 10
+ABI_VERSION = 11
 FLAG_WEIGHTS_READY = 1
 
 
@@ -41,8 +41,8 @@ class Fp8wError(RuntimeError):
 
 
 class LinearConfig(ctypes.Structure):
-    _fields_ = [("kernel", ctypes.c_int), ("ctas", ctypes.c_int), ("flags", ctypes.c_int),
-                ("reserved", ctypes.c_int * 5)]
+    _fields_ = [("kernel", ctypes.c_int), ("cluster", ctypes.c_int), ("tiles", ctypes.c_int),
+                ("flags", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
 
 
 _lib = None
@@ -68,7 +68,7 @@ def lib():
         L.fp8w_quantize_mx.restype = c.c_int
         L.fp8w_quantize_mx.argtypes = [P, c.c_int64, c.c_int64, P, P, P]
         L.fp8w_linear_mx.restype = c.c_int
-        L.fp8w_linear_mx.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P, c.c_size_t, P]
+        L.fp8w_linear_mx.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P]
         L.fp8w_dequantize_grouped.restype = c.c_int
         L.fp8w_dequantize_grouped.argtypes = [P, P, c.c_int, c.c_int64, c.c_int64, c.c_int, P, P]
         L.fp8w_dequantize_mx.restype = c.c_int
@@ -76,11 +76,9 @@ def lib():
         L.fp8w_dequantize.restype = c.c_int
         L.fp8w_dequantize.argtypes = [P, P, c.c_int64, c.c_int64, c.c_int, P, P]
         L.fp8w_linear.restype = c.c_int
-        L.fp8w_linear.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P, c.c_size_t, P]
-        L.fp8w_linear_workspace_size.restype = c.c_size_t
-        L.fp8w_linear_workspace_size.argtypes = [c.c_int64, c.c_int64, c.c_int64]
+        L.fp8w_linear.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P]
         L.fp8w_linear_ex.restype = c.c_int
-        L.fp8w_linear_ex.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P, c.c_size_t,
+        L.fp8w_linear_ex.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P,
                                      c.POINTER(LinearConfig), P]
         L.fp8w_linear_noalloc.restype = c.c_int
         L.fp8w_linear_noalloc.argtypes = [P, c.c_int, c.c_int64, c.c_int64, P, P, P, c.c_int64, P, P]
@@ -198,34 +196,13 @@ def dequantize(codes, scales, dtype=None, out=None):
     return out
 
 
-_workspaces = {}
-
-
-def workspace(device, nbytes):
-    """The zero-filled scratch buffer of a device, grown on demand.
-
-    One buffer per device: calls that may run concurrently on several streams
-    must pass their own `workspace_buffer`.  Growing allocates, so the first
-    tensor-core call on a device must not happen during CUDA-graph capture
-    (run it once eagerly first)."""
-    import torch
-    key = device.index if device.index is not None else torch.cuda.current_device()
-    ws = _workspaces.get(key)
-    if ws is None or ws.numel() < nbytes:
-        if torch.cuda.is_current_stream_capturing():
-            raise Fp8wError(7, "fp8w workspace must be allocated before CUDA-graph capture: "
-                               "run the call once eagerly first")
-        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
-        _workspaces[key] = ws
-    return ws
-
-
-def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_buffer=None, ctas=0,
+def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, cluster=0, tiles=0,
            weights_ready=False):
     """y[M, N] = round(scale[n] * sum_k x[m, k] * e4m3(codes[n, k]) + bias[n]).
 
-    kernel and ctas (the tensor-core kernel's grid size, 0 = from the shape)
-    override the automatic launch choice, for tests and tuning.
+    kernel, and for the tensor-core kernel cluster (CTAs per thread-block
+    cluster) with tiles (128-channel tiles a cluster shares), override the
+    automatic launch choice, for tests and tuning (0, 0 = from the shape).
     weights_ready: every write to codes and scales has completed before this
     call (FP8W_FLAG_WEIGHTS_READY): the kernels stream the codes without
     waiting for the preceding kernel in the stream.  Per-row scales only."""
@@ -250,15 +227,8 @@ def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_
         elif out.shape != (m, n) or out.dtype != x.dtype or not out.is_contiguous():
             raise ValueError("out must be a contiguous [M, N] tensor of x's dtype")
         if mx:
-            L = lib()
-            # the GEMV and the prefill GEMM need no workspace
-            need = 0 if (m == 1 and k % 512 == 0 and k <= 32768) or m > 64 else \
-                L.fp8w_linear_workspace_size(max(m, 2), n, k)
-            ws = None
-            if need:
-                ws = workspace_buffer if workspace_buffer is not None else workspace(x.device, need)
-            _check(L.fp8w_linear_mx(_ptr(x), _act(x.dtype), m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
-                                    _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(), _stream(x)))
+            _check(lib().fp8w_linear_mx(_ptr(x), _act(x.dtype), m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
+                                        _ptr(out), _stream(x)))
         else:
             _check(lib().fp8w_linear_grouped(_ptr(x), _act(x.dtype), m, k, _ptr(codes), _ptr(scales),
                                              k // scales.shape[1], _ptr(bias), n, _ptr(out), _stream(x)))
@@ -275,18 +245,12 @@ def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, workspace_
     act = _act(x.dtype)
     L = lib()
     stream = _stream(x)
-    need = L.fp8w_linear_workspace_size(min(max(m, 2), 64) if kernel == KERNEL_SKINNY else m, n, k)
-    ws = None
-    if need:
-        ws = workspace_buffer if workspace_buffer is not None else workspace(x.device, need)
-    ws_ptr, ws_bytes = (_ptr(ws), ws.numel()) if ws is not None else (None, 0)
-    if kernel == KERNEL_AUTO and ctas == 0 and not weights_ready:
-        st = L.fp8w_linear(_ptr(x), act, m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
-                           _ptr(out), ws_ptr, ws_bytes, stream)
+    if kernel == KERNEL_AUTO and cluster == 0 and not weights_ready:
+        st = L.fp8w_linear(_ptr(x), act, m, k, _ptr(codes), _ptr(scales), _ptr(bias), n, _ptr(out), stream)
     else:
-        cfg = LinearConfig(kernel, ctas, FLAG_WEIGHTS_READY if weights_ready else 0)
+        cfg = LinearConfig(kernel, cluster, tiles, FLAG_WEIGHTS_READY if weights_ready else 0)
         st = L.fp8w_linear_ex(_ptr(x), act, m, k, _ptr(codes), _ptr(scales), _ptr(bias), n,
-                              _ptr(out), ws_ptr, ws_bytes, ctypes.byref(cfg), stream)
+                              _ptr(out), ctypes.byref(cfg), stream)
     _check(st)
     return out
 

@@ -60,7 +60,6 @@ fp8w_status fp8w_quantize_ex(const void* w, int w_dtype, int64_t n, int64_t k, u
                        "fp8w_quantize_ex launch");
 }
 
-static size_t skinny_ws(void);
 // m > 64 runs the prefill GEMM.
 static bool use_prefill(int64_t m) { return m > 64; }
 
@@ -94,8 +93,7 @@ fp8w_status fp8w_quantize_mx(const float* w, int64_t n, int64_t k, uint8_t* code
 }
 
 fp8w_status fp8w_linear_mx(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
-                           const uint8_t* scales, const float* bias, int64_t n, void* y, void* workspace,
-                           size_t workspace_bytes, void* stream) {
+                           const uint8_t* scales, const float* bias, int64_t n, void* y, void* stream) {
     const float* sp = reinterpret_cast<const float*>(scales);  // E8M0 bytes, passed through
     fp8w_status st = check_linear(x, act_dtype, m, k, codes, sp, bias, n, y);
     if (st != FP8W_OK) return st;
@@ -109,14 +107,10 @@ fp8w_status fp8w_linear_mx(const void* x, int act_dtype, int64_t m, int64_t k, c
     if (m == 1 && k % 512 == 0 && fp8w::gemv_supports(k))
         return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear_mx gemv launch");
     // otherwise a tensor-core kernel, which folds the scales into bf16 weights:
-    // the prefill GEMM beyond 64 tokens (no workspace), the skinny kernel below
+    // the prefill GEMM beyond 64 tokens, the skinny kernel below
     if (act_dtype != FP8W_BF16) return FP8W_ERR_DTYPE;
     if (use_prefill(m)) return cuda_status(fp8w::launch_prefill(a, s), "fp8w_linear_mx prefill launch");
-    if (!workspace || !aligned(workspace, 256)) return FP8W_ERR_WORKSPACE;
-    const size_t need = skinny_ws();
-    if (need == 0) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear_mx device query");
-    if (workspace_bytes < need) return FP8W_ERR_WORKSPACE;
-    return cuda_status(fp8w::launch_skinny(a, workspace, 0, s), "fp8w_linear_mx tensor-core launch");
+    return cuda_status(fp8w::launch_skinny(a, nullptr, s), "fp8w_linear_mx tensor-core launch");
 }
 
 fp8w_status fp8w_dequantize(const uint8_t* codes, const float* scales, int64_t n, int64_t k, int out_dtype,
@@ -152,23 +146,12 @@ fp8w_status fp8w_dequantize_mx(const uint8_t* codes, const uint8_t* scales, int6
     return dequant_grouped(codes, scales, true, 32, n, k, out_dtype, w, stream, "fp8w_dequantize_mx launch");
 }
 
-static size_t skinny_ws(void) {
-    int sms = 0;
-    if (fp8w::device_sm_count(sms) != cudaSuccess) return 0;
-    return fp8w::skinny_workspace_size(sms);
-}
-
 // m == 1 runs the GEMV unless its x does not fit in shared memory.
 static bool use_gemv(int64_t m, int64_t k) { return m == 1 && fp8w::gemv_supports(k); }
 
-size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k) {
-    (void)n;
-    return use_gemv(m, k) || use_prefill(m) ? 0 : skinny_ws();
-}
-
 fp8w_status fp8w_linear_ex(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
-                           const float* scales, const float* bias, int64_t n, void* y, void* workspace,
-                           size_t workspace_bytes, const fp8w_linear_config* config, void* stream) {
+                           const float* scales, const float* bias, int64_t n, void* y,
+                           const fp8w_linear_config* config, void* stream) {
     fp8w_status st = check_linear(x, act_dtype, m, k, codes, scales, bias, n, y);
     if (st != FP8W_OK) return st;
     int kernel = config ? config->kernel : FP8W_KERNEL_AUTO;
@@ -177,8 +160,9 @@ fp8w_status fp8w_linear_ex(const void* x, int act_dtype, int64_t m, int64_t k, c
     if (kernel == FP8W_KERNEL_GEMV && !use_gemv(m, k)) return FP8W_ERR_CONFIG;
     if (kernel != FP8W_KERNEL_GEMV && kernel != FP8W_KERNEL_SKINNY && kernel != FP8W_KERNEL_PREFILL)
         return FP8W_ERR_CONFIG;
-    const int ctas = config ? config->ctas : 0;
-    if (ctas < 0 || (ctas != 0 && kernel != FP8W_KERNEL_SKINNY)) return FP8W_ERR_CONFIG;
+    const int cluster = config ? config->cluster : 0, tiles = config ? config->tiles : 0;
+    if ((cluster == 0) != (tiles == 0) || cluster < 0 || tiles < 0) return FP8W_ERR_CONFIG;
+    if (cluster != 0 && kernel != FP8W_KERNEL_SKINNY) return FP8W_ERR_CONFIG;
     const int flags = config ? config->flags : 0;
     if (flags & ~FP8W_FLAG_WEIGHTS_READY) return FP8W_ERR_CONFIG;
     if (config)
@@ -189,40 +173,22 @@ fp8w_status fp8w_linear_ex(const void* x, int act_dtype, int64_t m, int64_t k, c
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (kernel == FP8W_KERNEL_GEMV) return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear gemv launch");
     if (kernel == FP8W_KERNEL_PREFILL) return cuda_status(fp8w::launch_prefill(a, s), "fp8w_linear prefill launch");
-    if (!workspace || !aligned(workspace, 256)) return FP8W_ERR_WORKSPACE;
-    const size_t need = skinny_ws();
-    if (need == 0) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear device query");
-    if (workspace_bytes < need) return FP8W_ERR_WORKSPACE;
-    if (ctas != 0) {
-        int sms = 0;
-        if (fp8w::device_sm_count(sms) != cudaSuccess) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear device query");
-        if (ctas > sms) return FP8W_ERR_CONFIG;
+    if (cluster != 0) {
+        const fp8w::SkinnyShape shape{cluster, tiles};
+        if (!fp8w::skinny_shape_valid(shape, m, k)) return FP8W_ERR_CONFIG;
+        return cuda_status(fp8w::launch_skinny(a, &shape, s), "fp8w_linear tensor-core launch");
     }
-    return cuda_status(fp8w::launch_skinny(a, workspace, ctas, s), "fp8w_linear tensor-core launch");
+    return cuda_status(fp8w::launch_skinny(a, nullptr, s), "fp8w_linear tensor-core launch");
 }
 
 fp8w_status fp8w_linear(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
-                        const float* scales, const float* bias, int64_t n, void* y, void* workspace,
-                        size_t workspace_bytes, void* stream) {
-    return fp8w_linear_ex(x, act_dtype, m, k, codes, scales, bias, n, y, workspace, workspace_bytes, nullptr,
-                          stream);
+                        const float* scales, const float* bias, int64_t n, void* y, void* stream) {
+    return fp8w_linear_ex(x, act_dtype, m, k, codes, scales, bias, n, y, nullptr, stream);
 }
 
 fp8w_status fp8w_linear_noalloc(const void* x, int act_dtype, int64_t m, int64_t k, const uint8_t* codes,
                                 const float* scales, const float* bias, int64_t n, void* y, void* stream) {
-    fp8w_status st = check_linear(x, act_dtype, m, k, codes, scales, bias, n, y);
-    if (st != FP8W_OK) return st;
-    fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, scales, bias, y};
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (use_gemv(m, k)) return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear_noalloc gemv launch");
-    if (use_prefill(m)) return cuda_status(fp8w::launch_prefill(a, s), "fp8w_linear_noalloc prefill launch");
-    const size_t need = skinny_ws();
-    if (need == 0) return cuda_status(cudaErrorInvalidDevice, "fp8w_linear_noalloc device query");
-    if (need > fp8w::static_scratch_bytes()) return FP8W_ERR_SCRATCH;
-    void* scratch = nullptr;
-    const fp8w_status ss = cuda_status(fp8w::static_scratch(&scratch, s), "fp8w_linear_noalloc scratch set-up");
-    if (ss != FP8W_OK) return ss;
-    return cuda_status(fp8w::launch_skinny(a, scratch, 0, s), "fp8w_linear_noalloc tensor-core launch");
+    return fp8w_linear_ex(x, act_dtype, m, k, codes, scales, bias, n, y, nullptr, stream);
 }
 
 fp8w_status fp8w_quantize_act(const void* x, int act_dtype, int64_t m, int64_t k, uint8_t* x_codes, float* x_scales,
@@ -255,10 +221,6 @@ const char* fp8w_status_string(int status) {
         case FP8W_ERR_DTYPE: return "activation dtype must be FP8W_BF16 or FP8W_F16";
         case FP8W_ERR_CUDA: return "CUDA call failed (see fp8w_last_cuda_error)";
         case FP8W_ERR_CONFIG: return "invalid explicit launch configuration";
-        case FP8W_ERR_WORKSPACE: return "workspace NULL, not 256-byte aligned or smaller than fp8w_linear_workspace_size";
-        case FP8W_ERR_SCRATCH:
-            return "this device needs more scratch than fp8w_linear_noalloc's static FP8W_STATIC_SCRATCH_BYTES "
-                   "(more SMs than it covers): use fp8w_linear with a workspace";
         default: return "unknown status";
     }
 }

@@ -51,16 +51,16 @@ cudaError_t launch_dequantize_grouped(const uint8_t* codes, const void* scales, 
 cudaError_t launch_gemv(const LinearArgs& a, cudaStream_t st);
 bool gemv_supports(int64_t k);
 
-// K3: any m (32-row slabs, one launch each); needs a workspace of
-// skinny_workspace_size(sms) bytes, zero-filled before its first use.
-// ctas > 0 fixes the grid size (1..sms), 0 picks it from the shape.
-cudaError_t launch_skinny(const LinearArgs& a, void* workspace, int ctas, cudaStream_t st);
-size_t skinny_workspace_size(int sms);
-// Library-owned scratch of fp8w_linear_noalloc (a static device array of
-// static_scratch_bytes()); the first call per device looks up its address and
-// enqueues a clear of its counters on st.
-cudaError_t static_scratch(void** ptr, cudaStream_t st);
-size_t static_scratch_bytes();
+// K3: any m (16-, 32- or 64-token launches, 64-row slabs beyond); no
+// workspace.  Launch shape: clusters of `cl` CTAs (1..16), each taking `tpc`
+// consecutive 128-channel tiles; forced == nullptr picks it from the shape.
+struct SkinnyShape {
+    int cl;
+    int64_t tpc;
+};
+cudaError_t launch_skinny(const LinearArgs& a, const SkinnyShape* forced, cudaStream_t st);
+SkinnyShape skinny_shape(int64_t n, int64_t k, const int* active, int nt);
+bool skinny_shape_valid(const SkinnyShape& sh, int64_t m, int64_t k);
 cudaError_t device_sm_count(int& sms);
 // 2-D tiled tensor map with 128-byte swizzle: `inner` x `outer` elements,
 // rows of `row_bytes`, boxes of box_inner x box_outer.

@@ -1,4 +1,4 @@
-// skinny.cu -- kernel K3: the M <= 32 linear layer on the tcgen05 tensor cores,
+// skinny.cu -- kernel K3: the M <= 64 linear layer on the tcgen05 tensor cores,
 // "swap-AB": the weight channels are the 128-row A operand, the tokens the
 // narrow B operand.
 //
@@ -8,22 +8,23 @@
 // split-K so that all the GPU streams the weight).  That design targets
 // mma.sync on sm_80..sm_120; this one is built for sm_103a:
 //
-//  * Persistent grid, at most one CTA per SM.  The work is the list of units
-//    (channel tile of 128, k-block of 128).  Three launch shapes:
-//    - whole tiles, one CTA each, when the tile count nearly fills the GPU;
-//    - split: fewer tiles than SMs, each tile's k-blocks divided evenly over
-//      a thread-block cluster of 2, 4 or 8 CTAs, whose fp32 partials are
-//      summed through distributed shared memory at the end (each CTA adds
-//      up, in rank order, a slice of the tile's channels from every rank);
-//    - stream-K: more tiles than SMs; CTA c takes the contiguous units
-//      [c*U/P, (c+1)*U/P), and a tile that straddles CTAs is finished by the
-//      last contributor: partial fp32 tiles go to a caller-provided workspace
-//      and are summed in CTA order (deterministic); no CTA waits on another.
-//    A CTA takes its units in order, so the piece at the start of its range
-//    (the end of a tile another CTA began) is done first and published
-//    early; the CTA holding the start of that tile finishes it last and, as
-//    every other contributor has arrived by then, sums their partials
-//    straight from its registers without publishing its own.
+//  * At most one CTA per SM.  The work is the list of units (channel tile
+//    of 128, k-block of 128).  The grid is made of thread-block clusters of
+//    `cl` CTAs, each cluster taking `tpc` consecutive tiles and each of its
+//    ranks an even, contiguous share of their units:
+//    - cl = 1: whole tiles, tpc of them a CTA (one when they nearly fill
+//      the GPU);
+//    - tpc = 1, cl > 1: few tiles, each split over a cluster;
+//    - tpc > 1, cl > 1: more tiles than SMs (or an uneven count), shared.
+//    A rank takes the whole tiles of its range first and the one or two
+//    tiles it shares with neighbouring ranks last, holding their fp32
+//    accumulators in TMEM; at the end it stages them in its idle code ring,
+//    and after a cluster barrier every contributor of a shared tile adds up
+//    its block of the tile's channels over all contributors' partials, in
+//    rank order, through distributed shared memory.  Nothing is written to
+//    global memory but y, no state outlives the launch, and the sums do not
+//    depend on timing.  The host picks the shape with the fewest units per
+//    CTA among those whose clusters all fit on the GPU at once.
 //  * Warp 0 streams each unit's 128 x 128 code tile with TMA (128-byte
 //    swizzle; rows past N and k past K read as zeros) into the code ring of
 //    one of three dequantising warpgroups (units are dealt round-robin);
@@ -56,7 +57,7 @@
 //  * One epilogue warpgroup reads a finished tile's two accumulators with
 //    tcgen05.ld (thread r holds channel r for every token), adds them in a
 //    fixed order while the next tile accumulates, and stores
-//    y = round(fma(acc, scale, bias)) or, for a split tile, its partial.
+//    y = round(fma(acc, scale, bias)), or holds a shared tile's partial.
 //  * The control loops divide nothing per unit: a cursor walks (tile,
 //    k-block), since a 64-bit division costs a lone thread hundreds of cycles.
 //
@@ -139,52 +140,64 @@ struct SkinnySmem {
     }
 };
 
-// Workspace: [kMaxCtas arrival counters (uint32)][2 partial-tile slots per
-// CTA, each 128 channels x kMaxNT fp32, channel-major].  The counters must
-// be zero before the first call; every call leaves them zero.  Their region
-// has a fixed size, so calls with different grids never overlap it.
-constexpr int kMaxCtas = 1024;
-constexpr size_t kWsCountersBytes = kMaxCtas * 4;
-__host__ __device__ constexpr size_t ws_slot_floats() { return static_cast<size_t>(kMaxNT) * kTileN; }
-constexpr size_t skinny_workspace_bytes(int p) {
-    return kWsCountersBytes + 2 * static_cast<size_t>(p) * ws_slot_floats() * 4;
-}
-// Tokens whose cluster partials one thread loads before adding them up.
+// Partial tiles a rank holds at the end: at most two (the tile its range
+// starts in and the one it ends in), each 128 channels x NT tokens of fp32,
+// token-major, staged in the code ring once every unit is done.
+constexpr int kMaxHeld = 2;
+// Cluster sizes up to 16 (beyond 8 where the device allows non-portable
+// clusters); the finish reads contributors' partials 8 ranks at a time.
+constexpr int kMaxCluster = 16;
+constexpr int kRankGroup = 8;
+// Outputs whose remote partials one thread loads before adding them up.
 constexpr int kRedBatch = 4;
 
-// A split CTA takes at least this many units, so a small matrix is not cut
-// into more partial tiles than it has k-blocks to share.
-constexpr int64_t kMinUnitsPerCta = 4;
-// Contributors' partials are read this many at a time, all loads in flight
-// before any add.
-constexpr int kFixupBatch = 2;
-
-struct Partition {
-    int64_t units, p, nkb;
-    __device__ __forceinline__ int64_t begin(int64_t c) const { return c * units / p; }
-    // CTA whose range holds unit u
-    __device__ __forceinline__ int64_t owner(int64_t u) const {
-        int64_t c = u * p / units;
-        while (c + 1 < p && begin(c + 1) <= u) ++c;
-        while (c > 0 && begin(c) > u) --c;
-        return c;
+// The units of one cluster: its t_g tiles, tile-major, cluster-local index
+// (32-bit: the host keeps a cluster's units below 2^24); rank r takes the
+// contiguous range [begin(r), begin(r + 1)).
+struct ClusterRange {
+    int units;
+    int c;
+    __device__ __forceinline__ int begin(int r) const { return r * units / c; }
+    // the last rank whose range starts at or before u (every rank has units,
+    // so this is the rank whose range holds u)
+    __device__ __forceinline__ int owner(int u) const {
+        int r = u * c / units;
+        while (r + 1 < c && begin(r + 1) <= u) ++r;
+        while (r > 0 && begin(r) > u) --r;
+        return r;
     }
 };
 
-// Walks a CTA's units in order without divisions: (tile, kb) of the current
-// unit.
+// Walks a rank's units in processing order without divisions: the range
+// [a, b) (cluster-local units) is taken as [f, b) then [a, f), f the first
+// tile boundary at or after a (or b), so the whole tiles come first and the
+// one or two tiles the range shares with its neighbours come last; their
+// accumulators are then held until the cluster adds them up.  `tile` is the
+// global tile index.
 struct UnitCursor {
     int it;
     int tile, kb, nkb;
+    int u, a, f, b;
+    int a_tile, a_kb;  // tile and k-block of unit a
     __device__ __forceinline__ void next() {
         ++it;
+        ++u;
+        if (u == b && f > a) {
+            u = a;
+            tile = a_tile;
+            kb = a_kb;
+            return;
+        }
         if (++kb == nkb) {
             kb = 0;
             ++tile;
         }
     }
-    // units left in the current tile within the CTA's range
-    __device__ __forceinline__ int seg_left(int iters) const { return min(nkb - kb, iters - it); }
+    // units left in the current segment (the current tile within the run)
+    __device__ __forceinline__ int seg_left() const {
+        const int left = (u >= f ? b : f) - u;
+        return left < nkb - kb ? left : nkb - kb;
+    }
 };
 
 template <bool kBf16>
@@ -222,14 +235,25 @@ __device__ __forceinline__ void record_error(int code, volatile int* abort_flag,
 
 __device__ __forceinline__ void epilogue_bar() { asm volatile("bar.sync %0, 128;" ::"n"(kBarEpilogue) : "memory"); }
 
-// Arrival count of a split tile: release orders this CTA's partial stores
-// (made visible to this thread by the preceding CTA barrier) before the
-// increment; acquire orders the last contributor's reads after it.
-__device__ __forceinline__ uint32_t arrive_acq_rel(uint32_t* counter) {
-    uint32_t old;
-    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(counter) : "memory");
-    return old;
+// A cluster rank's fp32 partial, read after the cluster barrier that made it
+// visible (no compiler memory clobber, so loads of several ranks and tokens
+// can be in flight together; volatile keeps them after the barrier).
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
 }
+
+// One tile this rank shares with others of its cluster, as the finish sees
+// it from one epilogue thread: the thread adds up channel `col` (or none)
+// for tokens tok0, tok0 + tstep, ... over contributors r_lo .. r_lo + J - 1;
+// lo_slot is the staging slot of contributor r_lo's partial (the others'
+// is 0: the tile holds their first unit).
+struct SharedTile {
+    int64_t col;
+    int r_lo, J, tok0, tstep, lo_slot;
+    float sc, b;
+};
 
 // kMx: the weight carries E8M0 scale bytes e8[n, k / 32] (bf16 activations,
 // k % 128 == 0) instead of per-row scales; they enter the dequantised
@@ -238,8 +262,8 @@ template <int NT, bool kBf16, bool kMx = false>
 __global__ void __launch_bounds__(kThreads, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                   const float* __restrict__ scales, const uint8_t* __restrict__ e8, const float* __restrict__ bias,
-                  uint16_t* __restrict__ y, uint8_t* __restrict__ workspace, int m_rows, int m_row0, int64_t n,
-                  int64_t k, int split, int early) {
+                  uint16_t* __restrict__ y, int m_rows, int m_row0, int64_t n, int64_t k, int cl, int tpc,
+                  int early) {
     static_assert(!kMx || kBf16, "MX-style scales fold into bf16 weights only");
     using L = SkinnySmem<NT>;
     constexpr int kCS = L::kCodeSlots, kXS = L::kXSlots;
@@ -266,27 +290,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto x_smem = [&](int s) { return L::kXOff + s * L::kXStageBytes; };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 8);
     volatile int* ep_abort = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 12);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t tiles = (n + kTileN - 1) / kTileN;
     const int64_t nkb = (k + kBlockK - 1) / kBlockK;
-    const Partition part{tiles * nkb, static_cast<int64_t>(gridDim.x), nkb};
-    const int64_t c = blockIdx.x;
-    // split launches: cluster c / split takes tile c / split, its rank c % split
-    // an even share of the k-blocks; otherwise the contiguous range of units
-    const int64_t u0 = split > 1 ? (c / split) * nkb + (c % split) * nkb / split : part.begin(c);
-    const int64_t u1 = split > 1 ? (c / split) * nkb + (c % split + 1) * nkb / split : part.begin(c + 1);
-    const int iters = static_cast<int>(u1 - u0);
-    const int64_t t_first = u0 / nkb;
-    const int kb_first = static_cast<int>(u0 - t_first * nkb);
+    // cluster g (cl CTAs) takes tiles [g * tpc, min((g + 1) * tpc, tiles));
+    // its rank an even, contiguous share of their units (global unit index =
+    // tile * nkb + k-block)
+    const int g = static_cast<int>(blockIdx.x) / cl;
+    const int rank = static_cast<int>(blockIdx.x) - g * cl;
+    const int gt0 = g * tpc;  // the cluster's first tile
+    const int gtiles = static_cast<int>(tiles - gt0 < tpc ? tiles - gt0 : tpc);
+    const int nkb32 = static_cast<int>(nkb);
+    const ClusterRange cr{gtiles * nkb32, cl};
+    // this rank's cluster-local units [ua, ub); uf: the first tile boundary at
+    // or after ua, capped at ub
+    const int ua = cr.begin(rank), ub = cr.begin(rank + 1);
+    const int iters = ub - ua;
+    const int ua_tile = ua / nkb32, ua_kb = ua - ua_tile * nkb32;
+    const int ua_up = ua_kb == 0 ? ua : ua + (nkb32 - ua_kb);
+    const int uf = ua_up < ub ? ua_up : ub;
     auto cursor0 = [=]() {
         UnitCursor cu;
         cu.it = 0;
-        cu.nkb = static_cast<int>(nkb);
-        cu.tile = static_cast<int>(t_first);
-        cu.kb = kb_first;
+        cu.nkb = nkb32;
+        cu.a = ua;
+        cu.f = uf;
+        cu.b = ub;
+        cu.a_tile = gt0 + ua_tile;
+        cu.a_kb = ua_kb;
+        if (uf < ub) {
+            cu.u = uf;
+            cu.tile = gt0 + uf / nkb32;
+            cu.kb = 0;
+        } else {
+            cu.u = ua;
+            cu.tile = cu.a_tile;
+            cu.kb = ua_kb;
+        }
         return cu;
     };
 
@@ -330,6 +372,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem = *tmem_slot;
     }
+
+    // the tiles this rank shares, as its epilogue thread finishes them (set
+    // by the epilogue warps, used after every role is done)
+    // (two named entries: an array indexed at run time would live in local memory)
+    SharedTile sh0{-1, 0, 0, 0, 0, 1, 0.0f, 0.0f}, sh1{-1, 0, 0, 0, 0, 1, 0.0f, 0.0f};
+    int nshared = 0;
 
     if (warp == 0) {
         // ----------------------------------------------- code-tile producer --
@@ -414,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc = idesc_f16(kBf16, NT);
         UnitCursor cu = cursor0();
         int seg = 0, jj = 0;
-        int seg_len = iters > 0 ? cu.seg_left(iters) : 0;
+        int seg_len = iters > 0 ? cu.seg_left() : 0;
         int ra = w, rx = w;          // slots of this warp's next unit: A (unit % 6), activation (unit % kXS)
         uint32_t pa = 0, px = 0;     // their phase parities
         bool mine_in_seg = false;    // this warp has issued into the segment's accumulator
@@ -479,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mine_in_seg = false;
                 ++seg;
                 jj = 0;
-                if (it + 1 < iters) seg_len = cu.seg_left(iters);
+                if (it + 1 < iters) seg_len = cu.seg_left();
             }
         }
         // every MMA issued above completes before TMEM is released
@@ -491,31 +539,79 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;  // channel within the tile == TMEM lane
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-        const int etid = threadIdx.x - 32 * kFirstEpilogueWarp;  // 0..127
-        uint32_t* counters = reinterpret_cast<uint32_t*>(workspace);
-        float* slots = reinterpret_cast<float*>(workspace + kWsCountersBytes);
-        pdl_wait();  // the workspace and y may still be in use by the previous grid
+        pdl_wait();  // y may still be in use by the previous grid
+        // The finish of the tiles this rank shares (the tiles of its first and
+        // last units, when it does not cover them whole): their contributors
+        // r_lo .. r_hi split each tile's channels into contiguous blocks,
+        // contributor j taking the j-th; this thread takes one channel of the
+        // block for a stride of tokens (a warp reads and writes consecutive
+        // channels).  Worked out now, and its scale and bias read now, while
+        // the MMAs run: at the end those reads would wait behind the weight
+        // stream of the other CTAs.
+        if (cl > 1 && iters > 0) {
+            const int etid = r;  // 0..127
+            const int ub_tile = (ub - 1) / nkb32;
+            for (int side = 0; side < 2; ++side) {
+                const int tl = side == 0 ? ua_tile : ub_tile;
+                if (side == 1 && tl == ua_tile) break;
+                const int t_lo = tl * nkb32, t_hi = t_lo + nkb32;
+                if (ua <= t_lo && ub >= t_hi) continue;  // covered whole
+                SharedTile& st = nshared++ == 0 ? sh0 : sh1;
+                st.r_lo = cr.owner(t_lo);
+                st.J = cr.owner(t_hi - 1) - st.r_lo + 1;
+                st.lo_slot = cr.begin(st.r_lo) == t_lo ? 0 : 1;
+                const int j = rank - st.r_lo;
+                const int c0 = j * kTileN / st.J, c1 = (j + 1) * kTileN / st.J;
+                const int my_nch = c1 - c0;
+                st.tstep = kTileN / my_nch;
+                st.tok0 = etid / my_nch;
+                const int ci = etid - st.tok0 * my_nch;
+                st.col = -1;
+                st.sc = 0.0f;
+                st.b = 0.0f;
+                if (st.tok0 < st.tstep) {
+                    const int64_t col = static_cast<int64_t>(gt0 + tl) * kTileN + c0 + ci;
+                    if (col < n) {
+                        st.col = col;
+                        st.sc = kMx ? 1.0f : scales[col];
+                        st.b = bias ? bias[col] : 0.0f;
+                    }
+                }
+            }
+        }
+        // tokens [16h, 16h + 16) of the accumulators of buffer d, warp 0's
+        // first; a warp with no unit in the segment (a one-unit segment)
+        // wrote nothing there
+        auto load_acc = [&](int d, int h, int it0, int seg_len, float (&acc)[16]) {
+#pragma unroll
+            for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kMmaWarps; ++w) {
+                if (seg_len < kMmaWarps && ((it0 + kMmaWarps - w) % kMmaWarps) >= seg_len) continue;
+                uint32_t v[16];
+                tmem_ld_x16(lane_addr + kDCol0 + (w * L::kDBuf + d) * NT + h * 16, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 16; ++q) acc[q] += __uint_as_float(v[q]);
+            }
+        };
+        // a tile this rank shares with others stays in its accumulator until
+        // every unit is done (such tiles are processed last): buffer, first
+        // unit, length and staging slot (0: the tile of the rank's first unit)
+        // (two entries in registers: the arrays would live in local memory)
+        int hd0 = 0, hit0 = 0, hlen0 = 0, hslot0 = 0, hd1 = 0, hit1 = 0, hlen1 = 0, hslot1 = 0;
+        int nheld = 0;
         int seg = 0;
         UnitCursor cu = cursor0();
         for (int it = 0; it < iters; ++seg) {
             // segment: the units of one tile, contiguous in processing order
-            const int seg_len = cu.seg_left(iters);
+            const int seg_len = cu.seg_left();
             const int64_t tile = cu.tile;
             const bool whole = cu.kb == 0 && seg_len == cu.nkb;
             const int it0 = it;
             it += seg_len;
             for (int jj = 0; jj < seg_len; ++jj) cu.next();
             const int d = seg % L::kDBuf;
-            int64_t c_lo = 0, c_hi = 0;
-            bool all_in = false;
-            if (!whole && split == 1) {
-                c_lo = part.owner(tile * nkb);
-                c_hi = part.owner((tile + 1) * nkb - 1);
-                // every other contributor already arrived: this CTA finishes
-                // the tile from its registers (tested while the MMAs run, and
-                // again once the accumulator is ready)
-                if (etid == 0) all_in = ld_acquire_gpu(&counters[c_lo]) == static_cast<uint32_t>(c_hi - c_lo);
-            }
             bool ok = true;
             for (int w = 0; w < kMmaWarps; ++w)
                 ok = mbar_wait_warp(dready(w, d), static_cast<uint32_t>((seg / L::kDBuf) & 1), abort_flag) && ok;
@@ -523,165 +619,63 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) *ep_abort = 1;
                 record_error(kErrWaitMma, abort_flag);
             }
-            if (!whole && split == 1 && etid == 0) {
-                if (!all_in) all_in = ld_acquire_gpu(&counters[c_lo]) == static_cast<uint32_t>(c_hi - c_lo);
-                *last_flag = all_in ? 1 : 0;
-            }
             // the four epilogue warps leave together (ep_abort is written only
             // by them, before this barrier), so their named barriers stay matched
             epilogue_bar();
             if (*ep_abort) break;
-            const bool early = !whole && split == 1 && *last_flag;
             tc_fence_after();
+            if (!whole) {
+                const int slot = tile == gt0 + ua_tile ? 0 : 1;
+                if (nheld == 0) {
+                    hd0 = d, hit0 = it0, hlen0 = seg_len, hslot0 = slot;
+                } else {
+                    hd1 = d, hit1 = it0, hlen1 = seg_len, hslot1 = slot;
+                }
+                ++nheld;
+                continue;
+            }
             const int64_t col = tile * kTileN + r;
             const float sc = kMx ? 1.0f : col < n ? scales[col] : 0.0f;
             const float b = (bias && col < n) ? bias[col] : 0.0f;
-            const int64_t slot = 2 * c + (tile == t_first ? 0 : 1);
-            float* mine = slots + slot * ws_slot_floats() + r * kMaxNT;
-            const bool lo_first = !whole && part.begin(c_lo) == tile * nkb;
-            // every contributor after c_lo starts inside this tile (its first
-            // slot); c_lo used its first slot only if it starts exactly at the
-            // tile's first unit
-            auto slot_of = [&](int64_t cc) -> const float4* {
-                const int64_t cs = 2 * cc + ((cc > c_lo || lo_first) ? 0 : 1);
-                return reinterpret_cast<const float4*>(slots + cs * ws_slot_floats() + r * kMaxNT);
-            };
             // 16 tokens at a time, only as many as there are rows
 #pragma unroll 1
             for (int h = 0; h < NT / 16 && h * 16 < m_rows; ++h) {
-                // the MMA warps' accumulators, warp 0's first; a warp with no
-                // unit in the segment (a one-unit segment) wrote nothing
                 float acc[16];
-#pragma unroll
-                for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
-#pragma unroll
-                for (int w = 0; w < kMmaWarps; ++w) {
-                    if (seg_len < kMmaWarps && ((it0 + kMmaWarps - w) % kMmaWarps) >= seg_len) continue;
-                    uint32_t v[16];
-                    tmem_ld_x16(lane_addr + kDCol0 + (w * L::kDBuf + d) * NT + h * 16, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) acc[q] += __uint_as_float(v[q]);
-                }
-                if (split > 1) {
-                    // this rank's partial tile, token-major, into the free code ring
-                    float* pt = reinterpret_cast<float*>(smem + L::kCodesOff);
+                load_acc(d, h, it0, seg_len, acc);
+                if (col < n) {
 #pragma unroll
                     for (int q = 0; q < 16; ++q)
-                        if (h * 16 + q < m_rows) pt[(h * 16 + q) * kTileN + r] = acc[q];
-                } else if (whole || early) {
-                    if (early) {
-                        // contributors in CTA order, this CTA's own partial from
-                        // registers: the same sum the publishing path forms
-                        float tot[16];
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) tot[q] = 0.0f;
-                        for (int64_t cc = c_lo; cc <= c_hi; ++cc) {
-                            if (cc == c) {
-#pragma unroll
-                                for (int q = 0; q < 16; ++q) tot[q] += acc[q];
-                                continue;
-                            }
-                            float4 v[4];
-#pragma unroll
-                            for (int q = 0; q < 4; ++q)
-                                v[q] = h * 16 + 4 * q < m_rows ? __ldcg(slot_of(cc) + h * 4 + q)
-                                                               : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                tot[4 * q] += v[q].x;
-                                tot[4 * q + 1] += v[q].y;
-                                tot[4 * q + 2] += v[q].z;
-                                tot[4 * q + 3] += v[q].w;
-                            }
-                        }
-#pragma unroll
-                        for (int q = 0; q < 16; ++q) acc[q] = tot[q];
-                    }
-                    if (col < n) {
-#pragma unroll
-                        for (int q = 0; q < 16; ++q)
-                            if (h * 16 + q < m_rows)
-                                y[static_cast<int64_t>(h * 16 + q) * n + col] = round_out<kBf16>(fmaf(acc[q], sc, b));
-                    }
-                } else {
-                    float4* dst = reinterpret_cast<float4*>(mine + h * 16);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        if (h * 16 + 4 * q < m_rows)
-                            dst[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+                        if (h * 16 + q < m_rows)
+                            y[static_cast<int64_t>(h * 16 + q) * n + col] = round_out<kBf16>(fmaf(acc[q], sc, b));
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(dfree(d));
-
-            if (!whole && split == 1) {
-                if (early) {
-                    // every other contributor has arrived, so nobody else
-                    // touches the counter during this launch
-                    if (etid == 0) counters[c_lo] = 0u;
-                } else {
-                    // publish, count, and let the last contributor finish
-                    epilogue_bar();
-                    if (etid == 0) {
-                        const uint32_t old = arrive_acq_rel(&counters[c_lo]);
-                        const bool is_last = old == static_cast<uint32_t>(c_hi - c_lo);
-                        if (is_last) atomicExch(&counters[c_lo], 0u);
-                        *last_flag = is_last ? 1 : 0;
-                    }
-                    epilogue_bar();
-                    if (*last_flag) {
+        }
+        // every unit is done, so the code ring is idle: the held partial
+        // tiles go there, token-major, for the cluster to add up
+        if (!*ep_abort) {
 #pragma unroll 1
-                        for (int h = 0; h < NT / 16 && h * 16 < m_rows; ++h) {
-                            float acc[16];
+            for (int i = 0; i < nheld && i < kMaxHeld; ++i) {
+                const int hd = i == 0 ? hd0 : hd1, hit = i == 0 ? hit0 : hit1, hlen = i == 0 ? hlen0 : hlen1;
+                float* pt = reinterpret_cast<float*>(smem + L::kCodesOff) + (i == 0 ? hslot0 : hslot1) * (kTileN * NT);
+#pragma unroll 1
+                for (int h = 0; h < NT / 16 && h * 16 < m_rows; ++h) {
+                    float acc[16];
+                    load_acc(hd, h, hit, hlen, acc);
 #pragma unroll
-                            for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
-                            // contributors in CTA order, kFixupBatch at a time
-                            for (int64_t cb = c_lo; cb <= c_hi; cb += kFixupBatch) {
-                                float4 v[kFixupBatch][4];
-#pragma unroll
-                                for (int e = 0; e < kFixupBatch; ++e) {
-                                    const int64_t cc = cb + e;
-#pragma unroll
-                                    for (int q = 0; q < 4; ++q)
-                                        v[e][q] = (cc <= c_hi && h * 16 + 4 * q < m_rows)
-                                                      ? __ldcg(slot_of(cc) + h * 4 + q)
-                                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-                                }
-#pragma unroll
-                                for (int e = 0; e < kFixupBatch; ++e) {
-                                    if (cb + e > c_hi) break;
-#pragma unroll
-                                    for (int q = 0; q < 4; ++q) {
-                                        acc[4 * q] += v[e][q].x;
-                                        acc[4 * q + 1] += v[e][q].y;
-                                        acc[4 * q + 2] += v[e][q].z;
-                                        acc[4 * q + 3] += v[e][q].w;
-                                    }
-                                }
-                            }
-                            if (col < n) {
-#pragma unroll
-                                for (int q = 0; q < 16; ++q)
-                                    if (h * 16 + q < m_rows)
-                                        y[static_cast<int64_t>(h * 16 + q) * n + col] =
-                                            round_out<kBf16>(fmaf(acc[q], sc, b));
-                            }
-                        }
-                    }
+                    for (int q = 0; q < 16; ++q)
+                        if (h * 16 + q < m_rows) pt[(h * 16 + q) * kTileN + r] = acc[q];
                 }
-                // last_flag is rewritten at the next split segment
-                epilogue_bar();
             }
         }
     } else {
         // ------------------------------- dequantising warpgroups (8-19) --
         const int group = (warp - kFirstDequantWarp) >> 2;
         // MX: this thread's row's four scale bytes of a unit (one word), loaded
-        // a unit ahead; (mx_tile, mx_kb) is the unit after the current one
-        int64_t mx_tile = 0;
-        int mx_kb = 0;
+        // a unit ahead; mcu walks this group's units one ahead of the loop
+        UnitCursor mcu = cursor0();
         uint32_t mx_next = 0x7F7F7F7Fu;
         auto mx_load = [&](int64_t tile, int kb) -> uint32_t {
             const int64_t row = tile * kTileN + (warp & 3) * 32 + lane;
@@ -690,10 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         if constexpr (kMx) {
             if (!early) pdl_wait();  // the scales may come from the previous kernel
-            const int64_t u = u0 + group;
-            mx_tile = u / nkb;
-            mx_kb = static_cast<int>(u - mx_tile * nkb);
-            if (group < iters) mx_next = mx_load(mx_tile, mx_kb);
+            for (int i = 0; i < group; ++i) mcu.next();
+            if (group < iters) mx_next = mx_load(mcu.tile, mcu.kb);
         }
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;
@@ -708,12 +700,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t mx_word = 0u;
             if constexpr (kMx) {
                 mx_word = mx_next;
-                mx_kb += kLanes;
-                while (mx_kb >= nkb) {
-                    mx_kb -= static_cast<int>(nkb);
-                    ++mx_tile;
-                }
-                if (it + kLanes < iters) mx_next = mx_load(mx_tile, mx_kb);
+                for (int i = 0; i < kLanes; ++i) mcu.next();
+                if (it + kLanes < iters) mx_next = mx_load(mcu.tile, mcu.kb);
             }
             const uint32_t row = sbase + code_smem(group, s) + r * 128;
             uint4 cw[8];
@@ -789,52 +777,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     __syncthreads();
-    if (split > 1) {
-        // this rank adds up channels [ch0, ch0 + nch) of the tile over all
-        // ranks, in rank order, and writes y; split is a power of two, so a
-        // thread keeps one channel, whose scale and bias it fetches first
-        const bool red_thread = warp >= kFirstEpilogueWarp && warp < kFirstDequantWarp;
-        const int etid = threadIdx.x - 32 * kFirstEpilogueWarp;
-        const int nch = kTileN / split;
-        const int ch = static_cast<int>(c % split) * nch + (red_thread ? etid % nch : 0);
-        const int64_t col = (c / split) * kTileN + ch;
-        float sc = 0.0f, b = 0.0f;
-        if (red_thread && col < n) {
-            sc = kMx ? 1.0f : scales[col];
-            b = bias ? bias[col] : 0.0f;
-        }
-        // every rank's partial tile is in its shared memory
+    if (cl > 1) {
+        // Every rank's held partials are in its shared memory.  For each tile
+        // this rank shares (the tiles of its first and last units, when it
+        // does not cover them whole), its contributors r_lo..r_hi split the
+        // tile's outputs: contributor j adds up channels j, j + J, ... over all
+        // contributors in rank order (so in k order) and writes y.  Every
+        // thread of the CTA takes part; kRedBatch outputs' remote loads are
+        // issued before any sum, so their round trips overlap.
         cluster_sync_all();
-        if (red_thread && !*ep_abort && iters > 0) {
-            const uint32_t pt = sbase + L::kCodesOff;
-            if (col < n) {
-                // kRedBatch tokens' loads from all ranks are issued before any
-                // sum, so their remote round trips overlap
-                const int tstep = 128 / nch;
-                for (int tok0 = etid / nch; tok0 < m_rows; tok0 += kRedBatch * tstep) {
-                    float v[kRedBatch][8];
+        const bool epi = warp >= kFirstEpilogueWarp && warp < kFirstDequantWarp;
+        if (epi && !*ep_abort) {
+#pragma unroll 1
+            for (int i = 0; i < nshared && i < kMaxHeld; ++i) {
+                const SharedTile& st = i == 0 ? sh0 : sh1;
+                if (st.col < 0) continue;
+                const int ch = static_cast<int>(st.col % kTileN);
+                // contributors' partials of this tile, 8 ranks at a time, added
+                // in rank order; a contributor's staging slot is 0 if the tile
+                // holds its first unit
+                for (int tk0 = st.tok0; tk0 < m_rows; tk0 += kRedBatch * st.tstep) {
+                    float t[kRedBatch];
 #pragma unroll
-                    for (int e = 0; e < kRedBatch; ++e) {
-                        const int tok = tok0 + e * tstep;
-                        const uint32_t off = pt + static_cast<uint32_t>((tok * kTileN + ch) * 4);
+                    for (int e = 0; e < kRedBatch; ++e) t[e] = 0.0f;
+                    for (int rg = 0; rg < st.J; rg += kRankGroup) {
+                        float v[kRedBatch][kRankGroup];
 #pragma unroll
-                        for (int rr = 0; rr < 8; ++rr)
-                            if (rr < split && tok < m_rows) v[e][rr] = ld_shared_cluster_f32(mapa_shared(off, rr));
+                        for (int rr = 0; rr < kRankGroup; ++rr) {
+                            if (rg + rr >= st.J) break;
+                            const int rk = st.r_lo + rg + rr;
+                            const int slot = rg + rr == 0 ? st.lo_slot : 0;
+                            const uint32_t src = mapa_shared(
+                                sbase + L::kCodesOff + static_cast<uint32_t>((slot * kTileN * NT + ch) * 4), rk);
+#pragma unroll
+                            for (int e = 0; e < kRedBatch; ++e) {
+                                const int tk = tk0 + e * st.tstep;
+                                if (tk < m_rows) v[e][rr] = ld_dsmem_f32(src + static_cast<uint32_t>(tk * kTileN * 4));
+                            }
+                        }
+#pragma unroll
+                        for (int rr = 0; rr < kRankGroup; ++rr) {
+                            if (rg + rr >= st.J) break;
+#pragma unroll
+                            for (int e = 0; e < kRedBatch; ++e) t[e] += v[e][rr];
+                        }
                     }
 #pragma unroll
                     for (int e = 0; e < kRedBatch; ++e) {
-                        const int tok = tok0 + e * tstep;
-                        if (tok >= m_rows) break;
-                        float t = 0.0f;
-#pragma unroll
-                        for (int rr = 0; rr < 8; ++rr)
-                            if (rr < split) t += v[e][rr];
-                        y[static_cast<int64_t>(tok) * n + col] = round_out<kBf16>(fmaf(t, sc, b));
+                        const int tk = tk0 + e * st.tstep;
+                        if (tk < m_rows) y[static_cast<int64_t>(tk) * n + st.col] = round_out<kBf16>(fmaf(t[e], st.sc, st.b));
                     }
                 }
             }
         }
-        // no rank leaves while its partial may still be read
+        // no rank leaves while its partials may still be read
         cluster_sync_all();
     }
     if (warp == kMmaWarp) {
@@ -892,54 +888,97 @@ cudaError_t device_sm_count(int& sms) {
     return cudaSuccess;
 }
 
-// CTAs of the persistent grid.  Whole tiles when the tile count nearly
-// fills the GPU (no partial tiles, no fix-up); when it is well below the SM
-// count, each tile split evenly over s CTAs; otherwise stream-K over the SMs.
-// A split CTA gets at least kMinUnitsPerCta units, and P <= kMaxCtas.
-// Launch shape: the grid size, and the cluster size of a split launch (1 =
-// whole tiles or stream-K).
-struct SkinnyShape {
-    int64_t grid;
-    int split;
-};
+// Launch shape: clusters of `cl` CTAs, each cluster taking `tpc`
+// consecutive tiles (the last cluster may take fewer).  A CTA's time is its
+// units times the per-unit loop, so the shape with the fewest units per CTA
+// wins among those whose clusters all run at once: active[cl] is how many
+// clusters of cl CTAs the device holds at a time (a cluster lives in one GPC,
+// so a GPC whose SM count cl does not divide leaves SMs idle; active[1] is
+// the SM count).  Sharing tiles costs a fixed finish, counted in units
+// (measured on GB300 against whole tiles at a ~0.38 us unit): about 1 us
+// when a cluster splits one tile (kSplitUnits), about 3.3 us when its ranks
+// hold two shared tiles each (kSharedUnits: both partials wait for the end,
+// and a cluster starts only when all its SMs are free).  Each rank gets at
+// least kMinUnitsPerCta units (and
+// at least one of every cluster's, so cl <= nkb).  A 64-token launch keeps
+// one accumulator per MMA warp, so its CTAs may share at most one tile:
+// tpc == 1 when cl > 1.
+constexpr int kMinUnitsPerCta = 4;
+constexpr int kSplitUnits = 3;
+constexpr int kSharedUnits = 9;
+constexpr int64_t kMaxClusterUnits = 1 << 24;  // cluster-local unit indices are 32-bit
 
-constexpr int kMaxSplit = 8;  // portable cluster size
-
-SkinnyShape skinny_shape(int64_t n, int64_t k, int sms) {
+SkinnyShape skinny_shape(int64_t n, int64_t k, const int* active, int nt) {
     const int64_t tiles = (n + kTileN - 1) / kTileN;
     const int64_t nkb = (k + kBlockK - 1) / kBlockK;
-    const int64_t units = tiles * nkb;
-    const int64_t cap = sms < kMaxCtas ? sms : kMaxCtas;
-    if (tiles <= cap && 10 * tiles >= 7 * cap) return {tiles, 1};
-    if (tiles < cap) {
-        // each tile over a cluster of split CTAs (a power of two), each CTA
-        // with at least kMinUnitsPerCta k-blocks
-        int split = 1;
-        while (split * 2 <= kMaxSplit && tiles * split * 2 <= cap && split * 2 * kMinUnitsPerCta <= nkb) split *= 2;
-        return {tiles * split, split};
+    SkinnyShape best{1, (tiles + active[1] - 1) / active[1]};
+    int64_t best_cost = best.tpc * nkb;
+    for (int cl = 2; cl <= kMaxCluster && cl <= nkb; ++cl) {
+        const int64_t clusters_max = active[cl];
+        if (clusters_max < 1) continue;
+        const int64_t tpc = (tiles + clusters_max - 1) / clusters_max;
+        if (nt > 32 && tpc > 1) continue;
+        if (tpc * nkb >= kMaxClusterUnits) continue;
+        const int64_t per_cta = (tpc * nkb + cl - 1) / cl;
+        if (per_cta < kMinUnitsPerCta) continue;
+        const int64_t cost = per_cta + (tpc == 1 ? kSplitUnits : kSharedUnits);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = {cl, tpc};
+        }
     }
-    int64_t p = units / kMinUnitsPerCta;
-    if (p > cap) p = cap;
-    if (p < 1) p = 1;
-    return {p, 1};
+    return best;
+}
+
+bool skinny_shape_valid(const SkinnyShape& sh, int64_t m, int64_t k) {
+    const int64_t nkb = (k + kBlockK - 1) / kBlockK;
+    const int nt = m <= 16 ? 16 : m <= 32 ? 32 : 64;
+    return sh.cl >= 1 && sh.cl <= kMaxCluster && sh.tpc >= 1 && sh.cl <= nkb && sh.tpc * nkb < kMaxClusterUnits &&
+           (sh.cl == 1 || nt <= 32 || sh.tpc == 1);
 }
 
 template <int NT, bool kBf16, bool kMx = false>
-static cudaError_t launch_nt(const LinearArgs& a, void* workspace, int ctas, cudaStream_t st) {
+static cudaError_t launch_nt(const LinearArgs& a, const SkinnyShape* forced, cudaStream_t st) {
     using L = SkinnySmem<NT>;
     auto kern = skinny_kernel<NT, kBf16, kMx>;
+    // per device, once: the kernel's attributes, and how many clusters of
+    // each size the device holds at a time (0 where a size cannot launch)
     static std::once_flag attr_once[64];
+    static int active[64][kMaxCluster + 1];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once[dev & 63], [&] {
-        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     int sms = 0;
     e = device_sm_count(sms);
     if (e != cudaSuccess) return e;
+    cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once[dev], [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+        if (attr_err != cudaSuccess) return;
+        const bool nonportable =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess;
+        active[dev][1] = sms;
+        for (int cl = 2; cl <= kMaxCluster; ++cl) {
+            active[dev][cl] = 0;
+            if (cl > 8 && !nonportable) continue;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = static_cast<unsigned>(cl);
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            cudaLaunchConfig_t qc = {};
+            qc.gridDim = dim3(static_cast<unsigned>(cl * sms));
+            qc.blockDim = dim3(kThreads);
+            qc.dynamicSmemBytes = L::kAlloc;
+            qc.attrs = qa;
+            qc.numAttrs = 1;
+            int num = 0;
+            if (cudaOccupancyMaxActiveClusters(&num, kern, &qc) == cudaSuccess) active[dev][cl] = num;
+            else (void)cudaGetLastError();  // an unsupported size: leave it out
+        }
+    });
+    if (attr_err != cudaSuccess) return attr_err;
 
     CUtensorMap map_codes, map_x;
     if (!encode_2d(&map_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.codes, static_cast<uint64_t>(a.k),
@@ -949,92 +988,56 @@ static cudaError_t launch_nt(const LinearArgs& a, void* workspace, int ctas, cud
                    static_cast<uint64_t>(a.m), static_cast<uint64_t>(a.k) * 2, 64, NT))
         return cudaErrorInvalidValue;
 
-    // every CTA gets at least one unit: the fix-up counts CTAs, so an empty
-    // range inside a split tile would leave that tile unfinished
-    const int64_t units = ((a.n + kTileN - 1) / kTileN) * ((a.k + kBlockK - 1) / kBlockK);
-    SkinnyShape shape = ctas > 0 ? SkinnyShape{ctas, 1} : skinny_shape(a.n, a.k, sms);
-    if (shape.grid > units) shape.grid = units;
+    const SkinnyShape shape = forced ? *forced : skinny_shape(a.n, a.k, active[dev], NT);
+    const int64_t tiles = (a.n + kTileN - 1) / kTileN;
+    const int64_t clusters = (tiles + shape.tpc - 1) / shape.tpc;
     // programmatic dependent launch: this grid's prologue (barrier set-up,
     // TMEM allocation) overlaps the tail of the previous kernel in the
     // stream; every role waits for that kernel before touching global memory
+    // (the code producer too, unless the caller states the weights were
+    // complete before it)
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = static_cast<unsigned>(shape.split);
+    attr[1].val.clusterDim.x = static_cast<unsigned>(shape.cl);
     attr[1].val.clusterDim.y = 1;
     attr[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(shape.grid));
+    cfg.gridDim = dim3(static_cast<unsigned>(clusters * shape.cl));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = L::kAlloc;
     cfg.stream = st;
     cfg.attrs = attr;
-    cfg.numAttrs = shape.split > 1 ? 2 : 1;
+    cfg.numAttrs = shape.cl > 1 ? 2 : 1;
     uint16_t* yp = static_cast<uint16_t*>(a.y);
     for (int64_t m0 = 0; m0 < a.m; m0 += NT) {
         const int rows = static_cast<int>(a.m - m0 < NT ? a.m - m0 : NT);
         const float* sc = kMx ? nullptr : a.scales;
         const uint8_t* e8 = kMx ? reinterpret_cast<const uint8_t*>(a.scales) : nullptr;
-        e = cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, sc, e8, a.bias, yp + m0 * a.n,
-                               static_cast<uint8_t*>(workspace), rows, static_cast<int>(m0), a.n, a.k, shape.split,
+        e = cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, sc, e8, a.bias, yp + m0 * a.n, rows,
+                               static_cast<int>(m0), a.n, a.k, shape.cl, static_cast<int>(shape.tpc),
                                a.early ? 1 : 0);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
-size_t skinny_workspace_size(int sms) { return skinny_workspace_bytes(sms < kMaxCtas ? sms : kMaxCtas); }
-
-cudaError_t launch_skinny(const LinearArgs& a, void* workspace, int ctas, cudaStream_t st) {
+cudaError_t launch_skinny(const LinearArgs& a, const SkinnyShape* forced, cudaStream_t st) {
     const bool bf16 = a.act == 1;
+    if (forced && !skinny_shape_valid(*forced, a.m, a.k)) return cudaErrorInvalidConfiguration;
     if (a.e8m0) {
         // MX-style scales: bf16 activations, k % 128 == 0 (checked by the caller)
         if (!bf16 || a.group != 32 || a.k % 128 != 0) return cudaErrorInvalidValue;
-        if (a.m <= 16) return launch_nt<16, true, true>(a, workspace, ctas, st);
-        if (a.m <= 32) return launch_nt<32, true, true>(a, workspace, ctas, st);
-        return launch_nt<64, true, true>(a, workspace, ctas, st);
+        if (a.m <= 16) return launch_nt<16, true, true>(a, forced, st);
+        if (a.m <= 32) return launch_nt<32, true, true>(a, forced, st);
+        return launch_nt<64, true, true>(a, forced, st);
     }
-    if (a.m <= 16)
-        return bf16 ? launch_nt<16, true>(a, workspace, ctas, st) : launch_nt<16, false>(a, workspace, ctas, st);
-    if (a.m <= 32)
-        return bf16 ? launch_nt<32, true>(a, workspace, ctas, st) : launch_nt<32, false>(a, workspace, ctas, st);
+    if (a.m <= 16) return bf16 ? launch_nt<16, true>(a, forced, st) : launch_nt<16, false>(a, forced, st);
+    if (a.m <= 32) return bf16 ? launch_nt<32, true>(a, forced, st) : launch_nt<32, false>(a, forced, st);
     // 64 tokens a launch (slabs of 64 beyond): each weight tile is dequantised
     // once for all of them
-    return bf16 ? launch_nt<64, true>(a, workspace, ctas, st) : launch_nt<64, false>(a, workspace, ctas, st);
-}
-
-// Library-owned scratch for fp8w_linear_noalloc: the workspace of a grid of
-// up to kStaticScratchCtas CTAs, in device memory that exists as soon as this
-// module is loaded on a device, so that entry point allocates nothing.
-constexpr int kStaticScratchCtas = 160;
-constexpr size_t kStaticScratchBytes = skinny_workspace_bytes(kStaticScratchCtas);
-static_assert(kStaticScratchBytes == FP8W_STATIC_SCRATCH_BYTES, "fp8w.h states the static scratch size");
-static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
-
-size_t static_scratch_bytes() { return kStaticScratchBytes; }
-
-// First call on a device (with that device current): look up the array's
-// address and enqueue a clear of its arrival counters on `st`, ahead of the
-// kernel that will use them.  Later calls return the cached address.
-cudaError_t static_scratch(void** ptr, cudaStream_t st) {
-    static std::mutex mu;
-    static void* ptrs[64];
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lk(mu);
-    if (!ptrs[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (e != cudaSuccess) return e;
-        e = cudaMemsetAsync(p, 0, kWsCountersBytes, st);
-        if (e != cudaSuccess) return e;
-        ptrs[dev] = p;
-    }
-    *ptr = ptrs[dev];
-    return cudaSuccess;
+    return bf16 ? launch_nt<64, true>(a, forced, st) : launch_nt<64, false>(a, forced, st);
 }
 
 int read_skinny_device_error() {

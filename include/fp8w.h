@@ -17,10 +17,11 @@
  *
  * Conventions shared by every entry point:
  *  - Every data pointer is a DEVICE pointer owned by the caller.  The
- *    library allocates no device memory, frees nothing and never
- *    synchronises: it enqueues kernels on `stream` (a cudaStream_t; NULL is
- *    the legacy default stream) and returns.  Calls can be captured in a
- *    CUDA graph.
+ *    library allocates no device memory, needs no scratch, keeps no state
+ *    between calls, frees nothing and never synchronises: it enqueues
+ *    kernels on `stream` (a cudaStream_t; NULL is the legacy default stream)
+ *    and returns.  Calls can be captured in a CUDA graph, and calls on
+ *    different streams may run at the same time.
  *  - Arguments are checked on the host before any launch; on an error the
  *    outputs are untouched and no work is enqueued.  FP8W_ERR_CUDA means a
  *    CUDA runtime call failed (fp8w_last_cuda_error() names it).  Faults
@@ -39,7 +40,7 @@
 extern "C" {
 #endif
 
-#define FP8W_ABI_VERSION 10
+#define FP8W_ABI_VERSION 11
 
 #if defined(__GNUC__)
 #define FP8W_API __attribute__((visibility("default")))
@@ -54,10 +55,7 @@ typedef enum fp8w_status {
     FP8W_ERR_ALIGN = 3,     /* a pointer breaks its alignment rule */
     FP8W_ERR_DTYPE = 4,     /* activation dtype is not FP8W_BF16 / FP8W_F16 */
     FP8W_ERR_CUDA = 5,      /* a CUDA runtime/driver call failed */
-    FP8W_ERR_CONFIG = 6,    /* an explicit launch configuration is invalid */
-    FP8W_ERR_WORKSPACE = 7, /* workspace NULL, misaligned or too small */
-    FP8W_ERR_SCRATCH = 8    /* fp8w_linear_noalloc: the device needs more
-                               scratch than the library's static maximum */
+    FP8W_ERR_CONFIG = 6     /* an explicit launch configuration is invalid */
 } fp8w_status;
 
 /* Activation / output dtypes (FP8W_F32: fp8w_dequantize's output and
@@ -152,8 +150,6 @@ FP8W_API fp8w_status fp8w_quantize_mx(const float *w, int64_t n, int64_t k,
  *   y[i, r] = round_act( sum_j 2^(scales[r, j] - 127) * sum_{c in block j} x[i, c] * e4m3(codes[r, c]) + bias[r] ).
  *
  *   scales [n, k / 32] uint8, device, 16-byte aligned; k % 128 == 0.
- *   workspace, workspace_bytes: as fp8w_linear (fp8w_linear_workspace_size);
- *           may be NULL / 0 when the GEMV or the prefill GEMM (m > 64) runs.
  *   Other arguments as fp8w_linear.
  *
  * m == 1 with k % 512 == 0 and k <= 32768 runs the GEMV: a slot's rows of
@@ -169,8 +165,7 @@ FP8W_API fp8w_status fp8w_quantize_mx(const float *w, int64_t n, int64_t k,
  */
 FP8W_API fp8w_status fp8w_linear_mx(const void *x, int act_dtype, int64_t m, int64_t k,
                            const uint8_t *codes, const uint8_t *scales,
-                           const float *bias, int64_t n, void *y,
-                           void *workspace, size_t workspace_bytes, void *stream);
+                           const float *bias, int64_t n, void *y, void *stream);
 
 /*
  * fp8w_dequantize -- the dequantised weight, the pages' fallback form
@@ -219,31 +214,20 @@ FP8W_API fp8w_status fp8w_dequantize_mx(const uint8_t *codes, const uint8_t *sca
  *   scales [n] fp32, device, 4-byte aligned.
  *   bias   [n] fp32, device, 4-byte aligned, or NULL for no bias.
  *   y      [m, n] in act_dtype, device, 2-byte aligned (output).
- *   workspace, workspace_bytes: device scratch for the tensor-core kernel,
- *          256-byte aligned, at least fp8w_linear_workspace_size(m, n, k)
- *          bytes (NULL/0 allowed when that size is 0).  It must be
- *          zero-filled once before its first use; every completed call
- *          leaves it ready for the next.  Calls that may run at the same
- *          time (other streams) need separate workspaces.
  *   1 <= m <= FP8W_MAX_DIM, 1 <= n <= FP8W_MAX_DIM, 16 <= k <= FP8W_MAX_K,
- *   k % 16 == 0.  x and y must not overlap codes, scales, bias or workspace.
+ *   k % 16 == 0.  x and y must not overlap codes, scales or bias.
  *
  * m == 1 with k <= 32768 runs the GEMV kernel; 2 <= m <= 64 the
  * tensor-core kernel for few tokens (one launch of 16, 32 or 64 token
- * columns); m > 64 the prefill GEMM, which dequantises each 128-row weight
- * tile into shared memory once and multiplies it by 128- or 256-token tiles
- * (one launch; it uses no workspace).
+ * columns; thread-block clusters of CTAs share 128-channel tiles and add up
+ * their fp32 partials in distributed shared memory); m > 64 the prefill
+ * GEMM, which dequantises each 128-row weight tile into shared memory once
+ * and multiplies it by 128- or 256-token tiles.  Every path is one launch
+ * and needs no workspace.
  */
 FP8W_API fp8w_status fp8w_linear(const void *x, int act_dtype, int64_t m, int64_t k,
                         const uint8_t *codes, const float *scales,
-                        const float *bias, int64_t n, void *y,
-                        void *workspace, size_t workspace_bytes, void *stream);
-
-/* Workspace bytes fp8w_linear needs for this shape on the current device:
- * 0 when the GEMV kernel (m == 1, k <= 32768) or the prefill GEMM (m > 64)
- * runs.  FP8W_KERNEL_SKINNY chosen explicitly needs the size of the m == 2
- * shape at m == 1 and of the m == 64 shape beyond 64. */
-FP8W_API size_t fp8w_linear_workspace_size(int64_t m, int64_t n, int64_t k);
+                        const float *bias, int64_t n, void *y, void *stream);
 
 /* Explicit kernel choice, for tests and tuning; fp8w_linear uses
  * FP8W_KERNEL_AUTO. */
@@ -263,49 +247,33 @@ enum { FP8W_KERNEL_AUTO = 0, FP8W_KERNEL_GEMV = 1, FP8W_KERNEL_SKINNY = 2, FP8W_
 
 typedef struct fp8w_linear_config {
     int kernel;   /* FP8W_KERNEL_*; GEMV requires m == 1 and k <= 32768 */
-    int ctas;     /* FP8W_KERNEL_SKINNY only: CTAs of its persistent grid,
-                     1..number of SMs, or 0 to choose from the shape; must be
-                     0 for the other kernels */
+    int cluster;  /* FP8W_KERNEL_SKINNY only: CTAs per thread-block cluster,
+                     1..16 (beyond 8 only where the device allows
+                     non-portable clusters, else FP8W_ERR_CUDA) and at most
+                     ceil(k / 128); beyond 32 tokens only 1 unless
+                     tiles == 1; 0 (with tiles 0) chooses from the shape;
+                     must be 0 for the other kernels */
+    int tiles;    /* with cluster: 128-channel tiles each cluster shares
+                     (its ranks split their units evenly), >= 1 */
     int flags;    /* 0 or FP8W_FLAG_WEIGHTS_READY */
-    int reserved[5];  /* must be 0 */
+    int reserved[4];  /* must be 0 */
 } fp8w_linear_config;
 
-/* fp8w_linear with an explicit configuration (NULL = automatic).  The
- * skinny tensor-core kernel at m == 1 needs the workspace of the m == 2
- * shape, and beyond 64 tokens that of the m == 64 shape. */
+/* fp8w_linear with an explicit configuration (NULL = automatic). */
 FP8W_API fp8w_status fp8w_linear_ex(const void *x, int act_dtype, int64_t m, int64_t k,
                            const uint8_t *codes, const float *scales,
                            const float *bias, int64_t n, void *y,
-                           void *workspace, size_t workspace_bytes,
                            const fp8w_linear_config *config, void *stream);
 
 /*
- * fp8w_linear_noalloc -- fp8w_linear without a caller-provided workspace.
- * The pages have no counterpart: the operation is fp8w_linear's, and this
- * entry point exists only because the tensor-core kernel needs scratch.  It
- * serves callers that cannot hand over a device buffer: a plain C host
- * program whose device pointers come from another runtime and which has no
- * device allocator of its own, or a serving loop that must not allocate
- * once running (cudaMalloc can synchronise the device, and a fixed memory
- * budget leaves no room for ad-hoc buffers).  It calls no allocator.
- *
- * Arguments, checks, kernels and results are those of fp8w_linear.  The
- * scratch is a static device array of FP8W_STATIC_SCRATCH_BYTES bytes that
- * the library module holds on every device it is loaded on (the workspace of
- * a grid of up to 160 CTAs, one per SM); a device whose workspace would be
- * larger is refused with FP8W_ERR_SCRATCH before any launch.
- *
- * First call on a device: looks up the array's address (with that device
- * current) and enqueues a clear of its counters on `stream` ahead of the
- * kernel; make that first call before any CUDA-graph capture.  Every
- * completed call leaves the scratch ready for the next one.
- *
- * All calls on one device share the one scratch, so calls that may overlap
- * on the GPU (on other streams, or from other host threads) race and can
- * return wrong results: keep them in one stream, or use fp8w_linear with a
- * workspace per stream.
+ * fp8w_linear_noalloc -- the same call as fp8w_linear, kept for callers
+ * that cannot allocate device memory while they run (a serving loop with a
+ * fixed memory budget, where cudaMalloc could also synchronise the device,
+ * or a host program whose device pointers come from another runtime).  No
+ * path of the library uses scratch memory any more, so fp8w_linear itself
+ * serves them: arguments, checks, kernels and results are identical.  The
+ * pages have no counterpart.
  */
-#define FP8W_STATIC_SCRATCH_BYTES 10489856u
 FP8W_API fp8w_status fp8w_linear_noalloc(const void *x, int act_dtype, int64_t m, int64_t k,
                                 const uint8_t *codes, const float *scales,
                                 const float *bias, int64_t n, void *y, void *stream);

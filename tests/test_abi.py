@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_status_strings():
     L = fw.lib()
-    for s in range(9):
+    for s in range(7):
         assert L.fp8w_status_string(s)
     assert L.fp8w_status_string(99) == b"unknown status"
 
@@ -41,12 +41,13 @@ C16 = ctypes.c_void_p(0x300000)
 D16 = ctypes.c_void_p(0x400000)
 
 
-def _lin(x=A16, act=1, m=1, k=64, codes=B16, scales=C16, bias=None, n=8, y=D16, cfg=None, ws=None,
-         ws_bytes=0):
+# Every case below is refused on the host, before any launch: the pointers
+# are fake device addresses.
+def _lin(x=A16, act=1, m=1, k=64, codes=B16, scales=C16, bias=None, n=8, y=D16, cfg=None):
     L = fw.lib()
     if cfg is None:
-        return L.fp8w_linear(x, act, m, k, codes, scales, bias, n, y, ws, ws_bytes, None)
-    return L.fp8w_linear_ex(x, act, m, k, codes, scales, bias, n, y, ws, ws_bytes, ctypes.byref(cfg), None)
+        return L.fp8w_linear(x, act, m, k, codes, scales, bias, n, y, None)
+    return L.fp8w_linear_ex(x, act, m, k, codes, scales, bias, n, y, ctypes.byref(cfg), None)
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -62,31 +63,38 @@ def test_linear_rejects_bad_arguments(kw, status):
     assert _lin(**kw) == status
 
 
+def _cfg(kernel=fw.KERNEL_SKINNY, cluster=0, tiles=0, flags=0, reserved=0):
+    c = fw.LinearConfig(kernel, cluster, tiles, flags)
+    c.reserved[2] = reserved
+    return c
+
+
 @pytest.mark.parametrize("cfg", [
-    fw.LinearConfig(fw.KERNEL_GEMV),           # gemv needs m == 1 (m = 2 below)
-    fw.LinearConfig(7),                        # unknown kernel
-    fw.LinearConfig(-1),
-    fw.LinearConfig(fw.KERNEL_SKINNY, -3),     # negative grid size
-    fw.LinearConfig(fw.KERNEL_PREFILL, 8),     # the prefill GEMM takes no grid size
+    _cfg(fw.KERNEL_GEMV),                      # gemv needs m == 1 (m = 2 below)
+    _cfg(7), _cfg(-1),                         # unknown kernel
+    _cfg(cluster=-3, tiles=1), _cfg(cluster=2, tiles=-1),
+    _cfg(cluster=2), _cfg(tiles=3),            # cluster and tiles come together
+    _cfg(cluster=17, tiles=1),                 # beyond the largest cluster size
+    _cfg(cluster=4, tiles=1),                  # more ranks than k-blocks (k = 256: two)
+    _cfg(fw.KERNEL_PREFILL, 2, 1),             # only the tensor-core kernel takes a shape
+    _cfg(flags=2), _cfg(reserved=1),           # unknown flag, reserved field
 ])
 def test_linear_rejects_bad_config(cfg):
     assert _lin(m=2, k=256, cfg=cfg) == 6
 
 
-def test_gemv_rejects_a_grid_size():
-    assert _lin(m=1, k=256, cfg=fw.LinearConfig(fw.KERNEL_GEMV, 8)) == 6
+def test_gemv_rejects_a_cluster_shape():
+    assert _lin(m=1, k=256, cfg=_cfg(fw.KERNEL_GEMV, 2, 1)) == 6
+
+
+def test_tensor_core_kernel_beyond_32_tokens_shares_one_tile_at_most():
+    # 64-token launches hold one accumulator per MMA warp
+    assert _lin(m=40, k=1024, cfg=_cfg(cluster=2, tiles=3)) == 6
 
 
 def test_gemv_rejects_rows_longer_than_it_stages():
     # x of a GEMV row lives in shared memory: k <= 32768
     assert _lin(m=1, k=32768 + 16, cfg=fw.LinearConfig(fw.KERNEL_GEMV)) == 6
-
-
-@pytest.mark.parametrize("ws,ws_bytes", [(None, 0), (None, 1 << 30), (ctypes.c_void_p(0x600010), 1 << 30)])
-def test_tensor_core_path_rejects_missing_or_misaligned_workspace(ws, ws_bytes):
-    # NULL or non-256-byte-aligned workspace is refused before any CUDA call
-    assert _lin(m=2, k=256, ws=ws, ws_bytes=ws_bytes) == 7
-    assert _lin(m=1, k=256, ws=ws, ws_bytes=ws_bytes, cfg=fw.LinearConfig(fw.KERNEL_SKINNY)) == 7
 
 
 @pytest.mark.parametrize("args,status", [
@@ -176,14 +184,12 @@ def test_quantize_mx_takes_scale_bytes_at_any_alignment():
     (dict(scales=ctypes.c_void_p(0x300008)), 3),   # scale bytes: 16-byte aligned
     (dict(m=2, act=2), 4),                     # the tensor-core form folds the scales into bf16 weights
     (dict(m=1, k=384, act=2), 4),              # m == 1 but k % 512 != 0: the tensor-core form too
-    (dict(m=2), 7), (dict(m=1, k=384), 7),     # tensor-core form without a workspace
-    (dict(m=2, ws=ctypes.c_void_p(0x600010), ws_bytes=1 << 30), 7),   # misaligned workspace
 ])
 def test_linear_mx_rejects_bad_arguments(kw, status):
-    a = dict(x=A16, act=1, m=1, k=1024, codes=B16, scales=C16, bias=None, n=8, y=D16, ws=None, ws_bytes=0)
+    a = dict(x=A16, act=1, m=1, k=1024, codes=B16, scales=C16, bias=None, n=8, y=D16)
     a.update(kw)
     assert fw.lib().fp8w_linear_mx(a["x"], a["act"], a["m"], a["k"], a["codes"], a["scales"], a["bias"],
-                                   a["n"], a["y"], a["ws"], a["ws_bytes"], None) == status
+                                   a["n"], a["y"], None) == status
 
 
 @pytest.mark.parametrize("args,status", [

@@ -66,7 +66,7 @@ def gpu_quantize(w_np):
     return codes.cpu().numpy(), scales.cpu().numpy()
 
 
-def gpu_linear(x_bits, act, codes, scales, bias, kernel=fw.KERNEL_AUTO):
+def gpu_linear(x_bits, act, codes, scales, bias, kernel=fw.KERNEL_AUTO, cluster=0, tiles=0):
     m, k = x_bits.shape
     n = codes.shape[0]
     dt = _dt(act)
@@ -75,7 +75,7 @@ def gpu_linear(x_bits, act, codes, scales, bias, kernel=fw.KERNEL_AUTO):
     s = torch.from_numpy(np.ascontiguousarray(scales)).to(DEV)
     b = None if bias is None else torch.from_numpy(np.ascontiguousarray(bias)).to(DEV)
     ybuf, y = _guarded(m * n, dt, POISON16)
-    fw.linear(x, c, s, b, out=y.view(m, n), kernel=kernel)
+    fw.linear(x, c, s, b, out=y.view(m, n), kernel=kernel, cluster=cluster, tiles=tiles)
     torch.cuda.synchronize()
     _check_canaries(ybuf, m * n, POISON16)
     assert fw.device_error() == 0
@@ -203,23 +203,32 @@ def test_linear_parity(m, n, k, act):
 
 
 @pytest.mark.parametrize("n,k", [
-    (128, 128),      # one unit: a single CTA
-    (1000, 256),     # 16 units: fewer units than SMs
+    (128, 128),      # one unit
+    (1000, 256),     # 8 tiles x 2 k-blocks
     (2432, 1024),    # 19 tiles x 8 k-blocks = 152 units
-    (2560, 1024),    # 160 units: every CTA one unit, a few two
-    (1100, 4096),    # 9 tiles x 32: tiles split across several CTAs
-    (300, 14336),    # 3 tiles x 112 k-blocks: ~50 CTAs per tile
-    (20000, 272),    # 157 tiles x 3 (ragged k): tiles straddling CTAs
+    (1100, 4096),    # 9 tiles x 32
+    (300, 14336),    # 3 tiles x 112 k-blocks
+    (20000, 272),    # 157 tiles x 3 (ragged k): more tiles than SMs
+    (14336, 4096),   # the gate weight: 112 tiles x 32
 ])
 @pytest.mark.parametrize("m", [1, 2, 9, 32, 48, 64])
-def test_tensor_core_partitions(m, n, k):
-    """Stream-K partitions of every kind: whole tiles, tiles shared by two or
-    by many CTAs (finished from the workspace by the last to arrive), fewer
-    units than SMs, ragged N and K."""
+def test_tensor_core_shapes(m, n, k):
+    """The tensor-core kernel in its automatic launch shape and in forced
+    cluster shapes of every kind: whole tiles (one CTA a cluster, one or
+    several tiles each), a tile split over a cluster, clusters of 2..8 ranks
+    sharing 2..5 tiles (ranges that start and end inside tiles, a rank inside
+    one tile, the last cluster with fewer tiles), ragged N and K; every
+    output against the oracle."""
     c, codes, scales = _case(77 + m + n + k, m, n, k, oracle.ACT_BF16)
-    y = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], kernel=fw.KERNEL_SKINNY)
     ref = oracle.linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], threads=oracle.host_cores())
-    assert_parity(y, ref, oracle.ACT_BF16, (m, n, k))
+    nkb = -(-k // 128)
+    shapes = [(0, 0), (1, 1), (1, 3), (2, 1), (8, 1), (2, 3), (3, 2), (4, 3), (5, 2), (7, 5), (4, 1)]
+    for cl, tpc in shapes:
+        if cl > nkb or (m > 32 and cl > 1 and tpc > 1):
+            continue
+        y = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], kernel=fw.KERNEL_SKINNY,
+                       cluster=cl, tiles=tpc)
+        assert_parity(y, ref, oracle.ACT_BF16, (m, n, k, cl, tpc))
 
 
 @pytest.mark.parametrize("act", [oracle.ACT_BF16, oracle.ACT_F16])
@@ -273,17 +282,32 @@ def test_gemv_activation_range(kind):
         assert_parity(y, ref, oracle.ACT_BF16, kind)
 
 
-def test_workspace_left_ready_across_shapes():
-    """Back-to-back calls of different shapes share one workspace: each call
-    must leave the arrival counters at zero for the next."""
-    shapes = [(8, 1100, 4096), (3, 300, 14336), (32, 2560, 1024), (8, 1100, 4096)]
+def test_calls_on_two_streams_at_once_are_independent():
+    """The library keeps no state between calls: calls of different shapes
+    enqueued on two streams at the same time, over and over, give the same
+    bits as the same calls one at a time."""
+    shapes = [(8, 1100, 4096), (32, 14336, 4096), (3, 300, 14336), (16, 20000, 272)]
+    runs = []
     for i, (m, n, k) in enumerate(shapes):
         c, codes, scales = _case(500 + i, m, n, k, oracle.ACT_BF16)
-        y = gpu_linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], kernel=fw.KERNEL_SKINNY)
+        x = torch.from_numpy(c["x"].view(np.int16)).to(DEV).view(torch.bfloat16)
+        cd, sd, bd = (torch.from_numpy(v).to(DEV) for v in (codes, scales, c["bias"]))
         ref = oracle.linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"], threads=oracle.host_cores())
-        assert_parity(y, ref, oracle.ACT_BF16, (m, n, k))
-    ws = fw._workspaces[0]
-    assert int(ws[:4096].view(torch.int32).abs().sum()) == 0   # 1024 arrival counters
+        runs.append((x, cd, sd, bd, ref))
+    serial = [fw.linear(x, cd, sd, bd) for x, cd, sd, bd, _ in runs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(device=DEV), torch.cuda.Stream(device=DEV)]
+    outs = [[torch.empty_like(y) for y in serial] for _ in range(8)]
+    for rep in range(8):
+        for i, (x, cd, sd, bd, _) in enumerate(runs):
+            with torch.cuda.stream(streams[(i + rep) % 2]):
+                fw.linear(x, cd, sd, bd, out=outs[rep][i])
+    torch.cuda.synchronize()
+    for i, (_, _, _, _, ref) in enumerate(runs):
+        assert_parity(serial[i].view(torch.int16).cpu().numpy().view(np.uint16), ref, oracle.ACT_BF16, shapes[i])
+        for rep in range(8):
+            assert torch.equal(outs[rep][i].view(torch.int16), serial[i].view(torch.int16)), (rep, shapes[i])
+    assert fw.device_error() == 0
 
 
 @pytest.mark.parametrize("act", [oracle.ACT_BF16, oracle.ACT_F16])
@@ -361,11 +385,9 @@ def test_prefill_kernel_at_few_tokens(m):
     assert_parity(y, oracle.linear(c["x"], oracle.ACT_BF16, codes, scales, c["bias"]), oracle.ACT_BF16, m)
 
 
-def test_prefill_needs_no_workspace_and_captures_in_a_graph():
-    """m > 64 needs no workspace, so a first call can be captured in a CUDA
-    graph with nothing allocated before it."""
-    L = fw.lib()
-    assert L.fp8w_linear_workspace_size(65, 300, 1024) == 0 and L.fp8w_linear_workspace_size(64, 300, 1024) > 0
+def test_prefill_captures_in_a_graph():
+    """No path needs a workspace, so a prefill call can be captured in a CUDA
+    graph with nothing allocated for it."""
     c, codes, scales = _case(47, 100, 300, 1024, oracle.ACT_BF16)
     x = torch.from_numpy(c["x"].view(np.int16)).to(DEV).view(torch.bfloat16)
     cd, sd, bd = (torch.from_numpy(v).to(DEV) for v in (codes, scales, c["bias"]))
@@ -375,7 +397,7 @@ def test_prefill_needs_no_workspace_and_captures_in_a_graph():
     s = torch.cuda.Stream(device=DEV)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
-        fw.linear(x, cd, sd, bd, out=y, workspace_buffer=None)
+        fw.linear(x, cd, sd, bd, out=y)
     g.replay()
     torch.cuda.synchronize()
     got = y.view(torch.int16).cpu().numpy().view(np.uint16)

@@ -1,10 +1,11 @@
-"""fp8w_linear_noalloc (library-owned static scratch) against fp8w_linear
-(caller workspace), through the C ABI.
+"""fp8w_linear_noalloc, the entry point for callers that cannot allocate
+device memory while they run, against fp8w_linear and the oracle, through
+the C ABI.  No path of the library uses scratch memory, so the two entry
+points must agree bit for bit.
 
-Named to be collected last: it must pass in a fresh process, where its first
-call sets the scratch up, and after every other test has run.  Each case
-makes two calls in a row with different inputs, so the second one relies on
-the first having left the scratch's counters at zero.
+Named to be collected last: it must pass in a fresh process and after every
+other test has run.  Each case makes two calls in a row with different
+inputs, so the second one would expose any state the first left behind.
 """
 import ctypes
 
@@ -25,10 +26,11 @@ import fp8_weight_only_gb300 as fw  # noqa: E402
 
 DEV = torch.device("cuda:0")
 
-# (m, n, k, act): split tiles over many CTAs (counters used), whole tiles,
-# the GEMV path, two 32-row slabs, fp16
+# (m, n, k, act): a tile split over a cluster, whole tiles, the GEMV path,
+# 40 rows (one 64-token launch), fp16, and
+# the gate weight (clusters sharing tiles)
 CASES = [(8, 1024, 4096, oracle.ACT_BF16), (32, 4096, 1024, oracle.ACT_BF16), (1, 2048, 1024, oracle.ACT_BF16),
-         (40, 640, 2048, oracle.ACT_BF16), (22, 4096, 1024, oracle.ACT_F16)]
+         (40, 640, 2048, oracle.ACT_BF16), (22, 4096, 1024, oracle.ACT_F16), (8, 14336, 4096, oracle.ACT_BF16)]
 
 
 def _inputs(seed, m, n, k, act):
@@ -38,7 +40,7 @@ def _inputs(seed, m, n, k, act):
     bias = torch.from_numpy(c["bias"]).to(DEV)
     dt = torch.bfloat16 if act == oracle.ACT_BF16 else torch.float16
     x = torch.from_numpy(np.ascontiguousarray(c["x"]).view(np.int16)).to(DEV).view(dt)
-    return x, codes, scales, bias
+    return x, codes, scales, bias, c
 
 
 def _noalloc(x, codes, scales, bias):
@@ -59,13 +61,16 @@ def _bits(t):
 
 
 @pytest.mark.parametrize("m,n,k,act", CASES)
-def test_noalloc_matches_workspace_entry_point_twice(m, n, k, act):
+def test_noalloc_matches_fp8w_linear_and_the_oracle_twice(m, n, k, act):
     for call, seed in enumerate((7001 + m, 7002 + m)):
-        x, codes, scales, bias = _inputs(seed, m, n, k, act)
+        x, codes, scales, bias, c = _inputs(seed, m, n, k, act)
         y = _noalloc(x, codes, scales, bias)
         ref = fw.linear(x, codes, scales, bias)
         torch.cuda.synchronize()
-        c = compare(_bits(y), _bits(ref), act)
-        assert c["finite"], (call, c)
-        assert c["rel_l2"] <= REL_L2_MAX and c["min_cosine"] >= COSINE_MIN, (call, c)
+        assert np.array_equal(_bits(y), _bits(ref)), call
+        rc, rs = oracle.quantize(c["w"])
+        want = oracle.linear(c["x"], act, rc, rs, c["bias"], threads=oracle.host_cores())
+        cmp = compare(_bits(y), want, act)
+        assert cmp["finite"], (call, cmp)
+        assert cmp["rel_l2"] <= REL_L2_MAX and cmp["min_cosine"] >= COSINE_MIN, (call, cmp)
     assert fw.device_error() == 0
