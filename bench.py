@@ -11,18 +11,23 @@ value = algorithmic bytes of the step (codes N*K + scale 4N + bias 4N + x
 2MK + y 2MN per call) / device time of the step, in GB/s, timed over
 replays of the step captured in a CUDA graph.  Each step streams 654 MB of
 codes; two weight replicas alternate between the M passes so every weight
-read comes from HBM (inputs larger than L2, no reuse within 436 MB).
+read comes from HBM (inputs larger than L2, no reuse within 436 MB).  The
+weights are quantised and synchronised before the timed region, so the
+calls pass FP8W_FLAG_WEIGHTS_READY (the code stream starts while the
+previous kernel drains); the same step without the flag is reported too.
 
-Also printed: the quantiser's throughput on the seven matrices, per-kernel
-durations from an instrumented replay (device events recorded between the
-launches inside the graph), the roofline fraction of the dominant kernel,
-an end-to-end figure through the Python API with pinned host buffers, the
-CPU oracle on a bounded sample, and SM clocks sampled during the timed loop.
+Also printed: every call of the step and every configuration of the
+workload timed directly (graph-replayed back-to-back launches of that call
+alone over weight replicas larger than L2), the roofline fraction of the
+dominant kernel from those direct timings, the t(M)/t(1) ratios of the
+skinny sweep, the W8A8 path, the quantiser, the dequantiser, an end-to-end
+figure through the Python API with pinned host buffers, the CPU oracle on a
+bounded sample (linear and quantise) with the weight error report and the
+outputs' error against it, and SM clocks sampled during the timed loop.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
 import argparse
-import ctypes
 import hashlib
 import json
 import math
@@ -150,46 +155,6 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ---------------------------------------------------- device event helpers --
-
-class DriverEvents:
-    """cuEventRecordWithFlags(EXTERNAL) so that events recorded during graph
-    capture become timing nodes of the graph."""
-
-    def __init__(self):
-        self.cu = ctypes.CDLL("libcuda.so.1")
-        self.cu.cuEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p), ctypes.c_uint]
-        self.cu.cuEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
-        self.cu.cuEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p, ctypes.c_void_p]
-        self.cu.cuEventDestroy_v2.argtypes = [ctypes.c_void_p]
-        self.events = []
-
-    def create(self):
-        ev = ctypes.c_void_p()
-        rc = self.cu.cuEventCreate(ctypes.byref(ev), 0)
-        if rc != 0:
-            raise RuntimeError("cuEventCreate failed: %d" % rc)
-        self.events.append(ev)
-        return ev
-
-    def record(self, ev, stream_handle):
-        rc = self.cu.cuEventRecordWithFlags(ev, ctypes.c_void_p(stream_handle), 1)
-        if rc != 0:
-            raise RuntimeError("cuEventRecordWithFlags failed: %d" % rc)
-
-    def elapsed_ms(self, a, b):
-        ms = ctypes.c_float()
-        rc = self.cu.cuEventElapsedTime(ctypes.byref(ms), a, b)
-        if rc != 0:
-            raise RuntimeError("cuEventElapsedTime failed: %d" % rc)
-        return float(ms.value)
-
-    def close(self):
-        for ev in self.events:
-            self.cu.cuEventDestroy_v2(ev)
-        self.events = []
-
-
 # ------------------------------------------------------------- CPU baseline --
 
 CPU_STRIDE = 2  # the CPU sample takes every 2nd output channel of every call
@@ -224,6 +189,98 @@ def ordinal(i):
     return "%d%s" % (i, "th" if 10 <= i % 100 <= 20 else {1: "st", 2: "nd", 3: "rd"}.get(i % 10, "th"))
 
 
+def oracle_quantize_rows(w, threads):
+    """The oracle quantiser over row blocks on `threads` host threads (each
+    block one oracle call; ctypes releases the interpreter lock): the same
+    codes and scales as one call."""
+    import concurrent.futures as cf
+    import oracle
+    n = w.shape[0]
+    if threads <= 1 or n < 2 * threads:
+        return oracle.quantize(w)
+    edges = [n * i // threads for i in range(threads + 1)]
+    with cf.ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(lambda i: oracle.quantize(w[edges[i]:edges[i + 1]]), range(threads)))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])
+
+
+def cpu_quantize_timing(cores):
+    """The oracle quantiser timed on the host: the gate weight's first 2048
+    rows on one thread, and the whole gate weight on all cores."""
+    c = synthetic.case("decode_stack", 1, "gate")
+    w = c["w"]
+    sub = np.ascontiguousarray(w[:2048])
+    t0 = time.perf_counter()
+    oracle_quantize_rows(sub, 1)
+    dt1 = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle_quantize_rows(w, cores)
+    dtn = time.perf_counter() - t0
+    b1 = 5 * sub.size + 4 * sub.shape[0]
+    bn = 5 * w.size + 4 * w.shape[0]
+    return {"single_thread": {"gbs": round(b1 / dt1 / 1e9, 4), "seconds": round(dt1, 3), "cores": 1,
+                              "sample": "gate [14336 x 4096], its first 2048 rows"},
+            "all_cores": {"gbs": round(bn / dtn / 1e9, 4), "seconds": round(dtn, 3), "cores": cores,
+                          "sample": "gate [14336 x 4096], all rows, split over the threads"},
+            "unit": "GB/s", "bytes": "5 B per weight + 4 B per row", "kind": "oracle"}
+
+
+def _rel_cos(y_bits, ref_bits, act):
+    """rel_l2 over all outputs and the least per-row (per-token) cosine, fp64."""
+    def vals(b):
+        b = np.asarray(b, dtype=np.uint16)
+        if act == synthetic.ACT_F16:
+            return b.view(np.float16).astype(np.float64)
+        return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    y, r = vals(y_bits), vals(ref_bits)
+    rel = float(np.linalg.norm(y - r) / max(np.linalg.norm(r), 1e-300))
+    num = np.sum(y * r, axis=1)
+    den = np.linalg.norm(y, axis=1) * np.linalg.norm(r, axis=1)
+    cos = float(np.min(np.where(den > 0, num / np.where(den > 0, den, 1.0), 1.0)))
+    return rel, cos, float(np.mean(np.asarray(y_bits) == np.asarray(ref_bits)))
+
+
+def accuracy_report(gpu_ys, cores):
+    """The contract's report on every configuration: the weight error report
+    fp8_error(weight, q, scale) of each weight (rel_l2, worst channel,
+    underflow, crest), and the outputs the bench's GPU run produced against
+    the oracle (rel_l2, least per-token cosine, share bit-equal; every
+    channel of the small cases, every 4th of the 58.7 MB and decode-stack
+    weights)."""
+    import oracle
+    weights = {}
+    cases = {}
+    worst_rel, worst_cos = 0.0, 1.0
+    for key, ybits in gpu_ys.items():
+        name, m, matrix = key
+        c = synthetic.case(name, m, matrix) if name == "decode_stack" else \
+            synthetic.case(name, m) if name == "skinny_sweep" else synthetic.case(name)
+        wkey = (name, matrix)
+        if wkey not in weights:
+            codes, scales = oracle_quantize_rows(c["w"], cores)
+            rep = oracle.fp8_error(c["w"], codes, scales)
+            weights[wkey] = (codes, scales, {kk: round(float(v), 6) for kk, v in rep.items()})
+        codes, scales, _ = weights[wkey]
+        n = c["n"]
+        stride = 1 if n * c["k"] <= 2 ** 24 else 4
+        cols = np.arange(0, n, stride)
+        bias = None if c["bias"] is None else c["bias"][cols]
+        ref = oracle.linear(c["x"], c["act"], codes[cols], scales[cols], bias, threads=cores)
+        rel, cos, eq = _rel_cos(ybits[:, cols], ref, c["act"])
+        label = name if name in ("tiny_gemv", "outlier_gemv", "fp16_template") else \
+            "%s@M%d" % (name, m) if name == "skinny_sweep" else "%s@M%d" % (matrix, m)
+        cases[label] = {"rel_l2": float("%.3g" % rel), "min_cosine": round(cos, 7), "bit_equal": round(eq, 4),
+                        "channels": "all" if stride == 1 else "every %s" % ordinal(stride)}
+        worst_rel, worst_cos = max(worst_rel, rel), min(worst_cos, cos)
+    return {"max_rel_l2": float("%.3g" % worst_rel), "min_cosine": round(worst_cos, 7),
+            "gates": {"rel_l2": 2e-3, "min_cosine": 0.9999},
+            "fp8_error": {("%s:%s" % wk if wk[1] else wk[0]): rep for wk, (_, _, rep) in weights.items()},
+            "cases": cases,
+            "note": "weight report of fp8_error(weight, q, scale): rel_l2 = ||W - Wq||_F / ||W||_F, worst "
+                    "channel's, share of nonzero weights whose code is +-0, largest amax / rms of a row; outputs "
+                    "of the bench's own GPU run against the oracle's fp64 result rounded once"}
+
+
 def cpu_baseline_obj(gbs, dt, cores, stride=None):
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
             "sample": "the full step (21 calls, M=1,8,32) restricted to every %s output channel; "
@@ -253,18 +310,50 @@ def build_state(torch, fw, dev, replicas=2):
     return mats, wdev, xs, ys
 
 
-def enqueue_step(fw, mats, xs, ys, events=None, ev_list=None, stream_handle=None):
+def enqueue_step(fw, mats, xs, ys, weights_ready=True):
     launches = 0
-    for i, (m, name, n, k) in enumerate(step_calls()):
+    for (m, name, n, k) in step_calls():
         mt = mats[name]
         rep = synthetic.DECODE_STACK_M.index(m) % len(mt["codes"])
-        if events is not None:
-            events.record(ev_list[i], stream_handle)
-        fw.linear(xs[(m, name)], mt["codes"][rep], mt["scales"], mt["bias"], out=ys[(m, name)])
+        fw.linear(xs[(m, name)], mt["codes"][rep], mt["scales"], mt["bias"], out=ys[(m, name)],
+                  weights_ready=weights_ready)
         launches += 1
-    if events is not None:
-        events.record(ev_list[len(step_calls())], stream_handle)
     return launches
+
+
+def replay_us(torch, s, launch, launches, reps=5):
+    """Median device time per launch (us) of `launches` calls launch(i)
+    captured in one CUDA graph and replayed back to back (CUDA events on the
+    launching stream, after a warm-up replay)."""
+    with torch.cuda.stream(s):
+        launch(0)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(launches):
+            launch(i)
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3 / launches)
+    del g
+    return float(np.median(times))
+
+
+REPLICA_BYTES = 400 * 2 ** 20   # weight replicas of a directly timed call: > 3x the 129 MB L2
+
+
+def replicas(torch, codes, scales):
+    nrep = max(3, -(-REPLICA_BYTES // (codes.numel() * codes.element_size())))
+    return [(codes, scales)] + [(codes.clone(), scales.clone()) for _ in range(nrep - 1)]
 
 
 def kernel_name(m, k):
@@ -523,6 +612,167 @@ def run_prefill(torch, fw, dev, s, m=2048, launches=10):
             "kernel": "fp8w::prefill_kernel<256, 1>"}
 
 
+def direct_calls(torch, fw, mats, xs, dev, s, launches=40):
+    """Every call of the step timed alone: its launches graph-replayed back
+    to back over weight replicas larger than L2 (weights ready, as in the
+    step).  Returns {(m, name): us per launch}."""
+    out = {}
+    for (name, n, k) in synthetic.DECODE_STACK:
+        mt = mats[name]
+        reps = replicas(torch, mt["codes"][0], mt["scales"])
+        for m in synthetic.DECODE_STACK_M:
+            x = xs[(m, name)]
+            y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+
+            def launch(i, x=x, y=y):
+                cd, sd = reps[i % len(reps)]
+                fw.linear(x, cd, sd, mt["bias"], out=y, weights_ready=True)
+            out[(m, name)] = replay_us(torch, s, launch, launches)
+        del reps
+    return out
+
+
+def time_case(torch, fw, dev, s, c, weights_ready=True, launches=40):
+    """One configuration (synthetic.case dict) timed directly: device us per
+    launch over weight replicas larger than L2, and its algorithmic bytes."""
+    w = torch.from_numpy(c["w"]).to(dev)
+    codes, scales = fw.quantize(w)
+    del w
+    torch.cuda.synchronize()
+    dt = torch.bfloat16 if c["act"] == synthetic.ACT_BF16 else torch.float16
+    x = torch.from_numpy(np.ascontiguousarray(c["x"]).view(np.int16)).to(dev).view(dt)
+    bias = None if c["bias"] is None else torch.from_numpy(c["bias"]).to(dev)
+    y = torch.empty((c["m"], c["n"]), dtype=dt, device=dev)
+    reps = replicas(torch, codes, scales)
+
+    def launch(i):
+        cd, sd = reps[i % len(reps)]
+        fw.linear(x, cd, sd, bias, out=y, weights_ready=weights_ready)
+    us = replay_us(torch, s, launch, launches)
+    del reps
+    return us, call_bytes(c["m"], c["n"], c["k"], with_bias=c["bias"] is not None)
+
+
+def run_configs(torch, fw, dev, s, peak):
+    """The workload's configurations, each timed directly: tiny GEMV,
+    outlier GEMV, the skinny sweep at M = 1..32 on K = 4096, N = 14336 with
+    t(M) / t(1), the 58.7 MB weight at M = 1 in both orientations, and the
+    fp16 template (cold L2)."""
+    def entry(us, nbytes, m, n, k):
+        gbs = nbytes / us / 1e3
+        return {"us": round(us, 3), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                "tflops": round(2 * m * n * k / us / 1e6, 3), "bytes": nbytes}
+    out = {}
+    for name in ("tiny_gemv", "outlier_gemv", "fp16_template"):
+        c = synthetic.case(name)
+        us, nb = time_case(torch, fw, dev, s, c)
+        out[name] = entry(us, nb, c["m"], c["n"], c["k"])
+    sweep = {}
+    for m in (1,) + synthetic.SKINNY_M:
+        c = synthetic.case("skinny_sweep", m)
+        us, nb = time_case(torch, fw, dev, s, c)
+        sweep[str(m)] = entry(us, nb, m, c["n"], c["k"])
+    t1 = sweep["1"]["us"]
+    for m in synthetic.SKINNY_M:
+        sweep[str(m)]["t_over_t1"] = round(sweep[str(m)]["us"] / t1, 3)
+    out["skinny_sweep"] = sweep
+    # the north-star targets: M = 1 at >= 80% of the HBM peak on the 58.7 MB
+    # weight (both orientations), and t(M) <= 1.3 t(1) up to M = 32
+    c3 = synthetic.case("decode_stack", 1, "down")
+    us3, nb3 = time_case(torch, fw, dev, s, c3)
+    out["m1_targets"] = {
+        "gate_14336x4096": dict(sweep["1"], target_frac=0.8, met=sweep["1"]["frac"] >= 0.8),
+        "down_4096x14336": dict(entry(us3, nb3, 1, c3["n"], c3["k"]), target_frac=0.8),
+        "max_t_over_t1": max(sweep[str(m)]["t_over_t1"] for m in synthetic.SKINNY_M), "target_t_over_t1": 1.3}
+    out["m1_targets"]["down_4096x14336"]["met"] = out["m1_targets"]["down_4096x14336"]["frac"] >= 0.8
+    out["note"] = ("each case timed alone: graph-replayed back-to-back launches over weight replicas larger than "
+                   "L2 (cold L2), weights ready; frac of the measured HBM peak")
+    return out
+
+
+def run_w8a8(torch, fw, dev, s, peak):
+    """The W8A8 path: per-token activation quantisation, then the e4m3 x e4m3
+    tensor-core GEMM, on the gate and down weights at M = 1, 8, 32, and the
+    prefill shape against the fp8 tensor peak."""
+    out = {}
+    for name in ("gate", "down"):
+        c = synthetic.case("decode_stack", 32, name)
+        n, k = c["n"], c["k"]
+        w = torch.from_numpy(c["w"]).to(dev)
+        codes, scales = fw.quantize(w)
+        del w
+        bias = torch.from_numpy(c["bias"]).to(dev)
+        reps = replicas(torch, codes, scales)
+        for m in synthetic.DECODE_STACK_M:
+            x = torch.from_numpy(np.ascontiguousarray(c["x"][:m]).view(np.int16)).to(dev).view(torch.bfloat16)
+            qx, sx = fw.quantize_act(x)
+            y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+
+            def gemm(i):
+                cd, sd = reps[i % len(reps)]
+                fw.linear_w8a8(qx, sx, cd, sd, bias, out=y, weights_ready=True)
+
+            def both(i):
+                fw.quantize_act(x, qx, sx)
+                gemm(i)
+            us_g = replay_us(torch, s, gemm, 40)
+            us_b = replay_us(torch, s, both, 40)
+            nb = n * k + 8 * n + m * k + 4 * m + 2 * m * n
+            out["%s@M%d" % (name, m)] = {"gemm_us": round(us_g, 3), "gemm_gbs": round(nb / us_g / 1e3, 1),
+                                         "gemm_frac": round(nb / us_g / 1e3 / peak, 4),
+                                         "with_activation_quantise_us": round(us_b, 3)}
+        del reps
+    # prefill: compute-bound; the fp8 peak is the measured bf16 peak times
+    # the nominal fp8 / bf16 ratio (4.5 / 2.25 PFLOP/s)
+    c = synthetic.case("decode_stack", 1, "gate")
+    n, k = c["n"], c["k"]
+    w = torch.from_numpy(c["w"]).to(dev)
+    codes, scales = fw.quantize(w)
+    del w
+    m = 2048
+    x = torch.from_numpy(synthetic.to_bf16_bits(np.random.default_rng(m).standard_normal((m, k)).astype(np.float32))
+                         .view(np.int16)).to(dev).view(torch.bfloat16)
+    qx, sx = fw.quantize_act(x)
+    y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+    us = replay_us(torch, s, lambda i: fw.linear_w8a8(qx, sx, codes, scales, None, out=y), 10)
+    bf, src = bf16_peak()
+    tf = 2.0 * m * n * k / us / 1e6
+    out["prefill_gate_m2048"] = {"us": round(us, 2), "tflops": round(tf, 1), "peak_tflops": 2 * bf,
+                                 "frac_of_fp8_peak": round(tf / (2 * bf), 4),
+                                 "peak_source": src + " x 2 (nominal fp8 / bf16 dense ratio)"}
+    out["note"] = ("gemm: fp8w_linear_w8a8 alone, weights ready, graph-replayed over weight replicas larger than L2; "
+                   "bytes = codes + scales + bias + activation codes and scales + y; with_activation_quantise adds "
+                   "fp8w_quantize_act of the bf16 activations in front of every call")
+    return out
+
+
+def gpu_outputs(torch, fw, dev, ys):
+    """Outputs of the GPU path on every configuration, for the accuracy
+    report: the decode stack's from the last timed step, the others from one
+    call each (weights quantised on the GPU)."""
+    out = {}
+    torch.cuda.synchronize()
+    for (m, name, n, k) in step_calls():
+        out[("decode_stack", m, name)] = ys[(m, name)].view(torch.int16).cpu().numpy().view(np.uint16)
+    cases = [("tiny_gemv", None), ("outlier_gemv", None), ("fp16_template", None)] + \
+        [("skinny_sweep", m) for m in (1,) + synthetic.SKINNY_M]
+    codes = scales = None
+    for name, m in cases:
+        c = synthetic.case(name, m) if m is not None else synthetic.case(name)
+        if name != "skinny_sweep" or codes is None:
+            w = torch.from_numpy(c["w"]).to(dev)
+            codes, scales = fw.quantize(w)
+            del w
+        dt = torch.bfloat16 if c["act"] == synthetic.ACT_BF16 else torch.float16
+        x = torch.from_numpy(np.ascontiguousarray(c["x"]).view(np.int16)).to(dev).view(dt)
+        bias = None if c["bias"] is None else torch.from_numpy(c["bias"]).to(dev)
+        y = fw.linear(x, codes, scales, bias)
+        out[(name, m, None)] = y.view(torch.int16).cpu().numpy().view(np.uint16)
+        if name != "skinny_sweep":
+            codes = None
+    return out
+
+
 def run_ours(args, torch, dist):
     import fp8_weight_only_gb300 as fw
     ws, rank, local = dist_env()
@@ -574,33 +824,29 @@ def run_ours(args, torch, dist):
     n_ranks = ws
     value = job_value(step_bytes(), n_ranks, args.steps, ms_total)
 
-    # instrumented replay: external events between the launches inside a graph
-    per_call = None
-    try:
-        evs = DriverEvents()
-        ev_list = [evs.create() for _ in range(len(step_calls()) + 1)]
-        gi = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(gi, stream=s):
-            enqueue_step(fw, mats, xs, ys, evs, ev_list, s.cuda_stream)
-        reps = max(3, min(args.steps, 20))
-        acc = np.zeros(len(step_calls()))
-        for _ in range(2):
-            gi.replay()
-        torch.cuda.synchronize()
-        for _ in range(reps):
-            gi.replay()
-            torch.cuda.synchronize()
-            acc += [evs.elapsed_ms(ev_list[i], ev_list[i + 1]) for i in range(len(step_calls()))]
-        per_call_raw = acc / reps
-        # the events between launches keep consecutive kernels from
-        # overlapping (programmatic dependent launch), so the instrumented
-        # step is longer than the timed one: durations are scaled to the timed
-        # step, keeping each call's share
-        per_call = per_call_raw * (ms_step / float(per_call_raw.sum()))
-        del gi
-    except (OSError, RuntimeError) as e:  # pragma: no cover - reported in the JSON
-        per_call = None
-        instr_err = str(e)
+    # the same step without FP8W_FLAG_WEIGHTS_READY (every kernel waits for
+    # the previous one before its first code copy)
+    gnf = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gnf, stream=s):
+        enqueue_step(fw, mats, xs, ys, weights_ready=False)
+    nf_steps = max(3, min(args.steps, 500))
+    for _ in range(args.warmup):
+        gnf.replay()
+    torch.cuda.synchronize()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        f0.record(s)
+        for _ in range(nf_steps):
+            gnf.replay()
+        f1.record(s)
+    torch.cuda.synchronize()
+    ms_nf = f0.elapsed_time(f1) / nf_steps
+    del gnf
+
+    # every call of the step timed alone (direct device times, not shares of
+    # the step): the per-kernel and per-M figures and the roofline use these
+    per_call = direct_calls(torch, fw, mats, xs, dev, s)
     peak, peak_src = peaks()
 
     result = {"metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
@@ -612,7 +858,9 @@ def run_ours(args, torch, dist):
                          "bytes_per_step": step_bytes(), "flops_per_step": step_flops(),
                          "l2": "inputs larger than L2: 654 MB of codes per step, two weight replicas "
                                "alternate between the M passes",
-                         "graph": "step captured in one CUDA graph", "parallelism": "replicas (dp%d)" % ws},
+                         "graph": "step captured in one CUDA graph", "parallelism": "replicas (dp%d)" % ws,
+                         "weights_ready": "FP8W_FLAG_WEIGHTS_READY on every call: the weights are quantised and "
+                                          "synchronised before the timed region, as a serving loop loads them"},
               "clocks": clocks, "gpu_launches": launches_per_step * args.steps,
               "frac_of_hbm_peak": round(value / n_ranks / peak, 4), "peak_source": peak_src,
               "tflops": round(step_flops() * n_ranks / (ms_step / 1e3) / 1e12, 2),
@@ -620,48 +868,55 @@ def run_ours(args, torch, dist):
                          "ms_per_step_p10": round(float(np.percentile(chunk_ms, 10)), 5),
                          "ms_per_step_median": round(float(np.median(chunk_ms)), 5),
                          "ms_per_step_p90": round(float(np.percentile(chunk_ms, 90)), 5),
-                         "note": "per-step time of each of the chunks the timed steps fall into (rank 0)"}}
+                         "note": "per-step time of each of the chunks the timed steps fall into (rank 0)"},
+              "without_weights_ready": {"value": round(job_value(step_bytes(), n_ranks, 1, ms_nf), 2), "unit": "GB/s",
+                                        "ms_per_step": round(ms_nf, 5), "steps": nf_steps,
+                                        "note": "the same step, every call waiting for the previous kernel before "
+                                                "its first code copy"}}
 
-    if per_call is not None:
-        calls = step_calls()
-        by_kernel = {}
-        by_m = {}
-        for (m, name, n, k), ms in zip(calls, per_call):
-            kn = kernel_name(m, k)
-            d = by_kernel.setdefault(kn, {"ms": 0.0, "bytes": 0, "launches": 0})
-            d["ms"] += ms
-            d["bytes"] += call_bytes(m, n, k)
-            d["launches"] += 1
-            e = by_m.setdefault(m, {"ms": 0.0, "bytes": 0})
-            e["ms"] += ms
-            e["bytes"] += call_bytes(m, n, k)
-        total = sum(d["ms"] for d in by_kernel.values())
-        top = max(by_kernel, key=lambda kk: by_kernel[kk]["ms"])
-        d = by_kernel[top]
-        achieved = d["bytes"] / d["launches"] / (d["ms"] / d["launches"] / 1e3) / 1e9
-        traffic, traffic_src = stored_traffic(top)
-        result["roofline"] = {"bound": "hbm", "kernel": top, "achieved": round(achieved, 1),
-                              "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                              "traffic": traffic, "traffic_source": traffic_src,
-                              "algorithmic_bytes_per_launch": round(d["bytes"] / d["launches"]),
-                              "share": round(d["ms"] / total, 4),
-                              "note": "achieved = algorithmic bytes per launch / mean launch duration; durations "
-                                      "from device events between the launches of an instrumented graph replay, "
-                                      "scaled so that the calls add up to the timed step (shares kept); "
-                                      "peak is " + peak_src}
-        result["kernels"] = {kk: {"share": round(v["ms"] / total, 4), "launches_per_step": v["launches"],
-                                  "ms_per_step": round(v["ms"], 5),
-                                  "gbs": round(v["bytes"] / (v["ms"] / 1e3) / 1e9, 1)}
-                             for kk, v in by_kernel.items()}
-        result["per_m"] = {str(m): {"ms": round(v["ms"], 5), "gbs": round(v["bytes"] / (v["ms"] / 1e3) / 1e9, 1),
-                                    "frac": round(v["bytes"] / (v["ms"] / 1e3) / 1e9 / peak, 4)}
-                           for m, v in by_m.items()}
-        result["per_call_us"] = {"%s@M%d" % (name, m): round(ms * 1e3, 2)
-                                 for (m, name, n, k), ms in zip(calls, per_call)}
-        result["instrumented_step_ms"] = round(float(per_call_raw.sum()), 5)
-    else:
-        result["roofline"] = {"bound": "hbm", "achieved": None, "peak": peak, "unit": "GB/s", "frac": None,
-                              "traffic": None, "note": "instrumented replay failed: " + instr_err}
+    calls = step_calls()
+    by_kernel = {}
+    by_m = {}
+    for (m, name, n, k) in calls:
+        us = per_call[(m, name)]
+        kn = kernel_name(m, k)
+        d = by_kernel.setdefault(kn, {"us": 0.0, "bytes": 0, "launches": 0})
+        d["us"] += us
+        d["bytes"] += call_bytes(m, n, k)
+        d["launches"] += 1
+        e = by_m.setdefault(m, {"us": 0.0, "bytes": 0})
+        e["us"] += us
+        e["bytes"] += call_bytes(m, n, k)
+    total = sum(d["us"] for d in by_kernel.values())
+    top = max(by_kernel, key=lambda kk: by_kernel[kk]["us"])
+    d = by_kernel[top]
+    achieved = d["bytes"] / d["us"] / 1e3   # bytes per launch / mean launch time, GB/s
+    traffic, traffic_src = stored_traffic(top)
+    result["roofline"] = {"bound": "hbm", "kernel": top, "achieved": round(achieved, 1),
+                          "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                          "traffic": traffic, "traffic_source": traffic_src,
+                          "algorithmic_bytes_per_launch": round(d["bytes"] / d["launches"]),
+                          "mean_launch_us": round(d["us"] / d["launches"], 3),
+                          "share": round(d["us"] / total, 4),
+                          "note": "achieved = algorithmic bytes per launch / mean device time per launch, each of "
+                                  "the kernel's calls of the step timed directly (CUDA events around "
+                                  "graph-replayed back-to-back launches of that call over weight replicas larger "
+                                  "than L2, on the launching stream); share = its part of the summed call times; "
+                                  "peak is " + peak_src}
+    result["kernels"] = {kk: {"share": round(v["us"] / total, 4), "launches_per_step": v["launches"],
+                              "us_per_step": round(v["us"], 3),
+                              "gbs": round(v["bytes"] / v["us"] / 1e3, 1),
+                              "frac": round(v["bytes"] / v["us"] / 1e3 / peak, 4)}
+                         for kk, v in by_kernel.items()}
+    result["per_m"] = {str(m): {"us": round(v["us"], 3), "gbs": round(v["bytes"] / v["us"] / 1e3, 1),
+                                "frac": round(v["bytes"] / v["us"] / 1e3 / peak, 4)}
+                       for m, v in by_m.items()}
+    result["per_call_us"] = {"%s@M%d" % (name, m): round(per_call[(m, name)], 2) for (m, name, n, k) in calls}
+    result["per_call_note"] = ("each call timed alone (direct device time per launch); their sum, %.1f us, exceeds "
+                               "the step's %.1f us because the step's launches overlap (programmatic dependent "
+                               "launch)" % (total, ms_step * 1e3))
+    result["configs"] = run_configs(torch, fw, dev, s, peak)
+    result["w8a8"] = run_w8a8(torch, fw, dev, s, peak)
 
     result["fused_stack"] = run_fused(torch, fw, mats, xs, dev, s, min(args.steps, 500), args.warmup, peak)
 
@@ -860,6 +1115,8 @@ def run_ours(args, torch, dist):
                            "ms_per_step": round(eager_s / args.steps * 1e3, 4),
                            "note": "the same step issued eagerly from Python (21 fp8w.linear calls, two packed "
                                    "copies); host wall clock"}
+    if rank == 0 and not args.no_cpu:
+        result["_gpu_ys"] = gpu_outputs(torch, fw, dev, ys)
     err = fw.device_error()
     if err != 0:
         result["device_error"] = err
@@ -975,6 +1232,7 @@ def main():
         tdist.init_process_group("nccl")
         dist = tdist
     result = run_ours(args, torch, dist)
+    gpu_ys = result.pop("_gpu_ys", None)
     if rank == 0 and not args.no_cpu:
         import oracle
         cores = oracle.host_cores()
@@ -984,6 +1242,9 @@ def main():
         result["cpu_baseline"]["single_thread"] = {
             "value": round(gbs1, 4), "unit": "GB/s", "cores": 1, "seconds": round(dt1, 2),
             "sample": "every %s output channel of every call, one thread" % ordinal(CPU_STRIDE_1T)}
+        result["cpu_baseline"]["quantize"] = cpu_quantize_timing(cores)
+        # the oracle leg also checks this run's outputs and reports the weights' error
+        result["accuracy"] = accuracy_report(gpu_ys, cores)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
