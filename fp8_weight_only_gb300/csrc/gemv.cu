@@ -7,14 +7,20 @@
 // epilogue.
 //
 // GB300 layout of the work:
-//  * Persistent grid, one CTA per SM; CTA c owns the contiguous rows
-//    [c*N/P, (c+1)*N/P), so every SM streams the same bytes (+-1 row).
-//  * The last warp moves a slot of R whole rows (R*K contiguous bytes, up
-//    to 64 KB) per 1-D TMA bulk copy into a ring of slots.  A bulk copy costs
-//    the SM's TMA unit a fixed ~0.27 us whatever its size (measured: 4 KB
-//    copies stream 15 GB/s per SM, 64 KB copies 218 GB/s), so copies are
-//    large.
-//  * The CTA's rows are dealt round-robin to groups of G compute warps (16
+//  * The weight is cut into row blocks of R whole rows (up to 64 KB), one
+//    per CTA of the grid; a CTA does its own block and then, through the
+//    grid scheduler's cluster launch control, cancels CTAs that have not
+//    started yet and does their blocks (one request in flight).  SMs that
+//    free up early take more of the weight, so the launch ends evenly, and
+//    a CTA allowed to start before the previous kernel finishes (weights
+//    ready) streams its own block meanwhile; it asks for more only once
+//    that kernel is done.  Nothing outside the launch keeps count.
+//  * The last warp moves a block (R*K contiguous bytes) per 1-D TMA bulk
+//    copy into a ring of slots.  A bulk copy costs the SM's TMA unit a fixed
+//    ~0.27 us whatever its size (measured: 4 KB copies stream 15 GB/s per
+//    SM, 64 KB copies 218 GB/s), so copies are large (32 and 48 KB blocks
+//    measured slower on the 58.7 MB weights).
+//  * A slot's rows are dealt round-robin to groups of G compute warps (16
 //    warps; G = 1 when a slot holds many rows, more for long rows, so that
 //    two slots keep every warp busy); lane l of the group's warp w takes the
 //    16-code chunks (32w + l) + 32G*j of its rows, and a group of several
@@ -24,8 +30,8 @@
 //    slots ahead would otherwise wait on a slot a full ring cycle early and
 //    pass on the previous phase of the same parity.
 //  * x is staged once in shared memory (widened to fp32 for rows up to 8192
-//    codes, as 16-bit values beyond), and so are the CTA's scales and bias:
-//    after start-up the codes are the only stream.
+//    codes, as 16-bit values beyond); a row's scale and bias are read when
+//    its sum is done.
 //  * Codes are converted exactly by the hardware e4m3x2 -> f16x2 conversion
 //    and widened to fp32, and products go two at a time through the packed
 //    fma.rn.f32x2.  A warp computes two rows at once, so each activation it
@@ -48,7 +54,6 @@ constexpr int kGemvWarps = 16;                       // compute warps
 constexpr int kGemvThreads = 32 * (kGemvWarps + 1);  // + the producer warp
 constexpr int kGemvMaxSlots = 8;
 constexpr uint32_t kGemvSlotTarget = 64 * 1024;      // bytes per bulk copy, up to
-constexpr int kGemvStagedRows = 2048;                // most rows whose scale and bias are staged
 constexpr uint32_t kGemvSmemBudget = 224 * 1024;
 // Largest K the GEMV takes: x (2 bytes a value) and two 64 KB slots fit
 // beside the staged scales.
@@ -58,7 +63,6 @@ struct GemvGeom {
     int rows;         // rows per slot (R)
     int slots;        // slots in the ring (S)
     int g;            // warps per row group (1, 2, 4, 8 or 16)
-    int staged;       // rows of scale and bias staged in shared memory (a multiple of 32)
     uint32_t slot_bytes;
     uint32_t ring_bytes;   // code slots, then (per-group scales) scale slots
     uint32_t sslot_bytes;  // per-group scales: a slot's rows of scales (0 otherwise)
@@ -73,6 +77,32 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
         "l"(src), "r"(bytes), "r"(bar), "l"(pol)
         : "memory");
+}
+
+// Blackwell cluster launch control: ask the grid scheduler to cancel a CTA
+// of this grid that has not started yet, so that this CTA does its work
+// instead.  The 16-byte answer lands at `resp` (shared, 16-byte aligned) and
+// completes `bar` (expecting 16 bytes of transaction).
+__device__ __forceinline__ void cancel_request(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+// The answer: the x index of the cancelled CTA, or -1 if none was left.
+__device__ __forceinline__ int64_t cancel_answer(uint32_t resp) {
+    uint32_t ok, id;
+    asm volatile(
+        "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t.reg .b64 lo, hi;\n\t"
+        "ld.shared.v2.b64 {lo, hi}, [%2];\n\t"
+        "mov.b128 r, {lo, hi};\n\t"
+        "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t"
+        "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+        : "=r"(ok), "=r"(id)
+        : "r"(resp)
+        : "memory");
+    return ok ? static_cast<int64_t>(id) : -1;
 }
 
 // f16x2 -> two fp32 (the halves selected in the register, no extraction).
@@ -173,25 +203,26 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
     const uint32_t ring = smem_u32(smem);
     const int S = geo.slots, R = geo.rows;
-    // layout: ring (codes [S], then group scales [S]) | x [k] | scales, bias [geo.staged] | full, empty [kGemvMaxSlots] |
-    // group partial sums [kGemvWarps][2][kGemvWarps][RP] | abort flag
+    // layout: ring (codes [S], then group scales [S]) | x [k] | full, empty [kGemvMaxSlots] |
+    // group partial sums [kGemvWarps][2][kGemvWarps][RP] | abort flag | slot blocks [kGemvMaxSlots] |
+    // cancel answers [2] (16 B each) | their barriers [2]
     const uint32_t x_bytes = static_cast<uint32_t>(((k * (kF32X ? 4 : 2) + 127) / 128) * 128);
     uint16_t* xs = reinterpret_cast<uint16_t*>(smem + geo.ring_bytes);
-    float* sc_s = reinterpret_cast<float*>(smem + geo.ring_bytes + x_bytes);
-    float* bi_s = sc_s + geo.staged;
-    const uint32_t bar_full = smem_u32(bi_s + geo.staged);
+    const uint32_t bar_full = smem_u32(smem + geo.ring_bytes + x_bytes);
     const uint32_t bar_empty = bar_full + 8 * kGemvMaxSlots;
     auto full = [&](int s) { return bar_full + 8u * s; };
     auto empty = [&](int s) { return bar_empty + 8u * s; };
-    float* red = reinterpret_cast<float*>(smem + geo.ring_bytes + x_bytes + 8u * geo.staged + 16 * kGemvMaxSlots);
+    float* red = reinterpret_cast<float*>(smem + geo.ring_bytes + x_bytes + 16 * kGemvMaxSlots);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(red + kGemvWarps * 2 * kGemvWarps * RP);
+    // the row block of each slot (first row; rows, 0 = no more work)
+    int* slot_row0 = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(red + kGemvWarps * 2 * kGemvWarps * RP) + 16);
+    int* slot_rows = slot_row0 + kGemvMaxSlots;
+    const uint32_t resp0 = smem_u32(slot_rows + kGemvMaxSlots);  // 16-byte aligned (see the layout sizes)
+    auto resp = [&](int i) { return resp0 + 16u * i; };
+    auto cbar = [&](int i) { return resp0 + 32u + 8u * i; };
     const int G = geo.g, groups = kGemvWarps / G;
     const uint32_t sring = ring + static_cast<uint32_t>(S) * geo.slot_bytes;  // group scale slots
 
-    const int64_t P = gridDim.x;
-    const int64_t row0 = blockIdx.x * n / P, row1 = (blockIdx.x + 1) * n / P;
-    const int64_t nrows = row1 - row0;
-    const int64_t nslots = (nrows + R - 1) / R;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (warp == kGemvWarps) {
@@ -199,6 +230,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             mbar_init(full(i), 1);
             mbar_init(empty(i), kGemvWarps);  // one arrival per compute warp
         }
+        if (lane < 2) mbar_init(cbar(lane), 1);
         if (lane == 0) *abort_flag = 0;
         fence_mbar_init();
     }
@@ -214,17 +246,43 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             // the codes (and group scales) may come from the previous kernel,
             // unless the caller states that they were complete before it
             if (!geo.early) pdl_wait();
+            bool waited = !geo.early;
+            // Work: the row blocks of R rows, one per CTA of the grid.  This
+            // CTA does its own block, then cancels CTAs that have not started
+            // yet and does theirs (one request in flight at a time, answers
+            // alternating between two buffers), so SMs that free up early take
+            // more of the weight and the launch ends evenly.  It asks only
+            // once the previous grid is done: a CTA that starts early (while
+            // the previous kernel drains) would otherwise take over blocks it
+            // cannot compute yet, which CTAs starting later would have done.
+            int64_t blk = blockIdx.x;
+            int nreq = 0;             // cancel requests issued
+            bool pending = false;     // one is in flight
+            auto request = [&]() {
+                mbar_arrive_expect_tx(cbar(nreq & 1), 16u);
+                cancel_request(resp(nreq & 1), cbar(nreq & 1));
+                ++nreq;
+                pending = true;
+            };
             int64_t issued = 0;
             int s = 0;
             uint32_t ph = 0;
-            for (int64_t sl = 0; sl < nslots; ++sl) {
+            for (;;) {
                 if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) {
                     *abort_flag = 1;
                     atomicCAS(&g_gemv_error, 0, kErrWaitSlot);
                     break;
                 }
-                const int64_t r0 = row0 + sl * R;
-                const int64_t rows = (row1 - r0) < R ? (row1 - r0) : R;
+                if (blk < 0) {
+                    // no block left: the compute warps stop at this slot
+                    slot_rows[s] = 0;
+                    mbar_arrive(full(s));
+                    break;
+                }
+                const int64_t r0 = blk * R;
+                const int64_t rows = (n - r0) < R ? (n - r0) : R;
+                slot_row0[s] = static_cast<int>(r0);
+                slot_rows[s] = static_cast<int>(rows);
                 const uint32_t bytes = static_cast<uint32_t>(rows * k);
                 if constexpr (kGrouped) {
                     const uint32_t sbytes = static_cast<uint32_t>(rows * geo.ngroups * kScaleBytes);
@@ -241,12 +299,32 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
                     s = 0;
                     ph ^= 1u;
                 }
+                if (!waited) {
+                    pdl_wait();
+                    waited = true;
+                }
+                if (nreq == 0) request();
+                // the next block: the answer to the request in flight
+                blk = -1;
+                if (pending) {
+                    const int q = nreq - 1;
+                    if (!mbar_wait(cbar(q & 1), static_cast<uint32_t>((q >> 1) & 1), abort_flag)) {
+                        *abort_flag = 1;
+                        atomicCAS(&g_gemv_error, 0, kErrWaitSlot);
+                        break;
+                    }
+                    pending = false;
+                    blk = cancel_answer(resp(q & 1));
+                    if (blk >= 0) request();
+                }
             }
             if (*abort_flag) {
-                // let the copies in flight land before the CTA exits
+                // let the copies and the cancel answer in flight land before the CTA exits
                 for (int64_t j = (issued > S ? issued - S : 0); j < issued; ++j)
                     if (!mbar_wait_drain(full(static_cast<int>(j % S)), static_cast<uint32_t>((j / S) & 1)))
                         atomicCAS(&g_gemv_error, 0, kErrWaitDrain);
+                if (pending && !mbar_wait_drain(cbar((nreq - 1) & 1), static_cast<uint32_t>(((nreq - 1) >> 1) & 1)))
+                    atomicCAS(&g_gemv_error, 0, kErrWaitDrain);
             }
         }
         return;
@@ -287,14 +365,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
             }
         }
     }
-    const bool staged = nrows <= geo.staged;
-    if (staged) {
-        for (int64_t i = threadIdx.x; i < nrows; i += 32 * kGemvWarps) {
-            if constexpr (!kGrouped) sc_s[i] = scales[row0 + i];
-            bi_s[i] = bias ? bias[row0 + i] : 0.0f;
-        }
-    }
-    // the staged x, scales and bias are visible to every compute warp
+    // the staged x is visible to every compute warp
     asm volatile("bar.sync %0, %1;" ::"n"(15), "n"(32 * kGemvWarps) : "memory");  // ids 1..8: row groups
 
     const uint32_t xv = smem_u32(xs);
@@ -303,7 +374,7 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     int s = 0;
     uint32_t ph = 0;
     int parity = 0;
-    for (int64_t sl = 0; sl < nslots; ++sl) {
+    for (int64_t sl = 0;; ++sl) {
         bool ok = mbar_wait_warp(full(s), ph, abort_flag);
         if (!ok && lane == 0) {
             *abort_flag = 1;
@@ -313,11 +384,14 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
         // at the group's barrier below
         if (G > 1) ok = !bar_red_or(1 + grp, 32 * G, !ok);
         if (!ok) break;
-        const int64_t base = sl * R;  // CTA-local index of the slot's first row
-        const int rows = static_cast<int>((nrows - base) < R ? (nrows - base) : R);
-        // items of RP consecutive rows, item index (base / RP + r / RP) dealt
-        // round-robin: this group takes the items with index % groups == grp
-        const int64_t gbase = base / RP;
+        // the slot's row block (no rows: no more work)
+        const int rows = slot_rows[s];
+        if (rows == 0) break;
+        const int64_t row0 = slot_row0[s];
+        // items of RP consecutive rows, item index (sl * R / RP + r / RP)
+        // dealt round-robin: this group takes the items with index % groups
+        // == grp
+        const int64_t gbase = sl * R / RP;
         for (int r = static_cast<int>((grp - gbase % groups + groups) % groups) * RP; r < rows; r += groups * RP) {
             const int nr = rows - r < RP ? rows - r : RP;  // rows in this item (the slot's last may be short)
             const uint32_t rowp = ring + s * geo.slot_bytes + static_cast<uint32_t>(r * k);
@@ -396,13 +470,12 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
 #pragma unroll
                 for (int q = 0; q < RP; ++q) {
                     if (q >= nr) break;
-                    const int64_t i = base + r + q;
-                    const float bi = staged ? bi_s[i] : (bias ? bias[row0 + i] : 0.0f);
+                    const int64_t i = row0 + r + q;
+                    const float bi = bias ? bias[i] : 0.0f;
                     if constexpr (kGrouped) {
-                        y[row0 + i] = round_out<kBf16>(sum[q] + bi);  // the scales are applied already
+                        y[i] = round_out<kBf16>(sum[q] + bi);  // the scales are applied already
                     } else {
-                        const float sc = staged ? sc_s[i] : scales[row0 + i];
-                        y[row0 + i] = round_out<kBf16>(fmaf(sum[q], sc, bi));
+                        y[i] = round_out<kBf16>(fmaf(sum[q], scales[i], bi));
                     }
                 }
         }
@@ -416,9 +489,13 @@ __global__ void __launch_bounds__(kGemvThreads, 1)
     }
 }
 
-static uint32_t gemv_fixed_bytes(int64_t k, bool f32x, int staged) {
-    return static_cast<uint32_t>(((k * (f32x ? 4 : 2) + 127) / 128) * 128) + 8u * staged +
-           16 * kGemvMaxSlots + 4 * kGemvWarps * 2 * kGemvWarps * 2 + 16 + 128;
+// Shared memory beside the ring: x, the slot barriers, the row groups'
+// partial sums, the abort flag (16), the slots' row blocks (8 per slot), two
+// cancel answers (16 each) and their barriers (8 each), and 128 of slack
+// for the alignment of the base.
+static uint32_t gemv_fixed_bytes(int64_t k, bool f32x) {
+    return static_cast<uint32_t>(((k * (f32x ? 4 : 2) + 127) / 128) * 128) + 16 * kGemvMaxSlots +
+           4 * kGemvWarps * 2 * kGemvWarps * 2 + 16 + 8 * kGemvMaxSlots + 32 + 16 + 128;
 }
 
 template <bool kBf16>
@@ -430,18 +507,21 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     if (a.k > kGemvMaxK) return cudaErrorNotSupported;
     GemvGeom geo;
-    const int64_t grid = a.n < sms ? a.n : sms;
-    // scale and bias of a CTA's rows (at most ceil(n / grid)) are staged
-    const int64_t per_cta = (a.n + grid - 1) / grid;
-    geo.staged = static_cast<int>(per_cta > kGemvStagedRows ? kGemvStagedRows : (per_cta + 31) / 32 * 32);
-    // a slot holds whole rows, up to kGemvSlotTarget bytes; rows are computed
-    // in pairs, so slots hold an even number (x is staged as fp32 for rows up
-    // to 8192 codes, as 16-bit values beyond)
+    // a slot holds one row block: whole rows, up to kGemvSlotTarget bytes,
+    // and no more than the rows an SM would get if every SM took the same
+    // share (so that small matrices still spread over the GPU); rows are
+    // computed in pairs, so blocks hold an even number (x is staged as fp32
+    // for rows up to 8192 codes, as 16-bit values beyond).  The grid has one
+    // CTA per block; running CTAs take over the blocks of CTAs that have not
+    // started (cluster launch control).
     const int rp = 2;
     const bool f32x = a.k <= 8192;
     int64_t rows = kGemvSlotTarget / a.k;
+    const int64_t share = (a.n + sms - 1) / sms;
+    if (rows > share) rows = share + (share & 1);
     rows -= rows % rp;
     if (rows < rp) rows = rp;
+    const int64_t grid = (a.n + rows - 1) / rows;
     geo.rows = static_cast<int>(rows);
     geo.slot_bytes = static_cast<uint32_t>(((rows * a.k + 127) / 128) * 128);
     // per-group scales: a slot's rows of scales beside its codes
@@ -449,7 +529,7 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     geo.gshift = 0;
     while (grouped && (16 << geo.gshift) < a.group) ++geo.gshift;
     geo.sslot_bytes = static_cast<uint32_t>(((rows * geo.ngroups * sbytes + 127) / 128) * 128);
-    int64_t slots = (kGemvSmemBudget - gemv_fixed_bytes(a.k, f32x, geo.staged)) / (geo.slot_bytes + geo.sslot_bytes);
+    int64_t slots = (kGemvSmemBudget - gemv_fixed_bytes(a.k, f32x)) / (geo.slot_bytes + geo.sslot_bytes);
     if (slots > kGemvMaxSlots) slots = kGemvMaxSlots;
     if (slots < 2) return cudaErrorNotSupported;
     geo.slots = static_cast<int>(slots);
@@ -459,7 +539,7 @@ static cudaError_t launch_dt(const LinearArgs& a, cudaStream_t st) {
     geo.g = 1;
     while (geo.g < kGemvWarps && items * geo.g * 2 < kGemvWarps) geo.g *= 2;
     geo.early = a.early ? 1 : 0;
-    const uint32_t smem = geo.ring_bytes + gemv_fixed_bytes(a.k, f32x, geo.staged);
+    const uint32_t smem = geo.ring_bytes + gemv_fixed_bytes(a.k, f32x);
 
     const int kind = !grouped ? 0 : a.e8m0 ? 2 : 1;
     decltype(&gemv_kernel<2, kBf16, false, 0>) all[6] = {
