@@ -218,7 +218,7 @@ def linear(x, codes, scales, bias=None, out=None, kernel=KERNEL_AUTO, cluster=0,
     m, k = x.shape
     n = codes.shape[0]
     if scales.dim() == 2:
-        # per-group scales [N, K / group]: the GEMV's grouped form (M == 1)
+        # per-group scales [N, K / group] (fp32), or E8M0 bytes [N, K / 32]
         if codes.dim() != 2 or codes.shape[1] != k or scales.shape[0] != n or k % scales.shape[1] or \
                 (mx and scales.shape[1] * 32 != k) or (bias is not None and bias.numel() != n):
             raise ValueError("shape mismatch for per-group scales")

@@ -78,10 +78,17 @@ fp8w_status fp8w_linear_grouped(const void* x, int act_dtype, int64_t m, int64_t
                                 const float* scales, int group, const float* bias, int64_t n, void* y, void* stream) {
     fp8w_status st = check_linear(x, act_dtype, m, k, codes, scales, bias, n, y);
     if (st != FP8W_OK) return st;
-    if (m != 1 || !valid_group(group) || k % (4 * group) != 0 || !fp8w::gemv_supports(k)) return FP8W_ERR_SHAPE;
+    if (!valid_group(group) || k % group != 0) return FP8W_ERR_SHAPE;
     if (!aligned(scales, 16)) return FP8W_ERR_ALIGN;
     fp8w::LinearArgs a{x, act_dtype, m, k, n, codes, scales, bias, y, group};
-    return cuda_status(fp8w::launch_gemv(a, static_cast<cudaStream_t>(stream)), "fp8w_linear_grouped launch");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // m == 1: the GEMV, which bulk-copies each row's scales beside its codes
+    // (k % (4 * group) == 0); otherwise the tensor-core kernels' per-group
+    // form: the prefill GEMM beyond 64 tokens, the skinny kernel below
+    if (m == 1 && k % (4 * group) == 0 && fp8w::gemv_supports(k))
+        return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear_grouped gemv launch");
+    if (use_prefill(m)) return cuda_status(fp8w::launch_prefill(a, s), "fp8w_linear_grouped prefill launch");
+    return cuda_status(fp8w::launch_skinny(a, nullptr, s), "fp8w_linear_grouped tensor-core launch");
 }
 
 fp8w_status fp8w_quantize_mx(const float* w, int64_t n, int64_t k, uint8_t* codes, uint8_t* scales, void* stream) {
@@ -106,9 +113,9 @@ fp8w_status fp8w_linear_mx(const void* x, int act_dtype, int64_t m, int64_t k, c
     // codes (16-byte pieces: k % 512 == 0)
     if (m == 1 && k % 512 == 0 && fp8w::gemv_supports(k))
         return cuda_status(fp8w::launch_gemv(a, s), "fp8w_linear_mx gemv launch");
-    // otherwise a tensor-core kernel, which folds the scales into bf16 weights:
-    // the prefill GEMM beyond 64 tokens, the skinny kernel below
-    if (act_dtype != FP8W_BF16) return FP8W_ERR_DTYPE;
+    // otherwise a tensor-core kernel (the prefill GEMM beyond 64 tokens, the
+    // skinny kernel below): with bf16 activations the scales fold into the
+    // bf16 weights; with fp16, the per-group form decodes each byte to fp32
     if (use_prefill(m)) return cuda_status(fp8w::launch_prefill(a, s), "fp8w_linear_mx prefill launch");
     return cuda_status(fp8w::launch_skinny(a, nullptr, s), "fp8w_linear_mx tensor-core launch");
 }

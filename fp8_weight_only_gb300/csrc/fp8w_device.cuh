@@ -292,6 +292,32 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// The scale forms of the tensor-core kernels: one fp32 scale a row; E8M0
+// bytes per 32 codes folded into the dequantised bf16 weight; per-group
+// scales (fp32, or E8M0 bytes) applied to each group's own accumulator.
+constexpr int kModeRow = 0, kModeMxFold = 1, kModeGrouped = 2;
+
+// E8M0 byte -> fp32: 2^(b - 127); 0 is the subnormal 2^-127, 0xFF NaN.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t b) {
+    return b == 0xFFu ? __uint_as_float(0x7FC00000u) : b == 0u ? __uint_as_float(0x00400000u) : __uint_as_float(b << 23);
+}
+
+// Two fp32 values in one 64-bit register pair (low word = first).
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
+}
+// acc2 += a2 * b2, lane-wise on fp32 pairs (one packed FMA, each lane an
+// IEEE fma rounded to nearest: the same bits as two fmaf).
+__device__ __forceinline__ void ffma2(uint64_t& acc2, uint64_t a2, uint64_t b2) {
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2) : "l"(a2), "l"(b2));
+}
+// tot2[i] += s * (v[2i], v[2i + 1]) for the 16 fp32 values v of a TMEM load.
+__device__ __forceinline__ void ffma2_x16(uint64_t* tot2, const uint32_t (&v)[16], uint64_t s2) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        ffma2(tot2[i], static_cast<uint64_t>(v[2 * i]) | (static_cast<uint64_t>(v[2 * i + 1]) << 32), s2);
+}
+
 // Each thread of the warp writes 8 consecutive 32-bit columns of its lane.
 __device__ __forceinline__ void tmem_st_x8(uint32_t taddr, const uint32_t (&r)[8]) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),

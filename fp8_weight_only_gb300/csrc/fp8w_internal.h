@@ -16,7 +16,7 @@ struct LinearArgs {
     const float* scales;
     const float* bias;  // may be null
     void* y;
-    int64_t group = 0;  // 0: scales[n]; else scales[n, k / group] (GEMV only)
+    int64_t group = 0;  // 0: scales[n]; else scales[n, k / group]
     bool e8m0 = false;  // with group 32: scales are E8M0 bytes, not fp32
     bool early = false; // the weights were complete before the preceding kernel
                         // started: their copies may begin before it finishes
@@ -51,16 +51,17 @@ cudaError_t launch_dequantize_grouped(const uint8_t* codes, const void* scales, 
 cudaError_t launch_gemv(const LinearArgs& a, cudaStream_t st);
 bool gemv_supports(int64_t k);
 
-// K3: any m (16-, 32- or 64-token launches, 64-row slabs beyond); no
-// workspace.  Launch shape: clusters of `cl` CTAs (1..16), each taking `tpc`
+// K3: any m (16-, 32- or 64-token launches, 64-row slabs beyond; the
+// per-group form 16 or 32, 32-row slabs beyond); no workspace.  Launch shape: clusters of `cl` CTAs (1..16), each taking `tpc`
 // consecutive 128-channel tiles; forced == nullptr picks it from the shape.
 struct SkinnyShape {
     int cl;
     int64_t tpc;
 };
 cudaError_t launch_skinny(const LinearArgs& a, const SkinnyShape* forced, cudaStream_t st);
-SkinnyShape skinny_shape(int64_t n, int64_t k, const int* active, int nt);
-bool skinny_shape_valid(const SkinnyShape& sh, int64_t m, int64_t k);
+// grouped: the per-group form (a CTA shares at most one tile)
+SkinnyShape skinny_shape(int64_t n, int64_t k, const int* active, int nt, bool grouped = false);
+bool skinny_shape_valid(const SkinnyShape& sh, int64_t m, int64_t k, bool grouped = false);
 cudaError_t device_sm_count(int& sms);
 // 2-D tiled tensor map with 128-byte swizzle: `inner` x `outer` elements,
 // rows of `row_bytes`, boxes of box_inner x box_outer.

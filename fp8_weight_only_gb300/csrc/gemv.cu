@@ -112,14 +112,6 @@ __device__ __forceinline__ void f16x2_to_f32x2(uint32_t h, float& lo, float& hi)
         : "r"(h));
 }
 
-// Two fp32 values in one 64-bit register pair (low word = first).
-__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
-    return static_cast<uint64_t>(__float_as_uint(lo)) | (static_cast<uint64_t>(__float_as_uint(hi)) << 32);
-}
-// acc2 += a2 * b2, lane-wise on fp32 pairs (one packed FMA).
-__device__ __forceinline__ void ffma2(uint64_t& acc2, uint64_t a2, uint64_t b2) {
-    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2) : "l"(a2), "l"(b2));
-}
 // A 16-bit pair of x widened to an fp32 pair.
 template <bool kBf16>
 __device__ __forceinline__ uint64_t widen_x(uint32_t w) {

@@ -20,6 +20,7 @@
 //               (two accumulators, so the epilogue drains one tile while
 //               the next accumulates)
 //   warps 4-7   epilogue: TMEM -> fmaf(acc, scale, bias) -> bf16/fp16 -> y
+//   warps 16-19 (per-group form only) the second epilogue warpgroup
 //   warps 8-15  two dequantising warpgroups: warpgroup h converts the k-blocks
 //               with h = (index in the tile) % 2, one weight row a thread,
 //               e4m3 -> bf16/fp16 exactly (value * 2^-120 by byte moves, then
@@ -47,7 +48,9 @@ constexpr int kPCodeK = 128;                      // k of a code stage (two k-bl
 constexpr uint32_t kPCodeBytes = kPM * kPCodeK;   // 16 KB
 constexpr uint32_t kPABytes = kPM * kPK * 2;      // 16 KB
 constexpr int kPThreads = 512;
-constexpr int kPMmaWarp = 1, kPXWarp = 2, kPFirstEpiWarp = 4, kPFirstDqWarp = 8;
+constexpr int kPThreadsGrouped = 640;             // + the second epilogue warpgroup
+constexpr int kPMmaWarp = 1, kPXWarp = 2, kPFirstEpiWarp = 4, kPFirstDqWarp = 8, kPSecondEpiWarp = 16;
+constexpr int kPGAcc = 4;                         // per-group form: group accumulators (128 columns each)
 constexpr int kPBarTmem = 1;                      // named barrier: MMA warp + epilogue warps
 
 // Ring depths: the code ring is the deepest, since each CTA streams its
@@ -63,14 +66,17 @@ struct PrefillSmem {
     static constexpr uint32_t kAOff = kCodesOff + kPCS * kPCodeBytes;
     static constexpr uint32_t kXOff = kAOff + kPAS * kPABytes;
     static constexpr uint32_t kBarOff = kXOff + kPXS * kXBytes;
-    // cfull, cempty [kPCS] | afull, aempty [kPAS] | xfull, xempty [kPXS] | dfull, dempty [2] | drain
-    static constexpr uint32_t kNumBars = 2 * kPCS + 2 * kPAS + 2 * kPXS + 4 + 1;
+    // cfull, cempty [kPCS] | afull, aempty [kPAS] | xfull, xempty [kPXS] | dfull, dempty [2] | drain |
+    // gfull, gfree [kPGAcc] (per-group form)
+    static constexpr uint32_t kGBar0 = 2 * kPCS + 2 * kPAS + 2 * kPXS + 4 + 1;
+    static constexpr uint32_t kNumBars = kGBar0 + 2 * kPGAcc;
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;  // TMEM base, abort flag
     static constexpr uint32_t kBytes = kMiscOff + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
     static_assert(kAlloc <= 227 * 1024, "shared memory");
     static constexpr uint32_t kTmemCols = 2 * BN;
     static_assert(kTmemCols <= 512, "TMEM columns");
+    static_assert(kPGAcc * BN <= 512 || BN != 128, "TMEM columns (per-group form)");
 };
 
 __device__ __forceinline__ void prefill_error(int code, volatile int* abort_flag) {
@@ -80,16 +86,31 @@ __device__ __forceinline__ void prefill_error(int code, volatile int* abort_flag
 
 }  // namespace
 
-// kMx: E8M0 scale bytes e8[n, k / 32] instead of per-row scales (page "11.
-// Inference with NVFP4/MXFP8", section "MXFP8-Style FP8"; bf16 only, k % 128
-// == 0): each 32-code group's power of two is folded into the dequantised
-// weight, exactly, and the epilogue adds only the bias.
-template <int BN, bool kBf16, bool kMx>
-__global__ void __launch_bounds__(kPThreads, 1)
+// The scale forms (kMode):
+//  kModeRow      scales[n], in the epilogue.
+//  kModeMxFold   E8M0 scale bytes e8[n, k / 32] (page "11. Inference with
+//                NVFP4/MXFP8", section "MXFP8-Style FP8"; bf16 only, k % 128
+//                == 0): each 32-code group's power of two is folded into the
+//                dequantised weight, exactly, and the epilogue adds only the
+//                bias.
+//  kModeGrouped  one scale per run of gsz = 32, 64 or 128 codes of a row,
+//                fp32 scales[n, k / gsz] or E8M0 bytes e8[n, k / 32] (page
+//                "B04 Precision & Quantization", section "Post-training
+//                quantization versus quantization-aware training", the
+//                granularity table's per-group row).  BN = 128: each group's
+//                MMAs go to their own TMEM accumulator (a ring of kPGAcc), and
+//                eight epilogue warps (two per TMEM lane quarter, 64 tokens
+//                each) add every group's sums times its scale into fp32 totals
+//                held in registers.
+template <int BN, bool kBf16, int kMode>
+__global__ void __launch_bounds__(kMode == kModeGrouped ? kPThreadsGrouped : kPThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                    const float* __restrict__ scales, const uint8_t* __restrict__ e8, const float* __restrict__ bias,
-                   uint16_t* __restrict__ y, int64_t m, int64_t n, int64_t k, int early) {
+                   uint16_t* __restrict__ y, int64_t m, int64_t n, int64_t k, int early, int gsz) {
+    constexpr bool kMx = kMode == kModeMxFold;
+    constexpr bool kGrp = kMode == kModeGrouped;
     static_assert(!kMx || kBf16, "MX-style scales fold into bf16 weights only");
+    static_assert(!kGrp || BN == 128, "per-group form: 128-token tiles");
     using L = PrefillSmem<BN>;
     constexpr int kPCS = L::kPCS, kPAS = L::kPAS, kPXS = L::kPXS;
     extern __shared__ uint8_t smem_raw[];
@@ -105,6 +126,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
     auto dfull = [&](int d) { return bar0 + 8u * (2 * kPCS + 2 * kPAS + 2 * kPXS + d); };
     auto dempty = [&](int d) { return bar0 + 8u * (2 * kPCS + 2 * kPAS + 2 * kPXS + 2 + d); };
     const uint32_t drain = bar0 + 8u * (2 * kPCS + 2 * kPAS + 2 * kPXS + 4);
+    auto gfull = [&](int b) { return bar0 + 8u * (L::kGBar0 + b); };
+    auto gfree = [&](int b) { return bar0 + 8u * (L::kGBar0 + kPGAcc + b); };
+    constexpr uint32_t kTmemCols = kGrp ? 512u : L::kTmemCols;
+    constexpr int kEpiWarps = kGrp ? 8 : 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOff + 4);
 
@@ -133,6 +158,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 mbar_init(dempty(d), 4);  // the four epilogue warps
             }
             mbar_init(drain, 1);
+            for (int b = 0; b < kPGAcc; ++b) {
+                mbar_init(gfull(b), 1);           // MMA commit
+                mbar_init(gfree(b), kEpiWarps);   // every epilogue warp (per-group form)
+            }
             *abort_flag = 0;
             tma_prefetch_desc(&map_codes);
             tma_prefetch_desc(&map_x);
@@ -143,13 +172,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
     pdl_launch_dependents();
 
     uint32_t tmem = 0;
-    if (warp == kPMmaWarp || (warp >= kPFirstEpiWarp && warp < kPFirstDqWarp)) {
+    const bool epi_warp = (warp >= kPFirstEpiWarp && warp < kPFirstDqWarp) || (kGrp && warp >= kPSecondEpiWarp);
+    if (warp == kPMmaWarp || epi_warp) {
         if (warp == kPMmaWarp) {
-            tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+            tmem_alloc(smem_u32(tmem_slot), kTmemCols);
             tmem_relinquish();
         }
         tc_fence_before();
-        asm volatile("bar.sync %0, %1;" ::"n"(kPBarTmem), "n"(32 * 5) : "memory");
+        asm volatile("bar.sync %0, %1;" ::"n"(kPBarTmem), "n"(32 * (1 + kEpiWarps)) : "memory");
         tc_fence_after();
         tmem = *tmem_slot;
     }
@@ -213,6 +243,123 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 for (int64_t i = (kb_n > kPXS ? kb_n - kPXS : 0); i < kb_n; ++i)
                     if (!mbar_wait_drain(xfull(static_cast<int>(i % kPXS)), static_cast<uint32_t>((i / kPXS) & 1)))
                         atomicCAS(&g_prefill_error, 0, 4000 + kErrWaitDrain);
+            }
+        }
+    } else if (kGrp && warp == kPMmaWarp) {
+        // ------------------------------------- MMA issue, per-group form --
+        // The MMA at k = kg starts group kg / gsz when kg % gsz == 0 (into
+        // accumulator Gc % kPGAcc, once the epilogue has drained its last
+        // group) and ends it when kg + 16 reaches the next multiple of gsz
+        // (k % gsz == 0, so no group is cut off by the end of k).
+        constexpr uint32_t idesc = idesc_f16(kBf16, BN);
+        int64_t kb_n = 0;
+        int Gc = 0, gb = 0;  // groups issued (below 2^31), and the current one's accumulator
+        uint32_t g_tmem = tmem;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            for (int j = 0; j < nkb; ++j, ++kb_n) {
+                const int as = static_cast<int>(kb_n % kPAS), xs = static_cast<int>(kb_n % kPXS);
+                if (!mbar_wait_warp(afull(as), static_cast<uint32_t>((kb_n / kPAS) & 1), abort_flag) ||
+                    !mbar_wait_warp(xfull(xs), static_cast<uint32_t>((kb_n / kPXS) & 1), abort_flag)) {
+                    if (lane == 0) prefill_error(kErrWaitDequant, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a_addr = sbase + L::kAOff + as * kPABytes;
+                const uint32_t x_addr = sbase + L::kXOff + xs * L::kXBytes;
+#pragma unroll
+                for (int kk = 0; kk < kPK / 16; ++kk) {
+                    const int64_t kg = static_cast<int64_t>(j) * kPK + kk * 16;
+                    if (kg >= k) break;
+                    const int qg = static_cast<int>(kg & (gsz - 1));
+                    if (qg == 0) {
+                        gb = Gc & (kPGAcc - 1);
+                        if (!mbar_wait_warp(gfree(gb), static_cast<uint32_t>(((Gc / kPGAcc) & 1) ^ 1), abort_flag)) {
+                            if (lane == 0) prefill_error(kErrWaitMma, abort_flag);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        g_tmem = tmem + static_cast<uint32_t>(gb * BN);
+                    }
+                    mma_f16_ss_warp(g_tmem, smem_desc_sw128_kmajor(a_addr + kk * 32),
+                                    smem_desc_sw128_kmajor(x_addr + kk * 32), idesc, qg != 0);
+                    if (qg + 16 == gsz) {
+                        tc_commit_warp(gfull(gb));
+                        ++Gc;
+                    }
+                }
+                // both stages are free once these MMAs have read them
+                tc_commit_warp(aempty(as));
+                tc_commit_warp(xempty(xs));
+                __syncwarp();
+                if (!ok) break;
+            }
+        }
+        // every MMA issued above completes before TMEM is released
+        tc_commit_warp(drain);
+        if (!mbar_wait_drain(drain, 0) && lane == 0) atomicCAS(&g_prefill_error, 0, 4000 + kErrWaitDrain);
+        __syncwarp();
+    } else if (kGrp && epi_warp) {
+        // --------------------------------------- epilogue, per-group form --
+        // Warps 4-7 take tokens 0-63 of a tile, warps 16-19 tokens 64-127
+        // (warp w reads TMEM lanes 32 (w % 4) ..); thread r holds weight row
+        // r's totals for its 64 tokens as fp32 pairs.
+        const int quarter = warp & 3;
+        const int half = warp >= kPSecondEpiWarp ? 1 : 0;
+        const int r = quarter * 32 + lane;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(half * 64);
+        const int nsc = static_cast<int>(e8 ? (k >> 5) : k / gsz);  // scales a row == groups a tile
+        auto scale_at = [&](int64_t col, int j) -> float {
+            if (col >= n) return 0.0f;  // rows past n hold zero codes
+            return e8 ? e8m0_to_f32(__ldg(e8 + col * nsc + j)) : __ldg(scales + col * nsc + j);
+        };
+        pdl_wait();  // y may still be read, and the scales written, by the previous kernel
+        int Gc = 0;  // groups drained (below 2^31: tiles a CTA x k / 32)
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+            const int64_t cb = t / token_tiles, tb = t - cb * token_tiles;
+            const int64_t col = cb * kPM + r;
+            const int64_t tok0 = tb * BN;
+            const int ntok = static_cast<int>(m - tok0 < BN ? m - tok0 : BN);
+            const int mine = ntok - half * 64;  // tokens of this warp's half (may be <= 0)
+            uint64_t tot2[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) tot2[i] = 0ull;
+            float s_next = scale_at(col, 0);
+            for (int gi = 0; gi < nsc; ++gi, ++Gc) {
+                const float s = s_next;
+                if (gi + 1 < nsc) s_next = scale_at(col, gi + 1);
+                const int gb = Gc & (kPGAcc - 1);
+                if (!mbar_wait_warp(gfull(gb), static_cast<uint32_t>((Gc / kPGAcc) & 1), abort_flag)) {
+                    if (lane == 0) prefill_error(kErrWaitMma, abort_flag);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t s2 = pack2(s, s);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (c * 16 >= mine) break;
+                    uint32_t v[16];
+                    tmem_ld_x16(lane_addr + static_cast<uint32_t>(gb * BN + c * 16), v);
+                    tmem_wait_ld();
+                    ffma2_x16(tot2 + c * 8, v, s2);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(gfree(gb));
+            }
+            if (!ok) break;
+            if (col < n) {
+                const float b = bias ? bias[col] : 0.0f;
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    if (i >= mine) break;
+                    const float v = __uint_as_float(static_cast<uint32_t>(tot2[i >> 1] >> (32 * (i & 1))));
+                    y[(tok0 + half * 64 + i) * n + col] = round_out<kBf16>(v + b);
+                }
             }
         }
     } else if (warp == kPMmaWarp) {
@@ -292,7 +439,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(dempty(d));
         }
-    } else if (warp >= kPFirstDqWarp) {
+    } else if (warp >= kPFirstDqWarp && warp < kPFirstDqWarp + 8) {
         // ---------------------------------------------------- dequantising --
         const int h = (warp - kPFirstDqWarp) >> 2;  // warpgroup: k-blocks with j % 2 == h
         const int r = (warp & 3) * 32 + lane;       // weight row of the tile
@@ -396,14 +543,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
     __syncthreads();
     if (warp == kPMmaWarp) {
         tc_fence_after();
-        tmem_dealloc(tmem, L::kTmemCols);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-template <int BN, bool kBf16, bool kMx = false>
+template <int BN, bool kBf16, int kMode = kModeRow>
 static cudaError_t launch_bn(const LinearArgs& a, cudaStream_t st) {
     using L = PrefillSmem<BN>;
-    auto kern = prefill_kernel<BN, kBf16, kMx>;
+    constexpr bool kMx = kMode == kModeMxFold;
+    constexpr bool kGrp = kMode == kModeGrouped;
+    auto kern = prefill_kernel<BN, kBf16, kMode>;
     static std::once_flag attr_once[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -430,23 +579,30 @@ static cudaError_t launch_bn(const LinearArgs& a, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kPThreads);
+    cfg.blockDim = dim3(kGrp ? kPThreadsGrouped : kPThreads);
     cfg.dynamicSmemBytes = L::kAlloc;
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const float* sc = kMx ? nullptr : a.scales;
-    const uint8_t* e8 = kMx ? reinterpret_cast<const uint8_t*>(a.scales) : nullptr;
+    const bool bytes = kMx || (kGrp && a.e8m0);
+    const float* sc = bytes ? nullptr : a.scales;
+    const uint8_t* e8 = bytes ? reinterpret_cast<const uint8_t*>(a.scales) : nullptr;
     return cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, sc, e8, a.bias, static_cast<uint16_t*>(a.y), a.m, a.n,
-                              a.k, a.early ? 1 : 0);
+                              a.k, a.early ? 1 : 0, kGrp ? static_cast<int>(a.group) : 0);
 }
 
 cudaError_t launch_prefill(const LinearArgs& a, cudaStream_t st) {
     const bool bf16 = a.act == 1;
+    if (a.group != 0 && (!a.e8m0 || !bf16)) {
+        // per-group scales (fp32, or E8M0 bytes with fp16 activations)
+        if (a.k % a.group != 0 || (a.group != 32 && a.group != 64 && a.group != 128) || (a.e8m0 && a.group != 32))
+            return cudaErrorInvalidValue;
+        return bf16 ? launch_bn<128, true, kModeGrouped>(a, st) : launch_bn<128, false, kModeGrouped>(a, st);
+    }
     if (a.e8m0) {
         // MX-style scales: bf16 activations, k % 128 == 0 (checked by the caller)
         if (!bf16 || a.group != 32 || a.k % 128 != 0) return cudaErrorInvalidValue;
-        return a.m <= 128 ? launch_bn<128, true, true>(a, st) : launch_bn<256, true, true>(a, st);
+        return a.m <= 128 ? launch_bn<128, true, kModeMxFold>(a, st) : launch_bn<256, true, kModeMxFold>(a, st);
     }
     // 128-token tiles up to 128 tokens, 256 beyond
     if (a.m <= 128) return bf16 ? launch_bn<128, true>(a, st) : launch_bn<128, false>(a, st);

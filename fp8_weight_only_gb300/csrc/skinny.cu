@@ -123,7 +123,11 @@ struct SkinnySmem {
     static constexpr int kDoneSlots = NT == 16 ? 12 : 24;
     static_assert(kDoneSlots % kASlotsAll == 0 && kDoneSlots % kXSlots == 0, "unit-done ring");
     static constexpr uint32_t kLaneBars = kLanes * kBarsPerLane;
-    static constexpr uint32_t kNumBars = kLaneBars + kASlotsAll + kDoneSlots + kXSlots + 2 + 3 * kMmaWarps;
+    // per-group scales: the accumulator columns hold a ring of kGAcc group
+    // accumulators (NT columns each); gfull [kGAcc], gfree [kGAcc] follow drain
+    static constexpr int kGAcc = (kTmemCols - kDCol0) / NT;
+    static constexpr uint32_t kGBar0 = kLaneBars + kASlotsAll + kDoneSlots + kXSlots + 2 + 3 * kMmaWarps;
+    static constexpr uint32_t kNumBars = kGBar0 + 2 * kGAcc;
     // tmem base, abort flag, last-contributor flag, epilogue abort flag
     static constexpr uint32_t kMiscOff = kBarOff + kNumBars * 8;
     static constexpr uint32_t kBytes = kMiscOff + 16;
@@ -136,6 +140,7 @@ struct SkinnySmem {
         const uint32_t gi = i - kLaneBars;
         if (gi < static_cast<uint32_t>(kASlotsAll)) return 4u;  // aready
         const uint32_t di = static_cast<uint32_t>(kASlotsAll + kDoneSlots + kXSlots);
+        if (i >= kGBar0 + kGAcc) return 4u;                     // gfree
         return (gi == di || gi == di + 1) ? 4u : 1u;            // dfree
     }
 };
@@ -255,16 +260,32 @@ struct SharedTile {
     float sc, b;
 };
 
-// kMx: the weight carries E8M0 scale bytes e8[n, k / 32] (bf16 activations,
-// k % 128 == 0) instead of per-row scales; they enter the dequantised
-// weight, and the epilogue adds only the bias.
-template <int NT, bool kBf16, bool kMx = false>
+// The scale forms (kMode):
+//  kModeRow      scales[n], applied in the epilogue.
+//  kModeMxFold   E8M0 scale bytes e8[n, k / 32] (bf16 activations, k % 128
+//                == 0); they enter the dequantised weight, and the epilogue
+//                adds only the bias.
+//  kModeGrouped  one scale per run of gsz = 32, 64 or 128 codes of a row:
+//                fp32 scales[n, k / gsz], or E8M0 bytes e8[n, k / 32] (gsz
+//                32).  Page "B04 Precision & Quantization", section
+//                "Post-training quantization versus quantization-aware
+//                training", the granularity table's per-group row: each group's sum is
+//                its own product, scaled before it joins the row's total.
+//                The MMAs of a group go to their own TMEM accumulator (a ring
+//                of kGAcc); the epilogue drains each one, multiplies it by
+//                the group's scale and adds it to the tile's fp32 total in
+//                registers (at most 32 tokens a launch, and at most one
+//                shared tile a CTA).
+template <int NT, bool kBf16, int kMode = kModeRow>
 __global__ void __launch_bounds__(kThreads, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                   const float* __restrict__ scales, const uint8_t* __restrict__ e8, const float* __restrict__ bias,
                   uint16_t* __restrict__ y, int m_rows, int m_row0, int64_t n, int64_t k, int cl, int tpc,
-                  int early) {
+                  int early, int gsz) {
+    constexpr bool kMx = kMode == kModeMxFold;
+    constexpr bool kGrp = kMode == kModeGrouped;
     static_assert(!kMx || kBf16, "MX-style scales fold into bf16 weights only");
+    static_assert(!kGrp || NT <= 32, "per-group totals are held in registers: at most 32 tokens");
     using L = SkinnySmem<NT>;
     constexpr int kCS = L::kCodeSlots, kXS = L::kXSlots;
     extern __shared__ uint8_t smem_raw[];
@@ -283,6 +304,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto dfree = [&](int d) { return gbar(kAS + kDone + kXS + d); };
     auto dready = [&](int w, int d) { return gbar(kAS + kDone + kXS + 2 + 2 * w + d); };
     auto drain = [&](int w) { return gbar(kAS + kDone + kXS + 2 + 2 * kMmaWarps + w); };
+    constexpr int kGAcc = L::kGAcc;
+    auto gfull = [&](int b) { return bar0 + 8u * (L::kGBar0 + b); };
+    auto gfree = [&](int b) { return bar0 + 8u * (L::kGBar0 + kGAcc + b); };
+    // groups a unit, and MMAs (k = 16) a group (grouped form)
+    const int gpu = kGrp ? kBlockK / gsz : 1;
+    const int mpg = kGrp ? gsz / 16 : kBlockK / 16;
     // unit v's MMAs are done (v < 0: nothing to wait for)
     auto done_bar = [&](int v) { return udone(v % kDone); };
     auto done_parity = [&](int v) { return static_cast<uint32_t>((v / kDone) & 1); };
@@ -458,7 +485,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the loop (every condition is warp-uniform) and elect.sync picks the
         // lane that issues and commits.  Both warps walk every unit to keep
         // the tile segments in step.
+        // Per-group form: a warp waits for an accumulator's previous group to
+        // be drained by phase parity, which cannot tell that phase from the
+        // one before it; with two warps taking alternate units, a warp's
+        // waits stay within one phase only if the ring holds the groups of
+        // two units (kGAcc >= 2 gpu).  Otherwise warp 2 alone issues every
+        // unit, and its waits come in order.
         const int w = warp - kMmaWarp;
+        const int nw = (kGrp && kGAcc < 2 * gpu) ? 1 : kMmaWarps;  // issuing warps
         constexpr uint32_t idesc = idesc_f16(kBf16, NT);
         UnitCursor cu = cursor0();
         int seg = 0, jj = 0;
@@ -467,36 +501,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pa = 0, px = 0;     // their phase parities
         bool mine_in_seg = false;    // this warp has issued into the segment's accumulator
         bool failed = false;
-        if (w < iters && (!mbar_wait_warp(aready(ra), pa, abort_flag) || !mbar_wait_warp(xfull(rx), px, abort_flag))) {
+        if (w < nw && w < iters &&
+            (!mbar_wait_warp(aready(ra), pa, abort_flag) || !mbar_wait_warp(xfull(rx), px, abort_flag))) {
             if (lane == 0) record_error(kErrWaitDequant, abort_flag, aready(ra), bar0);
             failed = true;
         }
         for (int it = 0; it < iters && !failed; ++it) {
             const int d = seg % L::kDBuf;
-            if (jj == 0 &&
+            if (!kGrp && jj == 0 &&
                 !mbar_wait_warp(dfree(d), static_cast<uint32_t>(((seg / L::kDBuf) & 1) ^ 1), abort_flag)) {
                 // the epilogue has not drained this accumulator (two segments ago)
                 if (lane == 0) record_error(kErrWaitMma, abort_flag, dfree(d), bar0);
                 break;
             }
-            if ((it & 1) == w) {
-                // test this warp's next unit (it + 2) now; the answer is used
+            if (nw == 1 ? w == 0 : (it & 1) == w) {
+                // test this warp's next unit (it + nw) now; the answer is used
                 // after this unit's MMAs, which hide the tests' latency
-                const int ran = ra + kMmaWarps >= kAS ? ra + kMmaWarps - kAS : ra + kMmaWarps;
-                const int rxn = rx + kMmaWarps >= kXS ? rx + kMmaWarps - kXS : rx + kMmaWarps;
+                const int ran = ra + nw >= kAS ? ra + nw - kAS : ra + nw;
+                const int rxn = rx + nw >= kXS ? rx + nw - kXS : rx + nw;
                 const uint32_t pan = ran < ra ? pa ^ 1u : pa;
                 const uint32_t pxn = rxn < rx ? px ^ 1u : px;
-                const bool more = it + kMmaWarps < iters;
+                const bool more = it + nw < iters;
                 const bool next_a = !more || mbar_test_wait(aready(ran), pan);
                 const bool next_x = !more || mbar_test_wait(xfull(rxn), pxn);
                 tc_fence_after();
                 const uint32_t xs = sbase + x_smem(rx);
                 const uint32_t a_tmem = tmem + ra * kAColsPerSlot;  // slot ra = (group ra % 3, A slot ra / 3)
-                const uint32_t d_tmem = tmem + kDCol0 + (w * L::kDBuf + d) * NT;
+                if constexpr (kGrp) {
+                    // group G = it * gpu + q / mpg of the unit goes to accumulator
+                    // G % kGAcc, once the epilogue has drained its previous group
+                    uint32_t g_tmem = 0;
+                    int gb = 0;
 #pragma unroll
-                for (int q = 0; q < kBlockK / 16; ++q) {
-                    const uint64_t b_desc = smem_desc_sw128_kmajor(xs + (q >> 2) * L::kXBoxBytes + (q & 3) * 32);
-                    mma_f16_ts_warp(d_tmem, a_tmem + q * 8, b_desc, idesc, mine_in_seg || q > 0);
+                    for (int q = 0; q < kBlockK / 16; ++q) {
+                        const int qg = q & (mpg - 1);
+                        if (qg == 0) {
+                            const int G = it * gpu + q / mpg;
+                            gb = G & (kGAcc - 1);
+                            if (!mbar_wait_warp(gfree(gb), static_cast<uint32_t>(((G / kGAcc) & 1) ^ 1), abort_flag)) {
+                                if (lane == 0) record_error(kErrWaitMma, abort_flag, gfree(gb), bar0);
+                                failed = true;
+                                break;
+                            }
+                            tc_fence_after();
+                            g_tmem = tmem + kDCol0 + gb * NT;
+                        }
+                        const uint64_t b_desc = smem_desc_sw128_kmajor(xs + (q >> 2) * L::kXBoxBytes + (q & 3) * 32);
+                        mma_f16_ts_warp(g_tmem, a_tmem + q * 8, b_desc, idesc, qg != 0);
+                        if (qg == mpg - 1) tc_commit_warp(gfull(gb));
+                    }
+                    if (failed) break;
+                } else {
+                    const uint32_t d_tmem = tmem + kDCol0 + (w * L::kDBuf + d) * NT;
+#pragma unroll
+                    for (int q = 0; q < kBlockK / 16; ++q) {
+                        const uint64_t b_desc = smem_desc_sw128_kmajor(xs + (q >> 2) * L::kXBoxBytes + (q & 3) * 32);
+                        mma_f16_ts_warp(d_tmem, a_tmem + q * 8, b_desc, idesc, mine_in_seg || q > 0);
+                    }
                 }
                 tc_commit_warp(done_bar(it));  // frees the unit's A and activation slots
                 mine_in_seg = true;
@@ -515,6 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             cu.next();
+            if (kGrp) continue;  // the epilogue follows the group accumulators
             if (++jj == seg_len) {
                 // this warp's accumulator is ready when its MMAs of the tile are
                 // done (at once if it had no unit in the tile)
@@ -548,7 +610,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // channels).  Worked out now, and its scale and bias read now, while
         // the MMAs run: at the end those reads would wait behind the weight
         // stream of the other CTAs.
-        if (cl > 1 && iters > 0) {
+        // (The per-group form works it out after its loop instead: its
+        // registers hold the totals, and its finish reads no scale.)
+        auto plan_shared = [&]() {
             const int etid = r;  // 0..127
             const int ub_tile = (ub - 1) / nkb32;
             for (int side = 0; side < 2; ++side) {
@@ -573,100 +637,193 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int64_t col = static_cast<int64_t>(gt0 + tl) * kTileN + c0 + ci;
                     if (col < n) {
                         st.col = col;
-                        st.sc = kMx ? 1.0f : scales[col];
+                        st.sc = (kMx || kGrp) ? 1.0f : scales[col];
                         st.b = bias ? bias[col] : 0.0f;
                     }
                 }
             }
-        }
-        // tokens [16h, 16h + 16) of the accumulators of buffer d, warp 0's
-        // first; a warp with no unit in the segment (a one-unit segment)
-        // wrote nothing there
-        auto load_acc = [&](int d, int h, int it0, int seg_len, float (&acc)[16]) {
-#pragma unroll
-            for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kMmaWarps; ++w) {
-                if (seg_len < kMmaWarps && ((it0 + kMmaWarps - w) % kMmaWarps) >= seg_len) continue;
-                uint32_t v[16];
-                tmem_ld_x16(lane_addr + kDCol0 + (w * L::kDBuf + d) * NT + h * 16, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < 16; ++q) acc[q] += __uint_as_float(v[q]);
-            }
         };
-        // a tile this rank shares with others stays in its accumulator until
-        // every unit is done (such tiles are processed last): buffer, first
-        // unit, length and staging slot (0: the tile of the rank's first unit)
-        // (two entries in registers: the arrays would live in local memory)
-        int hd0 = 0, hit0 = 0, hlen0 = 0, hslot0 = 0, hd1 = 0, hit1 = 0, hlen1 = 0, hslot1 = 0;
-        int nheld = 0;
-        int seg = 0;
-        UnitCursor cu = cursor0();
-        for (int it = 0; it < iters; ++seg) {
-            // segment: the units of one tile, contiguous in processing order
-            const int seg_len = cu.seg_left();
-            const int64_t tile = cu.tile;
-            const bool whole = cu.kb == 0 && seg_len == cu.nkb;
-            const int it0 = it;
-            it += seg_len;
-            for (int jj = 0; jj < seg_len; ++jj) cu.next();
-            const int d = seg % L::kDBuf;
-            bool ok = true;
-            for (int w = 0; w < kMmaWarps; ++w)
-                ok = mbar_wait_warp(dready(w, d), static_cast<uint32_t>((seg / L::kDBuf) & 1), abort_flag) && ok;
-            if (!ok) {
-                if (lane == 0) *ep_abort = 1;
-                record_error(kErrWaitMma, abort_flag);
-            }
-            // the four epilogue warps leave together (ep_abort is written only
-            // by them, before this barrier), so their named barriers stay matched
-            epilogue_bar();
-            if (*ep_abort) break;
-            tc_fence_after();
-            if (!whole) {
-                const int slot = tile == gt0 + ua_tile ? 0 : 1;
-                if (nheld == 0) {
-                    hd0 = d, hit0 = it0, hlen0 = seg_len, hslot0 = slot;
-                } else {
-                    hd1 = d, hit1 = it0, hlen1 = seg_len, hslot1 = slot;
-                }
-                ++nheld;
-                continue;
-            }
-            const int64_t col = tile * kTileN + r;
-            const float sc = kMx ? 1.0f : col < n ? scales[col] : 0.0f;
-            const float b = (bias && col < n) ? bias[col] : 0.0f;
-            // 16 tokens at a time, only as many as there are rows
-#pragma unroll 1
-            for (int h = 0; h < NT / 16 && h * 16 < m_rows; ++h) {
-                float acc[16];
-                load_acc(d, h, it0, seg_len, acc);
-                if (col < n) {
+        if (!kGrp && cl > 1 && iters > 0) plan_shared();
+        if constexpr (kGrp) {
+            // Per-group scales: for each unit in processing order, each of its
+            // groups' accumulators is drained as soon as its MMAs are done and
+            // added to this channel's fp32 totals times the group's scale.
+            const int64_t nsc = e8 ? (k >> 5) : k / gsz;  // scales a row
+            const int gpr = static_cast<int>(nsc);
+            auto scale_at = [&](int64_t col, int j) -> float {
+                if (col >= n || j >= gpr) return 0.0f;  // rows past n, groups past k: zero codes
+                return e8 ? e8m0_to_f32(__ldg(e8 + col * nsc + j)) : __ldg(scales + col * nsc + j);
+            };
+            // the totals as fp32 pairs (packed FMAs); tot(t) is token t's
+            uint64_t tot2[NT / 2];
 #pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        if (h * 16 + q < m_rows)
-                            y[static_cast<int64_t>(h * 16 + q) * n + col] = round_out<kBf16>(fmaf(acc[q], sc, b));
-                }
+            for (int t = 0; t < NT / 2; ++t) tot2[t] = 0ull;
+            auto tot = [&](int t) { return __uint_as_float(static_cast<uint32_t>(tot2[t >> 1] >> (32 * (t & 1)))); };
+            // the scales of the unit after the current one, loaded a unit ahead
+            float sn[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            UnitCursor cu = cursor0();
+            if (iters > 0) {
+#pragma unroll
+                for (int sg = 0; sg < 4; ++sg)
+                    if (sg < gpu) sn[sg] = scale_at(static_cast<int64_t>(cu.tile) * kTileN + r, cu.kb * gpu + sg);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(dfree(d));
-        }
-        // every unit is done, so the code ring is idle: the held partial
-        // tiles go there, token-major, for the cluster to add up
-        if (!*ep_abort) {
-#pragma unroll 1
-            for (int i = 0; i < nheld && i < kMaxHeld; ++i) {
-                const int hd = i == 0 ? hd0 : hd1, hit = i == 0 ? hit0 : hit1, hlen = i == 0 ? hlen0 : hlen1;
-                float* pt = reinterpret_cast<float*>(smem + L::kCodesOff) + (i == 0 ? hslot0 : hslot1) * (kTileN * NT);
-#pragma unroll 1
+            bool held = false;
+            int G = 0;
+            bool ok = true;
+            for (int it = 0; it < iters && ok;) {
+                const int seg_len = cu.seg_left();
+                const int64_t col = static_cast<int64_t>(cu.tile) * kTileN + r;
+                const bool whole = cu.kb == 0 && seg_len == cu.nkb;
+                for (int jj = 0; jj < seg_len; ++jj, ++it) {
+                    float sc[4];
+#pragma unroll
+                    for (int sg = 0; sg < 4; ++sg) sc[sg] = sn[sg];
+                    cu.next();
+                    if (it + 1 < iters) {
+#pragma unroll
+                        for (int sg = 0; sg < 4; ++sg)
+                            if (sg < gpu) sn[sg] = scale_at(static_cast<int64_t>(cu.tile) * kTileN + r, cu.kb * gpu + sg);
+                    }
+#pragma unroll
+                    for (int sg = 0; sg < 4; ++sg) {
+                        if (sg >= gpu) break;
+                        const int gb = G & (kGAcc - 1);
+                        if (!mbar_wait_warp(gfull(gb), static_cast<uint32_t>((G / kGAcc) & 1), abort_flag)) {
+                            if (lane == 0) *ep_abort = 1;
+                            record_error(kErrWaitMma, abort_flag, gfull(gb), bar0);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        // 16 tokens at a time (registers: the totals stay resident)
+#pragma unroll
+                        for (int h = 0; h < NT / 16; ++h) {
+                            if (h * 16 >= m_rows) break;
+                            uint32_t v[16];
+                            tmem_ld_x16(lane_addr + kDCol0 + gb * NT + h * 16, v);
+                            tmem_wait_ld();
+                            ffma2_x16(tot2 + h * 8, v, pack2(sc[sg], sc[sg]));
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(gfree(gb));
+                        ++G;
+                    }
+                    if (!ok) break;
+                }
+                if (!ok) break;
+                if (!whole) {
+                    // the one tile this rank shares (clusters split single tiles
+                    // in this form): its totals are staged after the loop
+                    held = true;
+                    continue;
+                }
+                if (col < n) {
+                    const float b = bias ? bias[col] : 0.0f;
+#pragma unroll
+                    for (int t = 0; t < NT; ++t)
+                        if (t < m_rows) y[static_cast<int64_t>(t) * n + col] = round_out<kBf16>(tot(t) + b);
+                }
+#pragma unroll
+                for (int t = 0; t < NT / 2; ++t) tot2[t] = 0ull;
+            }
+            if (held && !*ep_abort) {
+                float* pt = reinterpret_cast<float*>(smem + L::kCodesOff);
+#pragma unroll
+                for (int t = 0; t < NT; ++t)
+                    if (t < m_rows) pt[t * kTileN + r] = tot(t);
+            }
+            if (cl > 1 && iters > 0) plan_shared();
+        } else {
+            // tokens [16h, 16h + 16) of the accumulators of buffer d, warp 0's
+            // first; a warp with no unit in the segment (a one-unit segment)
+            // wrote nothing there
+            auto load_acc = [&](int d, int h, int it0, int seg_len, float (&acc)[16]) {
+    #pragma unroll
+                for (int q = 0; q < 16; ++q) acc[q] = 0.0f;
+    #pragma unroll
+                for (int w = 0; w < kMmaWarps; ++w) {
+                    if (seg_len < kMmaWarps && ((it0 + kMmaWarps - w) % kMmaWarps) >= seg_len) continue;
+                    uint32_t v[16];
+                    tmem_ld_x16(lane_addr + kDCol0 + (w * L::kDBuf + d) * NT + h * 16, v);
+                    tmem_wait_ld();
+    #pragma unroll
+                    for (int q = 0; q < 16; ++q) acc[q] += __uint_as_float(v[q]);
+                }
+            };
+            // a tile this rank shares with others stays in its accumulator until
+            // every unit is done (such tiles are processed last): buffer, first
+            // unit, length and staging slot (0: the tile of the rank's first unit)
+            // (two entries in registers: the arrays would live in local memory)
+            int hd0 = 0, hit0 = 0, hlen0 = 0, hslot0 = 0, hd1 = 0, hit1 = 0, hlen1 = 0, hslot1 = 0;
+            int nheld = 0;
+            int seg = 0;
+            UnitCursor cu = cursor0();
+            for (int it = 0; it < iters; ++seg) {
+                // segment: the units of one tile, contiguous in processing order
+                const int seg_len = cu.seg_left();
+                const int64_t tile = cu.tile;
+                const bool whole = cu.kb == 0 && seg_len == cu.nkb;
+                const int it0 = it;
+                it += seg_len;
+                for (int jj = 0; jj < seg_len; ++jj) cu.next();
+                const int d = seg % L::kDBuf;
+                bool ok = true;
+                for (int w = 0; w < kMmaWarps; ++w)
+                    ok = mbar_wait_warp(dready(w, d), static_cast<uint32_t>((seg / L::kDBuf) & 1), abort_flag) && ok;
+                if (!ok) {
+                    if (lane == 0) *ep_abort = 1;
+                    record_error(kErrWaitMma, abort_flag);
+                }
+                // the four epilogue warps leave together (ep_abort is written only
+                // by them, before this barrier), so their named barriers stay matched
+                epilogue_bar();
+                if (*ep_abort) break;
+                tc_fence_after();
+                if (!whole) {
+                    const int slot = tile == gt0 + ua_tile ? 0 : 1;
+                    if (nheld == 0) {
+                        hd0 = d, hit0 = it0, hlen0 = seg_len, hslot0 = slot;
+                    } else {
+                        hd1 = d, hit1 = it0, hlen1 = seg_len, hslot1 = slot;
+                    }
+                    ++nheld;
+                    continue;
+                }
+                const int64_t col = tile * kTileN + r;
+                const float sc = kMx ? 1.0f : col < n ? scales[col] : 0.0f;
+                const float b = (bias && col < n) ? bias[col] : 0.0f;
+                // 16 tokens at a time, only as many as there are rows
+    #pragma unroll 1
                 for (int h = 0; h < NT / 16 && h * 16 < m_rows; ++h) {
                     float acc[16];
-                    load_acc(hd, h, hit, hlen, acc);
-#pragma unroll
-                    for (int q = 0; q < 16; ++q)
-                        if (h * 16 + q < m_rows) pt[(h * 16 + q) * kTileN + r] = acc[q];
+                    load_acc(d, h, it0, seg_len, acc);
+                    if (col < n) {
+    #pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            if (h * 16 + q < m_rows)
+                                y[static_cast<int64_t>(h * 16 + q) * n + col] = round_out<kBf16>(fmaf(acc[q], sc, b));
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(dfree(d));
+            }
+            // every unit is done, so the code ring is idle: the held partial
+            // tiles go there, token-major, for the cluster to add up
+            if (!*ep_abort) {
+    #pragma unroll 1
+                for (int i = 0; i < nheld && i < kMaxHeld; ++i) {
+                    const int hd = i == 0 ? hd0 : hd1, hit = i == 0 ? hit0 : hit1, hlen = i == 0 ? hlen0 : hlen1;
+                    float* pt = reinterpret_cast<float*>(smem + L::kCodesOff) + (i == 0 ? hslot0 : hslot1) * (kTileN * NT);
+    #pragma unroll 1
+                    for (int h = 0; h < NT / 16 && h * 16 < m_rows; ++h) {
+                        float acc[16];
+                        load_acc(hd, h, hit, hlen, acc);
+    #pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            if (h * 16 + q < m_rows) pt[(h * 16 + q) * kTileN + r] = acc[q];
+                    }
                 }
             }
         }
@@ -901,14 +1058,15 @@ cudaError_t device_sm_count(int& sms) {
 // and a cluster starts only when all its SMs are free).  Each rank gets at
 // least kMinUnitsPerCta units (and
 // at least one of every cluster's, so cl <= nkb).  A 64-token launch keeps
-// one accumulator per MMA warp, so its CTAs may share at most one tile:
-// tpc == 1 when cl > 1.
+// one accumulator per MMA warp, and the per-group form keeps a tile's totals
+// in registers, so their CTAs may share at most one tile: tpc == 1 when
+// cl > 1.
 constexpr int kMinUnitsPerCta = 4;
 constexpr int kSplitUnits = 3;
 constexpr int kSharedUnits = 9;
 constexpr int64_t kMaxClusterUnits = 1 << 24;  // cluster-local unit indices are 32-bit
 
-SkinnyShape skinny_shape(int64_t n, int64_t k, const int* active, int nt) {
+SkinnyShape skinny_shape(int64_t n, int64_t k, const int* active, int nt, bool grouped) {
     const int64_t tiles = (n + kTileN - 1) / kTileN;
     const int64_t nkb = (k + kBlockK - 1) / kBlockK;
     SkinnyShape best{1, (tiles + active[1] - 1) / active[1]};
@@ -917,7 +1075,7 @@ SkinnyShape skinny_shape(int64_t n, int64_t k, const int* active, int nt) {
         const int64_t clusters_max = active[cl];
         if (clusters_max < 1) continue;
         const int64_t tpc = (tiles + clusters_max - 1) / clusters_max;
-        if (nt > 32 && tpc > 1) continue;
+        if ((nt > 32 || grouped) && tpc > 1) continue;
         if (tpc * nkb >= kMaxClusterUnits) continue;
         const int64_t per_cta = (tpc * nkb + cl - 1) / cl;
         if (per_cta < kMinUnitsPerCta) continue;
@@ -930,17 +1088,19 @@ SkinnyShape skinny_shape(int64_t n, int64_t k, const int* active, int nt) {
     return best;
 }
 
-bool skinny_shape_valid(const SkinnyShape& sh, int64_t m, int64_t k) {
+bool skinny_shape_valid(const SkinnyShape& sh, int64_t m, int64_t k, bool grouped) {
     const int64_t nkb = (k + kBlockK - 1) / kBlockK;
     const int nt = m <= 16 ? 16 : m <= 32 ? 32 : 64;
     return sh.cl >= 1 && sh.cl <= kMaxCluster && sh.tpc >= 1 && sh.cl <= nkb && sh.tpc * nkb < kMaxClusterUnits &&
-           (sh.cl == 1 || nt <= 32 || sh.tpc == 1);
+           (sh.cl == 1 || (nt <= 32 && !grouped) || sh.tpc == 1);
 }
 
-template <int NT, bool kBf16, bool kMx = false>
+template <int NT, bool kBf16, int kMode = kModeRow>
 static cudaError_t launch_nt(const LinearArgs& a, const SkinnyShape* forced, cudaStream_t st) {
     using L = SkinnySmem<NT>;
-    auto kern = skinny_kernel<NT, kBf16, kMx>;
+    constexpr bool kMx = kMode == kModeMxFold;
+    constexpr bool kGrp = kMode == kModeGrouped;
+    auto kern = skinny_kernel<NT, kBf16, kMode>;
     // per device, once: the kernel's attributes, and how many clusters of
     // each size the device holds at a time (0 where a size cannot launch)
     static std::once_flag attr_once[64];
@@ -988,7 +1148,7 @@ static cudaError_t launch_nt(const LinearArgs& a, const SkinnyShape* forced, cud
                    static_cast<uint64_t>(a.m), static_cast<uint64_t>(a.k) * 2, 64, NT))
         return cudaErrorInvalidValue;
 
-    const SkinnyShape shape = forced ? *forced : skinny_shape(a.n, a.k, active[dev], NT);
+    const SkinnyShape shape = forced ? *forced : skinny_shape(a.n, a.k, active[dev], NT, kGrp);
     const int64_t tiles = (a.n + kTileN - 1) / kTileN;
     const int64_t clusters = (tiles + shape.tpc - 1) / shape.tpc;
     // programmatic dependent launch: this grid's prologue (barrier set-up,
@@ -1013,11 +1173,12 @@ static cudaError_t launch_nt(const LinearArgs& a, const SkinnyShape* forced, cud
     uint16_t* yp = static_cast<uint16_t*>(a.y);
     for (int64_t m0 = 0; m0 < a.m; m0 += NT) {
         const int rows = static_cast<int>(a.m - m0 < NT ? a.m - m0 : NT);
-        const float* sc = kMx ? nullptr : a.scales;
-        const uint8_t* e8 = kMx ? reinterpret_cast<const uint8_t*>(a.scales) : nullptr;
+        const bool bytes = kMx || (kGrp && a.e8m0);
+        const float* sc = bytes ? nullptr : a.scales;
+        const uint8_t* e8 = bytes ? reinterpret_cast<const uint8_t*>(a.scales) : nullptr;
         e = cudaLaunchKernelEx(&cfg, kern, map_codes, map_x, sc, e8, a.bias, yp + m0 * a.n, rows,
                                static_cast<int>(m0), a.n, a.k, shape.cl, static_cast<int>(shape.tpc),
-                               a.early ? 1 : 0);
+                               a.early ? 1 : 0, kGrp ? static_cast<int>(a.group) : 0);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -1025,13 +1186,24 @@ static cudaError_t launch_nt(const LinearArgs& a, const SkinnyShape* forced, cud
 
 cudaError_t launch_skinny(const LinearArgs& a, const SkinnyShape* forced, cudaStream_t st) {
     const bool bf16 = a.act == 1;
-    if (forced && !skinny_shape_valid(*forced, a.m, a.k)) return cudaErrorInvalidConfiguration;
+    // per-group scales (fp32, or E8M0 bytes with fp16 activations): the
+    // per-group form, 16 or 32 tokens a launch (32-row slabs beyond)
+    const bool grouped = a.group != 0 && (!a.e8m0 || !bf16);
+    if (forced && !skinny_shape_valid(*forced, a.m, a.k, grouped)) return cudaErrorInvalidConfiguration;
+    if (grouped) {
+        if (a.k % a.group != 0 || (a.group != 32 && a.group != 64 && a.group != 128) || (a.e8m0 && a.group != 32))
+            return cudaErrorInvalidValue;
+        if (a.m <= 16)
+            return bf16 ? launch_nt<16, true, kModeGrouped>(a, forced, st)
+                        : launch_nt<16, false, kModeGrouped>(a, forced, st);
+        return bf16 ? launch_nt<32, true, kModeGrouped>(a, forced, st) : launch_nt<32, false, kModeGrouped>(a, forced, st);
+    }
     if (a.e8m0) {
         // MX-style scales: bf16 activations, k % 128 == 0 (checked by the caller)
         if (!bf16 || a.group != 32 || a.k % 128 != 0) return cudaErrorInvalidValue;
-        if (a.m <= 16) return launch_nt<16, true, true>(a, forced, st);
-        if (a.m <= 32) return launch_nt<32, true, true>(a, forced, st);
-        return launch_nt<64, true, true>(a, forced, st);
+        if (a.m <= 16) return launch_nt<16, true, kModeMxFold>(a, forced, st);
+        if (a.m <= 32) return launch_nt<32, true, kModeMxFold>(a, forced, st);
+        return launch_nt<64, true, kModeMxFold>(a, forced, st);
     }
     if (a.m <= 16) return bf16 ? launch_nt<16, true>(a, forced, st) : launch_nt<16, false>(a, forced, st);
     if (a.m <= 32) return bf16 ? launch_nt<32, true>(a, forced, st) : launch_nt<32, false>(a, forced, st);

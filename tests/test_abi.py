@@ -147,18 +147,21 @@ def test_quantize_grouped_rejects_bad_arguments(args, status):
     assert fw.lib().fp8w_quantize_grouped(*args, None) == status
 
 
-def _lin_g(m=1, k=512, group=32, scales=C16, cfg=None):
+def _lin_g(m=1, k=512, group=32, scales=C16):
     return fw.lib().fp8w_linear_grouped(A16, 1, m, k, B16, scales, group, None, 8, D16, None)
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(m=2), 2),                      # the grouped form is the GEMV: m == 1
     (dict(group=16), 2), (dict(group=96), 2),
-    (dict(k=32 * 4 * 3 + 64, group=32), 2),   # k % (4 * group) != 0
-    (dict(k=65536, group=128), 2),       # beyond the GEMV's 32768
-    (dict(scales=ctypes.c_void_p(0x300004)), 3),   # scales are bulk-copied: 16-byte aligned
+    (dict(k=512 + 16, group=32), 2),     # k % group != 0
+    (dict(k=1024 + 64, group=128), 2),
+    (dict(m=0), 2), (dict(k=65536 + 128, group=128), 2),   # beyond FP8W_MAX_K
+    (dict(scales=ctypes.c_void_p(0x300004)), 3),   # scales: 16-byte aligned (the GEMV bulk-copies them)
+    (dict(m=40, scales=ctypes.c_void_p(0x300008)), 3),
 ])
 def test_linear_grouped_rejects_bad_arguments(kw, status):
+    # every case is refused on the host (any m is accepted now: the GEMV at
+    # m == 1, the tensor-core kernels' per-group form otherwise)
     assert _lin_g(**kw) == status
 
 
@@ -182,8 +185,7 @@ def test_quantize_mx_takes_scale_bytes_at_any_alignment():
     (dict(k=65536 + 128), 2),                  # beyond FP8W_MAX_K
     (dict(act=3), 4),
     (dict(scales=ctypes.c_void_p(0x300008)), 3),   # scale bytes: 16-byte aligned
-    (dict(m=2, act=2), 4),                     # the tensor-core form folds the scales into bf16 weights
-    (dict(m=1, k=384, act=2), 4),              # m == 1 but k % 512 != 0: the tensor-core form too
+    (dict(m=2, act=2, scales=ctypes.c_void_p(0x300001)), 3),   # fp16 beyond one token: the per-group form
 ])
 def test_linear_mx_rejects_bad_arguments(kw, status):
     a = dict(x=A16, act=1, m=1, k=1024, codes=B16, scales=C16, bias=None, n=8, y=D16)
