@@ -609,7 +609,7 @@ def run_prefill(torch, fw, dev, s, m=2048, launches=10):
     peak, src = bf16_peak()
     return {"shape": "[%d, 4096] x gate [14336 x 4096], bf16" % m, "us_per_launch": round(us, 2),
             "tflops": round(tf, 1), "frac_of_bf16_peak": round(tf / peak, 4), "peak_source": src,
-            "kernel": "fp8w::prefill_kernel<256, 1>"}
+            "kernel": "fp8w::prefill_kernel<256, 1, 0>"}
 
 
 def direct_calls(torch, fw, mats, xs, dev, s, launches=40):

@@ -30,7 +30,7 @@ SYMBOLS = ("fp8w_quantize", "fp8w_linear", "fp8w_linear_ex",
            "fp8w_linear_noalloc", "fp8w_dequantize", "fp8w_quantize_grouped", "fp8w_linear_grouped",
            "fp8w_quantize_mx", "fp8w_linear_mx", "fp8w_quantize_ex", "fp8w_dequantize_grouped",
            "fp8w_dequantize_mx", "fp8w_quantize_act", "fp8w_linear_w8a8")
-ABI_VERSION = 11
+ABI_VERSION = 12
 FLAG_WEIGHTS_READY = 1
 
 

@@ -40,7 +40,7 @@
 extern "C" {
 #endif
 
-#define FP8W_ABI_VERSION 11
+#define FP8W_ABI_VERSION 12
 
 #if defined(__GNUC__)
 #define FP8W_API __attribute__((visibility("default")))
@@ -116,12 +116,17 @@ FP8W_API fp8w_status fp8w_quantize_grouped(const float *w, int64_t n, int64_t k,
  * fp8w_linear_grouped -- fp8w_linear for codes with per-group scales:
  *   y[0, r] = round_act( sum_j scales[r, j] * sum_{c in group j} x[0, c] * e4m3(codes[r, c]) + bias[r] ).
  *
- * The GEMV kernel (m == 1 only: any other m is FP8W_ERR_SHAPE, not built
- * for the tensor-core kernel).  group 32, 64 or 128 with k % (4 * group) ==
- * 0 and k <= 32768; scales [n, k / group] fp32, 16-byte aligned (each slot's
- * rows of scales are bulk-copied beside its codes).  Other arguments as
- * fp8w_linear; fp32 accumulation, each 16-code partial sum scaled by its
- * group's scale, bias added once, one rounding.
+ * group 32, 64 or 128 with k % group == 0; scales [n, k / group] fp32,
+ * 16-byte aligned.  Other arguments as fp8w_linear.  fp32 accumulation, each
+ * group's partial sum times its scale, bias added once, one rounding:
+ *  - m == 1 with k % (4 * group) == 0 and k <= 32768: the GEMV (a slot's
+ *    rows of scales are bulk-copied beside its codes; each 16-code partial
+ *    sum is scaled by its group's scale);
+ *  - otherwise the tensor-core kernels' per-group form (the skinny kernel up
+ *    to m = 64 in launches of 16 or 32 tokens, the prefill GEMM beyond):
+ *    each group's products go to their own fp32 accumulator in tensor
+ *    memory, which is multiplied by the group's scale and added to the
+ *    output's fp32 total.
  */
 FP8W_API fp8w_status fp8w_linear_grouped(const void *x, int act_dtype, int64_t m, int64_t k,
                                 const uint8_t *codes, const float *scales, int group,
@@ -157,11 +162,13 @@ FP8W_API fp8w_status fp8w_quantize_mx(const float *w, int64_t n, int64_t k,
  * sum is scaled by its block's power of two, which adds no rounding (short
  * of over- or underflow); bias added once, one rounding.  Any other shape
  * runs a tensor-core kernel (the skinny one up to m = 64, the prefill GEMM
- * beyond), for bf16 activations only (FP8W_ERR_DTYPE for fp16): the scale is
- * folded into the dequantised bf16 weight, e4m3(q) *
- * 2^(b - 127), which is exact wherever that product is a bf16 number
- * (anything but products below 2^-130 or beyond the bf16 range), then fp32
- * accumulation, bias added once, one rounding.
+ * beyond).  With bf16 activations the scale is folded into the dequantised
+ * bf16 weight, e4m3(q) * 2^(b - 127), which is exact wherever that product
+ * is a bf16 number (anything but products below 2^-130 or beyond the bf16
+ * range).  With fp16 activations it is fp8w_linear_grouped's per-group form
+ * at group 32 with each byte decoded to its fp32 power of two (2^-127 for
+ * 0, NaN for 0xFF), which gives the same bits as that call on the decoded
+ * scales.  fp32 accumulation, bias added once, one rounding.
  */
 FP8W_API fp8w_status fp8w_linear_mx(const void *x, int act_dtype, int64_t m, int64_t k,
                            const uint8_t *codes, const uint8_t *scales,
