@@ -339,13 +339,16 @@ __global__ void __launch_bounds__(kMode == kModeGrouped ? kPThreadsGrouped : kPT
                 }
                 tc_fence_after();
                 const uint64_t s2 = pack2(s, s);
+                // 32 tokens a round trip (two loads in flight)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < 4; c += 2) {
                     if (c * 16 >= mine) break;
-                    uint32_t v[16];
-                    tmem_ld_x16(lane_addr + static_cast<uint32_t>(gb * BN + c * 16), v);
+                    uint32_t v0[16], v1[16];
+                    tmem_ld_x16(lane_addr + static_cast<uint32_t>(gb * BN + c * 16), v0);
+                    tmem_ld_x16(lane_addr + static_cast<uint32_t>(gb * BN + c * 16 + 16), v1);
                     tmem_wait_ld();
-                    ffma2_x16(tot2 + c * 8, v, s2);
+                    ffma2_x16(tot2 + c * 8, v0, s2);
+                    ffma2_x16(tot2 + c * 8 + 8, v1, s2);
                 }
                 tc_fence_before();
                 __syncwarp();
