@@ -490,28 +490,28 @@ def run_fused(torch, fw, mats, xs, dev, s, steps, warmup, peak):
 
 
 def run_grouped(torch, fw, dev, s, peak, launches=100):
-    """The M = 1 GEMV with per-group scales on the gate weight [14336 x 4096]
-    (fp32 scales per 128 and per 32, and the MX-style E8M0 byte per 32):
-    per-launch time over graph-replayed back-to-back launches, weight
-    replicas (codes and scales) rotating so every read comes from HBM."""
+    """The per-group forms on the gate weight [14336 x 4096] (fp32 scales per
+    128 and per 32, and the MX-style E8M0 byte per 32): the GEMV at M = 1,
+    the tensor-core kernel's per-group form at M = 8 and 32 (and fp16
+    activations with E8M0 bytes), and the prefill GEMM's per-group form at
+    M = 2048; per-launch time over graph-replayed back-to-back launches,
+    weight replicas (codes and scales) rotating so every read comes from HBM.
+    The M = 1 entries keep the keys g128, g32 and mx."""
     c = synthetic.case("decode_stack", 1, "gate")
     w = torch.from_numpy(c["w"]).to(dev)
-    x = torch.from_numpy(c["x"].view(np.int16)).to(dev).view(torch.bfloat16)
     bias = torch.from_numpy(c["bias"]).to(dev)
     n, k = w.shape
+    rng = np.random.default_rng(7)
     out = {}
-    for group in (128, 32, "mx"):
-        codes, scales = fw.quantize_mx(w) if group == "mx" else fw.quantize(w, group=group)
-        nrep = max(3, -(-3 * 129 * 2 ** 20 // codes.numel()))
-        reps = [(codes, scales)] + [(codes.clone(), scales.clone()) for _ in range(nrep - 1)]
-        y = torch.empty((1, n), dtype=torch.bfloat16, device=dev)
+
+    def timed(x, reps, y, nl):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(s):
-            fw.linear(x, codes, scales, bias, out=y)
+            fw.linear(x, reps[0][0], reps[0][1], bias, out=y)
             torch.cuda.synchronize()
             with torch.cuda.graph(g, stream=s):
-                for i in range(launches):
-                    cd, sd = reps[i % nrep]
+                for i in range(nl):
+                    cd, sd = reps[i % len(reps)]
                     fw.linear(x, cd, sd, bias, out=y)
         g.replay()
         torch.cuda.synchronize()
@@ -522,14 +522,43 @@ def run_grouped(torch, fw, dev, s, peak, launches=100):
             g.replay()
             e1.record(s)
         torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / launches
-        nbytes = n * k + scales.numel() * scales.element_size() + 4 * n + 2 * k + 2 * n
-        out[group if group == "mx" else "g%d" % group] = {"us_per_launch": round(us, 3), "gbs": round(nbytes / us / 1e3, 1),
-                              "frac": round(nbytes / us / 1e3 / peak, 4), "bytes": nbytes}
-        del g, reps
-    out["note"] = ("gate [14336 x 4096], M = 1, bf16; bytes = codes + group scales (4 B, or 1 B for the E8M0 "
-                   "byte of mx) + bias + x + y; "
-                   "graph-replayed back-to-back launches")
+        del g
+        return e0.elapsed_time(e1) * 1e3 / nl
+
+    for group in (128, 32, "mx"):
+        codes, scales = fw.quantize_mx(w) if group == "mx" else fw.quantize(w, group=group)
+        nrep = max(3, -(-3 * 129 * 2 ** 20 // codes.numel()))
+        reps = [(codes, scales)] + [(codes.clone(), scales.clone()) for _ in range(nrep - 1)]
+        name = group if group == "mx" else "g%d" % group
+        cases = [(1, torch.bfloat16), (8, torch.bfloat16), (32, torch.bfloat16)]
+        if group == "mx":
+            cases += [(8, torch.float16), (32, torch.float16)]
+        for m, dt in cases:
+            xf = rng.standard_normal((m, k)).astype(np.float32)
+            x = torch.from_numpy(xf).to(dev).to(dt)
+            y = torch.empty((m, n), dtype=dt, device=dev)
+            us = timed(x, reps, y, launches if m == 1 else 40)
+            nbytes = n * k + scales.numel() * scales.element_size() + 4 * n + 2 * m * k + 2 * m * n
+            key = name if m == 1 else "%s@M%d%s" % (name, m, "" if dt == torch.bfloat16 else "_fp16")
+            out[key] = {"us_per_launch": round(us, 3), "gbs": round(nbytes / us / 1e3, 1),
+                        "frac": round(nbytes / us / 1e3 / peak, 4), "bytes": nbytes}
+        del reps
+        if group != "mx":
+            # the prefill GEMM's per-group form, compute-bound: TFLOP/s
+            m = 2048
+            x = torch.from_numpy(rng.standard_normal((m, k)).astype(np.float32)).to(dev).to(torch.bfloat16)
+            y = torch.empty((m, n), dtype=torch.bfloat16, device=dev)
+            us = timed(x, [(codes, scales)], y, 10)
+            tf = 2.0 * m * n * k / us / 1e6
+            bpeak, src = bf16_peak()
+            out["%s@M%d" % (name, m)] = {"us_per_launch": round(us, 2), "tflops": round(tf, 1),
+                                         "frac_of_bf16_peak": round(tf / bpeak, 4)}
+        del codes, scales
+    out["note"] = ("gate [14336 x 4096], bf16 unless marked fp16; M = 1: the GEMV, M = 8 and 32: the tensor-core "
+                   "kernel's per-group form (each group's products in their own TMEM accumulator, scaled in the "
+                   "epilogue), M = 2048: the prefill GEMM's per-group form (TFLOP/s against the measured bf16 "
+                   "peak); bytes = codes + group scales (4 B, or 1 B for the E8M0 byte of mx) + bias + x + y; "
+                   "graph-replayed back-to-back launches over weight replicas larger than L2")
     return out
 
 
@@ -920,7 +949,7 @@ def run_ours(args, torch, dist):
 
     result["fused_stack"] = run_fused(torch, fw, mats, xs, dev, s, min(args.steps, 500), args.warmup, peak)
 
-    result["grouped_gemv"] = run_grouped(torch, fw, dev, s, peak)
+    result["grouped"] = run_grouped(torch, fw, dev, s, peak)
     result["warm_l2"] = run_warm_l2(torch, fw, dev, s)
     result["prefill"] = run_prefill(torch, fw, dev, s)
 
