@@ -252,8 +252,11 @@ __global__ void __launch_bounds__(kMode == kModeGrouped ? kPThreadsGrouped : kPT
         // group) and ends it when kg + 16 reaches the next multiple of gsz
         // (k % gsz == 0, so no group is cut off by the end of k).
         constexpr uint32_t idesc = idesc_f16(kBf16, BN);
+        // accumulators hold at most one k-block (g = 128 takes two, one per
+        // 64-code half, each scaled by the group's scale)
+        const int asz = gsz < kPK ? gsz : kPK;
         int64_t kb_n = 0;
-        int Gc = 0, gb = 0;  // groups issued (below 2^31), and the current one's accumulator
+        int Gc = 0, gb = 0;  // accumulators issued (below 2^31), and the current one
         uint32_t g_tmem = tmem;
         bool ok = true;
         for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(kMode == kModeGrouped ? kPThreadsGrouped : kPT
                 for (int kk = 0; kk < kPK / 16; ++kk) {
                     const int64_t kg = static_cast<int64_t>(j) * kPK + kk * 16;
                     if (kg >= k) break;
-                    const int qg = static_cast<int>(kg & (gsz - 1));
+                    const int qg = static_cast<int>(kg & (asz - 1));
                     if (qg == 0) {
                         gb = Gc & (kPGAcc - 1);
                         if (!mbar_wait_warp(gfree(gb), static_cast<uint32_t>(((Gc / kPGAcc) & 1) ^ 1), abort_flag)) {
@@ -285,7 +288,7 @@ __global__ void __launch_bounds__(kMode == kModeGrouped ? kPThreadsGrouped : kPT
                     }
                     mma_f16_ss_warp(g_tmem, smem_desc_sw128_kmajor(a_addr + kk * 32),
                                     smem_desc_sw128_kmajor(x_addr + kk * 32), idesc, qg != 0);
-                    if (qg + 16 == gsz) {
+                    if (qg + 16 == asz) {
                         tc_commit_warp(gfull(gb));
                         ++Gc;
                     }
@@ -311,12 +314,15 @@ __global__ void __launch_bounds__(kMode == kModeGrouped ? kPThreadsGrouped : kPT
         const int r = quarter * 32 + lane;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(half * 64);
         const int nsc = static_cast<int>(e8 ? (k >> 5) : k / gsz);  // scales a row == groups a tile
+        const int asz = gsz < kPK ? gsz : kPK;                       // k of an accumulator
+        const int apg = gsz / asz;                                   // accumulators a group (1 or 2)
+        const int nacc = nsc * apg;                                  // accumulators a tile
         auto scale_at = [&](int64_t col, int j) -> float {
             if (col >= n) return 0.0f;  // rows past n hold zero codes
             return e8 ? e8m0_to_f32(__ldg(e8 + col * nsc + j)) : __ldg(scales + col * nsc + j);
         };
         pdl_wait();  // y may still be read, and the scales written, by the previous kernel
-        int Gc = 0;  // groups drained (below 2^31: tiles a CTA x k / 32)
+        int Gc = 0;  // accumulators drained (below 2^31: tiles a CTA x k / 32)
         bool ok = true;
         for (int64_t t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
             const int64_t cb = t / token_tiles, tb = t - cb * token_tiles;
@@ -328,9 +334,10 @@ __global__ void __launch_bounds__(kMode == kModeGrouped ? kPThreadsGrouped : kPT
 #pragma unroll
             for (int i = 0; i < 32; ++i) tot2[i] = 0ull;
             float s_next = scale_at(col, 0);
-            for (int gi = 0; gi < nsc; ++gi, ++Gc) {
+            for (int ai = 0; ai < nacc; ++ai, ++Gc) {
+                // accumulator ai is (part of) group ai / apg
                 const float s = s_next;
-                if (gi + 1 < nsc) s_next = scale_at(col, gi + 1);
+                if (ai + 1 < nacc && (ai + 1) % apg == 0) s_next = scale_at(col, (ai + 1) / apg);
                 const int gb = Gc & (kPGAcc - 1);
                 if (!mbar_wait_warp(gfull(gb), static_cast<uint32_t>((Gc / kPGAcc) & 1), abort_flag)) {
                     if (lane == 0) prefill_error(kErrWaitMma, abort_flag);
@@ -344,9 +351,8 @@ __global__ void __launch_bounds__(kMode == kModeGrouped ? kPThreadsGrouped : kPT
                 for (int c = 0; c < 4; c += 2) {
                     if (c * 16 >= mine) break;
                     uint32_t v0[16], v1[16];
-                    tmem_ld_x16(lane_addr + static_cast<uint32_t>(gb * BN + c * 16), v0);
-                    tmem_ld_x16(lane_addr + static_cast<uint32_t>(gb * BN + c * 16 + 16), v1);
-                    tmem_wait_ld();
+                    tmem_ld2_x16_sync(lane_addr + static_cast<uint32_t>(gb * BN + c * 16),
+                                      lane_addr + static_cast<uint32_t>(gb * BN + c * 16 + 16), v0, v1);
                     ffma2_x16(tot2 + c * 8, v0, s2);
                     ffma2_x16(tot2 + c * 8 + 8, v1, s2);
                 }
@@ -429,8 +435,7 @@ __global__ void __launch_bounds__(kMode == kModeGrouped ? kPThreadsGrouped : kPT
             const int ntok = static_cast<int>(m - tok0 < BN ? m - tok0 : BN);
             for (int c0 = 0; c0 < ntok; c0 += 16) {
                 uint32_t v[16];
-                tmem_ld_x16(lane_addr + static_cast<uint32_t>(d * BN + c0), v);
-                tmem_wait_ld();
+                tmem_ld_x16_sync(lane_addr + static_cast<uint32_t>(d * BN + c0), v);
                 if (col < n) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)

@@ -700,8 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int h = 0; h < NT / 16; ++h) {
                             if (h * 16 >= m_rows) break;
                             uint32_t v[16];
-                            tmem_ld_x16(lane_addr + kDCol0 + gb * NT + h * 16, v);
-                            tmem_wait_ld();
+                            tmem_ld_x16_sync(lane_addr + kDCol0 + gb * NT + h * 16, v);
                             ffma2_x16(tot2 + h * 8, v, pack2(sc[sg], sc[sg]));
                         }
                         tc_fence_before();
@@ -745,8 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int w = 0; w < kMmaWarps; ++w) {
                     if (seg_len < kMmaWarps && ((it0 + kMmaWarps - w) % kMmaWarps) >= seg_len) continue;
                     uint32_t v[16];
-                    tmem_ld_x16(lane_addr + kDCol0 + (w * L::kDBuf + d) * NT + h * 16, v);
-                    tmem_wait_ld();
+                    tmem_ld_x16_sync(lane_addr + kDCol0 + (w * L::kDBuf + d) * NT + h * 16, v);
     #pragma unroll
                     for (int q = 0; q < 16; ++q) acc[q] += __uint_as_float(v[q]);
                 }

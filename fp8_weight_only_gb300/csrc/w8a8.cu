@@ -286,8 +286,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             float* pt = reinterpret_cast<float*>(smem);  // split: this rank's partial, token-major
             for (int c0 = 0; c0 < ntok; c0 += 16) {
                 uint32_t v[16];
-                tmem_ld_x16(lane_addr + static_cast<uint32_t>(d * BN + c0), v);
-                tmem_wait_ld();
+                tmem_ld_x16_sync(lane_addr + static_cast<uint32_t>(d * BN + c0), v);
                 if (split > 1) {
                     // every MMA of this CTA is done, so the stage ring is free
 #pragma unroll
