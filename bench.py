@@ -1163,23 +1163,31 @@ def run_profile_case(args):
     dev = torch.device("cuda:0")
     c = synthetic.case("decode_stack", m, name)
     w = torch.from_numpy(c["w"]).to(dev)
-    codes, scales = fw.quantize(w)
+    # per-group scales (--group 32, 64, 128 or mx): the automatic kernel choice
+    if args.group == "mx":
+        codes, scales = fw.quantize_mx(w)
+    elif args.group:
+        codes, scales = fw.quantize(w, group=int(args.group))
+    else:
+        codes, scales = fw.quantize(w)
     del w
+    kw = {} if args.group else {"kernel": args.kernel, "cluster": args.cluster, "tiles": args.tiles}
     nrep = max(3, -(-3 * 129 * 2 ** 20 // codes.numel()))   # replicas covering > 3x L2
     reps = [codes] + [codes.clone() for _ in range(nrep - 1)]
     bias = torch.from_numpy(c["bias"]).to(dev)
     x = torch.from_numpy(c["x"].view(np.int16)).to(dev).view(torch.bfloat16)
     y = torch.empty((m, c["n"]), dtype=torch.bfloat16, device=dev)
     for i in range(3):
-        fw.linear(x, reps[i % nrep], scales, bias, out=y, kernel=args.kernel, cluster=args.cluster, tiles=args.tiles)
+        fw.linear(x, reps[i % nrep], scales, bias, out=y, **kw)
     torch.cuda.synchronize()
-    out = {"case": args.profile, "kernel": args.kernel, "cluster": args.cluster, "tiles": args.tiles, "bytes": call_bytes(m, c["n"], c["k"])}
+    out = {"case": args.profile, "group": args.group, "kernel": args.kernel, "cluster": args.cluster, "tiles": args.tiles,
+           "bytes": call_bytes(m, c["n"], c["k"]) - 4 * c["n"] + scales.numel() * scales.element_size()}
     if args.reps > 3:
         s = torch.cuda.Stream()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             for i in range(args.reps):
-                fw.linear(x, reps[i % nrep], scales, bias, out=y, kernel=args.kernel, cluster=args.cluster, tiles=args.tiles)
+                fw.linear(x, reps[i % nrep], scales, bias, out=y, **kw)
         g.replay()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -1209,6 +1217,8 @@ def main():
     ap.add_argument("--kernel", type=int, default=0, help="with --profile: 0 auto, 1 gemv, 2 tensor-core (few tokens), 3 prefill GEMM")
     ap.add_argument("--cluster", type=int, default=0, help="with --profile: tensor-core CTAs per cluster (0 = from the shape)")
     ap.add_argument("--tiles", type=int, default=0, help="with --profile and --cluster: 128-channel tiles a cluster shares")
+    ap.add_argument("--group", default=None, choices=["32", "64", "128", "mx"],
+                    help="with --profile: per-group fp32 scales (or mx: E8M0 bytes), the automatic kernel choice")
     ap.add_argument("--record-traffic", default=None, metavar="CSV",
                     help="write profiles/dram_traffic_decode_stack.json from an ncu CSV (see TRAFFIC_COMMAND)")
     args = ap.parse_args()
