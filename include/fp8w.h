@@ -28,6 +28,11 @@
  *    inside a kernel surface on the caller's next synchronisation.
  *  - A kernel that gives up a bounded wait (it never should) records a
  *    nonzero code that fp8w_device_error() returns.
+ *  - On its first use on a device the library sets each kernel's
+ *    shared-memory attribute and reads the device's SM count and cluster
+ *    capacity, and keeps them for the process (the "state" above is about
+ *    calls, not this).  A cudaDeviceReset discards the attributes: a process
+ *    that resets the device must not call the library afterwards.
  *  - All matrices are row-major and densely packed (row stride = columns).
  */
 #ifndef FP8W_H
