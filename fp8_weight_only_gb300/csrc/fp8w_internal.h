@@ -67,6 +67,12 @@ cudaError_t device_sm_count(int& sms);
 // rows of `row_bytes`, boxes of box_inner x box_outer.
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer);
+// 3-D tensor map over a [rows, k] byte matrix (k % 128 == 0) seen as
+// (128 bytes of a k-block, row, k-block), 128-byte swizzle: a box of
+// box_rows rows and box_blocks consecutive k-blocks lands as box_blocks
+// tiles of box_rows x 128 bytes, one after the other.
+bool encode_3d_blocks(CUtensorMap* map, const void* base, uint64_t rows, uint64_t k, uint32_t box_rows,
+                      uint32_t box_blocks);
 
 // K4: m > 64 (prefill shapes), per-row scales; one launch, no workspace.
 cudaError_t launch_prefill(const LinearArgs& a, cudaStream_t st);

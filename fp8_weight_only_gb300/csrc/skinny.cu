@@ -1027,6 +1027,20 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint6
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_3d_blocks(CUtensorMap* map, const void* base, uint64_t rows, uint64_t k, uint32_t box_rows,
+                      uint32_t box_blocks) {
+    EncodeTiledFn fn = get_encode_fn();
+    if (!fn || k % 128 != 0) return false;
+    // byte (r, kb, c) of the [rows, k] matrix is at r * k + kb * 128 + c
+    const cuuint64_t dims[3] = {128, rows, k / 128};
+    const cuuint64_t strides[2] = {k, 128};
+    const cuuint32_t box[3] = {128, box_rows, box_blocks};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t device_sm_count(int& sms) {
     static int cache[64];
     static std::mutex mu;

@@ -63,11 +63,17 @@ constexpr int kWBarTmem = 1;              // named barrier: MMA warp + epilogue 
 constexpr int kWMaxSplit = 8;             // portable cluster size
 constexpr int kWMinKbPerCta = 4;          // a split CTA takes at least this many k-blocks
 
+// A stage holds kG k-blocks (fetched by one 3-D copy per operand when k %
+// 128 == 0, else one k-block by 2-D copies): the weight tiles first, then
+// the activation tiles.  Large copies matter: a 2-D copy of 128 rows x 128
+// bytes streams ~54 GB/s per SM, a 3-D one of four k-blocks ~128 GB/s.
 template <int BN>
 struct W8Smem {
+    static constexpr int kG = BN <= 16 ? 4 : BN <= 64 ? 3 : BN == 128 ? 2 : 1;
     static constexpr uint32_t kBBytes = BN * kWK;
-    static constexpr uint32_t kStageBytes = kWABytes + kBBytes;  // a multiple of 1024
-    static constexpr int kStages = BN <= 64 ? 8 : BN == 128 ? 6 : 4;
+    static constexpr uint32_t kXOff = kG * kWABytes;                 // activation tiles within a stage
+    static constexpr uint32_t kStageBytes = kG * (kWABytes + kBBytes);  // a multiple of 1024
+    static constexpr int kStages = BN == 256 ? 4 : 3;
     static constexpr uint32_t kBarOff = kStages * kStageBytes;
     // full, empty [kStages] | dfull, dempty [2] | drain
     static constexpr uint32_t kNumBars = 2 * kStages + 4 + 1;
@@ -115,7 +121,7 @@ template <int BN, bool kBf16>
 __global__ void __launch_bounds__(kWThreads, 1)
     w8a8_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_x,
                 const float* __restrict__ sx, const float* __restrict__ sw, const float* __restrict__ bias,
-                uint16_t* __restrict__ y, int64_t m, int64_t n, int64_t k, int split, int early) {
+                uint16_t* __restrict__ y, int64_t m, int64_t n, int64_t k, int split, int early, int g3) {
     using L = W8Smem<BN>;
     constexpr int kS = L::kStages;
     extern __shared__ uint8_t smem_raw[];
@@ -141,6 +147,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
     const int64_t t_step = split > 1 ? tiles : gridDim.x;
     const int kb0 = split > 1 ? rank * nkb / split : 0;
     const int kb1 = split > 1 ? (rank + 1) * nkb / split : nkb;
+    // k-blocks a stage, and the bytes its copies deliver (a 3-D box always
+    // delivers kG tiles, zeros past k)
+    const int gk = g3 ? L::kG : 1;
+    const uint32_t stage_tx = static_cast<uint32_t>(gk) * (kWABytes + L::kBBytes);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -180,14 +190,21 @@ __global__ void __launch_bounds__(kWThreads, 1)
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_x = policy_evict_last();
             // weight tiles of the first stages, before the dependency wait
+            auto load_w = [&](uint32_t st, int kb, int64_t cb, uint32_t bar) {
+                if (g3) tma_load_3d(st, &map_w, 0, static_cast<int32_t>(cb * kWM), kb, bar, pol_w);
+                else tma_load_2d(st, &map_w, kb * kWK, static_cast<int32_t>(cb * kWM), bar, pol_w);
+            };
+            auto load_x = [&](uint32_t st, int kb, int64_t tb, uint32_t bar) {
+                if (g3) tma_load_3d(st + L::kXOff, &map_x, 0, static_cast<int32_t>(tb * BN), kb, bar, pol_x);
+                else tma_load_2d(st + L::kXOff, &map_x, kb * kWK, static_cast<int32_t>(tb * BN), bar, pol_x);
+            };
             int pre = 0;
             if (early) {
                 for (int64_t t = t_first; t < tiles && pre < kS; t += t_step) {
                     const int64_t cb = t / ttiles;
-                    for (int kb = kb0; kb < kb1 && pre < kS; ++kb, ++pre) {
-                        mbar_arrive_expect_tx(full(pre), L::kStageBytes);
-                        tma_load_2d(sbase + pre * L::kStageBytes, &map_w, kb * kWK, static_cast<int32_t>(cb * kWM),
-                                    full(pre), pol_w);
+                    for (int kb = kb0; kb < kb1 && pre < kS; kb += gk, ++pre) {
+                        mbar_arrive_expect_tx(full(pre), stage_tx);
+                        load_w(sbase + pre * L::kStageBytes, kb, cb, full(pre));
                     }
                     if (split > 1) break;
                 }
@@ -197,7 +214,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             bool ok = true;
             for (int64_t t = t_first; t < tiles && ok; t += t_step) {
                 const int64_t cb = t / ttiles, tb = t - cb * ttiles;
-                for (int kb = kb0; kb < kb1; ++kb, ++i) {
+                for (int kb = kb0; kb < kb1; kb += gk, ++i) {
                     const int s = static_cast<int>(i % kS);
                     const uint32_t st = sbase + s * L::kStageBytes;
                     if (i >= pre) {
@@ -206,10 +223,10 @@ __global__ void __launch_bounds__(kWThreads, 1)
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(full(s), L::kStageBytes);
-                        tma_load_2d(st, &map_w, kb * kWK, static_cast<int32_t>(cb * kWM), full(s), pol_w);
+                        mbar_arrive_expect_tx(full(s), stage_tx);
+                        load_w(st, kb, cb, full(s));
                     }
-                    tma_load_2d(st + kWABytes, &map_x, kb * kWK, static_cast<int32_t>(tb * BN), full(s), pol_x);
+                    load_x(st, kb, tb, full(s));
                 }
                 if (split > 1) break;
             }
@@ -237,7 +254,7 @@ __global__ void __launch_bounds__(kWThreads, 1)
             }
             tc_fence_after();
             const uint32_t d_tmem = tmem + static_cast<uint32_t>(d * BN);
-            for (int kb = kb0; kb < kb1; ++kb, ++i) {
+            for (int kb = kb0; kb < kb1; kb += gk, ++i) {
                 const int s = static_cast<int>(i % kS);
                 if (!mbar_wait_warp(full(s), static_cast<uint32_t>((i / kS) & 1), abort_flag)) {
                     if (lane == 0) w8a8_error(kErrWaitTma, abort_flag);
@@ -246,11 +263,17 @@ __global__ void __launch_bounds__(kWThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t a_addr = sbase + s * L::kStageBytes;
-                const uint32_t b_addr = a_addr + kWABytes;
+                const uint32_t b_addr = a_addr + L::kXOff;
+                // the stage's k-blocks that are this CTA's (a 3-D box past kb1
+                // brings the next rank's, or zeros past k)
+                const int nb = kb1 - kb < gk ? kb1 - kb : gk;
+                for (int g = 0; g < nb; ++g) {
 #pragma unroll
-                for (int kk = 0; kk < kWK / 32; ++kk)
-                    mma_e4m3_ss_warp(d_tmem, smem_desc_sw128_kmajor(a_addr + kk * 32),
-                                     smem_desc_sw128_kmajor(b_addr + kk * 32), idesc, kb > kb0 || kk > 0);
+                    for (int kk = 0; kk < kWK / 32; ++kk)
+                        mma_e4m3_ss_warp(d_tmem, smem_desc_sw128_kmajor(a_addr + g * kWABytes + kk * 32),
+                                         smem_desc_sw128_kmajor(b_addr + g * L::kBBytes + kk * 32), idesc,
+                                         kb > kb0 || g > 0 || kk > 0);
+                }
                 tc_commit_warp(empty(s));  // the stage is free once these MMAs have read it
                 __syncwarp();
             }
@@ -370,13 +393,21 @@ static cudaError_t launch_w8a8_bn(const W8A8Args& a, cudaStream_t st) {
     int sms = 0;
     e = device_sm_count(sms);
     if (e != cudaSuccess) return e;
+    // 3-D copies of kG k-blocks when k is whole k-blocks, else 2-D of one
     CUtensorMap map_w, map_x;
-    if (!encode_2d(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_codes, static_cast<uint64_t>(a.k),
-                   static_cast<uint64_t>(a.n), static_cast<uint64_t>(a.k), kWK, kWM))
-        return cudaErrorInvalidValue;
-    if (!encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.x_codes, static_cast<uint64_t>(a.k),
-                   static_cast<uint64_t>(a.m), static_cast<uint64_t>(a.k), kWK, BN))
-        return cudaErrorInvalidValue;
+    const bool g3 = a.k % kWK == 0 && L::kG > 1;
+    if (g3) {
+        if (!encode_3d_blocks(&map_w, a.w_codes, static_cast<uint64_t>(a.n), static_cast<uint64_t>(a.k), kWM, L::kG) ||
+            !encode_3d_blocks(&map_x, a.x_codes, static_cast<uint64_t>(a.m), static_cast<uint64_t>(a.k), BN, L::kG))
+            return cudaErrorInvalidValue;
+    } else {
+        if (!encode_2d(&map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.w_codes, static_cast<uint64_t>(a.k),
+                       static_cast<uint64_t>(a.n), static_cast<uint64_t>(a.k), kWK, kWM))
+            return cudaErrorInvalidValue;
+        if (!encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.x_codes, static_cast<uint64_t>(a.k),
+                       static_cast<uint64_t>(a.m), static_cast<uint64_t>(a.k), kWK, BN))
+            return cudaErrorInvalidValue;
+    }
     const int64_t tiles = ((a.n + kWM - 1) / kWM) * ((a.m + BN - 1) / BN);
     const int64_t nkb = (a.k + kWK - 1) / kWK;
     // whole tiles on persistent CTAs when they nearly fill the GPU, else each
@@ -401,7 +432,7 @@ static cudaError_t launch_w8a8_bn(const W8A8Args& a, cudaStream_t st) {
     cfg.attrs = attr;
     cfg.numAttrs = split > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, map_w, map_x, a.x_scales, a.w_scales, a.bias, static_cast<uint16_t*>(a.y),
-                              a.m, a.n, a.k, split, a.early ? 1 : 0);
+                              a.m, a.n, a.k, split, a.early ? 1 : 0, g3 ? 1 : 0);
 }
 
 cudaError_t launch_w8a8(const W8A8Args& a, cudaStream_t st) {
