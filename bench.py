@@ -1177,17 +1177,28 @@ def run_profile_case(args):
     bias = torch.from_numpy(c["bias"]).to(dev)
     x = torch.from_numpy(c["x"].view(np.int16)).to(dev).view(torch.bfloat16)
     y = torch.empty((m, c["n"]), dtype=torch.bfloat16, device=dev)
+    if args.w8a8:
+        # the W8A8 GEMM on the same weight: activation codes made once
+        qx, sx = fw.quantize_act(x)
+        torch.cuda.synchronize()
+
+        def call(cd):
+            fw.linear_w8a8(qx, sx, cd, scales, bias, out=y)
+    else:
+        def call(cd):
+            fw.linear(x, cd, scales, bias, out=y, **kw)
     for i in range(3):
-        fw.linear(x, reps[i % nrep], scales, bias, out=y, **kw)
+        call(reps[i % nrep])
     torch.cuda.synchronize()
     out = {"case": args.profile, "group": args.group, "kernel": args.kernel, "cluster": args.cluster, "tiles": args.tiles,
-           "bytes": call_bytes(m, c["n"], c["k"]) - 4 * c["n"] + scales.numel() * scales.element_size()}
+           "bytes": call_bytes(m, c["n"], c["k"]) - 4 * c["n"] + scales.numel() * scales.element_size()
+           - (m * c["k"] - 4 * m if args.w8a8 else 0), "w8a8": bool(args.w8a8)}
     if args.reps > 3:
         s = torch.cuda.Stream()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             for i in range(args.reps):
-                fw.linear(x, reps[i % nrep], scales, bias, out=y, **kw)
+                call(reps[i % nrep])
         g.replay()
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
@@ -1217,6 +1228,7 @@ def main():
     ap.add_argument("--kernel", type=int, default=0, help="with --profile: 0 auto, 1 gemv, 2 tensor-core (few tokens), 3 prefill GEMM")
     ap.add_argument("--cluster", type=int, default=0, help="with --profile: tensor-core CTAs per cluster (0 = from the shape)")
     ap.add_argument("--tiles", type=int, default=0, help="with --profile and --cluster: 128-channel tiles a cluster shares")
+    ap.add_argument("--w8a8", action="store_true", help="with --profile: the W8A8 GEMM on the same weight")
     ap.add_argument("--group", default=None, choices=["32", "64", "128", "mx"],
                     help="with --profile: per-group fp32 scales (or mx: E8M0 bytes), the automatic kernel choice")
     ap.add_argument("--record-traffic", default=None, metavar="CSV",
