@@ -572,27 +572,31 @@ def run_warm_l2(torch, fw, dev, s, launches=200):
     bias = torch.from_numpy(c["bias"]).to(dev)
     codes, scales = fw.quantize(w)
     y = torch.empty((c["m"], c["n"]), dtype=torch.float16, device=dev)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(s):
-        fw.linear(x, codes, scales, bias, out=y)
-        torch.cuda.synchronize()
-        with torch.cuda.graph(g, stream=s):
-            for _ in range(launches):
-                fw.linear(x, codes, scales, bias, out=y)
-    g.replay()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s):
-        e0.record(s)
+    def timed(ready):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            fw.linear(x, codes, scales, bias, out=y, weights_ready=ready)
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g, stream=s):
+                for _ in range(launches):
+                    fw.linear(x, codes, scales, bias, out=y, weights_ready=ready)
         g.replay()
-        e1.record(s)
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / launches
-    del g
-    return {"us_per_launch": round(us, 3), "shape": "[22, 1024] x [1024, 4096], fp16",
-            "note": "same buffers, graph-replayed back-to-back launches (warm L2); context: the pages report "
-                    "5.6 us for this shape with a warm L2 on another GPU"}
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            g.replay()
+            e1.record(s)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / launches
+        del g
+        return round(us, 3)
+    return {"us_per_launch": timed(False), "us_per_launch_weights_ready": timed(True),
+            "shape": "[22, 1024] x [1024, 4096], fp16",
+            "note": "same buffers, graph-replayed back-to-back launches (warm L2), without and with the "
+                    "weights-ready flag (weights quantised before the stream's previous kernel, as in a "
+                    "serving loop); context: the pages report 5.6 us for this shape with a warm L2 on another GPU"}
 
 
 def bf16_peak():

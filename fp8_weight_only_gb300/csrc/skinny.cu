@@ -1064,17 +1064,18 @@ cudaError_t device_sm_count(int& sms) {
 // clusters of cl CTAs the device holds at a time (a cluster lives in one GPC,
 // so a GPC whose SM count cl does not divide leaves SMs idle; active[1] is
 // the SM count).  Sharing tiles costs a fixed finish, counted in units
-// (measured on GB300 against whole tiles at a ~0.38 us unit): about 1 us
-// when a cluster splits one tile (kSplitUnits), about 3.3 us when its ranks
-// hold two shared tiles each (kSharedUnits: both partials wait for the end,
-// and a cluster starts only when all its SMs are free).  Each rank gets at
-// least kMinUnitsPerCta units (and
-// at least one of every cluster's, so cl <= nkb).  A 64-token launch keeps
+// (measured on GB300 against whole tiles at a ~0.38 us unit): about 2 us
+// when a cluster splits one tile (kSplitUnits; [22, 1024] x [1024, 4096]
+// fp16, 8 k-blocks a tile: 5.1 us as 32 whole tiles, 5.9 us split over
+// clusters of 2), about 3.3 us when its ranks hold two shared tiles each
+// (kSharedUnits: both partials wait for the end, and a cluster starts only
+// when all its SMs are free).  Each rank gets at least kMinUnitsPerCta
+// units (and at least one of every cluster's, so cl <= nkb).  A 64-token launch keeps
 // one accumulator per MMA warp, and the per-group form keeps a tile's totals
 // in registers, so their CTAs may share at most one tile: tpc == 1 when
 // cl > 1.
 constexpr int kMinUnitsPerCta = 4;
-constexpr int kSplitUnits = 3;
+constexpr int kSplitUnits = 6;
 constexpr int kSharedUnits = 9;
 constexpr int64_t kMaxClusterUnits = 1 << 24;  // cluster-local unit indices are 32-bit
 
