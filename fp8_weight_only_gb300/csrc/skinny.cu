@@ -359,16 +359,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         return cu;
     };
 
-    // Start-up: warp 1 sets up the activation ring's barriers, warp 0 all the
-    // others; each then arrives at the start-up barrier without waiting and
-    // begins streaming, while the other warps wait there for both.
+    // Start-up: warp 0 sets up the code slots' barriers, warp 1 the
+    // activation ring's; each then arrives at the start-up barrier without
+    // waiting and begins streaming.  The MMA warp sets up the rest (used only
+    // by warps that wait at that barrier) before it joins them there, so no
+    // one warp spends ~1300 cycles on all of them while the stream waits.
     if (warp <= kXWarp) {
         // warp 1 sets up udone and xfull, [xb0, xb1): it is the first to wait on udone
         const uint32_t xb0 = static_cast<uint32_t>(L::kLaneBars + kAS);
         const uint32_t xb1 = xb0 + static_cast<uint32_t>(kDone + kXS);
         if (warp == 0) {
-            for (uint32_t i = lane; i < L::kNumBars; i += 32)
-                if (i < xb0 || i >= xb1) mbar_init(bar0 + 8 * i, L::arrivals(i));
+            // the code slots' barriers (the MMA warp sets up the others that
+            // neither producer uses before the start-up barrier)
+            for (uint32_t i = lane; i < L::kLaneBars; i += 32) mbar_init(bar0 + 8 * i, L::arrivals(i));
         } else {
             for (uint32_t i = xb0 + lane; i < xb1; i += 32) mbar_init(bar0 + 8 * i, L::arrivals(i));
             __syncwarp();
@@ -381,6 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_mbar_init();
         asm volatile("bar.arrive %0, %1;" ::"n"(kBarStart), "n"(kThreads) : "memory");
     } else {
+        if (warp == kMmaWarp) {
+            const uint32_t xb0 = static_cast<uint32_t>(L::kLaneBars + kAS);
+            const uint32_t xb1 = xb0 + static_cast<uint32_t>(kDone + kXS);
+            for (uint32_t i = L::kLaneBars + lane; i < L::kNumBars; i += 32)
+                if (i < xb0 || i >= xb1) mbar_init(bar0 + 8 * i, L::arrivals(i));
+            fence_mbar_init();
+        }
         asm volatile("bar.sync %0, %1;" ::"n"(kBarStart), "n"(kThreads) : "memory");
     }
     // let the next kernel in the stream start launching; its CTAs wait for
