@@ -385,6 +385,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("bar.arrive %0, %1;" ::"n"(kBarStart), "n"(kThreads) : "memory");
     } else {
         if (warp == kMmaWarp) {
+            // TMEM first (it waits for nothing here: one CTA per SM), then the
+            // barriers
+            tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+            tmem_relinquish();
             const uint32_t xb0 = static_cast<uint32_t>(L::kLaneBars + kAS);
             const uint32_t xb1 = xb0 + static_cast<uint32_t>(kDone + kXS);
             for (uint32_t i = L::kLaneBars + lane; i < L::kNumBars; i += 32)
@@ -396,14 +400,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // let the next kernel in the stream start launching; its CTAs wait for
     // this grid to complete before they read or write global memory
     pdl_launch_dependents();
-    // TMEM is allocated by the MMA warp while the producers already stream;
-    // the warps that use it meet the MMA warp at a named barrier first.
+    // TMEM was allocated by the MMA warp during start-up; the warps that use
+    // it meet the MMA warp at a named barrier first.
     uint32_t tmem = 0;
     if (warp >= kMmaWarp) {
-        if (warp == kMmaWarp) {
-            tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-            tmem_relinquish();
-        }
         tc_fence_before();
         asm volatile("bar.sync %0, %1;" ::"n"(kBarTmem), "n"(kThreads - 32 * kMmaWarp) : "memory");
         tc_fence_after();
