@@ -362,7 +362,7 @@ def kernel_name(m, k):
         # row pairs, bf16, fp32 x up to 8192 codes a row (16-bit x beyond), one scale a row
         return "fp8w::gemv_kernel<2, 1, 1, 0>" if k <= 8192 else "fp8w::gemv_kernel<2, 1, 0, 0>"
     # tokens a launch, bf16, per-row scales
-    return "fp8w::skinny_kernel<%d, 1, 0>" % (16 if m <= 16 else 32)
+    return "fp8w::skinny_kernel<%d, 1, 0, 1>" % (16 if m <= 16 else 32)
 
 
 KERNEL_SOURCES = {"skinny_kernel": ["skinny.cu", "fp8w_device.cuh"], "gemv_kernel": ["gemv.cu", "fp8w_device.cuh"]}

@@ -66,6 +66,7 @@
 // role's loop, lets its in-flight copies and MMAs finish, frees TMEM and
 // exits.
 #include <mutex>
+#include <type_traits>
 
 #include "fp8w_device.cuh"
 #include "fp8w_internal.h"
@@ -275,8 +276,12 @@ struct SharedTile {
 //                of kGAcc); the epilogue drains each one, multiplies it by
 //                the group's scale and adds it to the tile's fp32 total in
 //                registers (at most 32 tokens a launch, and at most one
-//                shared tile a CTA).
-template <int NT, bool kBf16, int kMode = kModeRow>
+//                shared tile a CTA).  kGpu = 128 / gsz groups a unit is a
+//                compile-time constant (one kernel per group size: with it
+//                known the hand-off loops unroll), and where the ring holds
+//                the groups of two units or more the hand-off goes once a
+//                unit rather than once a group.
+template <int NT, bool kBf16, int kMode = kModeRow, int kGpu = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     skinny_kernel(const __grid_constant__ CUtensorMap map_codes, const __grid_constant__ CUtensorMap map_x,
                   const float* __restrict__ scales, const uint8_t* __restrict__ e8, const float* __restrict__ bias,
@@ -308,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto gfull = [&](int b) { return bar0 + 8u * (L::kGBar0 + b); };
     auto gfree = [&](int b) { return bar0 + 8u * (L::kGBar0 + kGAcc + b); };
     // groups a unit, and MMAs (k = 16) a group (grouped form)
-    const int gpu = kGrp ? kBlockK / gsz : 1;
-    const int mpg = kGrp ? gsz / 16 : kBlockK / 16;
+    constexpr int gpu = kGrp ? kGpu : 1;                 // gsz == kBlockK / kGpu
+    constexpr int mpg = kBlockK / 16 / gpu;
     // unit v's MMAs are done (v < 0: nothing to wait for)
     auto done_bar = [&](int v) { return udone(v % kDone); };
     auto done_parity = [&](int v) { return static_cast<uint32_t>((v / kDone) & 1); };
@@ -502,7 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // two units (kGAcc >= 2 gpu).  Otherwise warp 2 alone issues every
         // unit, and its waits come in order.
         const int w = warp - kMmaWarp;
-        const int nw = (kGrp && kGAcc < 2 * gpu) ? 1 : kMmaWarps;  // issuing warps
+        constexpr int nw = (kGrp && kGAcc < 2 * gpu) ? 1 : kMmaWarps;  // issuing warps
+        // per-group form with several groups a unit: one hand-off a unit where
+        // the ring holds the groups of two units or more (g_per units)
+        constexpr int g_per = kGrp ? kGAcc / gpu : 1;
+        constexpr bool g_unit = kGrp && gpu > 1 && g_per >= 2;
         constexpr uint32_t idesc = idesc_f16(kBf16, NT);
         UnitCursor cu = cursor0();
         int seg = 0, jj = 0;
@@ -542,6 +551,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // G % kGAcc, once the epilogue has drained its previous group
                     uint32_t g_tmem = 0;
                     int gb = 0;
+                    if constexpr (g_unit) {
+                        // one hand-off a unit: the accumulator of the unit's last
+                        // group (the epilogue drains in order, so the unit's other
+                        // accumulators are free as well), one commit after its MMAs
+                        const int bl = (it * gpu + gpu - 1) & (kGAcc - 1);
+                        if (!mbar_wait_warp(gfree(bl), static_cast<uint32_t>(((it / g_per) & 1) ^ 1), abort_flag)) {
+                            if (lane == 0) record_error(kErrWaitMma, abort_flag, gfree(bl), bar0);
+                            failed = true;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int q = 0; q < kBlockK / 16; ++q) {
+                            const int qg = q & (mpg - 1);
+                            const uint64_t b_desc = smem_desc_sw128_kmajor(xs + (q >> 2) * L::kXBoxBytes + (q & 3) * 32);
+                            mma_f16_ts_warp(tmem + kDCol0 + ((it * gpu + q / mpg) & (kGAcc - 1)) * NT, a_tmem + q * 8,
+                                            b_desc, idesc, qg != 0);
+                        }
+                        tc_commit_warp(gfull(bl));
+                    } else
 #pragma unroll
                     for (int q = 0; q < kBlockK / 16; ++q) {
                         const int qg = q & (mpg - 1);
@@ -679,6 +708,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             bool held = false;
             int G = 0;
+            // one hand-off a unit where the MMA warps make one (the same rule)
+            constexpr int g_per_e = kGAcc / gpu;
+            constexpr bool g_unit_e = gpu > 1 && g_per_e >= 2;
             bool ok = true;
             for (int it = 0; it < iters && ok;) {
                 const int seg_len = cu.seg_left();
@@ -693,6 +725,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int sg = 0; sg < 4; ++sg)
                             if (sg < gpu) sn[sg] = scale_at(static_cast<int64_t>(cu.tile) * kTileN + r, cu.kb * gpu + sg);
+                    }
+                    if constexpr (g_unit_e) {
+                        // one hand-off a unit (the MMA warps commit once, on the
+                        // barrier of the unit's last group's accumulator)
+                        const int u = G / gpu;
+                        const int bl = (G + gpu - 1) & (kGAcc - 1);
+                        if (!mbar_wait_warp(gfull(bl), static_cast<uint32_t>((u / g_per_e) & 1), abort_flag)) {
+                            if (lane == 0) *ep_abort = 1;
+                            record_error(kErrWaitMma, abort_flag, gfull(bl), bar0);
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+#pragma unroll
+                        for (int sg = 0; sg < 4; ++sg) {
+                            if (sg >= gpu) break;
+                            const int gb = (G + sg) & (kGAcc - 1);
+#pragma unroll
+                            for (int h = 0; h < NT / 16; ++h) {
+                                if (h * 16 >= m_rows) break;
+                                uint32_t v[16];
+                                tmem_ld_x16_sync(lane_addr + kDCol0 + gb * NT + h * 16, v);
+                                ffma2_x16(tot2 + h * 8, v, pack2(sc[sg], sc[sg]));
+                            }
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(gfree(bl));
+                        G += gpu;
+                        continue;
                     }
 #pragma unroll
                     for (int sg = 0; sg < 4; ++sg) {
@@ -1118,12 +1180,12 @@ bool skinny_shape_valid(const SkinnyShape& sh, int64_t m, int64_t k, bool groupe
            (sh.cl == 1 || (nt <= 32 && !grouped) || sh.tpc == 1);
 }
 
-template <int NT, bool kBf16, int kMode = kModeRow>
+template <int NT, bool kBf16, int kMode = kModeRow, int kGpu = 1>
 static cudaError_t launch_nt(const LinearArgs& a, const SkinnyShape* forced, cudaStream_t st) {
     using L = SkinnySmem<NT>;
     constexpr bool kMx = kMode == kModeMxFold;
     constexpr bool kGrp = kMode == kModeGrouped;
-    auto kern = skinny_kernel<NT, kBf16, kMode>;
+    auto kern = skinny_kernel<NT, kBf16, kMode, kGpu>;
     // per device, once: the kernel's attributes, and how many clusters of
     // each size the device holds at a time (0 where a size cannot launch)
     static std::once_flag attr_once[64];
@@ -1216,10 +1278,18 @@ cudaError_t launch_skinny(const LinearArgs& a, const SkinnyShape* forced, cudaSt
     if (grouped) {
         if (a.k % a.group != 0 || (a.group != 32 && a.group != 64 && a.group != 128) || (a.e8m0 && a.group != 32))
             return cudaErrorInvalidValue;
-        if (a.m <= 16)
-            return bf16 ? launch_nt<16, true, kModeGrouped>(a, forced, st)
-                        : launch_nt<16, false, kModeGrouped>(a, forced, st);
-        return bf16 ? launch_nt<32, true, kModeGrouped>(a, forced, st) : launch_nt<32, false, kModeGrouped>(a, forced, st);
+        // one kernel per group count a unit (1, 2 or 4 groups of 128, 64 or 32)
+        auto by_groups = [&](auto gpu_tag) -> cudaError_t {
+            constexpr int kG = decltype(gpu_tag)::value;
+            if (a.m <= 16)
+                return bf16 ? launch_nt<16, true, kModeGrouped, kG>(a, forced, st)
+                            : launch_nt<16, false, kModeGrouped, kG>(a, forced, st);
+            return bf16 ? launch_nt<32, true, kModeGrouped, kG>(a, forced, st)
+                        : launch_nt<32, false, kModeGrouped, kG>(a, forced, st);
+        };
+        if (a.group == 128) return by_groups(std::integral_constant<int, 1>{});
+        if (a.group == 64) return by_groups(std::integral_constant<int, 2>{});
+        return by_groups(std::integral_constant<int, 4>{});
     }
     if (a.e8m0) {
         // MX-style scales: bf16 activations, k % 128 == 0 (checked by the caller)
