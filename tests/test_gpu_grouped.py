@@ -93,6 +93,21 @@ def test_linear_grouped_gate_every_output(m):
     assert_parity(got, ref, oracle.ACT_BF16, ("gate", m))
 
 
+@pytest.mark.parametrize("group", [64, 128])
+def test_linear_grouped_prefill_gate_repeatable(group):
+    """The prefill GEMM's per-group form on the whole 14336 x 4096 gate matrix
+    (130 tokens: two token tiles, every SM walking several weight tiles):
+    three launches give the same bits, and every output is within the
+    tolerance of the oracle."""
+    m, n, k = 130, 14336, 4096
+    c, codes, scales = _grouped_case(97 + group, m, n, k, group, oracle.ACT_BF16)
+    runs = [_run(c["x"], oracle.ACT_BF16, codes, scales, c["bias"]) for _ in range(3)]
+    assert np.array_equal(runs[0], runs[1]) and np.array_equal(runs[0], runs[2])
+    ref = oracle.linear_grouped(c["x"], oracle.ACT_BF16, codes, scales, group, c["bias"],
+                                threads=oracle.host_cores())
+    assert_parity(runs[0], ref, oracle.ACT_BF16, ("gate prefill", group))
+
+
 def test_linear_grouped_one_group_scale_equals_the_row_scale():
     """Every group of a row with the row's scale: the per-group product equals
     the per-channel one within the tolerance (the scale is applied per group
