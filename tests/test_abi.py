@@ -224,3 +224,37 @@ def test_dequantize_grouped_rejects_bad_arguments(args, status):
 ])
 def test_dequantize_mx_rejects_bad_arguments(args, status):
     assert fw.lib().fp8w_dequantize_mx(*args, None) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((A16, 0, 2, 64, B16, C16), 4),            # fp32 activations: bf16 or fp16 only
+    ((A16, 3, 2, 64, B16, C16), 4),
+    ((None, 1, 2, 64, B16, C16), 1), ((A16, 1, 2, 64, None, C16), 1), ((A16, 2, 2, 64, B16, None), 1),
+    ((A16, 1, 0, 64, B16, C16), 2), ((A16, 1, 2, 24, B16, C16), 2), ((A16, 2, 2, 65536 + 16, B16, C16), 2),
+    ((ctypes.c_void_p(0x100008), 1, 2, 64, B16, C16), 3),
+    ((A16, 1, 2, 64, ctypes.c_void_p(0x200004), C16), 3),
+    ((A16, 1, 2, 64, B16, ctypes.c_void_p(0x300002)), 3),
+])
+def test_quantize_act_rejects_bad_arguments(args, status):
+    assert fw.lib().fp8w_quantize_act(*args, None) == status
+
+
+E16 = ctypes.c_void_p(0x500000)
+
+
+def _w8a8(xc=A16, xs=B16, m=2, k=64, wc=C16, ws=D16, bias=None, n=8, y=E16, out=1, flags=0):
+    return fw.lib().fp8w_linear_w8a8(xc, xs, m, k, wc, ws, bias, n, y, out, flags, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(xc=None), 1), (dict(xs=None), 1), (dict(wc=None), 1), (dict(ws=None), 1), (dict(y=None), 1),
+    (dict(out=0), 4), (dict(out=3), 4),
+    (dict(m=0), 2), (dict(n=0), 2), (dict(k=8), 2), (dict(k=40), 2), (dict(k=65536 + 16), 2),
+    (dict(m=-1), 2), (dict(n=2 ** 31), 2),
+    (dict(xc=ctypes.c_void_p(0x100008)), 3), (dict(wc=ctypes.c_void_p(0x300004)), 3),
+    (dict(xs=ctypes.c_void_p(0x200002)), 3), (dict(ws=ctypes.c_void_p(0x400001)), 3),
+    (dict(bias=ctypes.c_void_p(0x600002)), 3), (dict(y=ctypes.c_void_p(0x500001)), 3),
+    (dict(flags=2), 6), (dict(flags=-1), 6),
+])
+def test_linear_w8a8_rejects_bad_arguments(kw, status):
+    assert _w8a8(**kw) == status
