@@ -119,7 +119,7 @@ FP8W_API fp8w_status fp8w_quantize_grouped(const float *w, int64_t n, int64_t k,
 
 /*
  * fp8w_linear_grouped -- fp8w_linear for codes with per-group scales:
- *   y[0, r] = round_act( sum_j scales[r, j] * sum_{c in group j} x[0, c] * e4m3(codes[r, c]) + bias[r] ).
+ *   y[i, r] = round_act( sum_j scales[r, j] * sum_{c in group j} x[i, c] * e4m3(codes[r, c]) + bias[r] ).
  *
  * group 32, 64 or 128 with k % group == 0; scales [n, k / group] fp32,
  * 16-byte aligned.  Other arguments as fp8w_linear.  fp32 accumulation, each
