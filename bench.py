@@ -709,7 +709,7 @@ def run_configs(torch, fw, dev, s, peak):
     for m in synthetic.SKINNY_M:
         sweep[str(m)]["t_over_t1"] = round(sweep[str(m)]["us"] / t1, 3)
     out["skinny_sweep"] = sweep
-    # the benchmark spec's targets: M = 1 at >= 80% of the HBM peak on the 58.7 MB
+    # the targets: M = 1 at >= 80% of the HBM peak on the 58.7 MB
     # weight (both orientations), and t(M) <= 1.3 t(1) up to M = 32
     c3 = synthetic.case("decode_stack", 1, "down")
     us3, nb3 = time_case(torch, fw, dev, s, c3)
